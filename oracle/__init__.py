@@ -1,0 +1,203 @@
+"""CPU oracle for paged grouped-query attention decode (fp64, plain C).
+
+TEST INFRASTRUCTURE ONLY.  The GPU library never imports, links or calls
+anything in this package; only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` do.  It shares no code with the CUDA path.
+
+The arithmetic lives in ``pgd_oracle.c`` (see its header for the passages of
+the pages each routine follows); this module only compiles it with gcc and
+marshals numpy arrays through ctypes.
+
+Routines (all fp64):
+  decode          softmax(q . K^T * scale) . V per query head, the definition
+  weights         the attention weights of one (sequence, head)
+  online_log2     the one-pass log2-space online softmax, in the pages' order
+  split_partials  per-partition (max, exp-sum, normalised output) partials
+  merge_partials  the split-KV reduce of those partials
+  page_reads      the physical pages the method must read, per KV head
+  half_to_double  IEEE binary16 decoding
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pgd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ORC_ERRORS = {1: "bad shape", 2: "bad sequence length", 3: "page id out of range",
+              4: "out of memory"}
+
+
+def build(force: bool = False) -> str:
+    """Compile pgd_oracle.c into oracle/liboracle.so with gcc (-O2 -fopenmp)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_half_to_double.restype = D
+        lib.oracle_paged_gqa_decode.argtypes = [P] * 6 + [D] + [I] * 8
+        lib.oracle_paged_gqa_decode.restype = I
+        lib.oracle_attention_weights.argtypes = [P] * 5 + [D] + [I] * 9
+        lib.oracle_attention_weights.restype = I
+        lib.oracle_online_log2.argtypes = [P] * 6 + [D] + [I] * 8
+        lib.oracle_online_log2.restype = I
+        lib.oracle_split_partials.argtypes = [P] * 8 + [D] + [I] * 10
+        lib.oracle_split_partials.restype = I
+        lib.oracle_merge_partials.argtypes = [P] * 4 + [I] * 4
+        lib.oracle_merge_partials.restype = I
+        lib.oracle_page_reads.argtypes = [P] * 3 + [I] * 5
+        lib.oracle_page_reads.restype = I
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = I
+        _lib = lib
+        return lib
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def _i32(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc):
+    if rc != 0:
+        raise ValueError(f"oracle rejected the inputs: {ORC_ERRORS.get(rc, rc)}")
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _dims(q, k_cache, block_tables):
+    S, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    assert D == D2, (D, D2)
+    MB = block_tables.shape[1] if block_tables.ndim == 2 else 1
+    return S, Hq, Hkv, D, BS, MB, NB
+
+
+def half_to_double(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.oracle_half_to_double(int(b)) for b in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, threads=None):
+    """out[S, Hq, D] (fp64) = softmax(q . K^T * scale) . V per query head."""
+    lib = _load()
+    q, k, v = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, Hkv, D, BS, MB, NB = _dims(q, k, bt)
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_paged_gqa_decode(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(bt),
+                                       _ptr(sl), float(scale), S, Hq, Hkv, D, BS, MB, NB,
+                                       int(threads or max_threads())))
+    return out
+
+
+def weights(q, k_cache, block_tables, seq_lens, scale, s, h):
+    """Attention weights w[t], t < seq_lens[s], of query head h of sequence s."""
+    lib = _load()
+    q, k = _u16(q), _u16(k_cache)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, Hkv, D, BS, MB, NB = _dims(q, k, bt)
+    w = np.zeros(max(int(sl[s]), 1), dtype=np.float64)
+    _check(lib.oracle_attention_weights(_ptr(w), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl),
+                                        float(scale), int(s), int(h), S, Hq, Hkv, D, BS,
+                                        MB, NB))
+    return w[: int(sl[s])]
+
+
+def online_log2(q, k_cache, v_cache, block_tables, seq_lens, scale, threads=None):
+    """The one-pass log2-space online softmax form of ``decode``."""
+    lib = _load()
+    q, k, v = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, Hkv, D, BS, MB, NB = _dims(q, k, bt)
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_online_log2(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
+                                  float(scale), S, Hq, Hkv, D, BS, MB, NB,
+                                  int(threads or max_threads())))
+    return out
+
+
+def split_partials(q, k_cache, v_cache, block_tables, seq_lens, scale, P, NPmax=None,
+                   threads=None):
+    """(m, l, o): log2-space max [S,Hq,NP], exp-sum [S,Hq,NP], normalised
+    partial output [S,Hq,NP,D] of every P-token partition."""
+    lib = _load()
+    q, k, v = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, Hkv, D, BS, MB, NB = _dims(q, k, bt)
+    if NPmax is None:
+        NPmax = max(1, max([(int(x) + P - 1) // P for x in sl] or [1]))
+    m = np.empty((S, Hq, NPmax), dtype=np.float64)
+    l = np.empty((S, Hq, NPmax), dtype=np.float64)
+    o = np.empty((S, Hq, NPmax, D), dtype=np.float64)
+    _check(lib.oracle_split_partials(_ptr(m), _ptr(l), _ptr(o), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(bt), _ptr(sl), float(scale), S, Hq, Hkv, D, BS,
+                                     MB, NB, int(P), int(NPmax),
+                                     int(threads or max_threads())))
+    return m, l, o
+
+
+def merge_partials(m, l, o):
+    """out[S, Hq, D] from the partition partials (the split-KV reduce)."""
+    lib = _load()
+    m = np.ascontiguousarray(m, dtype=np.float64)
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    S, Hq, NPmax, D = o.shape
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_merge_partials(_ptr(out), _ptr(m), _ptr(l), _ptr(o), S, Hq, D, NPmax))
+    return out
+
+
+def page_reads(block_tables, seq_lens, num_kv_heads, block_size, num_blocks):
+    """reads[S, Hkv, MB]: the physical page ids read per (sequence, KV head),
+    -1 past the sequence's last page."""
+    lib = _load()
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, MB = bt.shape
+    reads = np.empty((S, num_kv_heads, MB), dtype=np.int32)
+    _check(lib.oracle_page_reads(_ptr(reads), _ptr(bt), _ptr(sl), S, int(num_kv_heads),
+                                 int(block_size), MB, int(num_blocks)))
+    return reads

@@ -1,0 +1,422 @@
+/*
+ * Plain CPU oracle for single-token grouped-query attention over a paged
+ * fp16 KV cache.  TEST INFRASTRUCTURE ONLY: the GPU library never links,
+ * loads or calls this file; only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg do.
+ *
+ * Everything here is written for a reader checking it against the pages
+ * by eye: no blocking, no fusion, no reordering beyond what the definition
+ * states, fp64 arithmetic throughout, OpenMP only across independent
+ * (sequence, query head) pairs so the summation order of every output
+ * element is fixed.
+ *
+ * Sources (page title, section):
+ *   - "vllm-metal: hand-written Metal Paged Attention" (cf-1.com), section
+ *     "What is Paged Attention": the KV cache is cut into fixed-size pages and
+ *     a per-sequence page table (block_tables) maps logical page -> physical
+ *     page.
+ *   - same page, "Metal parallel model": work is split per
+ *     (partition, KV head, sequence); the query heads that share one KV head
+ *     form a group.
+ *   - same page, "Four speed-up tricks", item 1: softmax in log2 space, log2(e)
+ *     folded into the scale so every exponential is exp2; running max and
+ *     exp-sum kept in one pass (online softmax).
+ *   - same page, "Four speed-up tricks", item 4: long contexts are cut into
+ *     256/512-token partitions; each partition writes a log2-space
+ *     (max, exp-sum) pair plus its *normalised* partial output, and a
+ *     separate reduce merges them.
+ *   - "voxtral.c single-token attention" (dpshk.com), section "Single-token
+ *     attention kernel": GQA with 32 query heads mapped onto 8 KV heads.
+ *
+ * Layouts (readings where the pages are silent):
+ *   q            [S][Hq][D]           IEEE binary16 bit patterns
+ *   k_cache      [NB][Hkv][BS][D]     IEEE binary16 bit patterns
+ *   v_cache      [NB][Hkv][BS][D]
+ *   block_tables [S][MB]              int32 physical page ids
+ *   seq_lens     [S]                  int32, 0 <= L <= MB*BS
+ *   out          [S][Hq][D]           fp64
+ * Query head h reads KV head h / (Hq/Hkv) (integer division).
+ * Token t of sequence s lives in physical page block_tables[s][t / BS],
+ * row t % BS.  Page-table entries at or past ceil(L/BS) are never read.
+ * A sequence of length 0 has an all-zero output row.
+ *
+ * Parity pins for every function are in tests/test_oracle.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Error codes returned by every entry point. */
+#define ORC_OK 0
+#define ORC_BAD_SHAPE 1      /* a size is non-positive or Hq % Hkv != 0 */
+#define ORC_BAD_LENGTH 2     /* a sequence length is < 0 or > MB*BS      */
+#define ORC_BAD_PAGE 3       /* a page id that must be read is outside [0, NB) */
+#define ORC_NO_MEMORY 4
+
+/* IEEE 754 binary16 -> double, from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * exponent 0: subnormal, value = fraction * 2^-24;
+ * exponent 31: infinity (fraction 0) or NaN;
+ * otherwise value = (1024 + fraction) * 2^(exponent - 25). */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);
+    return sign ? -v : v;
+}
+
+/* Lookup table of all 65536 binary16 values, filled once from the
+ * definition above (a cache of that function, nothing more). */
+static double g_h2d[65536];
+static int g_h2d_ready = 0;
+
+static void h2d_init(void)
+{
+    if (g_h2d_ready)
+        return;
+    for (int i = 0; i < 65536; ++i)
+        g_h2d[i] = oracle_half_to_double((uint16_t)i);
+    g_h2d_ready = 1;
+}
+
+static int check_inputs(const int32_t *block_tables, const int32_t *seq_lens,
+                        int S, int Hq, int Hkv, int D, int BS, int MB, int NB)
+{
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || BS <= 0 || MB <= 0 || NB <= 0)
+        return ORC_BAD_SHAPE;
+    if (Hq % Hkv != 0)
+        return ORC_BAD_SHAPE;
+    for (int s = 0; s < S; ++s) {
+        long L = seq_lens[s];
+        if (L < 0 || L > (long)MB * BS)
+            return ORC_BAD_LENGTH;
+        long npages = (L + BS - 1) / BS;
+        for (long j = 0; j < npages; ++j) {
+            int32_t pp = block_tables[(long)s * MB + j];
+            if (pp < 0 || pp >= NB)
+                return ORC_BAD_PAGE;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Address of row t of sequence s, KV head g: page-table lookup
+ * (cf-1.com, "What is Paged Attention"). */
+static const uint16_t *kv_row(const uint16_t *cache, const int32_t *block_tables,
+                              int s, long t, int g, int Hkv, int D, int BS, int MB)
+{
+    int32_t pp = block_tables[(long)s * MB + t / BS];
+    long row = ((long)pp * Hkv + g) * BS + t % BS;
+    return cache + row * D;
+}
+
+/* z_t = scale * sum_d q[d] * k_t[d] for every token t < L of (s, h). */
+static void logits(double *z, const uint16_t *q, const uint16_t *k_cache,
+                   const int32_t *block_tables, double scale, int s, int h, long L,
+                   int Hq, int Hkv, int D, int BS, int MB)
+{
+    int G = Hq / Hkv;
+    int g = h / G;
+    const uint16_t *qh = q + ((long)s * Hq + h) * D;
+    for (long t = 0; t < L; ++t) {
+        const uint16_t *kt = kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += g_h2d[qh[d]] * g_h2d[kt[d]];
+        z[t] = scale * dot;
+    }
+}
+
+/*
+ * The definition: out[s][h] = sum_t w_t v_t with
+ * w_t = exp(z_t - max z) / sum_u exp(z_u - max z).
+ * (Natural exp; equal to the log2/exp2 form of the pages mathematically.)
+ */
+int oracle_paged_gqa_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables,
+                            const int32_t *seq_lens, double scale, int S, int Hq,
+                            int Hkv, int D, int BS, int MB, int NB, int num_threads)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    h2d_init();
+    int G = Hq / Hkv;
+    long pairs = (long)S * Hq;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+    for (long sh = 0; sh < pairs; ++sh) {
+        int s = (int)(sh / Hq), h = (int)(sh % Hq);
+        int g = h / G;
+        long L = seq_lens[s];
+        double *o = out + sh * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        if (L == 0)
+            continue;
+        double *z = (double *)malloc(sizeof(double) * (size_t)L);
+        if (!z) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        logits(z, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        double zmax = -INFINITY;
+        for (long t = 0; t < L; ++t)
+            if (z[t] > zmax)
+                zmax = z[t];
+        double den = 0.0;
+        for (long t = 0; t < L; ++t)
+            den += exp(z[t] - zmax);
+        for (long t = 0; t < L; ++t) {
+            double w = exp(z[t] - zmax) / den;
+            const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+            for (int d = 0; d < D; ++d)
+                o[d] += w * g_h2d[vt[d]];
+        }
+        free(z);
+    }
+    return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
+/* Attention weights w_t of one (s, h), for the sum-to-one and closed-form
+ * pins.  w must hold seq_lens[s] doubles. */
+int oracle_attention_weights(double *w, const uint16_t *q, const uint16_t *k_cache,
+                             const int32_t *block_tables, const int32_t *seq_lens,
+                             double scale, int s, int h, int S, int Hq, int Hkv, int D,
+                             int BS, int MB, int NB)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    if (s < 0 || s >= S || h < 0 || h >= Hq)
+        return ORC_BAD_SHAPE;
+    h2d_init();
+    long L = seq_lens[s];
+    if (L == 0)
+        return ORC_OK;
+    logits(w, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+    double zmax = -INFINITY;
+    for (long t = 0; t < L; ++t)
+        if (w[t] > zmax)
+            zmax = w[t];
+    double den = 0.0;
+    for (long t = 0; t < L; ++t)
+        den += exp(w[t] - zmax);
+    for (long t = 0; t < L; ++t)
+        w[t] = exp(w[t] - zmax) / den;
+    return ORC_OK;
+}
+
+/*
+ * One-pass online softmax in log2 space, the order the pages describe
+ * (cf-1.com, "Four speed-up tricks", item 1): scores are taken as
+ * x_t = z_t * log2(e); a running max m and running exp2-sum l are carried
+ * over the tokens; on a new max the sum and the accumulated output are
+ * rescaled by exp2(m_old - m_new).
+ */
+int oracle_online_log2(double *out, const uint16_t *q, const uint16_t *k_cache,
+                       const uint16_t *v_cache, const int32_t *block_tables,
+                       const int32_t *seq_lens, double scale, int S, int Hq, int Hkv,
+                       int D, int BS, int MB, int NB, int num_threads)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    h2d_init();
+    int G = Hq / Hkv;
+    const double log2e = 1.0 / log(2.0);
+    long pairs = (long)S * Hq;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+    for (long sh = 0; sh < pairs; ++sh) {
+        int s = (int)(sh / Hq), h = (int)(sh % Hq);
+        int g = h / G;
+        long L = seq_lens[s];
+        double *o = out + sh * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        if (L == 0)
+            continue;
+        const uint16_t *qh = q + sh * D;
+        double m = -INFINITY, l = 0.0;
+        for (long t = 0; t < L; ++t) {
+            const uint16_t *kt = kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+            const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += g_h2d[qh[d]] * g_h2d[kt[d]];
+            double x = scale * dot * log2e;
+            double m_new = x > m ? x : m;
+            double alpha = exp2(m - m_new); /* exp2(-inf) = 0 on the first token */
+            double p = exp2(x - m_new);
+            l = alpha * l + p;
+            for (int d = 0; d < D; ++d)
+                o[d] = alpha * o[d] + p * g_h2d[vt[d]];
+            m = m_new;
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= l;
+    }
+    return ORC_OK;
+}
+
+/*
+ * Split-KV partials (cf-1.com, "Four speed-up tricks", item 4).
+ * Partition p of sequence s covers logical tokens [p*P, min((p+1)*P, L)).
+ * For every (s, h, p < ceil(L/P)), with x_t = z_t * log2(e):
+ *   m[s][h][p]    = max_t x_t                       (log2-space max)
+ *   l[s][h][p]    = sum_t exp2(x_t - m)             (exp-sum)
+ *   o[s][h][p][:] = sum_t exp2(x_t - m) v_t / l     (normalised output)
+ * Entries for p >= ceil(L/P) (up to NPmax) are m = -inf, l = 0, o = 0.
+ * P may be any positive integer.
+ */
+int oracle_split_partials(double *m_out, double *l_out, double *o_out,
+                          const uint16_t *q, const uint16_t *k_cache,
+                          const uint16_t *v_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, double scale, int S, int Hq, int Hkv,
+                          int D, int BS, int MB, int NB, int P, int NPmax,
+                          int num_threads)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    if (P <= 0 || NPmax <= 0)
+        return ORC_BAD_SHAPE;
+    for (int s = 0; s < S; ++s)
+        if (((long)seq_lens[s] + P - 1) / P > NPmax)
+            return ORC_BAD_SHAPE;
+    h2d_init();
+    int G = Hq / Hkv;
+    const double log2e = 1.0 / log(2.0);
+    long pairs = (long)S * Hq;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+    for (long sh = 0; sh < pairs; ++sh) {
+        int s = (int)(sh / Hq), h = (int)(sh % Hq);
+        int g = h / G;
+        long L = seq_lens[s];
+        for (int p = 0; p < NPmax; ++p) {
+            m_out[sh * NPmax + p] = -INFINITY;
+            l_out[sh * NPmax + p] = 0.0;
+            for (int d = 0; d < D; ++d)
+                o_out[(sh * NPmax + p) * D + d] = 0.0;
+        }
+        if (L == 0)
+            continue;
+        double *z = (double *)malloc(sizeof(double) * (size_t)L);
+        if (!z) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        logits(z, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        long np = (L + P - 1) / P;
+        for (long p = 0; p < np; ++p) {
+            long t0 = p * P, t1 = t0 + P < L ? t0 + P : L;
+            double m = -INFINITY;
+            for (long t = t0; t < t1; ++t)
+                if (z[t] * log2e > m)
+                    m = z[t] * log2e;
+            double l = 0.0;
+            for (long t = t0; t < t1; ++t)
+                l += exp2(z[t] * log2e - m);
+            double *o = o_out + (sh * NPmax + p) * D;
+            for (long t = t0; t < t1; ++t) {
+                double w = exp2(z[t] * log2e - m);
+                const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+                for (int d = 0; d < D; ++d)
+                    o[d] += w * g_h2d[vt[d]];
+            }
+            for (int d = 0; d < D; ++d)
+                o[d] /= l;
+            m_out[sh * NPmax + p] = m;
+            l_out[sh * NPmax + p] = l;
+        }
+        free(z);
+    }
+    return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
+/*
+ * Merge of the partition partials (the reduce of cf-1.com, "Four speed-up
+ * tricks", item 4), per (s, h):
+ *   M   = max_p m_p
+ *   w_p = l_p * exp2(m_p - M)
+ *   out = sum_p w_p o_p / sum_p w_p
+ * Partitions with l_p = 0 (empty) are skipped; if all are empty the output
+ * row is zero.
+ */
+int oracle_merge_partials(double *out, const double *m_in, const double *l_in,
+                          const double *o_in, int S, int Hq, int D, int NPmax)
+{
+    if (S < 0 || Hq <= 0 || D <= 0 || NPmax <= 0)
+        return ORC_BAD_SHAPE;
+    long pairs = (long)S * Hq;
+    for (long sh = 0; sh < pairs; ++sh) {
+        double *o = out + sh * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        double M = -INFINITY;
+        for (int p = 0; p < NPmax; ++p)
+            if (l_in[sh * NPmax + p] > 0.0 && m_in[sh * NPmax + p] > M)
+                M = m_in[sh * NPmax + p];
+        if (M == -INFINITY)
+            continue;
+        double den = 0.0;
+        for (int p = 0; p < NPmax; ++p) {
+            double l = l_in[sh * NPmax + p];
+            if (!(l > 0.0))
+                continue;
+            double w = l * exp2(m_in[sh * NPmax + p] - M);
+            den += w;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * o_in[(sh * NPmax + p) * D + d];
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= den;
+    }
+    return ORC_OK;
+}
+
+/*
+ * The set of physical pages the method reads: for every (s, KV head g),
+ * reads[s][g][j] = block_tables[s][j] for j < ceil(L/BS), and -1 for the
+ * rest of the row (MB entries).  Every query head of the group reads the
+ * same pages, so the set is per KV head.
+ */
+int oracle_page_reads(int32_t *reads, const int32_t *block_tables, const int32_t *seq_lens,
+                      int S, int Hkv, int BS, int MB, int NB)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hkv, Hkv, 1, BS, MB, NB);
+    if (rc)
+        return rc;
+    for (int s = 0; s < S; ++s) {
+        long npages = ((long)seq_lens[s] + BS - 1) / BS;
+        for (int g = 0; g < Hkv; ++g)
+            for (long j = 0; j < MB; ++j)
+                reads[((long)s * Hkv + g) * MB + j] =
+                    j < npages ? block_tables[(long)s * MB + j] : -1;
+    }
+    return ORC_OK;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
