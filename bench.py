@@ -1,0 +1,387 @@
+"""Benchmark: paged GQA decode on GB300 — KV-cache GB/s, % of HBM peak, us/call.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--partition P] [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one decode call (partition kernel + split-KV reduce) over the whole
+seeded synthetic workload (default ``batch_decode``: 64 sequences, GQA
+(32, 8, 128), block size 16, lengths U{512..4096}, partition 512), inputs
+resident in HBM.  K steps are timed with CUDA events after W warm-up steps;
+the K/V bytes per step (~0.6 GB) exceed the 129 MB L2, so there is no flush
+between steps.  Prints one JSON line.
+
+N > 1 (torchrun): every rank runs the same workload on its own GPU
+(independent replicas, no collective on the data path); rank 0 prints the
+aggregate: value = N * bytes / max-over-ranks time.
+
+``--impl reference`` times the CPU oracle (fp64, all host cores) on a
+bounded sample of the same workload instead, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode: KV-cache GB/s (% of GB300 HBM peak) and µs per call"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names, flags[1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------- helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_time(w, seqs, min_seconds=10.0, max_reps=50):
+    """Times the CPU oracle on the listed sequences; returns
+    (seconds per rep, KV bytes per rep, threads, reps)."""
+    import oracle
+
+    c = w.compact(seqs)
+    kv = int(c["seq_lens"].astype("int64").sum()) * w.Hkv * w.D * 4
+    threads = oracle.max_threads()
+    reps, total = 0, 0.0
+    while reps < max_reps and (total < min_seconds or reps < 1):
+        t0 = time.perf_counter()
+        oracle.decode(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["seq_lens"],
+                      c["scale"], threads=threads)
+        total += time.perf_counter() - t0
+        reps += 1
+    return total / reps, kv, threads, reps
+
+
+def sample_seqs(w, kv_budget_bytes):
+    """Leading sequences of the workload up to a K/V byte budget (>= 1)."""
+    lens = w.lens
+    per = w.Hkv * w.D * 4
+    acc, seqs = 0, []
+    for s in range(w.S):
+        if seqs and acc + int(lens[s]) * per > kv_budget_bytes:
+            break
+        seqs.append(s)
+        acc += int(lens[s]) * per
+    return seqs
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    import torch
+    from paged_gqa_decode_03_gb300.workloads import make_workload
+
+    w = make_workload(args.workload, device="cpu")
+    import oracle
+
+    oracle.build()
+    # size each step's sample so that warm-up + K steps take ~ args.ref_seconds
+    probe = w.compact([0])
+    t0 = time.perf_counter()
+    oracle.decode(probe["q"], probe["k_cache"], probe["v_cache"], probe["block_tables"],
+                  probe["seq_lens"], probe["scale"])
+    per_byte = (time.perf_counter() - t0) / max(1, int(w.lens[0]) * w.Hkv * w.D * 4)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup) / max(per_byte, 1e-12)
+    seqs = sample_seqs(w, min(budget, args.ref_sample_bytes))
+    c = w.compact(seqs)
+    kv = int(c["seq_lens"].astype("int64").sum()) * w.Hkv * w.D * 4
+    threads = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.decode(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["seq_lens"],
+                      c["scale"], threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["seq_lens"],
+                      c["scale"], threads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = kv / dt / 1e9
+    sample = (f"{len(seqs)} of {w.S} sequences of {args.workload} ({kv / 1e9:.3f} GB K/V per "
+              f"step), fp64 oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_gqa_decode_03_gb300 as pgd
+    from paged_gqa_decode_03_gb300.workloads import make_workload
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    pgd.load_library()
+
+    w = make_workload(args.workload, device=dev)
+    P = w.P if args.partition is None else args.partition
+    kv_bytes = w.kv_bytes()
+    alg_bytes = w.total_bytes()
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pgd.paged_gqa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
+                             w.scale, P, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pgd.pgd_check_device_error(stream) == 0
+    P_used = pgd.pgd_last_partition_size()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peak, peak_kind = measured_peaks()
+
+    # ---- timed region: K production steps, events on the launching stream;
+    # every step also records events around the partition kernel (the
+    # library's timing hook) for the roofline's per-launch duration.
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in kb + ka:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            pgd.pgd_set_timing_events(kb[i], ka[i])
+            step()
+        ev1.record(stream)
+        barrier()
+        pgd.pgd_set_timing_events(None, None)
+    clocks = clk.summary()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_per_step = elapsed_ms / args.steps
+    kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(args.steps))
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- same K steps without the per-launch events (exact production sequence)
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    ms_plain = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
+
+    # ---- end to end through the public API with host buffers: per step the
+    # step's inputs (q, block_tables, seq_lens) go host->device from pinned
+    # memory and the output comes back; the K/V cache stays resident.
+    q_h = w.q.cpu().pin_memory()
+    bt_h = w.block_tables.cpu().pin_memory()
+    sl_h = w.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, bt_d, sl_d = torch.empty_like(w.q), torch.empty_like(w.block_tables), torch.empty_like(
+        w.seq_lens)
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 4
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        pgd.paged_gqa_decode(out, q_d, w.k_cache, w.v_cache, bt_d, sl_d, w.scale, P,
+                             stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    barrier()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps)
+    e2e_value = world * kv_bytes / e2e_s / 1e9
+
+    # ---- CPU baseline: the oracle on this host (rank 0, N == 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        seqs = list(range(w.S))
+        sec, kv_s, threads, reps = oracle_time(w, seqs, min_seconds=args.cpu_seconds)
+        cpu = {"value": kv_s / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"all {len(seqs)} sequences of {args.workload} "
+                         f"({kv_s / 1e9:.3f} GB K/V), {reps} reps, fp64 C oracle, "
+                         f"{sec * 1e3:.1f} ms per call"}
+
+    if rank == 0:
+        achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+        traffic = None
+        tfile = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tfile):
+            try:
+                traffic = json.load(open(tfile)).get(f"{args.workload}:P{P_used}")
+            except Exception:
+                traffic = None
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "config": {"workload": args.workload, "num_seqs": w.S,
+                       "gqa": [w.Hq, w.Hkv, w.D], "block_size": w.BS,
+                       "partition_size": P_used, "requested_partition": P,
+                       "kv_bytes_per_step": kv_bytes, "num_blocks": w.NB,
+                       "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
+                       "accumulate": "fp32", "parallelism": f"replicas x{world}",
+                       "ms_per_step_without_kernel_events": ms_plain},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",
+                         "kernel": "paged_gqa_partial_kernel",
+                         "kernel_ms": kern_ms,
+                         "algorithmic_bytes_per_launch": alg_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="batch_decode")
+    ap.add_argument("--partition", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample-bytes", type=float, default=1.6e8)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+/*
+ * pgd.h — paged grouped-query attention decode on GB300 (sm_103a).
+ *
+ * One decode step of attention for a batch of sequences whose keys and
+ * values live in a paged fp16 KV cache.  For every sequence s and query
+ * head h:
+ *
+ *     out[s][h][:] = softmax( q[s][h] . K_s^T * scale ) . V_s
+ *
+ * where K_s, V_s are the seq_lens[s] cached tokens of KV head
+ * h / (num_q_heads / num_kv_heads), gathered page by page through the
+ * sequence's row of block_tables.
+ *
+ * Sources (page title, section):
+ *   "vllm-metal: hand-written Metal Paged Attention" (cf-1.com):
+ *     - "What is Paged Attention": the KV cache is cut into fixed-size pages;
+ *       the block_tables page table maps a sequence's logical page to a
+ *       physical page.
+ *     - "Metal parallel model": work per (partition, KV head, sequence), with
+ *       all query heads of one GQA group together so each K/V page is read
+ *       once per group.
+ *     - "Four speed-up tricks", 1: log2-space online softmax with exp2.
+ *     - "Four speed-up tricks", 4: split-KV partitions of 256 or 512 tokens,
+ *       partials written as log2-space (max, exp-sum) plus the normalised
+ *       partial output, merged by a separate reduce.
+ *     - "Dispatch layer": supported GQA geometries (32,8,128), (24,4,256),
+ *       (16,2,128), (16,2,256) with block sizes 32/16/8; partition choice
+ *       from the GPU's core count; 512 MiB cap on the per-call scratch.
+ *     - "Hands-on": diagnostics reporting the partition size last used.
+ *   "voxtral.c" (dpshk.com), "Single-token attention kernel": GQA head
+ *     mapping (32 query heads onto 8 KV heads), fp16 KV cache.
+ *
+ * Data layout (all row-major, contiguous; the pages leave it open):
+ *   q             [num_seqs][num_q_heads][head_dim]             fp16 (IEEE binary16 bits)
+ *   k_cache       [num_blocks][num_kv_heads][block_size][head_dim] fp16
+ *   v_cache       [num_blocks][num_kv_heads][block_size][head_dim] fp16
+ *   block_tables  [num_seqs][max_blocks_per_seq]                 int32 physical page ids
+ *   seq_lens      [num_seqs]                                     int32
+ *   out           [num_seqs][num_q_heads][head_dim]             fp32
+ * Token t of sequence s is row t % block_size of physical page
+ * block_tables[s][t / block_size].  Entries at or past
+ * ceil(seq_lens[s] / block_size) are never read, nor are the rows of the
+ * last page past the sequence end.  A sequence of length 0 gets an all-zero
+ * output row.
+ *
+ * Supported: head_dim in {128, 256}; block_size in {8, 16, 32};
+ * num_q_heads % num_kv_heads == 0 with a group of 1..8 query heads per KV
+ * head (this covers the four geometries of the pages and any other group of
+ * at most 8); partition_size in {256, 512} or 0 to let the library choose.
+ *
+ * Memory: every array is device memory owned by the caller.  q, k_cache and
+ * v_cache must be 16-byte aligned; the int32 arrays and out 4-byte aligned.
+ * num_blocks * num_kv_heads * block_size must be below 2^31.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and never synchronises the host.  The call
+ * validates all host-side arguments before launching anything; on any error
+ * it returns a non-zero status, launches nothing and leaves a message for
+ * pgd_last_error().  It never aborts, exits or throws.
+ *
+ * Device-side checks: a physical page id outside [0, num_blocks) or a
+ * sequence length outside [0, max_blocks_per_seq * block_size] found while
+ * the kernels run is never dereferenced (the page reads as zeros, the
+ * length is clamped) and sets a bit in a per-process device error word;
+ * pgd_check_device_error() reports and clears it.
+ */
+#ifndef PGD_H
+#define PGD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pgd_status {
+    PGD_OK = 0,
+    PGD_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment          */
+    PGD_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, block size, G  */
+    PGD_ERR_WORKSPACE = 3,    /* scratch above the 512 MiB cap, or too small   */
+    PGD_ERR_CUDA = 4,         /* a CUDA runtime call failed                    */
+    PGD_ERR_DEVICE = 5        /* the kernels flagged bad data (see below)      */
+} pgd_status;
+
+/* Bits of the device error word (pgd_check_device_error). */
+#define PGD_DEVERR_PAGE_RANGE 1u   /* a page id to be read was outside [0, num_blocks) */
+#define PGD_DEVERR_SEQ_LEN 2u      /* a length was < 0 or > max_blocks_per_seq*block_size */
+#define PGD_DEVERR_TIMEOUT 4u      /* an internal pipeline wait gave up (never expected)  */
+
+/* Upper bound of the per-call scratch, after the pages' 512 MiB GQA cap. */
+#define PGD_MAX_WORKSPACE_BYTES ((size_t)512 << 20)
+
+/*
+ * paged_gqa_decode — the decode step described above.
+ *
+ * scale            multiplies q . k before the softmax (e.g. 1/sqrt(head_dim)).
+ * partition_size   tokens per split-KV partition: 256, 512, or 0 for the
+ *                  scheduler's choice from the SM count and the length
+ *                  bound max_blocks_per_seq * block_size.
+ * max_blocks_per_seq  row stride of block_tables; also bounds every length.
+ * num_blocks       pages in each cache array (bounds every page id).
+ * stream           cudaStream_t to run on.
+ *
+ * Scratch for the partition partials is taken from a stream-ordered memory
+ * pool owned by the library and returned in stream order, so calls on
+ * different streams do not share it.  Use paged_gqa_decode_ex to supply it.
+ */
+pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables,
+                            const int32_t *seq_lens, float scale, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int partition_size, int max_blocks_per_seq, int num_blocks,
+                            void *stream);
+
+/*
+ * pgd_plan — the partition size a call with these sizes would use (resolving
+ * partition_size == 0 on the current device) and the scratch bytes it needs
+ * (0 when no sequence can span more than one partition).  Does not launch.
+ */
+pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, int partition_size, int max_blocks_per_seq,
+                    int *chosen_partition_size, size_t *workspace_bytes);
+
+/*
+ * paged_gqa_decode_ex — paged_gqa_decode with caller-owned scratch and an
+ * optional page trace.
+ *
+ * workspace        device memory of at least the bytes pgd_plan reports,
+ *                  256-byte aligned; may be NULL when that is 0.  Its
+ *                  contents need no initialisation; it must not be used by
+ *                  anything else until the call's work on `stream` is done.
+ * page_trace       NULL, or int32 device memory [num_seqs][num_kv_heads]
+ *                  [max_blocks_per_seq].  For every page the kernel reads it
+ *                  stores, at [s][kv_head][logical page], the physical id it
+ *                  used to form the address.  Entries it does not read are
+ *                  left untouched (fill with -1 beforehand to check that
+ *                  nothing past a sequence's last page is read).
+ */
+pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_cache,
+                               const uint16_t *v_cache, const int32_t *block_tables,
+                               const int32_t *seq_lens, float scale, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int partition_size, int max_blocks_per_seq,
+                               int num_blocks, void *workspace, size_t workspace_bytes,
+                               int32_t *page_trace, void *stream);
+
+/* Partition size used by this thread's last successful call (0 if none);
+ * the diagnostic of the pages' "Hands-on" section. */
+int pgd_last_partition_size(void);
+
+/* Message for this thread's last failed call ("" if none). */
+const char *pgd_last_error(void);
+
+/*
+ * pgd_check_device_error — waits for `stream`, then reads and clears the
+ * device error word of the current device.  *bits (if not NULL) receives the
+ * PGD_DEVERR_* bits set since the last check.  Returns PGD_ERR_DEVICE if any
+ * bit was set, PGD_ERR_CUDA if the wait itself failed, PGD_OK otherwise.
+ */
+pgd_status pgd_check_device_error(void *stream, unsigned *bits);
+
+/*
+ * pgd_set_timing_events — measurement hook.  When both are non-NULL, every
+ * later call on this thread records `before` (a cudaEvent_t) on its stream
+ * just before the partition kernel and `after` just after it, so the kernel's
+ * own duration can be read with cudaEventElapsedTime.  NULLs turn it off.
+ */
+pgd_status pgd_set_timing_events(void *before, void *after);
+
+/* Number of SMs and resident partition-kernel CTAs per SM the scheduler
+ * assumes for (head_dim, block_size) on the current device. */
+pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas_per_sm);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pgd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGD_H */

@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -29,6 +30,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pgd_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_STAMP = os.path.join(_HERE, "liboracle.arch")
 _lock = threading.Lock()
 _lib = None
 
@@ -38,7 +40,9 @@ ORC_ERRORS = {1: "bad shape", 2: "bad sequence length", 3: "page id out of range
 
 def build(force: bool = False) -> str:
     """Compile pgd_oracle.c into oracle/liboracle.so with gcc (-O2 -fopenmp)."""
-    if (not force and os.path.exists(_LIB_PATH)
+    arch = platform.machine()
+    same_arch = os.path.exists(_STAMP) and open(_STAMP).read().strip() == arch
+    if (not force and same_arch and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
@@ -46,6 +50,8 @@ def build(force: bool = False) -> str:
            "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(_STAMP, "w") as f:
+        f.write(arch + "\n")
     return _LIB_PATH
 
 

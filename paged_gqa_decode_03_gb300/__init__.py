@@ -1,1 +1,222 @@
-"""Paged grouped-query attention decode for GB300 (sm_103a)."""
+"""Paged grouped-query attention decode for GB300 (sm_103a).
+
+Thin Python binding of the C-ABI library ``libpgd.so`` (declared in
+``include/pgd.h``): it only turns torch tensors into pointers and sizes and
+calls the library, which runs every step of the computation in its CUDA
+kernels.  There is no other implementation behind these functions: if the
+library is missing they raise.
+
+    import paged_gqa_decode_03_gb300 as pgd
+    pgd.paged_gqa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                         partition_size=0)
+
+Shapes (contiguous, on one CUDA device):
+    q            fp16  [num_seqs, num_q_heads, head_dim]
+    k_cache      fp16  [num_blocks, num_kv_heads, block_size, head_dim]
+    v_cache      fp16  same as k_cache
+    block_tables int32 [num_seqs, max_blocks_per_seq]
+    seq_lens     int32 [num_seqs]
+    out          fp32  [num_seqs, num_q_heads, head_dim]   (written)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "pgd_plan", "pgd_last_partition_size",
+           "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
+           "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpgd.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS_NAMES = {0: "PGD_OK", 1: "PGD_ERR_INVALID_ARG", 2: "PGD_ERR_UNSUPPORTED",
+                3: "PGD_ERR_WORKSPACE", 4: "PGD_ERR_CUDA", 5: "PGD_ERR_DEVICE"}
+DEVERR_PAGE_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+
+# Every exported symbol of include/pgd.h with its ctypes signature.
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "paged_gqa_decode": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
+    "paged_gqa_decode_ex": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
+    "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
+    "pgd_last_partition_size": (_I, []),
+    "pgd_last_error": (ctypes.c_char_p, []),
+    "pgd_check_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "pgd_set_timing_events": (_I, [_P, _P]),
+    "pgd_device_info": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "pgd_version": (_I, []),
+}
+
+
+class PGDError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libpgd.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m paged_gqa_decode_03_gb300.build` (there is no fallback path)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _raise(status: int):
+    if status != 0:
+        msg = load_library().pgd_last_error()
+        raise PGDError(status, msg.decode() if msg else "")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _sizes(out, q, k_cache, v_cache, block_tables, seq_lens):
+    _check(q, "q", torch.float16, 3)
+    _check(k_cache, "k_cache", torch.float16, 4)
+    _check(v_cache, "v_cache", torch.float16, 4)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(out, "out", torch.float32, 3)
+    S, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("inconsistent shapes: q %s, k %s, v %s, out %s" % (
+            tuple(q.shape), tuple(k_cache.shape), tuple(v_cache.shape), tuple(out.shape)))
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens do not have num_seqs rows")
+    return S, Hq, Hkv, D, BS, block_tables.shape[1], NB
+
+
+def paged_gqa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                     partition_size: int = 0, stream=None) -> None:
+    """Decode attention into ``out`` (asynchronous on ``stream``)."""
+    lib = load_library()
+    S, Hq, Hkv, D, BS, MB, NB = _sizes(out, q, k_cache, v_cache, block_tables, seq_lens)
+    st = lib.paged_gqa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv, D,
+                              BS, int(partition_size), MB, NB, _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def paged_gqa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                        partition_size: int = 0, workspace=None, page_trace=None,
+                        stream=None) -> None:
+    """As ``paged_gqa_decode`` with caller scratch (a uint8 CUDA tensor of at
+    least ``pgd_plan(...)[1]`` bytes, or None when that is 0) and an optional
+    int32 page trace [num_seqs, num_kv_heads, max_blocks_per_seq]."""
+    lib = load_library()
+    S, Hq, Hkv, D, BS, MB, NB = _sizes(out, q, k_cache, v_cache, block_tables, seq_lens)
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if page_trace is not None:
+        _check(page_trace, "page_trace", torch.int32, 3)
+        if tuple(page_trace.shape) != (S, Hkv, MB):
+            raise ValueError(f"page_trace must be [{S}, {Hkv}, {MB}]")
+    st = lib.paged_gqa_decode_ex(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv,
+                                 D, BS, int(partition_size), MB, NB, _ptr(workspace), ws_bytes,
+                                 _ptr(page_trace), _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def pgd_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, partition_size,
+             max_blocks_per_seq):
+    """(partition size used, scratch bytes needed) on the current device."""
+    lib = load_library()
+    p = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    _raise(lib.pgd_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                        partition_size, max_blocks_per_seq, ctypes.byref(p), ctypes.byref(b)))
+    return p.value, b.value
+
+
+def pgd_last_partition_size() -> int:
+    return int(load_library().pgd_last_partition_size())
+
+
+def pgd_last_error() -> str:
+    m = load_library().pgd_last_error()
+    return m.decode() if m else ""
+
+
+def pgd_check_device_error(stream=None) -> int:
+    """Waits for ``stream``; returns and clears the device error bits."""
+    lib = load_library()
+    bits = ctypes.c_uint(0)
+    dev = torch.cuda.current_device()
+    st = lib.pgd_check_device_error(_stream_handle(stream, dev), ctypes.byref(bits))
+    if st not in (0, 5):
+        _raise(st)
+    return bits.value
+
+
+def pgd_set_timing_events(before=None, after=None) -> None:
+    """Record ``before``/``after`` (torch.cuda.Event, enable_timing=True)
+    around the partition kernel of every later call on this thread; None
+    turns it off.  Events never recorded are first recorded once on the
+    current stream so that they exist."""
+    lib = load_library()
+    for ev in (before, after):
+        if ev is not None and not ev.cuda_event:
+            ev.record()
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
+    _raise(lib.pgd_set_timing_events(b, a))
+
+
+def pgd_device_info(head_dim: int, block_size: int):
+    """(number of SMs, resident partition-kernel CTAs per SM)."""
+    lib = load_library()
+    n = ctypes.c_int(0)
+    c = ctypes.c_int(0)
+    _raise(lib.pgd_device_info(head_dim, block_size, ctypes.byref(n), ctypes.byref(c)))
+    return n.value, c.value
+
+
+def pgd_version() -> int:
+    return int(load_library().pgd_version())

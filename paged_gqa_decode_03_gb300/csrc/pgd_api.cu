@@ -1,0 +1,441 @@
+// C ABI of the paged GQA decode library (declared in include/pgd.h):
+// argument validation, the partition scheduler, TMA descriptor encoding,
+// scratch management and the kernel launches.  Nothing here runs any part
+// of the attention arithmetic on the host.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pgd.h"
+#include "pgd_internal.h"
+
+namespace pgd {
+namespace {
+
+thread_local std::string t_last_error;
+thread_local int t_last_partition = 0;
+thread_local cudaEvent_t t_ev_before = nullptr;
+thread_local cudaEvent_t t_ev_after = nullptr;
+
+pgd_status fail(pgd_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+pgd_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(PGD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ per-device state
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    int num_sms = 0;
+    int ctas[2][3] = {};            // [D == 256][block size 8/16/32]
+    unsigned *err_word = nullptr;   // address of g_device_error on this device
+    cudaMemPool_t pool = nullptr;   // stream-ordered scratch
+};
+
+DeviceState g_dev[kMaxDevices];
+
+__device__ unsigned g_device_error;
+
+int bs_index(int bs) { return bs == 8 ? 0 : bs == 16 ? 1 : 2; }
+
+cudaError_t init_device(int dev, DeviceState &st)
+{
+    cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    const int sizes[3] = {8, 16, 32};
+    for (int i = 0; i < 3; ++i) {
+        if ((e = occupancy_d128(sizes[i], &st.ctas[0][i])) != cudaSuccess)
+            return e;
+        if ((e = occupancy_d256(sizes[i], &st.ctas[1][i])) != cudaSuccess)
+            return e;
+    }
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error)) !=
+        cudaSuccess)
+        return e;
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if ((e = cudaMemPoolCreate(&st.pool, &props)) != cudaSuccess)
+        return e;
+    uint64_t keep = ~0ull;  // keep freed scratch in the pool between calls
+    return cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+}
+
+pgd_status device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PGD_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    DeviceState &st = g_dev[dev];
+    std::call_once(st.once, [&] { st.init_error = init_device(dev, st); });
+    if (st.init_error != cudaSuccess)
+        return cuda_fail(st.init_error, "device set-up");
+    *out = &st;
+    return PGD_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+pgd_status encode_fn(EncodeTiledFn *fn)
+{
+    static std::once_flag once;
+    static EncodeTiledFn f = nullptr;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                               cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    if (!f)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                    cudaGetErrorString(err));
+    *fn = f;
+    return PGD_OK;
+}
+
+// One cache array [NB][Hkv][BS][D] viewed as a 2-D tensor of NB*Hkv*BS rows
+// of D halves; a copy box is `box_rows` rows by 64 halves (128 bytes, the
+// swizzle span), so a page's K or V rows arrive as D/64 swizzled slabs.
+pgd_status encode_cache_map(CUtensorMap *map, const void *base, long long rows, int D,
+                            int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PGD_OK;
+}
+
+// ------------------------------------------------------------------ validation & plan
+struct Plan {
+    int P;             // partition size
+    int NPmax;         // partitions of the longest possible sequence
+    size_t ws_bytes;   // scratch bytes (0 when NPmax == 1)
+    size_t off_l, off_o;
+    int grid;          // partition-kernel CTAs
+    int reduce_blocks;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+pgd_status check_sizes(int S, int Hq, int Hkv, int D, int BS, int P, int MB)
+{
+    if (S < 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_seqs %d < 0", S);
+    if (Hq <= 0 || Hkv <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "head counts must be positive (%d, %d)", Hq, Hkv);
+    if (Hq % Hkv != 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", Hq,
+                    Hkv);
+    if (Hq / Hkv > kMaxGroup)
+        return fail(PGD_ERR_UNSUPPORTED, "GQA group of %d query heads exceeds %d", Hq / Hkv,
+                    kMaxGroup);
+    if (D != 128 && D != 256)
+        return fail(PGD_ERR_UNSUPPORTED, "head_dim %d not in {128, 256}", D);
+    if (BS != 8 && BS != 16 && BS != 32)
+        return fail(PGD_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", BS);
+    if (P != 0 && P != kPartitionSmall && P != kPartitionLarge)
+        return fail(PGD_ERR_INVALID_ARG, "partition_size %d not in {0, 256, 512}", P);
+    if (MB <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", MB);
+    if ((long long)MB * BS > (1ll << 30))
+        return fail(PGD_ERR_UNSUPPORTED, "length bound %lld above 2^30", (long long)MB * BS);
+    return PGD_OK;
+}
+
+// Partition scheduler (the pages' "Dispatch layer": try 512 first, then
+// 256, counting only full partitions, against a work budget scaled by the
+// GPU's core count).  Here the budget is four units per resident CTA of the
+// persistent kernel, and full partitions are counted at the length bound
+// MB*BS because the lengths themselves stay on the device.
+int choose_partition(int S, int Hkv, int maxlen, int num_sms, int ctas_per_sm)
+{
+    const long long target = 4ll * num_sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    const long long full512 = (long long)S * Hkv * (maxlen / kPartitionLarge);
+    return full512 >= target ? kPartitionLarge : kPartitionSmall;
+}
+
+pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan *plan)
+{
+    pgd_status st = check_sizes(S, Hq, Hkv, D, BS, P, MB);
+    if (st)
+        return st;
+    DeviceState *ds;
+    if ((st = device_state(&ds)))
+        return st;
+    const int ctas = ds->ctas[D == 256][bs_index(BS)];
+    if (ctas < 1)
+        return fail(PGD_ERR_UNSUPPORTED, "partition kernel does not fit on an SM");
+    const int maxlen = MB * BS;
+    if (P == 0)
+        P = choose_partition(S, Hkv, maxlen, ds->num_sms, ctas);
+    plan->P = P;
+    plan->NPmax = (maxlen + P - 1) / P;
+    const size_t rows = (size_t)S * Hq * plan->NPmax;
+    if (plan->NPmax > 1) {
+        plan->off_l = align256(rows * 4);
+        plan->off_o = plan->off_l + align256(rows * 4);
+        plan->ws_bytes = plan->off_o + align256(rows * D * 4);
+    } else {
+        plan->off_l = plan->off_o = 0;
+        plan->ws_bytes = 0;
+    }
+    if (plan->ws_bytes > kMaxWorkspaceBytes)
+        return fail(PGD_ERR_WORKSPACE,
+                    "partials need %zu bytes, above the %zu-byte cap (lower the length bound "
+                    "or the batch)",
+                    plan->ws_bytes, kMaxWorkspaceBytes);
+    const long long units = (long long)S * Hkv * plan->NPmax;
+    const long long slots = (long long)ds->num_sms * ctas;
+    plan->grid = (int)(units < slots ? (units > 0 ? units : 1) : slots);
+    plan->reduce_blocks =
+        (int)(((long long)S * Hq + kReduceWarpsPerBlock - 1) / kReduceWarpsPerBlock);
+    if (plan->reduce_blocks < 1)
+        plan->reduce_blocks = 1;
+    return PGD_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
+               int Hkv, int D, int BS, int P, int MB, int NB, void *workspace, size_t ws_bytes,
+               bool own_workspace, int32_t *page_trace, void *stream_v)
+{
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return fail(PGD_ERR_INVALID_ARG, "null array argument");
+    if (!std::isfinite(scale))
+        return fail(PGD_ERR_INVALID_ARG, "scale is not finite");
+    if (NB <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_blocks %d <= 0", NB);
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return fail(PGD_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+        (page_trace && !aligned(page_trace, 4)))
+        return fail(PGD_ERR_INVALID_ARG, "int32 arrays must be 4-byte aligned");
+    pgd_status st = check_sizes(S, Hq, Hkv, D, BS, P, MB);
+    if (st)
+        return st;
+    const long long rows = (long long)NB * Hkv * BS;
+    if (rows >= (1ll << 31))
+        return fail(PGD_ERR_UNSUPPORTED, "num_blocks*num_kv_heads*block_size = %lld >= 2^31",
+                    rows);
+    if (!own_workspace && workspace && !aligned(workspace, 256))
+        return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    Plan plan;
+    if ((st = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan)))
+        return st;
+    DeviceState *ds;
+    if ((st = device_state(&ds)))
+        return st;
+    t_last_partition = plan.P;
+    if (S == 0)
+        return PGD_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaError_t e;
+
+    char *ws = static_cast<char *>(workspace);
+    if (plan.ws_bytes) {
+        if (own_workspace) {
+            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), plan.ws_bytes,
+                                             ds->pool, stream)) != cudaSuccess)
+                return cuda_fail(e, "scratch allocation");
+        } else {
+            if (!ws || ws_bytes < plan.ws_bytes)
+                return fail(PGD_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed",
+                            ws ? ws_bytes : (size_t)0, plan.ws_bytes);
+        }
+    }
+
+    const int box = BS < (D == 128 ? Shape<128>::T : Shape<256>::T)
+                        ? BS
+                        : (D == 128 ? Shape<128>::T : Shape<256>::T);
+    alignas(64) CUtensorMap tk, tv;
+    if ((st = encode_cache_map(&tk, k_cache, rows, D, box)) ||
+        (st = encode_cache_map(&tv, v_cache, rows, D, box))) {
+        if (own_workspace && ws)
+            cudaFreeAsync(ws, stream);
+        return st;
+    }
+
+    DecodeParams p = {};
+    p.out = out;
+    p.q = reinterpret_cast<const __half *>(q);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.ws_m = plan.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr;
+    p.ws_l = plan.ws_bytes ? reinterpret_cast<float *>(ws + plan.off_l) : nullptr;
+    p.ws_o = plan.ws_bytes ? reinterpret_cast<float *>(ws + plan.off_o) : nullptr;
+    p.page_trace = page_trace;
+    p.err = ds->err_word;
+    p.scale_log2 = scale * 1.4426950408889634f;  // log2(e) folded into the scale
+    p.S = S;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.P = plan.P;
+    p.MB = MB;
+    p.NB = NB;
+    p.NPmax = plan.NPmax;
+    p.wait_budget_ns = kWaitBudgetNs;
+
+    LaunchConfig lc;
+    lc.grid = plan.grid;
+    lc.reduce_blocks = plan.reduce_blocks;
+    lc.stream = stream;
+    lc.ev_before = t_ev_before;
+    lc.ev_after = t_ev_after;
+    e = D == 128 ? launch_decode_d128(BS, page_trace != nullptr, tk, tv, p, lc)
+                 : launch_decode_d256(BS, page_trace != nullptr, tk, tv, p, lc);
+    if (own_workspace && ws) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess)
+            e = e2;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kernel launch");
+    t_last_error.clear();
+    return PGD_OK;
+}
+
+}  // namespace
+}  // namespace pgd
+
+using namespace pgd;
+
+extern "C" {
+
+pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables,
+                            const int32_t *seq_lens, float scale, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int partition_size,
+                            int max_blocks_per_seq, int num_blocks, void *stream)
+{
+    return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, nullptr, 0, true, nullptr, stream);
+}
+
+pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_cache,
+                               const uint16_t *v_cache, const int32_t *block_tables,
+                               const int32_t *seq_lens, float scale, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int partition_size, int max_blocks_per_seq, int num_blocks,
+                               void *workspace, size_t workspace_bytes, int32_t *page_trace,
+                               void *stream)
+{
+    return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, workspace, workspace_bytes, false, page_trace, stream);
+}
+
+pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, int partition_size, int max_blocks_per_seq,
+                    int *chosen_partition_size, size_t *workspace_bytes)
+{
+    Plan plan;
+    pgd_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              partition_size, max_blocks_per_seq, &plan);
+    if (st)
+        return st;
+    if (chosen_partition_size)
+        *chosen_partition_size = plan.P;
+    if (workspace_bytes)
+        *workspace_bytes = plan.ws_bytes;
+    return PGD_OK;
+}
+
+int pgd_last_partition_size(void) { return t_last_partition; }
+
+const char *pgd_last_error(void) { return t_last_error.c_str(); }
+
+pgd_status pgd_check_device_error(void *stream, unsigned *bits)
+{
+    DeviceState *ds;
+    pgd_status st = device_state(&ds);
+    if (st)
+        return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "stream synchronize");
+    unsigned v = 0, zero = 0;
+    if ((e = cudaMemcpy(&v, ds->err_word, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(ds->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+        return cuda_fail(e, "device error word");
+    if (bits)
+        *bits = v;
+    if (v)
+        return fail(PGD_ERR_DEVICE, "device-side checks flagged 0x%x", v);
+    return PGD_OK;
+}
+
+pgd_status pgd_set_timing_events(void *before, void *after)
+{
+    if ((before == nullptr) != (after == nullptr))
+        return fail(PGD_ERR_INVALID_ARG, "give both timing events or neither");
+    t_ev_before = static_cast<cudaEvent_t>(before);
+    t_ev_after = static_cast<cudaEvent_t>(after);
+    return PGD_OK;
+}
+
+pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas_per_sm)
+{
+    if ((head_dim != 128 && head_dim != 256) ||
+        (block_size != 8 && block_size != 16 && block_size != 32))
+        return fail(PGD_ERR_UNSUPPORTED, "no kernel for head_dim %d, block_size %d", head_dim,
+                    block_size);
+    DeviceState *ds;
+    pgd_status st = device_state(&ds);
+    if (st)
+        return st;
+    if (num_sms)
+        *num_sms = ds->num_sms;
+    if (ctas_per_sm)
+        *ctas_per_sm = ds->ctas[head_dim == 256][bs_index(block_size)];
+    return PGD_OK;
+}
+
+int pgd_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Shared host/device definitions of the GPU path: one set of constants for
+// the launcher and the kernels so the two cannot drift (the pages' vllm-metal
+// keeps its partition and block sizes in one constants file shared with the
+// shaders, "Three Metal kernels" section).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace pgd {
+
+// Partition sizes of the split-KV scheme ("Four speed-up tricks", 4).
+constexpr int kPartitionLarge = 512;
+constexpr int kPartitionSmall = 256;
+// Most query heads per KV head one CTA handles (one n8 tensor-core tile).
+constexpr int kMaxGroup = 8;
+// Cap on the per-call scratch ("Dispatch layer": 512 MiB).
+constexpr size_t kMaxWorkspaceBytes = size_t(512) << 20;
+// Bound on every internal pipeline wait before it reports a timeout.
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+
+// Device error bits (mirror PGD_DEVERR_* of pgd.h).
+constexpr unsigned kErrPageRange = 1u;
+constexpr unsigned kErrSeqLen = 2u;
+constexpr unsigned kErrTimeout = 4u;
+
+// Kernel shape per head_dim: tokens per pipeline stage (T), consumer warps
+// (NC), stages in the shared-memory ring (NS).
+template <int D> struct Shape;
+template <> struct Shape<128> {
+    static constexpr int T = 64, NC = 4, NS = 3;
+};
+template <> struct Shape<256> {
+    static constexpr int T = 32, NC = 4, NS = 3;
+};
+
+template <int D> __host__ __device__ constexpr int stage_kv_bytes() { return Shape<D>::T * D * 2; }  // K or V
+template <int D> __host__ __device__ constexpr int stage_q_bytes() { return kMaxGroup * D * 2; }
+template <int D> __host__ __device__ constexpr int stage_bytes() { return 2 * stage_kv_bytes<D>() + stage_q_bytes<D>(); }
+// Dynamic shared memory: the ring plus slack to align it to 1024 bytes
+// (required by the 128-byte swizzle of the tensor copies).
+template <int D> __host__ __device__ constexpr size_t dyn_smem_bytes()
+{
+    return size_t(Shape<D>::NS) * stage_bytes<D>() + 1024;
+}
+
+struct DecodeParams {
+    float *out;                   // [S][Hq][D]
+    const __half *q;              // [S][Hq][D]
+    const int32_t *block_tables;  // [S][MB]
+    const int32_t *seq_lens;      // [S]
+    float *ws_m;                  // [S][Hq][NPmax] log2-space partition max
+    float *ws_l;                  // [S][Hq][NPmax] partition exp2-sum
+    float *ws_o;                  // [S][Hq][NPmax][D] normalised partition output
+    int32_t *page_trace;          // [S][Hkv][MB] or null
+    unsigned *err;                // device error word
+    float scale_log2;             // scale * log2(e)
+    int S, Hq, Hkv, G, P, MB, NB, NPmax;
+    uint64_t wait_budget_ns;
+};
+
+struct LaunchConfig {
+    int grid;            // partition-kernel CTAs (persistent)
+    int reduce_blocks;   // reduce-kernel CTAs
+    cudaStream_t stream;
+    cudaEvent_t ev_before, ev_after;  // optional timing hook (both or neither)
+};
+
+// Per-head_dim entry points (pgd_kernels_d128.cu / pgd_kernels_d256.cu).
+cudaError_t launch_decode_d128(int block_size, bool trace, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const DecodeParams &p,
+                               const LaunchConfig &lc);
+cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const DecodeParams &p,
+                               const LaunchConfig &lc);
+// Resident partition-kernel CTAs per SM for (head_dim, block_size).
+cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
+cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
+
+constexpr int kReduceWarpsPerBlock = 4;
+
+}  // namespace pgd

@@ -1,0 +1,19 @@
+// Instantiations of the decode kernels for head_dim 128 (block sizes 8/16/32,
+// with and without the page trace).
+#include "pgd_kernels.cuh"
+
+namespace pgd {
+
+cudaError_t launch_decode_d128(int block_size, bool trace, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const DecodeParams &p,
+                               const LaunchConfig &lc)
+{
+    return launch_decode_dispatch<128>(block_size, trace, tk, tv, p, lc);
+}
+
+cudaError_t occupancy_d128(int block_size, int *ctas_per_sm)
+{
+    return occupancy_dispatch<128>(block_size, ctas_per_sm);
+}
+
+}  // namespace pgd

@@ -1,0 +1,126 @@
+"""Host-side tests of the C ABI: the library loads, exports every function
+include/pgd.h declares, and rejects bad arguments with the documented status
+before touching the GPU (these run without one)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import paged_gqa_decode_03_gb300 as pgd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pgd.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return pgd.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "paged_gqa_decode" in names and len(names) >= 9, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pgd.h but not exported"
+        assert n in pgd.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_version(lib):
+    assert lib.pgd_version() >= 100
+
+
+# Fake, aligned, non-null device addresses: validation must reject the call
+# before any of them is used.
+A = ctypes.c_void_p(1 << 20)
+
+
+def call(lib, S=4, Hq=32, Hkv=8, D=128, BS=16, P=512, MB=64, NB=1024, scale=0.088,
+         ptrs=None):
+    p = ptrs or [A] * 6
+    return lib.paged_gqa_decode(*p, ctypes.c_float(scale), S, Hq, Hkv, D, BS, P, MB, NB,
+                                ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_null_arrays_rejected(lib, i):
+    ptrs = [A] * 6
+    ptrs[i] = ctypes.c_void_p(0)
+    assert call(lib, ptrs=ptrs) == INVALID
+    assert "null" in lib.pgd_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), UNSUPPORTED), (dict(D=192), UNSUPPORTED),
+    (dict(BS=4), UNSUPPORTED), (dict(BS=64), UNSUPPORTED),
+    (dict(P=128), INVALID), (dict(P=1024), INVALID), (dict(P=-1), INVALID),
+    (dict(Hq=30, Hkv=8), INVALID), (dict(Hq=0), INVALID), (dict(Hkv=0), INVALID),
+    (dict(Hq=32, Hkv=2), UNSUPPORTED),      # 16 query heads per KV head > 8
+    (dict(MB=0), INVALID), (dict(S=-1), INVALID), (dict(NB=0), INVALID),
+    (dict(NB=1 << 27, Hkv=8, BS=16), UNSUPPORTED),   # rows >= 2^31
+    (dict(scale=math.inf), INVALID), (dict(scale=math.nan), INVALID),
+])
+def test_bad_sizes_rejected(lib, kw, status):
+    assert call(lib, **kw) == status
+    assert lib.pgd_last_error().decode() != ""
+
+
+def test_misaligned_rejected(lib):
+    ptrs = [A] * 6
+    ptrs[1] = ctypes.c_void_p((1 << 20) + 8)     # q not 16-byte aligned
+    assert call(lib, ptrs=ptrs) == INVALID
+    ptrs = [A] * 6
+    ptrs[4] = ctypes.c_void_p((1 << 20) + 2)     # block_tables not 4-byte aligned
+    assert call(lib, ptrs=ptrs) == INVALID
+
+
+def test_ex_workspace_alignment_rejected(lib):
+    r = lib.paged_gqa_decode_ex(*([A] * 6), ctypes.c_float(0.1), 4, 32, 8, 128, 16, 512, 64,
+                                1024, ctypes.c_void_p((1 << 20) + 16), 1 << 20,
+                                ctypes.c_void_p(0), ctypes.c_void_p(0))
+    assert r == INVALID
+
+
+@pytest.mark.parametrize("args,status", [
+    ((4, 32, 8, 100, 16, 512, 64), UNSUPPORTED),
+    ((4, 32, 8, 128, 12, 512, 64), UNSUPPORTED),
+    ((4, 32, 8, 128, 16, 300, 64), INVALID),
+    ((4, 32, 7, 128, 16, 512, 64), INVALID),
+])
+def test_plan_validation(lib, args, status):
+    p = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    assert lib.pgd_plan(*args, ctypes.byref(p), ctypes.byref(b)) == status
+
+
+def test_timing_events_need_both(lib):
+    assert lib.pgd_set_timing_events(ctypes.c_void_p(8), ctypes.c_void_p(0)) == INVALID
+    assert lib.pgd_set_timing_events(ctypes.c_void_p(0), ctypes.c_void_p(0)) == OK
+
+
+def test_device_info_rejects_unbuilt_shapes(lib):
+    n, c = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.pgd_device_info(64, 16, ctypes.byref(n), ctypes.byref(c)) == UNSUPPORTED
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros((1, 4, 128), dtype=torch.float16)
+    k = torch.zeros((2, 1, 16, 128), dtype=torch.float16)
+    bt = torch.zeros((1, 2), dtype=torch.int32)
+    sl = torch.ones((1,), dtype=torch.int32)
+    out = torch.zeros((1, 4, 128), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        pgd.paged_gqa_decode(out, q, k, k, bt, sl, 0.1)
+    with pytest.raises(TypeError):
+        pgd.paged_gqa_decode(out, q.float(), k, k, bt, sl, 0.1)
