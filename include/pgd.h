@@ -52,6 +52,9 @@
  * v_cache must be 16-byte aligned; the int32 arrays and out 4-byte aligned.
  * num_blocks * num_kv_heads * block_size must be below 2^31.
  *
+ * A call with num_seqs == 0 checks the sizes, does nothing else and may pass
+ * null array pointers.
+ *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and never synchronises the host.  The call
  * validates all host-side arguments before launching anything; on any error

@@ -48,6 +48,8 @@ struct DeviceState {
     int num_sms = 0;
     int ctas[2][3] = {};            // [D == 256][block size 8/16/32]
     unsigned *err_word = nullptr;   // address of g_device_error on this device
+    std::once_flag pool_once;       // the pool is made on first library-owned scratch
+    cudaError_t pool_error = cudaSuccess;
     cudaMemPool_t pool = nullptr;   // stream-ordered scratch
 };
 
@@ -69,14 +71,17 @@ cudaError_t init_device(int dev, DeviceState &st)
         if ((e = occupancy_d256(sizes[i], &st.ctas[1][i])) != cudaSuccess)
             return e;
     }
-    if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error)) !=
-        cudaSuccess)
-        return e;
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error);
+}
+
+cudaError_t init_pool(int dev, DeviceState &st)
+{
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
     props.location.id = dev;
-    if ((e = cudaMemPoolCreate(&st.pool, &props)) != cudaSuccess)
+    cudaError_t e = cudaMemPoolCreate(&st.pool, &props);
+    if (e != cudaSuccess)
         return e;
     uint64_t keep = ~0ull;  // keep freed scratch in the pool between calls
     return cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
@@ -95,6 +100,20 @@ pgd_status device_state(DeviceState **out)
     if (st.init_error != cudaSuccess)
         return cuda_fail(st.init_error, "device set-up");
     *out = &st;
+    return PGD_OK;
+}
+
+// The library's scratch pool on the current device (created on first use).
+pgd_status device_pool(DeviceState &st, cudaMemPool_t *pool)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    std::call_once(st.pool_once, [&] { st.pool_error = init_pool(dev, st); });
+    if (st.pool_error != cudaSuccess)
+        return cuda_fail(st.pool_error, "scratch pool set-up");
+    *pool = st.pool;
     return PGD_OK;
 }
 
@@ -242,6 +261,15 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
                int Hkv, int D, int BS, int P, int MB, int NB, void *workspace, size_t ws_bytes,
                bool own_workspace, int32_t *page_trace, void *stream_v)
 {
+    if (S == 0) {  // nothing to read or write: only the sizes are checked
+        Plan plan;
+        pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan);
+        if (st0)
+            return st0;
+        t_last_partition = plan.P;
+        t_last_error.clear();
+        return PGD_OK;
+    }
     if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
         return fail(PGD_ERR_INVALID_ARG, "null array argument");
     if (!std::isfinite(scale))
@@ -269,16 +297,17 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     if ((st = device_state(&ds)))
         return st;
     t_last_partition = plan.P;
-    if (S == 0)
-        return PGD_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     cudaError_t e;
 
     char *ws = static_cast<char *>(workspace);
     if (plan.ws_bytes) {
         if (own_workspace) {
-            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), plan.ws_bytes,
-                                             ds->pool, stream)) != cudaSuccess)
+            cudaMemPool_t pool;
+            if ((st = device_pool(*ds, &pool)))
+                return st;
+            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), plan.ws_bytes, pool,
+                                             stream)) != cudaSuccess)
                 return cuda_fail(e, "scratch allocation");
         } else {
             if (!ws || ws_bytes < plan.ws_bytes)

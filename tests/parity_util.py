@@ -45,10 +45,8 @@ def run(w, P=None, trace=False, workspace=False, stream=None):
         pt = None
         if trace:
             pt = torch.full((w.S, w.Hkv, w.MB), -1, dtype=torch.int32, device=w.q.device)
-        ws = None
-        if workspace:
-            _, nbytes = pgd.pgd_plan(w.S, w.Hq, w.Hkv, w.D, w.BS, P, w.MB)
-            ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=w.q.device)
+        _, nbytes = pgd.pgd_plan(w.S, w.Hq, w.Hkv, w.D, w.BS, P, w.MB)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=w.q.device) if nbytes else None
         pgd.paged_gqa_decode_ex(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
                                 w.scale, P, workspace=ws, page_trace=pt, stream=stream)
         torch.cuda.synchronize()
