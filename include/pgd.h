@@ -148,6 +148,40 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
                                int num_blocks, void *workspace, size_t workspace_bytes,
                                int32_t *page_trace, void *stream);
 
+/*
+ * paged_gqa_decode_noalloc — paged_gqa_decode that allocates nothing.
+ * (No counterpart on the pages: this entry point exists for callers, not
+ * for the method.)
+ *
+ * For callers that must not allocate device memory while they run: a
+ * serving loop whose memory is all reserved up front by its own allocator
+ * (a late cudaMalloc could fail or fragment it), code that may not block on
+ * an allocation (cudaMalloc and cudaFree can synchronise the device), or
+ * code that forbids dynamic allocation after start-up.  The caller still
+ * passes every input and the output, exactly as for paged_gqa_decode.
+ *
+ * The partition partials go to a fixed array of PGD_NOALLOC_SCRATCH_BYTES
+ * compiled into the library (every GPU on which the library is used holds
+ * it until the process exits).  The call never calls cudaMalloc, cudaFree or
+ * any other allocating routine.  Sizes whose partials need more than that
+ * (see pgd_plan) are rejected with PGD_ERR_WORKSPACE before any launch.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.
+ * Every call shares the one array: calls whose work overlaps on the GPU
+ * (other streams, other threads) race on it, so serialise them.  The array
+ * keeps the last call's contents; nothing in it needs to start at zero
+ * (every partial is written before it is read within a call).
+ */
+#define PGD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_t *k_cache,
+                                    const uint16_t *v_cache, const int32_t *block_tables,
+                                    const int32_t *seq_lens, float scale, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int partition_size, int max_blocks_per_seq,
+                                    int num_blocks, void *stream);
+
 /* Partition size used by this thread's last successful call (0 if none);
  * the diagnostic of the pages' "Hands-on" section. */
 int pgd_last_partition_size(void);

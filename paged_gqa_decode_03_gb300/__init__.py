@@ -26,7 +26,7 @@ import threading
 
 import torch
 
-__all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "pgd_plan", "pgd_last_partition_size",
+__all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -44,6 +44,7 @@ _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "paged_gqa_decode": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_ex": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
+    "paged_gqa_decode_noalloc": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -161,6 +162,28 @@ def paged_gqa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
                                  _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv,
                                  D, BS, int(partition_size), MB, NB, _ptr(workspace), ws_bytes,
                                  _ptr(page_trace), _stream_handle(stream, q.device))
+    _raise(st)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20  # PGD_NOALLOC_SCRATCH_BYTES of include/pgd.h
+
+
+def paged_gqa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                             partition_size: int = 0, stream=None) -> None:
+    """``paged_gqa_decode`` for callers that must not allocate device memory
+    while they run (a memory budget reserved up front by their own
+    allocator, no blocking on cudaMalloc/cudaFree, no allocation after
+    start-up).  Partials go to a fixed 64 MiB array inside the library;
+    larger requests raise PGDError (PGD_ERR_WORKSPACE).  The first call on a
+    device looks up that array's address, so make it before any stream
+    capture.  All calls share the array: serialise calls that would overlap
+    on the GPU."""
+    lib = load_library()
+    S, Hq, Hkv, D, BS, MB, NB = _sizes(out, q, k_cache, v_cache, block_tables, seq_lens)
+    st = lib.paged_gqa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq,
+                                      Hkv, D, BS, int(partition_size), MB, NB,
+                                      _stream_handle(stream, q.device))
     _raise(st)
 
 

@@ -15,6 +15,12 @@
 #include "../../include/pgd.h"
 #include "pgd_internal.h"
 
+// Scratch of paged_gqa_decode_noalloc: a fixed array in this library's
+// device image, so that entry point never allocates.  Every GPU on which the
+// library is used holds these PGD_NOALLOC_SCRATCH_BYTES until the process
+// exits.  All calls of paged_gqa_decode_noalloc on a device share it.
+static __device__ __align__(256) unsigned char pgd_noalloc_scratch[PGD_NOALLOC_SCRATCH_BYTES];
+
 namespace pgd {
 namespace {
 
@@ -367,6 +373,33 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     return PGD_OK;
 }
 
+// Device address of pgd_noalloc_scratch, looked up once per device (with
+// that device current) on the first paged_gqa_decode_noalloc call there.
+struct NoAllocScratch {
+    std::once_flag once;
+    cudaError_t error = cudaSuccess;
+    void *ptr = nullptr;
+};
+
+NoAllocScratch g_noalloc[kMaxDevices];
+
+pgd_status noalloc_scratch(void **ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PGD_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    NoAllocScratch &st = g_noalloc[dev];
+    std::call_once(st.once,
+                   [&] { st.error = cudaGetSymbolAddress(&st.ptr, pgd_noalloc_scratch); });
+    if (st.error != cudaSuccess)
+        return cuda_fail(st.error, "address of the static scratch");
+    *ptr = st.ptr;
+    return PGD_OK;
+}
+
 }  // namespace
 }  // namespace pgd
 
@@ -396,6 +429,32 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
                num_blocks, workspace, workspace_bytes, false, page_trace, stream);
+}
+
+pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_t *k_cache,
+                                    const uint16_t *v_cache, const int32_t *block_tables,
+                                    const int32_t *seq_lens, float scale, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int partition_size, int max_blocks_per_seq,
+                                    int num_blocks, void *stream)
+{
+    Plan plan;
+    pgd_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              partition_size, max_blocks_per_seq, &plan);
+    if (st)
+        return st;
+    if (plan.ws_bytes > PGD_NOALLOC_SCRATCH_BYTES)
+        return fail(PGD_ERR_WORKSPACE,
+                    "these sizes need %zu bytes of scratch, more than the %zu bytes of static "
+                    "scratch of paged_gqa_decode_noalloc; use paged_gqa_decode or "
+                    "paged_gqa_decode_ex",
+                    plan.ws_bytes, (size_t)PGD_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)))
+        return st;
+    return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, scratch, PGD_NOALLOC_SCRATCH_BYTES, false, nullptr, stream);
 }
 
 pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
