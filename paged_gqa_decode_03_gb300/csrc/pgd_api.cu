@@ -149,9 +149,13 @@ pgd_status encode_fn(EncodeTiledFn *fn)
     return PGD_OK;
 }
 
-// One cache array [NB][Hkv][BS][D] viewed as a 2-D tensor of NB*Hkv*BS rows
-// of D halves; a copy box is `box_rows` rows by 64 halves (128 bytes, the
-// swizzle span), so a page's K or V rows arrive as D/64 swizzled slabs.
+// One cache array [NB][Hkv][BS][D] viewed as a 3-D tensor
+//   (64 halves within a 128-byte slab) x (NB*Hkv*BS rows, stride D*2 bytes)
+//   x (D/64 slabs, stride 128 bytes),
+// so one copy box of 64 x box_rows x D/64 brings box_rows whole rows of a
+// page and lands in shared memory as [slab][row][128 B], each slab 128-byte
+// swizzled (the span the tensor-core operand loads read without bank
+// conflicts).
 pgd_status encode_cache_map(CUtensorMap *map, const void *base, long long rows, int D,
                             int box_rows)
 {
@@ -159,11 +163,11 @@ pgd_status encode_cache_map(CUtensorMap *map, const void *base, long long rows, 
     pgd_status st = encode_fn(&fn);
     if (st)
         return st;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -253,8 +257,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     const long long units = (long long)S * Hkv * plan->NPmax;
     const long long slots = (long long)ds->num_sms * ctas;
     plan->grid = (int)(units < slots ? (units > 0 ? units : 1) : slots);
-    plan->reduce_blocks =
-        (int)(((long long)S * Hq + kReduceWarpsPerBlock - 1) / kReduceWarpsPerBlock);
+    plan->reduce_blocks = (int)((long long)S * Hq);
     if (plan->reduce_blocks < 1)
         plan->reduce_blocks = 1;
     return PGD_OK;

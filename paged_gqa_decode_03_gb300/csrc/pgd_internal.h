@@ -80,6 +80,6 @@ cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk
 cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
 cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
 
-constexpr int kReduceWarpsPerBlock = 4;
+constexpr int kReduceThreads = 256;  // reduce kernel: one CTA per (sequence, query head)
 
 }  // namespace pgd

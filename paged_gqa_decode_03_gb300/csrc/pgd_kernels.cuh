@@ -9,9 +9,11 @@
 //    partial last partitions, and dealt round-robin to the CTAs.
 //      * producer warp: loads the unit's page-table entries with one
 //        coalesced warp load, broadcasts each physical page id with a warp
-//        shuffle, and issues TMA tensor copies of the page's K and V rows
-//        (128-byte swizzled, evict-first) plus one bulk copy of the group's
-//        queries into a ring of shared-memory stages guarded by mbarriers.
+//        shuffle, and issues one TMA tensor copy of the page's K rows and one
+//        of its V rows (3-D box: 64 halves x rows x 128-byte slabs, so each
+//        slab lands 128-byte swizzled; evict-first) plus one bulk copy of the
+//        group's queries, into a ring of shared-memory stages guarded by
+//        mbarriers.  Stage layout: [page][slab][row][128 B].
 //      * consumer warps: per stage of T tokens, S^T = K Q^T on tensor cores
 //        (mma.sync m16n8k16, fp16 in, fp32 accumulate), scores exchanged
 //        through shared memory, one log2-space online-softmax update with
@@ -44,6 +46,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     constexpr int T = Shape<D>::T, NC = Shape<D>::NC, NS = Shape<D>::NS;
     constexpr int SLABS = D / 64;          // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
+    constexpr int PAGE_BYTES = BOX * D * 2;  // one copy: BOX rows of one page, all slabs
     constexpr int KT = D / 16;             // k-steps of QK (over head_dim)
     constexpr int KS = T / 16;             // k-steps of PV (over tokens)
     constexpr int QKW = T / 16;            // consumer warps computing a QK tile
@@ -92,17 +95,14 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
         int k = 0;  // stages issued by this CTA
         bool ok = true;
 
-        // Issues every stage of unit (s, g, partition pi) of a sequence of length L.
-        auto produce = [&](int s, int g, int pi, int L) -> bool {
+        // Issues every stage of unit (s, g, partition pi) of a sequence of
+        // length L whose page ids (entries pg0 .. pg0+63 of its page-table
+        // row, two per lane) are already in id0 / id1.
+        auto produce = [&](int s, int g, int pi, int L, int id0, int id1) -> bool {
             const int tok0 = pi * P;
             const int n = min(P, L - tok0);
             const bool direct = L <= P;
             const int pg0 = tok0 / BS;
-            const int npages = (n + BS - 1) / BS;  // <= 64
-            // page-table walk: 32 entries per coalesced warp load
-            const int32_t *bt = p.block_tables + (size_t)s * MB + pg0;
-            const int id0 = lane < npages ? __ldg(bt + lane) : 0;
-            const int id1 = lane + 32 < npages ? __ldg(bt + 32 + lane) : 0;
             const int nst = (n + T - 1) / T;
             for (int st = 0; st < nst; ++st, ++k) {
                 const int slot = k % NS;
@@ -132,8 +132,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     hdr[slot].valid = valid;
                     hdr[slot].flags = (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
                                       (direct ? kDirect : 0);
-                    const uint32_t bytes =
-                        pc * SLABS * BOX * 128 * 2 + (st == 0 ? G * D * 2 : 0);
+                    const uint32_t bytes = pc * PAGE_BYTES * 2 + (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
                 for (int jj = 0; jj < pc; ++jj) {
@@ -149,12 +148,11 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         }
                         if (TRACE)
                             p.page_trace[((size_t)s * Hkv + g) * MB + pg0 + j] = id;
-                        const uint32_t dk = sb + jj * BOX * 128;
-#pragma unroll
-                        for (int c = 0; c < SLABS; ++c) {
-                            tma_load_2d(dk + c * T * 128, &tmap_k, c * 64, y, fb, pol);
-                            tma_load_2d(dk + KV_BYTES + c * T * 128, &tmap_v, c * 64, y, fb, pol);
-                        }
+                        // one copy per page for K and one for V: BOX rows x D
+                        // halves, landing as [slab][row][128 B] (swizzled)
+                        const uint32_t dk = sb + jj * PAGE_BYTES;
+                        tma_load_3d(dk, &tmap_k, 0, y, 0, fb, pol);
+                        tma_load_3d(dk + KV_BYTES, &tmap_v, 0, y, 0, fb, pol);
                     }
                 }
                 if (st == 0 && lane == 0)
@@ -164,52 +162,99 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             return true;
         };
 
-        // Static round-robin over the unit list: full partitions of every
-        // sequence (partition-major, KV head fastest), then the partial
-        // last partition of every sequence (one per KV head).
-        long long next_u = blockIdx.x;
+        // Page-table walk of one unit: its (<= 64) page ids, 32 per
+        // coalesced warp load.
+        auto load_ids = [&](int s, int pi, int L, int &id0, int &id1) {
+            const int tok0 = pi * P;
+            const int npages = (min(P, L - tok0) + BS - 1) / BS;
+            const int32_t *bt = p.block_tables + (size_t)s * MB + tok0 / BS;
+            id0 = lane < npages ? __ldg(bt + lane) : 0;
+            id1 = lane + 32 < npages ? __ldg(bt + 32 + lane) : 0;
+        };
+
+        // This CTA's units, in order: a static round-robin over the list
+        // "full partitions of every sequence (partition-major, KV head
+        // fastest), then the partial last partition of every sequence (one
+        // per KV head)".  Warp-uniform state; sequences are scanned 32 at a
+        // time.
+        int it_phase = 0, it_s0 = 0, it_L = 0, it_cnt = 0, it_incl = 0, it_total = 0;
+        bool it_loaded = false;
+        long long next_u = blockIdx.x, base = 0;
         const long long ustride = gridDim.x;
-        long long base = 0;
-        for (int phase = 0; phase < 2 && ok; ++phase) {
-            for (int s0 = 0; s0 < S && ok; s0 += 32) {
-                const int s = s0 + lane;
-                int L = 0;
-                if (s < S) {
-                    L = __ldg(p.seq_lens + s);
-                    if (L < 0 || L > maxlen) {
-                        if (phase == 0 && blockIdx.x == 0)
-                            atomicOr(p.err, kErrSeqLen);
-                        L = L < 0 ? 0 : maxlen;
+        auto advance = [&](int &us, int &ug, int &upi, int &uL) -> bool {
+            for (;;) {
+                if (!it_loaded) {
+                    if (it_phase == 2)
+                        return false;
+                    if (it_s0 >= S) {
+                        ++it_phase;
+                        it_s0 = 0;
+                        continue;
                     }
-                }
-                const int cnt = phase == 0 ? (L / P) * Hkv : ((L % P) ? Hkv : 0);
-                int incl = cnt;
+                    const int s = it_s0 + lane;
+                    int L = 0;
+                    if (s < S) {
+                        L = __ldg(p.seq_lens + s);
+                        if (L < 0 || L > maxlen) {
+                            if (it_phase == 0 && blockIdx.x == 0)
+                                atomicOr(p.err, kErrSeqLen);
+                            L = L < 0 ? 0 : maxlen;
+                        }
+                    }
+                    const int cnt = it_phase == 0 ? (L / P) * Hkv : ((L % P) ? Hkv : 0);
+                    int incl = cnt;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(~0u, incl, o);
-                    if (lane >= o)
-                        incl += v;
-                }
-                const int total = __shfl_sync(~0u, incl, 31);
-                while (ok && next_u < base + total) {
-                    const int r = (int)(next_u - base);
-                    const int j = __ffs(__ballot_sync(~0u, incl > r)) - 1;
-                    const int ex = __shfl_sync(~0u, incl - cnt, j);
-                    const int Lj = __shfl_sync(~0u, L, j);
-                    const int rr = r - ex;
-                    int g, pi;
-                    if (phase == 0) {
-                        pi = rr / Hkv;
-                        g = rr - pi * Hkv;
-                    } else {
-                        pi = Lj / P;
-                        g = rr;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_up_sync(~0u, incl, o);
+                        if (lane >= o)
+                            incl += v;
                     }
-                    ok = produce(s0 + j, g, pi, Lj);
-                    next_u += ustride;
+                    it_L = L;
+                    it_cnt = cnt;
+                    it_incl = incl;
+                    it_total = __shfl_sync(~0u, incl, 31);
+                    it_loaded = true;
                 }
-                base += total;
+                if (next_u < base + it_total) {
+                    const int r = (int)(next_u - base);
+                    const int j = __ffs(__ballot_sync(~0u, it_incl > r)) - 1;
+                    const int ex = __shfl_sync(~0u, it_incl - it_cnt, j);
+                    uL = __shfl_sync(~0u, it_L, j);
+                    us = it_s0 + j;
+                    const int rr = r - ex;
+                    if (it_phase == 0) {
+                        upi = rr / Hkv;
+                        ug = rr - upi * Hkv;
+                    } else {
+                        upi = uL / P;
+                        ug = rr;
+                    }
+                    next_u += ustride;
+                    return true;
+                }
+                base += it_total;
+                it_s0 += 32;
+                it_loaded = false;
             }
+        };
+
+        int cs = 0, cg = 0, cpi = 0, cL = 0, cid0 = 0, cid1 = 0;
+        bool has = advance(cs, cg, cpi, cL);
+        if (has)
+            load_ids(cs, cpi, cL, cid0, cid1);
+        while (has && ok) {
+            int ns_ = 0, ng = 0, npi = 0, nL = 0, nid0 = 0, nid1 = 0;
+            const bool has_next = advance(ns_, ng, npi, nL);
+            if (has_next)  // in flight while this unit's stages are issued
+                load_ids(ns_, npi, nL, nid0, nid1);
+            ok = produce(cs, cg, cpi, cL, cid0, cid1);
+            cs = ns_;
+            cg = ng;
+            cpi = npi;
+            cL = nL;
+            cid0 = nid0;
+            cid1 = nid1;
+            has = has_next;
         }
         if (ok) {  // end-of-work marker
             const int slot = k % NS;
@@ -291,7 +336,8 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 uint8_t *vs = ring_ptr + slot * STAGE + KV_BYTES;
                 for (int r = valid + w; r < T; r += NC)
                     if (lane < SLABS * 8)
-                        *reinterpret_cast<uint4 *>(vs + (lane >> 3) * T * 128 + r * 128 +
+                        *reinterpret_cast<uint4 *>(vs + (r / BOX) * PAGE_BYTES +
+                                                   (lane >> 3) * (BOX * 128) + (r % BOX) * 128 +
                                                    (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
             }
@@ -302,13 +348,14 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 if (t0 < valid) {
                     const int mi = lane >> 3, r = lane & 7;
                     const int tok = t0 + r + (mi & 1) * 8;
-                    const uint32_t rowaddr = sb + tok * 128;
+                    const uint32_t rowaddr =
+                        sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
                     const int sw = tok & 7;
 #pragma unroll
                     for (int kk = 0; kk < KT; ++kk) {
                         const int dim = kk * 16 + (mi >> 1) * 8;
                         const uint32_t addr =
-                            rowaddr + (dim >> 6) * (T * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
+                            rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(addr, a0, a1, a2, a3);
                         if (kk & 1)
@@ -372,12 +419,13 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             for (int ks = 0; ks < KS; ++ks) {
                 const int tok = ks * 16 + r + (mi >> 1) * 8;
                 const int sw = tok & 7;
-                const uint32_t rowaddr = sb + KV_BYTES + tok * 128;
+                const uint32_t rowaddr =
+                    sb + KV_BYTES + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
                     const int dim = (w * MT + i) * 16 + (mi & 1) * 8;
                     const uint32_t addr =
-                        rowaddr + (dim >> 6) * (T * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
+                        rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
                     uint32_t v0, v1, v2, v3;
                     ldsm_x4_t(addr, v0, v1, v2, v3);
                     mma_16816(o[i], v0, v1, v2, v3, pb[ks][0], pb[ks][1]);
@@ -425,65 +473,103 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     }
 }
 
-// One warp per (sequence, query head): out = sum_p w_p o_p / sum_p w_p with
-// w_p = l_p * exp2(m_p - max_p m_p); zeros for empty sequences.
+// One CTA per (sequence, query head): out = sum_p w_p o_p / sum_p w_p with
+// w_p = l_p * exp2(m_p - max_p m_p); zeros for empty sequences; nothing for
+// single-partition sequences (written by the partition kernel).  Thread t
+// owns float4 column t % (D/4) of the partitions p = t / (D/4) (mod groups),
+// with several partial rows in flight per thread.
 template <int D>
-__global__ void __launch_bounds__(kReduceWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kReduceThreads)
     paged_gqa_reduce_kernel(const DecodeParams p, int max_len)
 {
     griddep_wait();
-    constexpr int V4 = D / 128;  // float4 per lane
-    const int gw = blockIdx.x * kReduceWarpsPerBlock + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.S * p.Hq)
+    constexpr int V4 = D / 4;                     // float4 per row
+    constexpr int GROUPS = kReduceThreads / V4;   // partitions handled at once
+    constexpr int NW = kReduceThreads / 32;
+    __shared__ float red[NW];
+    __shared__ float4 acc_s[GROUPS][V4];
+    __shared__ float den_s[GROUPS];
+    const int sh = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (sh >= p.S * p.Hq)
         return;
-    const int s = gw / p.Hq;
+    const int s = sh / p.Hq;
     int L = __ldg(p.seq_lens + s);
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
-    float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)gw * D);
+    float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)sh * D);
     if (L == 0) {
-#pragma unroll
-        for (int v = 0; v < V4; ++v)
-            o4[lane + 32 * v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid < V4)
+            o4[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
     const int np = (L + p.P - 1) / p.P;
     if (np == 1)
         return;
-    const float *mp = p.ws_m + (size_t)gw * p.NPmax;
-    const float *lp = p.ws_l + (size_t)gw * p.NPmax;
+    const float *mp = p.ws_m + (size_t)sh * p.NPmax;
+    const float *lp = p.ws_l + (size_t)sh * p.NPmax;
+    // pass 1: M = max over non-empty partitions of m_p
     float M = -INFINITY;
-    for (int i = lane; i < np; i += 32)
+    for (int i = tid; i < np; i += kReduceThreads)
         if (lp[i] > 0.f)
             M = fmaxf(M, mp[i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(~0u, M, off));
-    float4 acc[V4];
+    if (lane == 0)
+        red[warp] = M;
+    __syncthreads();
+    M = red[0];
 #pragma unroll
-    for (int v = 0; v < V4; ++v)
-        acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 1; i < NW; ++i)
+        M = fmaxf(M, red[i]);
+    // pass 2: weighted sum of the normalised partial rows
+    const int col = tid % V4, grp = tid / V4;
+    const float4 *op = reinterpret_cast<const float4 *>(p.ws_o + (size_t)sh * p.NPmax * D);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    const float4 *op = reinterpret_cast<const float4 *>(p.ws_o + (size_t)gw * p.NPmax * D);
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
-        const float li = lp[i];
-        const float wi = li > 0.f ? li * ex2(mp[i] - M) : 0.f;
-        den += wi;
+    constexpr int U = 4;
+    for (int i0 = grp; i0 < np; i0 += GROUPS * U) {
+        float wv[U];
+        float4 x[U];
 #pragma unroll
-        for (int v = 0; v < V4; ++v) {
-            const float4 x = op[(size_t)i * (D / 4) + lane + 32 * v];
-            acc[v].x += wi * x.x;
-            acc[v].y += wi * x.y;
-            acc[v].z += wi * x.z;
-            acc[v].w += wi * x.w;
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * GROUPS;
+            wv[u] = 0.f;
+            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < np) {
+                const float li = lp[i];
+                wv[u] = li > 0.f ? li * ex2(mp[i] - M) : 0.f;
+                x[u] = op[(size_t)i * V4 + col];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            den += wv[u];
+            acc.x += wv[u] * x[u].x;
+            acc.y += wv[u] * x[u].y;
+            acc.z += wv[u] * x[u].z;
+            acc.w += wv[u] * x[u].w;
         }
     }
-    const float inv = 1.f / den;
+    acc_s[grp][col] = acc;
+    if (col == 0)
+        den_s[grp] = den;
+    __syncthreads();
+    if (tid < V4) {
+        float4 a = acc_s[0][tid];
+        float d = den_s[0];
 #pragma unroll
-    for (int v = 0; v < V4; ++v)
-        o4[lane + 32 * v] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv,
-                                        acc[v].w * inv);
+        for (int gi = 1; gi < GROUPS; ++gi) {
+            const float4 b = acc_s[gi][tid];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+            d += den_s[gi];
+        }
+        const float inv = 1.f / d;
+        o4[tid] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    }
 }
 
 // ---------------------------------------------------------------- launch
@@ -512,7 +598,7 @@ cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3(lc.reduce_blocks);
-    rcfg.blockDim = dim3(kReduceWarpsPerBlock * 32);
+    rcfg.blockDim = dim3(kReduceThreads);
     rcfg.stream = lc.stream;
     rcfg.attrs = attr;
     rcfg.numAttrs = 1;
