@@ -36,6 +36,25 @@ METRIC = "paged GQA decode: KV-cache GB/s (% of GB300 HBM peak) and µs per call
 FALLBACK_HBM_GBS = 6800.0
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# partition kernel from one ncu capture (profiles/), valid only for the
+# kernel sources they were taken on (hash of csrc/ below).
+TRAFFIC = {
+    "cb551b807428031d": {("batch_decode", 512): 633_336_576 + 5_317_120},
+}
+
+
+def kernel_source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_gqa_decode_03_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -247,39 +266,44 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
 
-    # ---- timed region: K production steps, events on the launching stream;
-    # every step also records events around the partition kernel (the
-    # library's timing hook) for the roofline's per-launch duration.
+    # ---- timed region, two passes of K steps each, events on the launching
+    # stream.  Pass 1 is the production launch sequence (partition kernel,
+    # then the reduce with programmatic dependent launch): `value` and
+    # `ms_per_step`.  Pass 2 also records events around every partition
+    # kernel (the library's timing hook) for the roofline's per-launch
+    # duration; those events sit between the two kernels and cost the
+    # overlap, so its step time is reported separately.
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for e in kb + ka:
         e.record(stream)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        for _ in range(max(args.warmup, 3)):  # clocks back up after the sampler's start
+            step()
         barrier()
         ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+        ev2.record(stream)
         for i in range(args.steps):
             pgd.pgd_set_timing_events(kb[i], ka[i])
             step()
-        ev1.record(stream)
+        ev3.record(stream)
         barrier()
         pgd.pgd_set_timing_events(None, None)
     clocks = clk.summary()
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1))
     ms_per_step = elapsed_ms / args.steps
+    ms_instrumented = max_over_ranks(ev2.elapsed_time(ev3)) / args.steps
     kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(args.steps))
     value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
-
-    # ---- same K steps without the per-launch events (exact production sequence)
-    barrier()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    barrier()
-    ms_plain = max_over_ranks(ev0.elapsed_time(ev1)) / args.steps
 
     # ---- end to end through the public API with host buffers: per step the
     # step's inputs (q, block_tables, seq_lens) go host->device from pinned
@@ -325,13 +349,7 @@ def run_ours(args):
 
     if rank == 0:
         achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-        traffic = None
-        tfile = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tfile):
-            try:
-                traffic = json.load(open(tfile)).get(f"{args.workload}:P{P_used}")
-            except Exception:
-                traffic = None
+        traffic = TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, P_used))
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -344,7 +362,7 @@ def run_ours(args):
                        "kv_bytes_per_step": kv_bytes, "num_blocks": w.NB,
                        "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
                        "accumulate": "fp32", "parallelism": f"replicas x{world}",
-                       "ms_per_step_without_kernel_events": ms_plain},
+                       "ms_per_step_with_kernel_events": ms_instrumented},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",

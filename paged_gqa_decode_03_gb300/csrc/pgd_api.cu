@@ -240,6 +240,12 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
         P = choose_partition(S, Hkv, maxlen, ds->num_sms, ctas);
     plan->P = P;
     plan->NPmax = (maxlen + P - 1) / P;
+    // the kernels count pipeline stages in 32-bit integers
+    const long long stage_bound =
+        (long long)S * Hkv * ((long long)maxlen / 32 + plan->NPmax);
+    if (stage_bound >= (1ll << 31))
+        return fail(PGD_ERR_UNSUPPORTED, "batch of %d sequences x %d KV heads x %d tokens too large",
+                    S, Hkv, maxlen);
     const size_t rows = (size_t)S * Hq * plan->NPmax;
     if (plan->NPmax > 1) {
         plan->off_l = align256(rows * 4);
@@ -341,9 +347,10 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.q = reinterpret_cast<const __half *>(q);
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
-    p.ws_m = plan.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr;
-    p.ws_l = plan.ws_bytes ? reinterpret_cast<float *>(ws + plan.off_l) : nullptr;
-    p.ws_o = plan.ws_bytes ? reinterpret_cast<float *>(ws + plan.off_o) : nullptr;
+    const bool partials = plan.NPmax > 1;
+    p.ws_m = partials ? reinterpret_cast<float *>(ws) : nullptr;
+    p.ws_l = partials ? reinterpret_cast<float *>(ws + plan.off_l) : nullptr;
+    p.ws_o = partials ? reinterpret_cast<float *>(ws + plan.off_o) : nullptr;
     p.page_trace = page_trace;
     p.err = ds->err_word;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e) folded into the scale

@@ -27,6 +27,9 @@ constexpr unsigned kErrPageRange = 1u;
 constexpr unsigned kErrSeqLen = 2u;
 constexpr unsigned kErrTimeout = 4u;
 
+// Sequence lengths the partition kernel keeps in shared memory.
+constexpr int kLensCap = 256;
+
 // Kernel shape per head_dim: tokens per pipeline stage (T), consumer warps
 // (NC), stages in the shared-memory ring (NS).
 template <int D> struct Shape;
@@ -80,6 +83,6 @@ cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk
 cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
 cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
 
-constexpr int kReduceThreads = 256;  // reduce kernel: one CTA per (sequence, query head)
+constexpr int kReduceThreads = 128;  // reduce kernel: one CTA per (sequence, query head)
 
 }  // namespace pgd

@@ -1,11 +1,10 @@
 // Kernels of the paged GQA decode path (sm_103a).
 //
 // 1. paged_gqa_partial_kernel — persistent, warp-specialised.  One CTA per
-//    SM slot walks a static share of the work units; a unit is one
-//    (sequence, KV head, partition) triple: at most `P` consecutive logical
-//    tokens of one sequence, for all query heads of one GQA group
-//    ("vllm-metal", sections "Metal parallel model" and "Four speed-up
-//    tricks", 4).  Units are enumerated full partitions first, then the
+//    SM slot; a unit is one (sequence, KV head, partition) triple: at most
+//    `P` consecutive logical tokens of one sequence, for all query heads of
+//    one GQA group ("vllm-metal", sections "Metal parallel model" and "Four
+//    speed-up tricks", 4).  Units are listed full partitions first, then the
 //    partial last partitions, and dealt round-robin to the CTAs.
 //      * producer warp: loads the unit's page-table entries with one
 //        coalesced warp load, broadcasts each physical page id with a warp
@@ -31,6 +30,8 @@
 
 namespace pgd {
 
+// Stage flags: first / last stage of a unit; the sequence has one partition
+// (its output is written directly); end of work.
 enum : int { kFirst = 1, kLast = 2, kDirect = 4, kTerm = 8 };
 
 struct StageHeader {
@@ -72,6 +73,19 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Sequence lengths, clamped, staged in shared memory for the producer's
+    // walk over the work list (read from global memory past kLensCap).
+    __shared__ int lens_s[kLensCap];
+    const bool lens_in_smem = p.S <= kLensCap;
+    if (lens_in_smem) {
+        const int maxlen = p.MB * BS;
+        for (int i = threadIdx.x; i < p.S; i += blockDim.x) {
+            const int raw = __ldg(p.seq_lens + i);
+            if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
+                atomicOr(p.err, kErrSeqLen);
+            lens_s[i] = raw < 0 ? 0 : (raw > maxlen ? maxlen : raw);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
@@ -95,15 +109,17 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
         int k = 0;  // stages issued by this CTA
         bool ok = true;
 
+        auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > maxlen ? maxlen : L); };
+
         // Issues every stage of unit (s, g, partition pi) of a sequence of
-        // length L whose page ids (entries pg0 .. pg0+63 of its page-table
-        // row, two per lane) are already in id0 / id1.
+        // length L; the unit's page ids (<= 64, two per lane) are in id0 /
+        // id1.  The first stage also brings the group's queries.
         auto produce = [&](int s, int g, int pi, int L, int id0, int id1) -> bool {
             const int tok0 = pi * P;
             const int n = min(P, L - tok0);
-            const bool direct = L <= P;
             const int pg0 = tok0 / BS;
             const int nst = (n + T - 1) / T;
+            const int fixed = L <= P ? kDirect : 0;
             for (int st = 0; st < nst; ++st, ++k) {
                 const int slot = k % NS;
                 bool w = true;
@@ -130,8 +146,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     hdr[slot].g = g;
                     hdr[slot].p = pi;
                     hdr[slot].valid = valid;
-                    hdr[slot].flags = (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
-                                      (direct ? kDirect : 0);
+                    hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0);
                     const uint32_t bytes = pc * PAGE_BYTES * 2 + (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
@@ -172,16 +187,26 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             id1 = lane + 32 < npages ? __ldg(bt + 32 + lane) : 0;
         };
 
-        // This CTA's units, in order: a static round-robin over the list
-        // "full partitions of every sequence (partition-major, KV head
-        // fastest), then the partial last partition of every sequence (one
-        // per KV head)".  Warp-uniform state; sequences are scanned 32 at a
-        // time.
+        // clamped length of sequence s (< S)
+        auto len_at = [&](int s) -> int {
+            if (lens_in_smem)
+                return lens_s[s];
+            const int raw = __ldg(p.seq_lens + s);
+            if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
+                atomicOr(p.err, kErrSeqLen);
+            return clamp_len(raw);
+        };
+
+        // ---- Work list: the full partitions of every sequence
+        // (partition-major, KV head fastest), then the partial last partition
+        // of every sequence (one unit per KV head), dealt round-robin: CTA c
+        // takes units c, c + grid, ...  seek() walks the list forward
+        // (warp-uniform state, sequences scanned 32 at a time) to the unit of
+        // index u.
         int it_phase = 0, it_s0 = 0, it_L = 0, it_cnt = 0, it_incl = 0, it_total = 0;
         bool it_loaded = false;
-        long long next_u = blockIdx.x, base = 0;
-        const long long ustride = gridDim.x;
-        auto advance = [&](int &us, int &ug, int &upi, int &uL) -> bool {
+        long long base = 0;
+        auto seek = [&](long long u, int &us, int &ug, int &upi, int &uL) -> bool {
             for (;;) {
                 if (!it_loaded) {
                     if (it_phase == 2)
@@ -191,16 +216,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         it_s0 = 0;
                         continue;
                     }
-                    const int s = it_s0 + lane;
-                    int L = 0;
-                    if (s < S) {
-                        L = __ldg(p.seq_lens + s);
-                        if (L < 0 || L > maxlen) {
-                            if (it_phase == 0 && blockIdx.x == 0)
-                                atomicOr(p.err, kErrSeqLen);
-                            L = L < 0 ? 0 : maxlen;
-                        }
-                    }
+                    const int L = it_s0 + lane < S ? len_at(it_s0 + lane) : 0;
                     const int cnt = it_phase == 0 ? (L / P) * Hkv : ((L % P) ? Hkv : 0);
                     int incl = cnt;
 #pragma unroll
@@ -215,8 +231,8 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     it_total = __shfl_sync(~0u, incl, 31);
                     it_loaded = true;
                 }
-                if (next_u < base + it_total) {
-                    const int r = (int)(next_u - base);
+                if (u < base + it_total) {
+                    const int r = (int)(u - base);
                     const int j = __ffs(__ballot_sync(~0u, it_incl > r)) - 1;
                     const int ex = __shfl_sync(~0u, it_incl - it_cnt, j);
                     uL = __shfl_sync(~0u, it_L, j);
@@ -229,7 +245,6 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         upi = uL / P;
                         ug = rr;
                     }
-                    next_u += ustride;
                     return true;
                 }
                 base += it_total;
@@ -237,16 +252,25 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 it_loaded = false;
             }
         };
+        long long static_u = blockIdx.x;
+        auto fetch = [&]() -> long long {
+            const long long u = static_u;
+            static_u += gridDim.x;
+            return u;
+        };
 
         int cs = 0, cg = 0, cpi = 0, cL = 0, cid0 = 0, cid1 = 0;
-        bool has = advance(cs, cg, cpi, cL);
+        bool has = seek(fetch(), cs, cg, cpi, cL);
         if (has)
             load_ids(cs, cpi, cL, cid0, cid1);
+        long long nu = has ? fetch() : 0;  // next unit index, fetched one unit ahead
         while (has && ok) {
             int ns_ = 0, ng = 0, npi = 0, nL = 0, nid0 = 0, nid1 = 0;
-            const bool has_next = advance(ns_, ng, npi, nL);
-            if (has_next)  // in flight while this unit's stages are issued
+            const bool has_next = seek(nu, ns_, ng, npi, nL);
+            if (has_next) {  // its page ids are in flight meanwhile
                 load_ids(ns_, npi, nL, nid0, nid1);
+                nu = fetch();
+            }
             ok = produce(cs, cg, cpi, cL, cid0, cid1);
             cs = ns_;
             cg = ng;
@@ -473,102 +497,138 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     }
 }
 
-// One CTA per (sequence, query head): out = sum_p w_p o_p / sum_p w_p with
-// w_p = l_p * exp2(m_p - max_p m_p); zeros for empty sequences; nothing for
-// single-partition sequences (written by the partition kernel).  Thread t
-// owns float4 column t % (D/4) of the partitions p = t / (D/4) (mod groups),
-// with several partial rows in flight per thread.
+// One CTA of four warps per (sequence, query head): merges the partials of
+// its partitions, out = sum_i w_i o_i / sum_i w_i with
+// w_i = l_i * exp2(m_i - max m); zeros for empty sequences; nothing for
+// single-partition sequences (written by the partition kernel).  The length
+// is an input, read before waiting for the partition kernel; each warp then
+// loads the (max, exp-sum) of its pieces lane-parallel and the rows of the
+// non-empty ones several at a time.
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads)
     paged_gqa_reduce_kernel(const DecodeParams p, int max_len)
 {
-    griddep_wait();
-    constexpr int V4 = D / 4;                     // float4 per row
-    constexpr int GROUPS = kReduceThreads / V4;   // partitions handled at once
     constexpr int NW = kReduceThreads / 32;
-    __shared__ float red[NW];
-    __shared__ float4 acc_s[GROUPS][V4];
-    __shared__ float den_s[GROUPS];
+    constexpr int V4 = D / 4;       // float4 per row
+    constexpr int PL = V4 / 32;     // float4 per lane
+    constexpr int U = 8;            // rows in flight per warp
+    __shared__ float m_s[NW], den_s[NW];
+    __shared__ float4 acc_s[NW][V4];
     const int sh = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (sh >= p.S * p.Hq)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (sh >= p.S * p.Hq) {
+        griddep_wait();
         return;
+    }
     const int s = sh / p.Hq;
     int L = __ldg(p.seq_lens + s);
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
     float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)sh * D);
+    const int np = (L + p.P - 1) / p.P;
+    griddep_wait();
     if (L == 0) {
-        if (tid < V4)
-            o4[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = threadIdx.x; i < V4; i += kReduceThreads)
+            o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    const int np = (L + p.P - 1) / p.P;
     if (np == 1)
         return;
+    const int nslots = np;
     const float *mp = p.ws_m + (size_t)sh * p.NPmax;
     const float *lp = p.ws_l + (size_t)sh * p.NPmax;
-    // pass 1: M = max over non-empty partitions of m_p
-    float M = -INFINITY;
-    for (int i = tid; i < np; i += kReduceThreads)
-        if (lp[i] > 0.f)
-            M = fmaxf(M, mp[i]);
+    const float4 *op = reinterpret_cast<const float4 *>(p.ws_o + (size_t)sh * p.NPmax * D);
+
+    // warp `warp` owns slots warp, warp + NW, ...; lane j of round r holds
+    // slot warp + NW * (j + 32 r)
+    float Mw = -INFINITY;
+    for (int r = 0; warp + NW * 32 * r < nslots; ++r) {
+        const int i = warp + NW * (lane + 32 * r);
+        if (i < nslots && lp[i] > 0.f)
+            Mw = fmaxf(Mw, mp[i]);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(~0u, M, off));
-    if (lane == 0)
-        red[warp] = M;
-    __syncthreads();
-    M = red[0];
+        Mw = fmaxf(Mw, __shfl_xor_sync(~0u, Mw, off));
+    float4 acc[PL];
 #pragma unroll
-    for (int i = 1; i < NW; ++i)
-        M = fmaxf(M, red[i]);
-    // pass 2: weighted sum of the normalised partial rows
-    const int col = tid % V4, grp = tid / V4;
-    const float4 *op = reinterpret_cast<const float4 *>(p.ws_o + (size_t)sh * p.NPmax * D);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int v = 0; v < PL; ++v)
+        acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    constexpr int U = 4;
-    for (int i0 = grp; i0 < np; i0 += GROUPS * U) {
-        float wv[U];
-        float4 x[U];
+    for (int r = 0; warp + NW * 32 * r < nslots; ++r) {
+        const int i = warp + NW * (lane + 32 * r);
+        float wl = 0.f;
+        if (i < nslots) {
+            const float li = lp[i];
+            if (li > 0.f)
+                wl = li * ex2(mp[i] - Mw);
+        }
+        unsigned mask = __ballot_sync(~0u, wl > 0.f);
+        while (mask) {
+            int src[U];
+            float wu[U];
+            float4 x[U][PL];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * GROUPS;
-            wv[u] = 0.f;
-            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < np) {
-                const float li = lp[i];
-                wv[u] = li > 0.f ? li * ex2(mp[i] - M) : 0.f;
-                x[u] = op[(size_t)i * V4 + col];
+            for (int u = 0; u < U; ++u) {
+                src[u] = -1;
+                if (mask) {
+                    src[u] = __ffs(mask) - 1;
+                    mask &= mask - 1;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                wu[u] = __shfl_sync(~0u, wl, src[u] < 0 ? 0 : src[u]);
+                if (src[u] >= 0) {
+                    const int slot = warp + NW * (src[u] + 32 * r);
+#pragma unroll
+                    for (int v = 0; v < PL; ++v)
+                        x[u][v] = op[(size_t)slot * V4 + lane + 32 * v];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (src[u] < 0)
+                    continue;
+                den += wu[u];
+#pragma unroll
+                for (int v = 0; v < PL; ++v) {
+                    acc[v].x += wu[u] * x[u][v].x;
+                    acc[v].y += wu[u] * x[u][v].y;
+                    acc[v].z += wu[u] * x[u][v].z;
+                    acc[v].w += wu[u] * x[u][v].w;
+                }
             }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            den += wv[u];
-            acc.x += wv[u] * x[u].x;
-            acc.y += wv[u] * x[u].y;
-            acc.z += wv[u] * x[u].z;
-            acc.w += wv[u] * x[u].w;
-        }
     }
-    acc_s[grp][col] = acc;
-    if (col == 0)
-        den_s[grp] = den;
-    __syncthreads();
-    if (tid < V4) {
-        float4 a = acc_s[0][tid];
-        float d = den_s[0];
+    if (lane == 0) {
+        m_s[warp] = Mw;
+        den_s[warp] = den;
+    }
 #pragma unroll
-        for (int gi = 1; gi < GROUPS; ++gi) {
-            const float4 b = acc_s[gi][tid];
-            a.x += b.x;
-            a.y += b.y;
-            a.z += b.z;
-            a.w += b.w;
-            d += den_s[gi];
+    for (int v = 0; v < PL; ++v)
+        acc_s[warp][lane + 32 * v] = acc[v];
+    __syncthreads();
+    float M = m_s[0];
+#pragma unroll
+    for (int wi = 1; wi < NW; ++wi)
+        M = fmaxf(M, m_s[wi]);
+    for (int c = threadIdx.x; c < V4; c += kReduceThreads) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        float d = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < NW; ++wi) {
+            if (!(den_s[wi] > 0.f))
+                continue;
+            const float sc = ex2(m_s[wi] - M);
+            const float4 b = acc_s[wi][c];
+            a.x += sc * b.x;
+            a.y += sc * b.y;
+            a.z += sc * b.z;
+            a.w += sc * b.w;
+            d += sc * den_s[wi];
         }
         const float inv = 1.f / d;
-        o4[tid] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+        o4[c] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
 }
 
