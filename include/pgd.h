@@ -108,6 +108,13 @@ typedef enum pgd_status {
  * Scratch for the partition partials is taken from a stream-ordered memory
  * pool owned by the library and returned in stream order, so calls on
  * different streams do not share it.  Use paged_gqa_decode_ex to supply it.
+ *
+ * Work is handed out to the GPU's thread blocks through a 4-byte counter
+ * that the library keeps per (device, stream) it has run on; the call
+ * leaves it at zero for the next call on that stream.  The counters of a
+ * device (1024 of them, 128 bytes apart) are allocated and
+ * zeroed by the first call on that device: make that first call outside
+ * any stream capture.
  */
 pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cache,
                             const uint16_t *v_cache, const int32_t *block_tables,
@@ -162,9 +169,12 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
  *
  * The partition partials go to a fixed array of PGD_NOALLOC_SCRATCH_BYTES
  * compiled into the library (every GPU on which the library is used holds
- * it until the process exits).  The call never calls cudaMalloc, cudaFree or
- * any other allocating routine.  Sizes whose partials need more than that
- * (see pgd_plan) are rejected with PGD_ERR_WORKSPACE before any launch.
+ * it until the process exits); its first 256 bytes hold this entry point's
+ * work counter, zero at load and left at zero by every call.  The call never
+ * calls cudaMalloc, cudaFree or any other allocating routine.  Sizes whose
+ * partials need more than the rest of the array (pgd_plan's figure above
+ * PGD_NOALLOC_SCRATCH_BYTES - 256) are rejected with PGD_ERR_WORKSPACE before
+ * any launch.
  *
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.

@@ -8,6 +8,8 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -175,6 +177,133 @@ pgd_status encode_cache_map(CUtensorMap *map, const void *base, long long rows, 
     return PGD_OK;
 }
 
+// ------------------------------------------------------------------ claim counters
+// The partition kernel hands out work units with a 4-byte counter that must
+// read 0 at launch; the reduce kernel zeroes it at the end of every call.
+// The library keeps one counter per (device, stream) it has run on: calls on
+// one stream are serialised and can reuse it, calls on different streams
+// never share one.  A counter whose call failed to launch is zeroed in
+// stream order before its next use.
+constexpr int kCounterSlots = 1024;
+constexpr int kCounterStride = 32;  // unsigned words: 128 bytes apart
+
+struct CounterPool {
+    std::once_flag once;
+    cudaError_t error = cudaSuccess;
+    unsigned *base = nullptr;
+    std::mutex mu;
+    std::unordered_map<uintptr_t, int> slot_of;
+    std::vector<char> dirty;
+};
+
+CounterPool g_counters[kMaxDevices];
+
+cudaError_t init_counters(CounterPool &cp)
+{
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&cp.base),
+                               sizeof(unsigned) * kCounterSlots * kCounterStride);
+    if (e != cudaSuccess)
+        return e;
+    if ((e = cudaMemset(cp.base, 0, sizeof(unsigned) * kCounterSlots * kCounterStride)) !=
+        cudaSuccess)
+        return e;
+    cp.dirty.assign(kCounterSlots, 0);
+    return cudaDeviceSynchronize();
+}
+
+// The counter of `stream` on the current device (null when all slots are
+// taken); *reset tells the caller to zero it in stream order first.
+pgd_status stream_counter(cudaStream_t stream, unsigned **counter, int *slot, bool *reset)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    CounterPool &cp = g_counters[dev];
+    std::call_once(cp.once, [&] { cp.error = init_counters(cp); });
+    if (cp.error != cudaSuccess)
+        return cuda_fail(cp.error, "claim-counter set-up");
+    std::lock_guard<std::mutex> lock(cp.mu);
+    const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+    auto it = cp.slot_of.find(key);
+    int i;
+    if (it != cp.slot_of.end()) {
+        i = it->second;
+    } else if ((int)cp.slot_of.size() < kCounterSlots) {
+        i = (int)cp.slot_of.size();
+        cp.slot_of.emplace(key, i);
+    } else {
+        *counter = nullptr;
+        *slot = -1;
+        *reset = false;
+        return PGD_OK;
+    }
+    *counter = cp.base + (size_t)i * kCounterStride;
+    *slot = i;
+    *reset = cp.dirty[i] != 0;
+    cp.dirty[i] = 0;
+    return PGD_OK;
+}
+
+void mark_counter_dirty(int slot)
+{
+    int dev = 0;
+    if (slot < 0 || cudaGetDevice(&dev) != cudaSuccess)
+        return;
+    std::lock_guard<std::mutex> lock(g_counters[dev].mu);
+    g_counters[dev].dirty[slot] = 1;
+}
+
+// Descriptors of the last few (k_cache, v_cache) pairs used by this thread:
+// encoding them is the largest host cost of a call, and a decode loop calls
+// with the same caches every step.
+struct MapCacheEntry {
+    const void *k, *v;
+    long long rows;
+    int D, box, dev;
+    alignas(64) CUtensorMap tk;
+    alignas(64) CUtensorMap tv;
+};
+constexpr int kMapCache = 8;
+thread_local MapCacheEntry t_maps[kMapCache];
+thread_local int t_maps_used = 0, t_maps_next = 0;
+
+pgd_status cache_maps(const void *k, const void *v, long long rows, int D, int box,
+                      const CUtensorMap **tk, const CUtensorMap **tv)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    for (int i = 0; i < t_maps_used; ++i) {
+        MapCacheEntry &c = t_maps[i];
+        if (c.k == k && c.v == v && c.rows == rows && c.D == D && c.box == box && c.dev == dev) {
+            *tk = &c.tk;
+            *tv = &c.tv;
+            return PGD_OK;
+        }
+    }
+    MapCacheEntry &c = t_maps[t_maps_next];
+    pgd_status st;
+    if ((st = encode_cache_map(&c.tk, k, rows, D, box)) ||
+        (st = encode_cache_map(&c.tv, v, rows, D, box))) {
+        c.k = c.v = nullptr;
+        return st;
+    }
+    c.k = k;
+    c.v = v;
+    c.rows = rows;
+    c.D = D;
+    c.box = box;
+    c.dev = dev;
+    t_maps_next = (t_maps_next + 1) % kMapCache;
+    if (t_maps_used < kMapCache)
+        ++t_maps_used;
+    *tk = &c.tk;
+    *tv = &c.tv;
+    return PGD_OK;
+}
+
 // ------------------------------------------------------------------ validation & plan
 struct Plan {
     int P;             // partition size
@@ -274,7 +403,8 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
                int Hkv, int D, int BS, int P, int MB, int NB, void *workspace, size_t ws_bytes,
-               bool own_workspace, int32_t *page_trace, void *stream_v)
+               bool own_workspace, int32_t *page_trace, void *stream_v,
+               unsigned *counter = nullptr)
 {
     if (S == 0) {  // nothing to read or write: only the sizes are checked
         Plan plan;
@@ -334,12 +464,35 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     const int box = BS < (D == 128 ? Shape<128>::T : Shape<256>::T)
                         ? BS
                         : (D == 128 ? Shape<128>::T : Shape<256>::T);
-    alignas(64) CUtensorMap tk, tv;
-    if ((st = encode_cache_map(&tk, k_cache, rows, D, box)) ||
-        (st = encode_cache_map(&tv, v_cache, rows, D, box))) {
+    const CUtensorMap *tk = nullptr, *tv = nullptr;
+    if ((st = cache_maps(k_cache, v_cache, rows, D, box, &tk, &tv))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
+    }
+
+    // claim counter: given (static scratch), this stream's, or a per-call one
+    int slot = -1;
+    unsigned *own_counter = nullptr;
+    if (!counter) {
+        bool reset = false;
+        if ((st = stream_counter(stream, &counter, &slot, &reset))) {
+            if (own_workspace && ws)
+                cudaFreeAsync(ws, stream);
+            return st;
+        }
+        if (!counter) {  // every slot taken: a zeroed counter for this call only
+            cudaMemPool_t pool;
+            if ((st = device_pool(*ds, &pool)))
+                return st;
+            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&own_counter), 256, pool,
+                                             stream)) != cudaSuccess)
+                return cuda_fail(e, "counter allocation");
+            counter = own_counter;
+            reset = true;
+        }
+        if (reset && (e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream)) != cudaSuccess)
+            return cuda_fail(e, "counter reset");
     }
 
     DecodeParams p = {};
@@ -352,6 +505,7 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.ws_l = partials ? reinterpret_cast<float *>(ws + plan.off_l) : nullptr;
     p.ws_o = partials ? reinterpret_cast<float *>(ws + plan.off_o) : nullptr;
     p.page_trace = page_trace;
+    p.counter = counter;
     p.err = ds->err_word;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e) folded into the scale
     p.S = S;
@@ -359,6 +513,7 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
     p.P = plan.P;
+    p.logP = plan.P == kPartitionLarge ? 9 : 8;
     p.MB = MB;
     p.NB = NB;
     p.NPmax = plan.NPmax;
@@ -370,15 +525,22 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     lc.stream = stream;
     lc.ev_before = t_ev_before;
     lc.ev_after = t_ev_after;
-    e = D == 128 ? launch_decode_d128(BS, page_trace != nullptr, tk, tv, p, lc)
-                 : launch_decode_d256(BS, page_trace != nullptr, tk, tv, p, lc);
+    e = D == 128 ? launch_decode_d128(BS, page_trace != nullptr, *tk, *tv, p, lc)
+                 : launch_decode_d256(BS, page_trace != nullptr, *tk, *tv, p, lc);
     if (own_workspace && ws) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess)
             e = e2;
     }
-    if (e != cudaSuccess)
+    if (own_counter) {
+        cudaError_t e2 = cudaFreeAsync(own_counter, stream);
+        if (e == cudaSuccess)
+            e = e2;
+    }
+    if (e != cudaSuccess) {
+        mark_counter_dirty(slot);  // the reduce may not have zeroed it
         return cuda_fail(e, "kernel launch");
+    }
     t_last_error.clear();
     return PGD_OK;
 }
@@ -453,18 +615,20 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                               partition_size, max_blocks_per_seq, &plan);
     if (st)
         return st;
-    if (plan.ws_bytes > PGD_NOALLOC_SCRATCH_BYTES)
+    if (plan.ws_bytes > PGD_NOALLOC_SCRATCH_BYTES - 256)
         return fail(PGD_ERR_WORKSPACE,
                     "these sizes need %zu bytes of scratch, more than the %zu bytes of static "
                     "scratch of paged_gqa_decode_noalloc; use paged_gqa_decode or "
                     "paged_gqa_decode_ex",
-                    plan.ws_bytes, (size_t)PGD_NOALLOC_SCRATCH_BYTES);
+                    plan.ws_bytes, (size_t)PGD_NOALLOC_SCRATCH_BYTES - 256);
     void *scratch = nullptr;
     if ((st = noalloc_scratch(&scratch)))
         return st;
+    // [256 B: claim counter, zero at load and after every call][partials]
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
-               num_blocks, scratch, PGD_NOALLOC_SCRATCH_BYTES, false, nullptr, stream);
+               num_blocks, static_cast<char *>(scratch) + 256, PGD_NOALLOC_SCRATCH_BYTES - 256,
+               false, nullptr, stream, static_cast<unsigned *>(scratch));
 }
 
 pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -195,6 +195,15 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held as mma fragments
+// (thread t: row t/4, columns 2(t%4), 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);

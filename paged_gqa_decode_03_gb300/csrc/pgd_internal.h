@@ -27,17 +27,19 @@ constexpr unsigned kErrPageRange = 1u;
 constexpr unsigned kErrSeqLen = 2u;
 constexpr unsigned kErrTimeout = 4u;
 
-// Sequence lengths the partition kernel keeps in shared memory.
+// Sequence lengths the partition kernel keeps in shared memory, and the
+// most pipeline stages a partial partition can have (512 / 32).
 constexpr int kLensCap = 256;
+constexpr int kMaxTailStages = 16;
 
 // Kernel shape per head_dim: tokens per pipeline stage (T), consumer warps
-// (NC), stages in the shared-memory ring (NS).
+// (NC, one 16-token tile each), stages in the shared-memory ring (NS).
 template <int D> struct Shape;
 template <> struct Shape<128> {
     static constexpr int T = 64, NC = 4, NS = 3;
 };
 template <> struct Shape<256> {
-    static constexpr int T = 32, NC = 4, NS = 3;
+    static constexpr int T = 32, NC = 2, NS = 3;
 };
 
 template <int D> __host__ __device__ constexpr int stage_kv_bytes() { return Shape<D>::T * D * 2; }  // K or V
@@ -59,9 +61,10 @@ struct DecodeParams {
     float *ws_l;                  // [S][Hq][NPmax] partition exp2-sum
     float *ws_o;                  // [S][Hq][NPmax][D] normalised partition output
     int32_t *page_trace;          // [S][Hkv][MB] or null
+    unsigned *counter;            // work-claim counter: 0 at launch, reset by the reduce
     unsigned *err;                // device error word
     float scale_log2;             // scale * log2(e)
-    int S, Hq, Hkv, G, P, MB, NB, NPmax;
+    int S, Hq, Hkv, G, P, logP, MB, NB, NPmax;
     uint64_t wait_budget_ns;
 };
 

@@ -5,7 +5,9 @@
 //    `P` consecutive logical tokens of one sequence, for all query heads of
 //    one GQA group ("vllm-metal", sections "Metal parallel model" and "Four
 //    speed-up tricks", 4).  Units are listed full partitions first, then the
-//    partial last partitions, and dealt round-robin to the CTAs.
+//    partial last partitions (largest first); each CTA starts with one unit
+//    and claims the next from a counter shortly before it has issued the
+//    current one, so that slower CTAs take fewer units.
 //      * producer warp: loads the unit's page-table entries with one
 //        coalesced warp load, broadcasts each physical page id with a warp
 //        shuffle, and issues one TMA tensor copy of the page's K rows and one
@@ -24,6 +26,8 @@
 //    (sequence, query head) ("Four speed-up tricks", 4) and writes zeros for
 //    empty sequences.  Launched with programmatic dependent launch.
 #pragma once
+
+#include <atomic>
 
 #include "pgd_device.cuh"
 #include "pgd_internal.h"
@@ -48,23 +52,20 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     constexpr int SLABS = D / 64;          // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
     constexpr int PAGE_BYTES = BOX * D * 2;  // one copy: BOX rows of one page, all slabs
-    constexpr int KT = D / 16;             // k-steps of QK (over head_dim)
-    constexpr int KS = T / 16;             // k-steps of PV (over tokens)
-    constexpr int QKW = T / 16;            // consumer warps computing a QK tile
-    constexpr int MT = D / 16 / NC;        // 16-row O^T tiles per consumer warp
-    constexpr int SST = T + 4;             // score-exchange row stride (floats)
+    constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
     constexpr int KV_BYTES = stage_kv_bytes<D>();
     constexpr int STAGE = stage_bytes<D>();
-    static_assert(QKW <= NC, "at most one QK tile per consumer warp");
-    static_assert(MT * NC * 16 == D, "O^T tiles must split evenly");
+    constexpr int OST = D + 4;             // merge buffer row stride (floats)
+    static_assert(NC * 16 == T, "one 16-token tile per consumer warp per stage");
     static_assert(BS <= T ? (T % BS == 0) : (BS % T == 0), "stage/page sizes");
     static_assert(STAGE % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle alignment");
+    static_assert(NC * kMaxGroup * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
 
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[NS];
     __shared__ __align__(8) uint64_t empty_bar[NS];
+    __shared__ __align__(8) uint64_t merge_bar;
     __shared__ StageHeader hdr[NS];
-    __shared__ float s_buf[2][kMaxGroup][SST];
     __shared__ int abort_flag;
 
     const uint32_t dyn_base = smem_addr(dyn_smem);
@@ -73,17 +74,71 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Sequence lengths, clamped, staged in shared memory for the producer's
-    // walk over the work list (read from global memory past kLensCap).
+    // ---- Work list (see the producer): the full partitions of every
+    // sequence, then one partial last partition per sequence and KV head,
+    // largest first.  With at most kLensCap sequences the whole CTA stages
+    // the clamped lengths, counts the full units and sorts the sequences
+    // with a partial last partition by its stage count (counting sort) into
+    // shared memory; beyond that the producer scans global memory.
     __shared__ int lens_s[kLensCap];
+    __shared__ int tail_order[kLensCap];
+    __shared__ int bucket[kMaxTailStages + 1];  // counts, then cursors
+    __shared__ int nfull_s, ntail_s;
     const bool lens_in_smem = p.S <= kLensCap;
-    if (lens_in_smem) {
+    {
         const int maxlen = p.MB * BS;
-        for (int i = threadIdx.x; i < p.S; i += blockDim.x) {
-            const int raw = __ldg(p.seq_lens + i);
-            if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
-                atomicOr(p.err, kErrSeqLen);
-            lens_s[i] = raw < 0 ? 0 : (raw > maxlen ? maxlen : raw);
+        if (threadIdx.x <= kMaxTailStages)
+            bucket[threadIdx.x] = 0;
+        if (threadIdx.x == 0)
+            nfull_s = 0;
+        __syncthreads();
+        if (lens_in_smem) {
+            int nf = 0;
+            for (int i = threadIdx.x; i < p.S; i += blockDim.x) {
+                const int raw = __ldg(p.seq_lens + i);
+                if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
+                    atomicOr(p.err, kErrSeqLen);
+                const int L = raw < 0 ? 0 : (raw > maxlen ? maxlen : raw);
+                lens_s[i] = L;
+                nf += L >> p.logP;
+                const int tail = L & (p.P - 1);
+                if (tail)
+                    atomicAdd(&bucket[(tail + T - 1) / T], 1);
+            }
+            nf = (int)__reduce_add_sync(~0u, (unsigned)nf);
+            if ((threadIdx.x & 31) == 0 && nf)
+                atomicAdd(&nfull_s, nf);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && lens_in_smem) {  // cursors: largest tails first
+            int acc = 0;
+            for (int b = kMaxTailStages; b >= 1; --b) {
+                const int c = bucket[b];
+                bucket[b] = acc;
+                acc += c;
+            }
+            ntail_s = acc;
+        }
+        __syncthreads();
+        // stable scatter by one warp, in sequence order, so every CTA builds
+        // the same list (claimed unit indices must mean the same unit in all)
+        if (lens_in_smem && threadIdx.x < 32) {
+            const int lane0 = threadIdx.x;
+            for (int s0 = 0; s0 < p.S; s0 += 32) {
+                const int i = s0 + lane0;
+                const int tail = i < p.S ? (lens_s[i] & (p.P - 1)) : 0;
+                const int b = tail ? (tail + T - 1) / T : 0;
+                const unsigned same = __match_any_sync(~0u, b);
+                const int rank = __popc(same & ((1u << lane0) - 1));
+                const int pos = b ? bucket[b] + rank : 0;
+                __syncwarp();
+                if (b) {
+                    tail_order[pos] = i;
+                    if (rank == 0)
+                        bucket[b] += __popc(same);
+                }
+                __syncwarp();
+            }
         }
     }
     if (threadIdx.x == 0) {
@@ -91,6 +146,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             mbar_init(smem_addr(&full_bar[i]), 1);
             mbar_init(smem_addr(&empty_bar[i]), NC);
         }
+        mbar_init(smem_addr(&merge_bar), NC);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -114,6 +170,17 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
         // Issues every stage of unit (s, g, partition pi) of a sequence of
         // length L; the unit's page ids (<= 64, two per lane) are in id0 /
         // id1.  The first stage also brings the group's queries.
+        // Next unit index: units 0 .. grid-1 are the CTAs' first units; the
+        // rest are claimed from the counter, late (two stages before the
+        // current unit is fully issued) so that a slow CTA holds little
+        // unstarted work at the end.
+        long long claimed = -1;
+        auto claim = [&]() {
+            unsigned u = 0;
+            if (lane == 0)
+                u = atomicAdd(p.counter, 1u);
+            claimed = (long long)__shfl_sync(~0u, u, 0) + gridDim.x;
+        };
         auto produce = [&](int s, int g, int pi, int L, int id0, int id1) -> bool {
             const int tok0 = pi * P;
             const int n = min(P, L - tok0);
@@ -121,6 +188,8 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             const int nst = (n + T - 1) / T;
             const int fixed = L <= P ? kDirect : 0;
             for (int st = 0; st < nst; ++st, ++k) {
+                if (claimed < 0 && nst - st <= 2)
+                    claim();
                 const int slot = k % NS;
                 bool w = true;
                 if (lane == 0)
@@ -197,12 +266,12 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             return clamp_len(raw);
         };
 
-        // ---- Work list: the full partitions of every sequence
-        // (partition-major, KV head fastest), then the partial last partition
-        // of every sequence (one unit per KV head), dealt round-robin: CTA c
-        // takes units c, c + grid, ...  seek() walks the list forward
-        // (warp-uniform state, sequences scanned 32 at a time) to the unit of
-        // index u.
+        // ---- This CTA's units.  seek() walks the list "full partitions of
+        // every sequence (partition-major, KV head fastest), then the partial
+        // last partition of every sequence (one per KV head, sequence
+        // order)" forward to the unit of index u (warp-uniform state,
+        // sequences scanned 32 at a time).  With the lengths in shared memory
+        // the partial partitions come instead from tail_order, largest first.
         int it_phase = 0, it_s0 = 0, it_L = 0, it_cnt = 0, it_incl = 0, it_total = 0;
         bool it_loaded = false;
         long long base = 0;
@@ -252,33 +321,37 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 it_loaded = false;
             }
         };
-        long long static_u = blockIdx.x;
-        auto fetch = [&]() -> long long {
-            const long long u = static_u;
-            static_u += gridDim.x;
-            return u;
+        const long long nfull_units = lens_in_smem ? (long long)nfull_s * Hkv : -1;
+        const long long n_units = lens_in_smem ? nfull_units + (long long)ntail_s * Hkv : -1;
+        auto decode = [&](long long u, int &us, int &ug, int &upi, int &uL) -> bool {
+            if (!lens_in_smem)
+                return seek(u, us, ug, upi, uL);
+            if (u >= n_units)
+                return false;
+            if (u < nfull_units)
+                return seek(u, us, ug, upi, uL);
+            const long long ti = u - nfull_units;
+            us = tail_order[ti / Hkv];
+            ug = (int)(ti % Hkv);
+            uL = lens_s[us];
+            upi = uL / P;
+            return true;
         };
 
         int cs = 0, cg = 0, cpi = 0, cL = 0, cid0 = 0, cid1 = 0;
-        bool has = seek(fetch(), cs, cg, cpi, cL);
+        bool has = decode(blockIdx.x, cs, cg, cpi, cL);
         if (has)
             load_ids(cs, cpi, cL, cid0, cid1);
-        long long nu = has ? fetch() : 0;  // next unit index, fetched one unit ahead
         while (has && ok) {
-            int ns_ = 0, ng = 0, npi = 0, nL = 0, nid0 = 0, nid1 = 0;
-            const bool has_next = seek(nu, ns_, ng, npi, nL);
-            if (has_next) {  // its page ids are in flight meanwhile
-                load_ids(ns_, npi, nL, nid0, nid1);
-                nu = fetch();
-            }
+            claimed = -1;
             ok = produce(cs, cg, cpi, cL, cid0, cid1);
-            cs = ns_;
-            cg = ng;
-            cpi = npi;
-            cL = nL;
-            cid0 = nid0;
-            cid1 = nid1;
-            has = has_next;
+            if (!ok)
+                break;
+            if (claimed < 0)
+                claim();
+            has = decode(claimed, cs, cg, cpi, cL);
+            if (has)
+                load_ids(cs, cpi, cL, cid0, cid1);
         }
         if (ok) {  // end-of-work marker
             const int slot = k % NS;
@@ -306,194 +379,227 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     }
 
     // ================================================================ consumers
+    // Consumer warp w owns token tile w (tokens [16w, 16w+16)) of every
+    // stage and runs its own log2-space online softmax over the whole of
+    // head_dim for the group's query heads; the NC warps merge their states
+    // once per unit, in the shared memory of the unit's last stage.
     const int w = warp;
-    const int gb = lane >> 2;       // B-fragment column: query head of the softmax rows
-    const int tq = (lane & 3) * 2;  // B-fragment token pair / C-fragment head pair
-    float o[MT][4];
+    const int gb = lane >> 2;            // C-fragment row: token within the tile
+    const int tq = (lane & 3) * 2;       // C-fragment columns: query heads tq, tq+1
+    const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix index, row in it
+    const int t0 = 16 * w;               // this warp's tile within a stage
+    float o[KT][4];                      // O^T[D x 8]: row 16 i + gb (+8), columns tq, tq+1
+    uint32_t qf[KT][2];                  // Q^T B-fragments
 #pragma unroll
-    for (int i = 0; i < MT; ++i)
+    for (int i = 0; i < KT; ++i) {
         o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    uint32_t qf[KT][2];
-#pragma unroll
-    for (int i = 0; i < KT; ++i)
         qf[i][0] = qf[i][1] = 0u;
-    float m_run = -INFINITY, l_run = 0.f;
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads tq, tq+1 (log2 units)
+    float l0 = 0.f, l1 = 0.f;              // this lane's share of the running exp2-sums
+    uint32_t msync = 0;                    // merge-barrier phases passed
+
+    // Bounded rendezvous of the NC consumer warps (false: give up).
+    auto consumers_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&merge_bar));
+        const bool ok = mbar_wait_bounded(smem_addr(&merge_bar), msync & 1, &abort_flag,
+                                          p.wait_budget_ns);
+        ++msync;
+        return ok;
+    };
 
     for (int k = 0;; ++k) {
         const int slot = k % NS;
         const uint32_t sb = ring + slot * STAGE;
-        const bool ok = mbar_wait_bounded(smem_addr(&full_bar[slot]), (k / NS) & 1, &abort_flag,
-                                          p.wait_budget_ns);
-        int hs = 0, hg = 0, hp = 0, valid = 0, flags = kTerm;
-        if (ok) {
-            hs = hdr[slot].s;
-            hg = hdr[slot].g;
-            hp = hdr[slot].p;
-            valid = hdr[slot].valid;
-            flags = hdr[slot].flags;
-        } else {
+        uint8_t *const sp = ring_ptr + slot * STAGE;
+        if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), (k / NS) & 1, &abort_flag,
+                               p.wait_budget_ns)) {
             if (lane == 0 && !abort_flag)
                 atomicOr(p.err, kErrTimeout);
             abort_flag = 1;
-        }
-        float *const sx = &s_buf[k & 1][0][0];
-        if (ok && !(flags & kTerm)) {
-            if (flags & kFirst) {
-                m_run = -INFINITY;
-                l_run = 0.f;
-#pragma unroll
-                for (int i = 0; i < MT; ++i)
-                    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-                if (w < QKW) {
-                    const uint8_t *qs = ring_ptr + slot * STAGE + 2 * KV_BYTES;
-                    const bool live = gb < p.G;
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        const uint8_t *qrow = qs + (gb * D + kk * 16 + tq) * 2;
-                        qf[kk][0] = live ? *reinterpret_cast<const uint32_t *>(qrow) : 0u;
-                        qf[kk][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16) : 0u;
-                    }
-                }
-            }
-            if (valid < T) {
-                // rows past the unit's end: zero V so 0-weights never meet NaN
-                uint8_t *vs = ring_ptr + slot * STAGE + KV_BYTES;
-                for (int r = valid + w; r < T; r += NC)
-                    if (lane < SLABS * 8)
-                        *reinterpret_cast<uint4 *>(vs + (r / BOX) * PAGE_BYTES +
-                                                   (lane >> 3) * (BOX * 128) + (r % BOX) * 128 +
-                                                   (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
-                fence_proxy_async_smem();
-            }
-            if (w < QKW) {
-                // S^T[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8]
-                const int t0 = w * 16;
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                if (t0 < valid) {
-                    const int mi = lane >> 3, r = lane & 7;
-                    const int tok = t0 + r + (mi & 1) * 8;
-                    const uint32_t rowaddr =
-                        sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
-                    const int sw = tok & 7;
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        const int dim = kk * 16 + (mi >> 1) * 8;
-                        const uint32_t addr =
-                            rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(addr, a0, a1, a2, a3);
-                        if (kk & 1)
-                            mma_16816(c1, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                        else
-                            mma_16816(c0, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                    }
-                }
-                const float sc = p.scale_log2;
-                const int ta = t0 + gb, tb = ta + 8;  // C rows: tokens; C columns tq, tq+1: heads
-                sx[tq * SST + ta] = ta < valid ? (c0[0] + c1[0]) * sc : -INFINITY;
-                sx[(tq + 1) * SST + ta] = ta < valid ? (c0[1] + c1[1]) * sc : -INFINITY;
-                sx[tq * SST + tb] = tb < valid ? (c0[2] + c1[2]) * sc : -INFINITY;
-                sx[(tq + 1) * SST + tb] = tb < valid ? (c0[3] + c1[3]) * sc : -INFINITY;
-            }
-        }
-        if (bar_sync_or(1, NC * 32, !ok) || (flags & kTerm))
             break;
-
-        // ---- log2-space online softmax over the stage's T tokens, head gb
-        float x[KS][4];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const float *row = sx + gb * SST + ks * 16 + tq;
-            x[ks][0] = row[0];
-            x[ks][1] = row[1];
-            x[ks][2] = row[8];
-            x[ks][3] = row[9];
-            mx = fmaxf(mx, fmaxf(fmaxf(x[ks][0], x[ks][1]), fmaxf(x[ks][2], x[ks][3])));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = ex2(m_run - m_new);
-        uint32_t pb[KS][2];
-        float ls = 0.f;
+        const int flags = hdr[slot].flags;
+        if (flags & kTerm)
+            break;
+        const int hs = hdr[slot].s, hg = hdr[slot].g, hp = hdr[slot].p;
+        const int valid = hdr[slot].valid;
+        if (flags & kFirst) {
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            const uint8_t *qs = sp + 2 * KV_BYTES;
+            const bool live = gb < p.G;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            pb[ks][0] = pack_half2(ex2(x[ks][0] - m_new), ex2(x[ks][1] - m_new));
-            pb[ks][1] = pack_half2(ex2(x[ks][2] - m_new), ex2(x[ks][3] - m_new));
-            const float2 f0 = unpack_half2(pb[ks][0]), f1 = unpack_half2(pb[ks][1]);
-            ls += (f0.x + f0.y) + (f1.x + f1.y);
+            for (int i = 0; i < KT; ++i) {
+                o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+                const uint8_t *qrow = qs + (gb * D + i * 16 + tq) * 2;
+                qf[i][0] = live ? *reinterpret_cast<const uint32_t *>(qrow) : 0u;
+                qf[i][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16) : 0u;
+            }
         }
-        l_run = l_run * alpha + ls;
-        m_run = m_new;
-        const float a0 = __shfl_sync(~0u, alpha, (lane & 3) * 8);
-        const float a1 = __shfl_sync(~0u, alpha, (lane & 3) * 8 + 4);
+        if (t0 < valid) {
+            if (t0 + 16 > valid) {
+                // rows of this tile past the unit's end: zero V so that
+                // zero weights never meet stale or NaN rows
+                const int r_lo = valid, nrow = t0 + 16 - valid;
+                for (int idx = lane; idx < nrow * SLABS * 8; idx += 32) {
+                    const int r = r_lo + idx / (SLABS * 8), c = idx % (SLABS * 8);
+                    *reinterpret_cast<uint4 *>(sp + KV_BYTES + (r / BOX) * PAGE_BYTES +
+                                               (c >> 3) * (BOX * 128) + (r % BOX) * 128 +
+                                               (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // S^T[16 tokens x 8 heads] = K[tile] . Q^T
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int tok = t0 + r8 + (mi & 1) * 8;
+                const uint32_t rowaddr = sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                const int sw = tok & 7;
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            o[i][0] *= a0;
-            o[i][1] *= a1;
-            o[i][2] *= a0;
-            o[i][3] *= a1;
-        }
-
-        // ---- O^T[this warp's D/NC rows x 8 heads] += V^T . P^T
-        {
-            const int mi = lane >> 3, r = lane & 7;
+                for (int kk = 0; kk < KT; ++kk) {
+                    const int dim = kk * 16 + (mi >> 1) * 8;
+                    const uint32_t addr =
+                        rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(addr, a0, a1, a2, a3);
+                    if (kk & 1)
+                        mma_16816(c1, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                    else
+                        mma_16816(c0, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                }
+            }
+            const float sc = p.scale_log2;
+            const bool va = t0 + gb < valid, vb = t0 + gb + 8 < valid;
+            const float x0 = va ? (c0[0] + c1[0]) * sc : -INFINITY;  // token gb,   head tq
+            const float x1 = va ? (c0[1] + c1[1]) * sc : -INFINITY;  // token gb,   head tq+1
+            const float x2 = vb ? (c0[2] + c1[2]) * sc : -INFINITY;  // token gb+8, head tq
+            const float x3 = vb ? (c0[3] + c1[3]) * sc : -INFINITY;  // token gb+8, head tq+1
+            // ---- one online-softmax step over the tile (token 0 of the tile is valid,
+            // so every column max is finite)
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int tok = ks * 16 + r + (mi >> 1) * 8;
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const uint32_t pa = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // P[gb][tq..tq+1]
+            const uint32_t pb = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // P[gb+8][..]
+            const float2 fa = unpack_half2(pa), fb = unpack_half2(pb);
+            l0 = l0 * al0 + (fa.x + fb.x);
+            l1 = l1 * al1 + (fa.y + fb.y);
+#pragma unroll
+            for (int i = 0; i < KT; ++i) {
+                o[i][0] *= al0;
+                o[i][1] *= al1;
+                o[i][2] *= al0;
+                o[i][3] *= al1;
+            }
+            // P^T as the B operand of O^T += V^T . P^T: register transpose
+            const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
+            {
+                const int tok = t0 + r8 + (mi >> 1) * 8;
                 const int sw = tok & 7;
                 const uint32_t rowaddr =
                     sb + KV_BYTES + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
 #pragma unroll
-                for (int i = 0; i < MT; ++i) {
-                    const int dim = (w * MT + i) * 16 + (mi & 1) * 8;
+                for (int i = 0; i < KT; ++i) {
+                    const int dim = i * 16 + (mi & 1) * 8;
                     const uint32_t addr =
                         rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
                     uint32_t v0, v1, v2, v3;
                     ldsm_x4_t(addr, v0, v1, v2, v3);
-                    mma_16816(o[i], v0, v1, v2, v3, pb[ks][0], pb[ks][1]);
+                    mma_16816(o[i], v0, v1, v2, v3, b0, b1);
                 }
             }
         }
+
+        if (!(flags & kLast)) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&empty_bar[slot]));
+            continue;
+        }
+
+        // ---- end of the unit: merge the NC warps' states through this
+        // stage's shared memory (still held), then write the output row or
+        // the partition partial, then release the stage.
+        float *mg_m = reinterpret_cast<float *>(sp);            // [NC][8]
+        float *mg_l = mg_m + NC * kMaxGroup;                     // [NC][8]
+        float *mg_o = mg_l + NC * kMaxGroup;                     // [NC][8][OST]
+        float lt0 = l0, lt1 = l1;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            lt0 += __shfl_xor_sync(~0u, lt0, off);
+            lt1 += __shfl_xor_sync(~0u, lt1, off);
+        }
+        if (!consumers_sync())  // every warp is done reading the stage
+            break;
+        if (gb == 0) {
+            mg_m[w * kMaxGroup + tq] = m0;
+            mg_m[w * kMaxGroup + tq + 1] = m1;
+            mg_l[w * kMaxGroup + tq] = lt0;
+            mg_l[w * kMaxGroup + tq + 1] = lt1;
+        }
+        {
+            float *ow = mg_o + w * kMaxGroup * OST;
+#pragma unroll
+            for (int i = 0; i < KT; ++i) {
+                const int d = i * 16 + gb;
+                ow[tq * OST + d] = o[i][0];
+                ow[(tq + 1) * OST + d] = o[i][1];
+                ow[tq * OST + d + 8] = o[i][2];
+                ow[(tq + 1) * OST + d + 8] = o[i][3];
+            }
+        }
+        if (!consumers_sync())  // all states written
+            break;
+        {
+            const int G = p.G;
+            const bool direct = flags & kDirect;
+            for (int idx = threadIdx.x; idx < G * (D / 4); idx += NC * 32) {
+                const int g = idx / (D / 4), d4 = idx % (D / 4);
+                float M = -INFINITY;
+#pragma unroll
+                for (int wi = 0; wi < NC; ++wi)
+                    M = fmaxf(M, mg_m[wi * kMaxGroup + g]);
+                float den = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int wi = 0; wi < NC; ++wi) {
+                    const float scw = ex2(mg_m[wi * kMaxGroup + g] - M);
+                    den += scw * mg_l[wi * kMaxGroup + g];
+                    const float4 v =
+                        *reinterpret_cast<const float4 *>(mg_o + (wi * kMaxGroup + g) * OST + 4 * d4);
+                    acc.x += scw * v.x;
+                    acc.y += scw * v.y;
+                    acc.z += scw * v.z;
+                    acc.w += scw * v.w;
+                }
+                const float inv = 1.f / den;
+                const size_t h = (size_t)hs * p.Hq + hg * G + g;
+                float4 *dst = direct
+                                  ? reinterpret_cast<float4 *>(p.out + h * D)
+                                  : reinterpret_cast<float4 *>(p.ws_o + (h * p.NPmax + hp) * D);
+                dst[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (!direct && d4 == 0) {
+                    p.ws_m[h * p.NPmax + hp] = M;
+                    p.ws_l[h * p.NPmax + hp] = den;
+                }
+            }
+        }
+        if (!consumers_sync())  // every warp is done with the merge buffer
+            break;
+        fence_proxy_async_smem();  // generic writes to the stage before its next copies
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&empty_bar[slot]));
-
-        if (flags & kLast) {
-            float lt = l_run + __shfl_xor_sync(~0u, l_run, 1);
-            lt += __shfl_xor_sync(~0u, lt, 2);
-            const float l0 = __shfl_sync(~0u, lt, (lane & 3) * 8);
-            const float l1 = __shfl_sync(~0u, lt, (lane & 3) * 8 + 4);
-            const float i0 = 1.f / l0, i1 = 1.f / l1;
-            const int h0 = hg * p.G + tq;
-            float *dst;
-            size_t hstride;
-            if (flags & kDirect) {
-                dst = p.out + ((size_t)hs * p.Hq + h0) * D;
-                hstride = D;
-            } else {
-                dst = p.ws_o + (((size_t)hs * p.Hq + h0) * p.NPmax + hp) * D;
-                hstride = (size_t)p.NPmax * D;
-            }
-#pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                const int d = (w * MT + i) * 16 + gb;
-                if (tq < p.G) {
-                    dst[d] = o[i][0] * i0;
-                    dst[d + 8] = o[i][2] * i0;
-                }
-                if (tq + 1 < p.G) {
-                    dst[hstride + d] = o[i][1] * i1;
-                    dst[hstride + d + 8] = o[i][3] * i1;
-                }
-            }
-            if (!(flags & kDirect) && w == 0 && (lane & 3) == 0 && gb < p.G) {
-                const size_t idx = ((size_t)hs * p.Hq + hg * p.G + gb) * p.NPmax + hp;
-                p.ws_m[idx] = m_run;
-                p.ws_l[idx] = lt;
-            }
-        }
     }
 }
 
@@ -526,6 +632,8 @@ __global__ void __launch_bounds__(kReduceThreads)
     float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)sh * D);
     const int np = (L + p.P - 1) / p.P;
     griddep_wait();
+    if (sh == 0 && threadIdx.x == 0 && p.counter)
+        *p.counter = 0;  // the partition kernel is done with it: ready for the next call
     if (L == 0) {
         for (int i = threadIdx.x; i < V4; i += kReduceThreads)
             o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -633,13 +741,32 @@ __global__ void __launch_bounds__(kReduceThreads)
 }
 
 // ---------------------------------------------------------------- launch
+// Raises the partition kernel's dynamic shared-memory limit, once per
+// device and instantiation.
+template <int D, int BS, bool TRACE>
+cudaError_t ensure_smem_attribute()
+{
+    static std::atomic<unsigned long long> done{0};  // bit per device ordinal < 64
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem_bytes<D>());
+    if (e == cudaSuccess)
+        done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 template <int D, int BS, bool TRACE>
 cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv,
                                const DecodeParams &p, const LaunchConfig &lc)
 {
     auto kern = paged_gqa_partial_kernel<D, BS, TRACE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)dyn_smem_bytes<D>());
+    cudaError_t e = ensure_smem_attribute<D, BS, TRACE>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -669,8 +796,7 @@ template <int D, int BS>
 cudaError_t occupancy_impl(int *ctas)
 {
     auto kern = paged_gqa_partial_kernel<D, BS, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)dyn_smem_bytes<D>());
+    cudaError_t e = ensure_smem_attribute<D, BS, false>();
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, (Shape<D>::NC + 1) * 32,

@@ -151,3 +151,34 @@ def test_streams_and_empty_batch():
     pgd.paged_gqa_decode(e, w.q[:0], w.k_cache, w.v_cache, w.block_tables[:0], w.seq_lens[:0],
                          w.scale, 512)
     torch.cuda.synchronize()
+
+
+def test_repeated_full_calls_identical():
+    """Units are claimed dynamically, so which CTA computes what changes from
+    call to call; the result must not (and must match the oracle)."""
+    w = make_workload("batch_decode", device=DEV)
+    ref = oracle_out(w)
+    first = run(w)
+    assert_parity(first.cpu().numpy(), ref, "batch_decode call 0")
+    for i in range(4):
+        again = run(w)
+        assert torch.equal(first, again), f"call {i + 1} differs"
+
+
+def test_concurrent_streams_match_serial():
+    """Calls on two streams at once use separate claim counters."""
+    wa = make_workload("batch_decode", device=DEV, S=48, seed=31)
+    wb = make_workload("ragged_tails", device=DEV, S=64, seed=32)
+    ra, rb = run(wa), run(wb)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        oa = torch.full_like(ra, float("nan"))
+        ob = torch.full_like(rb, float("nan"))
+        torch.cuda.synchronize()
+        for _ in range(2):  # interleave launches on the two streams
+            pgd.paged_gqa_decode(oa, wa.q, wa.k_cache, wa.v_cache, wa.block_tables,
+                                 wa.seq_lens, wa.scale, wa.P, stream=sa)
+            pgd.paged_gqa_decode(ob, wb.q, wb.k_cache, wb.v_cache, wb.block_tables,
+                                 wb.seq_lens, wb.scale, wb.P, stream=sb)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ra) and torch.equal(ob, rb)

@@ -48,7 +48,7 @@ def test_noalloc_matches_default_on_consecutive_calls(lib):
              (make_workload("batch_decode", device=DEV, S=40, seed=22), 512)]
     for w, P in cases:
         _, need = pgd.pgd_plan(w.S, w.Hq, w.Hkv, w.D, w.BS, P, w.MB)
-        assert 0 < need <= pgd.NOALLOC_SCRATCH_BYTES
+        assert 0 < need <= pgd.NOALLOC_SCRATCH_BYTES - 256
         ref = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
         pgd.paged_gqa_decode(ref, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
                              w.scale, P)
