@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # partition kernel from one ncu capture (profiles/), valid only for the
 # kernel sources they were taken on (hash of csrc/ below).
 TRAFFIC = {
-    "cb551b807428031d": {("batch_decode", 512): 633_336_576 + 5_317_120},
+    "5b2a9b24854f33e7": {("batch_decode", 512): 633_325_568 + 5_516_800},
 }
 
 
@@ -306,22 +306,29 @@ def run_ours(args):
     value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers: per step the
-    # step's inputs (q, block_tables, seq_lens) go host->device from pinned
-    # memory and the output comes back; the K/V cache stays resident.
-    q_h = w.q.cpu().pin_memory()
-    bt_h = w.block_tables.cpu().pin_memory()
-    sl_h = w.seq_lens.cpu().pin_memory()
+    # step's inputs (q, block_tables, seq_lens, packed in one pinned buffer)
+    # go host->device in one copy and the output comes back; the K/V cache
+    # stays resident, as it does in a decode loop.
+    def _align(n):
+        return (n + 255) // 256 * 256
+    nq, nbt, nsl = w.q.numel() * 2, w.block_tables.numel() * 4, w.seq_lens.numel() * 4
+    oq, obt, osl = 0, _align(nq), _align(nq) + _align(nbt)
+    nin = osl + nsl
+    h_in = torch.empty(nin, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nin, dtype=torch.uint8, device=dev)
+    h_in[oq:oq + nq].view(torch.float16).copy_(w.q.cpu().view(-1))
+    h_in[obt:obt + nbt].view(torch.int32).copy_(w.block_tables.cpu().view(-1))
+    h_in[osl:osl + nsl].view(torch.int32).copy_(w.seq_lens.cpu().view(-1))
+    q_d = d_in[oq:oq + nq].view(torch.float16).view(w.q.shape)
+    bt_d = d_in[obt:obt + nbt].view(torch.int32).view(w.block_tables.shape)
+    sl_d = d_in[osl:osl + nsl].view(torch.int32).view(w.seq_lens.shape)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d, bt_d, sl_d = torch.empty_like(w.q), torch.empty_like(w.block_tables), torch.empty_like(
-        w.seq_lens)
-    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    h2d = nq + nbt + nsl
     d2h = out_h.numel() * 4
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         pgd.paged_gqa_decode(out, q_d, w.k_cache, w.v_cache, bt_d, sl_d, w.scale, P,
                              stream=stream)
         out_h.copy_(out, non_blocking=True)
