@@ -136,6 +136,27 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x across the ranks (the slowest rank's time).  Uses
+    the process group's backend: a CUDA tensor for nccl, a CPU one for gloo."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(kv_bytes_per_rank: int, local_ms_per_step: float, world: int,
+                       device=None) -> tuple:
+    """(GB/s of the whole job, ms per step of the slowest rank) for N
+    independent replicas each doing kv_bytes_per_rank per step."""
+    ms = max_over_ranks(local_ms_per_step, world, device)
+    return world * kv_bytes_per_rank / (ms * 1e-3) / 1e9, ms
+
+
 def oracle_time(w, seqs, min_seconds=10.0, max_reps=50):
     """Times the CPU oracle on the listed sequences; returns
     (seconds per rep, KV bytes per rep, threads, reps)."""
@@ -257,12 +278,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     peak, peak_kind = measured_peaks()
 
@@ -299,11 +314,10 @@ def run_ours(args):
         barrier()
         pgd.pgd_set_timing_events(None, None)
     clocks = clk.summary()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1))
-    ms_per_step = elapsed_ms / args.steps
-    ms_instrumented = max_over_ranks(ev2.elapsed_time(ev3)) / args.steps
+    value, ms_per_step = replica_throughput(kv_bytes, ev0.elapsed_time(ev1) / args.steps, world,
+                                            dev)
+    ms_instrumented = max_over_ranks(ev2.elapsed_time(ev3) / args.steps, world, dev)
     kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(args.steps))
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers: per step the
     # step's inputs (q, block_tables, seq_lens, packed in one pinned buffer)
@@ -341,8 +355,9 @@ def run_ours(args):
     for _ in range(e2e_steps):
         e2e_step()
     barrier()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps)
-    e2e_value = world * kv_bytes / e2e_s / 1e9
+    e2e_value, e2e_ms = replica_throughput(kv_bytes, (time.perf_counter() - t0) / e2e_steps * 1e3,
+                                           world, dev)
+    e2e_s = e2e_ms * 1e-3
 
     # ---- CPU baseline: the oracle on this host (rank 0, N == 1 only)
     cpu = None

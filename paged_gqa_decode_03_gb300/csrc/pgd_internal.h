@@ -86,6 +86,9 @@ cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk
 cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
 cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
 
-constexpr int kReduceThreads = 128;  // reduce kernel: one CTA per (sequence, query head)
+// Reduce kernel: one CTA per (sequence, query head); two warps suffice for
+// head_dim 128 (whose workloads have at most 16 partitions per sequence) and
+// keep every CTA resident at once, four for 256.
+template <int D> __host__ __device__ constexpr int reduce_threads() { return D == 128 ? 64 : 128; }
 
 }  // namespace pgd

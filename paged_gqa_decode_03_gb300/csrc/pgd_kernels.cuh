@@ -603,7 +603,8 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     }
 }
 
-// One CTA of four warps per (sequence, query head): merges the partials of
+// One CTA (two warps for head_dim 128, four for 256) per (sequence, query
+// head): merges the partials of
 // its partitions, out = sum_i w_i o_i / sum_i w_i with
 // w_i = l_i * exp2(m_i - max m); zeros for empty sequences; nothing for
 // single-partition sequences (written by the partition kernel).  The length
@@ -611,9 +612,10 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
 // loads the (max, exp-sum) of its pieces lane-parallel and the rows of the
 // non-empty ones several at a time.
 template <int D>
-__global__ void __launch_bounds__(kReduceThreads)
+__global__ void __launch_bounds__(reduce_threads<D>())
     paged_gqa_reduce_kernel(const DecodeParams p, int max_len)
 {
+    constexpr int kReduceThreads = reduce_threads<D>();
     constexpr int NW = kReduceThreads / 32;
     constexpr int V4 = D / 4;       // float4 per row
     constexpr int PL = V4 / 32;     // float4 per lane
@@ -785,7 +787,7 @@ cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3(lc.reduce_blocks);
-    rcfg.blockDim = dim3(kReduceThreads);
+    rcfg.blockDim = dim3(reduce_threads<D>());
     rcfg.stream = lc.stream;
     rcfg.attrs = attr;
     rcfg.numAttrs = 1;
