@@ -156,6 +156,30 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
                                int32_t *page_trace, void *stream);
 
 /*
+ * paged_gqa_decode_append — the KV-cache append of the decode step fused
+ * with the decode: for every sequence s with seq_lens[s] = L >= 1, the newest
+ * token's key and value, k_new[s][kv_head][:] and v_new[s][kv_head][:], are
+ * written into the cache at token L-1 (row (L-1) % block_size of physical
+ * page block_tables[s][(L-1) / block_size], which the caller has allocated),
+ * and the decode then attends over all L tokens, the newest one included.
+ * One launch: the newest row is taken from k_new / v_new while its page is
+ * staged, and written to the cache for the next steps.  (The step before the
+ * decode path; "voxtral.c", "Next steps", plans a further fusion of its RoPE-K
+ * and KV-cache write path.)
+ *
+ * k_new, v_new  [num_seqs][num_kv_heads][head_dim] fp16, device, 16-byte
+ *               aligned.  Sequences of length 0 append nothing.
+ * k_cache, v_cache are written (one row per sequence and KV head); all other
+ * arguments as for paged_gqa_decode, whose scratch handling it shares.
+ */
+pgd_status paged_gqa_decode_append(float *out, const uint16_t *q, const uint16_t *k_new,
+                                   const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache,
+                                   const int32_t *block_tables, const int32_t *seq_lens,
+                                   float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int partition_size,
+                                   int max_blocks_per_seq, int num_blocks, void *stream);
+
+/*
  * paged_gqa_decode_noalloc — paged_gqa_decode that allocates nothing.
  * (No counterpart on the pages: this entry point exists for callers, not
  * for the method.)

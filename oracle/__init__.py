@@ -15,6 +15,8 @@ Routines (all fp64):
   split_partials  per-partition (max, exp-sum, normalised output) partials
   merge_partials  the split-KV reduce of those partials
   page_reads      the physical pages the method must read, per KV head
+  append_kv       the decode step's KV-cache append (newest token's row)
+  decode_append   append_kv on copies of the caches, then decode
   half_to_double  IEEE binary16 decoding
 """
 from __future__ import annotations
@@ -79,6 +81,8 @@ def _load():
         lib.oracle_merge_partials.restype = I
         lib.oracle_page_reads.argtypes = [P] * 3 + [I] * 5
         lib.oracle_page_reads.restype = I
+        lib.oracle_append_kv.argtypes = [P] * 6 + [I] * 6
+        lib.oracle_append_kv.restype = I
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = I
         _lib = lib
@@ -207,3 +211,25 @@ def page_reads(block_tables, seq_lens, num_kv_heads, block_size, num_blocks):
     _check(lib.oracle_page_reads(_ptr(reads), _ptr(bt), _ptr(sl), S, int(num_kv_heads),
                                  int(block_size), MB, int(num_blocks)))
     return reads
+
+
+def append_kv(k_cache, v_cache, k_new, v_new, block_tables, seq_lens):
+    """Writes k_new / v_new [S, Hkv, D] at token seq_lens[s] - 1 of each
+    sequence into copies of the caches; returns the new (k_cache, v_cache)."""
+    lib = _load()
+    k = _u16(k_cache).copy()
+    v = _u16(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    NB, Hkv, BS, D = k.shape
+    S, MB = bt.shape
+    _check(lib.oracle_append_kv(_ptr(k), _ptr(v), _ptr(kn), _ptr(vn), _ptr(bt), _ptr(sl), S,
+                                Hkv, D, BS, MB, NB))
+    return k.view(np.float16), v.view(np.float16)
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, scale,
+                  threads=None):
+    """The decode step with its KV-cache append: append_kv, then decode."""
+    k, v = append_kv(k_cache, v_cache, k_new, v_new, block_tables, seq_lens)
+    return decode(q, k, v, block_tables, seq_lens, scale, threads)

@@ -412,6 +412,37 @@ int oracle_page_reads(int32_t *reads, const int32_t *block_tables, const int32_t
     return ORC_OK;
 }
 
+/*
+ * KV-cache append of a decode step: for every sequence s with L = seq_lens[s]
+ * >= 1 and every KV head g, the newest token's key and value (k_new, v_new:
+ * [S][Hkv][D]) are written at token L-1, i.e. row (L-1) % BS of physical page
+ * block_tables[s][(L-1) / BS] (the page-table mapping of "vllm-metal", "What
+ * is Paged Attention").  The caches are modified in place.  Sequences of
+ * length 0 append nothing.
+ */
+int oracle_append_kv(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                     const uint16_t *v_new, const int32_t *block_tables, const int32_t *seq_lens,
+                     int S, int Hkv, int D, int BS, int MB, int NB)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hkv, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    for (int s = 0; s < S; ++s) {
+        long L = seq_lens[s];
+        if (L == 0)
+            continue;
+        int32_t pp = block_tables[(long)s * MB + (L - 1) / BS];
+        for (int g = 0; g < Hkv; ++g) {
+            long row = ((long)pp * Hkv + g) * BS + (L - 1) % BS;
+            for (int d = 0; d < D; ++d) {
+                k_cache[row * D + d] = k_new[((long)s * Hkv + g) * D + d];
+                v_cache[row * D + d] = v_new[((long)s * Hkv + g) * D + d];
+            }
+        }
+    }
+    return ORC_OK;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -26,7 +26,8 @@ import threading
 
 import torch
 
-__all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc", "pgd_plan", "pgd_last_partition_size",
+__all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
+           "paged_gqa_decode_append", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -45,6 +46,7 @@ SIGNATURES = {
     "paged_gqa_decode": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_ex": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
     "paged_gqa_decode_noalloc": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
+    "paged_gqa_decode_append": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -162,6 +164,25 @@ def paged_gqa_decode_ex(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
                                  _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv,
                                  D, BS, int(partition_size), MB, NB, _ptr(workspace), ws_bytes,
                                  _ptr(page_trace), _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def paged_gqa_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                            scale, partition_size: int = 0, stream=None) -> None:
+    """Writes each sequence's newest K/V row (k_new, v_new: fp16 [num_seqs,
+    num_kv_heads, head_dim]) into the cache at token seq_lens[s] - 1, then
+    decodes over all seq_lens[s] tokens, in one launch."""
+    lib = load_library()
+    S, Hq, Hkv, D, BS, MB, NB = _sizes(out, q, k_cache, v_cache, block_tables, seq_lens)
+    _check(k_new, "k_new", torch.float16, 3)
+    _check(v_new, "v_new", torch.float16, 3)
+    if tuple(k_new.shape) != (S, Hkv, D) or tuple(v_new.shape) != (S, Hkv, D):
+        raise ValueError(f"k_new / v_new must be [{S}, {Hkv}, {D}]")
+    st = lib.paged_gqa_decode_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                     _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     _ptr(seq_lens), float(scale), S, Hq, Hkv, D, BS,
+                                     int(partition_size), MB, NB,
+                                     _stream_handle(stream, q.device))
     _raise(st)
 
 

@@ -404,7 +404,8 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
                const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
                int Hkv, int D, int BS, int P, int MB, int NB, void *workspace, size_t ws_bytes,
                bool own_workspace, int32_t *page_trace, void *stream_v,
-               unsigned *counter = nullptr)
+               unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
+               const uint16_t *v_new = nullptr)
 {
     if (S == 0) {  // nothing to read or write: only the sizes are checked
         Plan plan;
@@ -506,6 +507,10 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.ws_o = partials ? reinterpret_cast<float *>(ws + plan.off_o) : nullptr;
     p.page_trace = page_trace;
     p.counter = counter;
+    p.k_new = reinterpret_cast<const __half *>(k_new);
+    p.v_new = reinterpret_cast<const __half *>(v_new);
+    p.k_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(k_cache));
+    p.v_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(v_cache));
     p.err = ds->err_word;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e) folded into the scale
     p.S = S;
@@ -601,6 +606,22 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
                num_blocks, workspace, workspace_bytes, false, page_trace, stream);
+}
+
+pgd_status paged_gqa_decode_append(float *out, const uint16_t *q, const uint16_t *k_new,
+                                   const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache,
+                                   const int32_t *block_tables, const int32_t *seq_lens,
+                                   float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int partition_size,
+                                   int max_blocks_per_seq, int num_blocks, void *stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(PGD_ERR_INVALID_ARG, "null k_new / v_new");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(PGD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, nullptr, 0, true, nullptr, stream, nullptr, k_new, v_new);
 }
 
 pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_t *k_cache,

@@ -63,6 +63,10 @@ struct DecodeParams {
     int32_t *page_trace;          // [S][Hkv][MB] or null
     unsigned *counter;            // work-claim counter: 0 at launch, reset by the reduce
     unsigned *err;                // device error word
+    const __half *k_new;          // [S][Hkv][D] newest token's K (fused append) or null
+    const __half *v_new;          // [S][Hkv][D] newest token's V
+    __half *k_cache;              // caches, written at the newest token's row (append)
+    __half *v_cache;
     float scale_log2;             // scale * log2(e)
     int S, Hq, Hkv, G, P, logP, MB, NB, NPmax;
     uint64_t wait_budget_ns;

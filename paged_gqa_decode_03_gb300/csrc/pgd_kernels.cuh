@@ -35,11 +35,13 @@
 namespace pgd {
 
 // Stage flags: first / last stage of a unit; the sequence has one partition
-// (its output is written directly); end of work.
-enum : int { kFirst = 1, kLast = 2, kDirect = 4, kTerm = 8 };
+// (its output is written directly); the stage holds the sequence's newest
+// token, whose K/V come from k_new / v_new (fused append); end of work.
+enum : int { kFirst = 1, kLast = 2, kDirect = 4, kAppend = 16, kTerm = 32 };
 
 struct StageHeader {
-    int s, g, p, valid, flags, pad;
+    int s, g, p, valid, flags;
+    int app_row;  // kAppend: row of the newest token in the [NB*Hkv*BS][D] cache view, -1: none
 };
 
 template <int D, int BS, bool TRACE>
@@ -187,6 +189,9 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             const int pg0 = tok0 / BS;
             const int nst = (n + T - 1) / T;
             const int fixed = L <= P ? kDirect : 0;
+            // fused append: the stage holding token L-1 (last stage of the
+            // last partition) carries it
+            const bool app_unit = p.k_new != nullptr && pi == (L - 1) / P;
             for (int st = 0; st < nst; ++st, ++k) {
                 if (claimed < 0 && nst - st <= 2)
                     claim();
@@ -210,12 +215,23 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 }
                 const uint32_t sb = ring + slot * STAGE;
                 const uint32_t fb = smem_addr(&full_bar[slot]);
+                // fused append: cache row of token L-1 (its page is the unit's
+                // page (L-1)/BS - pg0), published with the header
+                int app_row = -1;
+                if (app_unit && st == nst - 1) {
+                    const int ja = (L - 1) / BS - pg0;
+                    const int ida = __shfl_sync(~0u, ja < 32 ? id0 : id1, ja & 31);
+                    if ((unsigned)ida < (unsigned)p.NB)
+                        app_row = (ida * Hkv + g) * BS + (L - 1) % BS;
+                }
                 if (lane == 0) {
                     hdr[slot].s = s;
                     hdr[slot].g = g;
                     hdr[slot].p = pi;
                     hdr[slot].valid = valid;
-                    hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0);
+                    hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
+                                      (app_unit && st == nst - 1 ? kAppend : 0);
+                    hdr[slot].app_row = app_row;
                     const uint32_t bytes = pc * PAGE_BYTES * 2 + (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
@@ -232,6 +248,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         }
                         if (TRACE)
                             p.page_trace[((size_t)s * Hkv + g) * MB + pg0 + j] = id;
+
                         // one copy per page for K and one for V: BOX rows x D
                         // halves, landing as [slab][row][128 B] (swizzled)
                         const uint32_t dk = sb + jj * PAGE_BYTES;
@@ -449,6 +466,28 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     *reinterpret_cast<uint4 *>(sp + KV_BYTES + (r / BOX) * PAGE_BYTES +
                                                (c >> 3) * (BOX * 128) + (r % BOX) * 128 +
                                                (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            if ((flags & kAppend) && valid - 1 >= t0 && valid - 1 < t0 + 16) {
+                // fused append: the newest token (row valid-1 of the stage,
+                // in this warp's tile) takes its K and V from k_new / v_new,
+                // in the staged page (same 128-byte swizzle as the copies)
+                // and in the cache for the next steps
+                const int r = valid - 1;
+                const int app_row = hdr[slot].app_row;
+                const size_t src = ((size_t)hs * p.Hkv + hg) * D;
+                for (int c = lane; c < D / 8; c += 32) {
+                    const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + src + c * 8);
+                    const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src + c * 8);
+                    const int off = (r / BOX) * PAGE_BYTES + (c >> 3) * (BOX * 128) +
+                                    (r % BOX) * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sp + off) = kv;
+                    *reinterpret_cast<uint4 *>(sp + KV_BYTES + off) = vv;
+                    if (app_row >= 0) {
+                        *reinterpret_cast<uint4 *>(p.k_cache + (size_t)app_row * D + c * 8) = kv;
+                        *reinterpret_cast<uint4 *>(p.v_cache + (size_t)app_row * D + c * 8) = vv;
+                    }
                 }
                 __syncwarp();
             }

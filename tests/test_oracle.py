@@ -303,3 +303,61 @@ def test_rejects_bad_inputs():
     bt = inp["block_tables"].copy()
     bt[2, 1:] = -5                        # entries past the last page are not read
     oracle.decode(**{**inp, "block_tables": bt}, scale=w.scale)
+
+
+# ---------------------------------------------------------------- KV-cache append
+def _new_kv(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    kn = torch.randn((w.S, w.Hkv, w.D), generator=g).to(torch.float16).numpy()
+    vn = torch.randn((w.S, w.Hkv, w.D), generator=g).to(torch.float16).numpy()
+    return kn, vn
+
+
+def test_append_writes_only_the_newest_rows():
+    w = _small(seed=21, lens=(0, 1, 8, 13), BS=4)
+    kn, vn = _new_kv(w, 1)
+    inp = _np(w)
+    k2, v2 = oracle.append_kv(inp["k_cache"], inp["v_cache"], kn, vn, inp["block_tables"],
+                              inp["seq_lens"])
+    expect_k = inp["k_cache"].view(np.uint16).copy()
+    expect_v = inp["v_cache"].view(np.uint16).copy()
+    for s in range(w.S):          # where the generator placed token L-1
+        L = int(w.lens[s])
+        if L == 0:
+            continue
+        page = int(w.page_ids[w.page_offsets[s] + (L - 1) // w.BS])
+        expect_k[page, :, (L - 1) % w.BS] = kn[s].view(np.uint16)
+        expect_v[page, :, (L - 1) % w.BS] = vn[s].view(np.uint16)
+    assert np.array_equal(k2.view(np.uint16), expect_k)
+    assert np.array_equal(v2.view(np.uint16), expect_v)
+
+
+def test_append_then_decode_closed_forms():
+    # L = 1: the output is the appended value; poison in the slot is overwritten
+    w = _small(seed=22, lens=(1, 1, 1), BS=8)
+    inp = _np(w)
+    for s in range(w.S):
+        page = int(w.page_ids[w.page_offsets[s]])
+        inp["k_cache"][page, :, 0] = np.float16("nan")
+        inp["v_cache"][page, :, 0] = np.float16("nan")
+    kn, vn = _new_kv(w, 2)
+    out = oracle.decode_append(inp["q"], kn, vn, inp["k_cache"], inp["v_cache"],
+                               inp["block_tables"], inp["seq_lens"], w.scale)
+    G = w.Hq // w.Hkv
+    for s in range(w.S):
+        for h in range(w.Hq):
+            assert np.array_equal(out[s, h], vn[s, h // G].astype(np.float64))
+    # longer: equals the plain decode of caches holding the new rows
+    w = _small(seed=23, lens=(5, 16, 33), BS=4)
+    inp = _np(w)
+    kn, vn = _new_kv(w, 3)
+    k2, v2 = inp["k_cache"].copy(), inp["v_cache"].copy()
+    for s in range(w.S):
+        L = int(w.lens[s])
+        page = int(w.page_ids[w.page_offsets[s] + (L - 1) // w.BS])
+        k2[page, :, (L - 1) % w.BS] = kn[s]
+        v2[page, :, (L - 1) % w.BS] = vn[s]
+    a = oracle.decode_append(inp["q"], kn, vn, inp["k_cache"], inp["v_cache"],
+                             inp["block_tables"], inp["seq_lens"], w.scale)
+    b = oracle.decode(inp["q"], k2, v2, inp["block_tables"], inp["seq_lens"], w.scale)
+    assert np.array_equal(a, b)
