@@ -57,36 +57,83 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    D = ctypes.c_double
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = D
+    lib.oracle_paged_gqa_decode.argtypes = [P] * 6 + [D] + [I] * 8
+    lib.oracle_paged_gqa_decode.restype = I
+    lib.oracle_attention_weights.argtypes = [P] * 5 + [D] + [I] * 9
+    lib.oracle_attention_weights.restype = I
+    lib.oracle_online_log2.argtypes = [P] * 6 + [D] + [I] * 8
+    lib.oracle_online_log2.restype = I
+    lib.oracle_split_partials.argtypes = [P] * 8 + [D] + [I] * 10
+    lib.oracle_split_partials.restype = I
+    lib.oracle_merge_partials.argtypes = [P] * 4 + [I] * 4
+    lib.oracle_merge_partials.restype = I
+    lib.oracle_page_reads.argtypes = [P] * 3 + [I] * 5
+    lib.oracle_page_reads.restype = I
+    lib.oracle_append_kv.argtypes = [P] * 6 + [I] * 6
+    lib.oracle_append_kv.restype = I
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = I
+    return lib
+
+
+_override = threading.local()
+
+
 def _load():
+    """The oracle library: the one built from pgd_oracle.c, or the library
+    selected by ``using()`` on this thread (the tests' planted mistakes)."""
     global _lib
+    lib = getattr(_override, "lib", None)
+    if lib is not None:
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
         build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        I = ctypes.c_int
-        D = ctypes.c_double
-        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
-        lib.oracle_half_to_double.restype = D
-        lib.oracle_paged_gqa_decode.argtypes = [P] * 6 + [D] + [I] * 8
-        lib.oracle_paged_gqa_decode.restype = I
-        lib.oracle_attention_weights.argtypes = [P] * 5 + [D] + [I] * 9
-        lib.oracle_attention_weights.restype = I
-        lib.oracle_online_log2.argtypes = [P] * 6 + [D] + [I] * 8
-        lib.oracle_online_log2.restype = I
-        lib.oracle_split_partials.argtypes = [P] * 8 + [D] + [I] * 10
-        lib.oracle_split_partials.restype = I
-        lib.oracle_merge_partials.argtypes = [P] * 4 + [I] * 4
-        lib.oracle_merge_partials.restype = I
-        lib.oracle_page_reads.argtypes = [P] * 3 + [I] * 5
-        lib.oracle_page_reads.restype = I
-        lib.oracle_append_kv.argtypes = [P] * 6 + [I] * 6
-        lib.oracle_append_kv.restype = I
-        lib.oracle_max_threads.argtypes = []
-        lib.oracle_max_threads.restype = I
-        _lib = lib
-        return lib
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
+        return _lib
+
+
+class using:
+    """Context manager: route this module's functions to another compiled
+    copy of the oracle (a shared library path) on the current thread."""
+
+    def __init__(self, path):
+        self.lib = _bind(ctypes.CDLL(path))
+
+    def __enter__(self):
+        self.prev = getattr(_override, "lib", None)
+        _override.lib = self.lib
+        return self
+
+    def __exit__(self, *exc):
+        _override.lib = self.prev
+
+
+def compile_source(src_text: str, out_path: str) -> str:
+    """Compiles a C source text with the oracle's flags into out_path."""
+    import tempfile
+    with tempfile.NamedTemporaryFile("w", suffix=".c", delete=False) as f:
+        f.write(src_text)
+        c_path = f.name
+    try:
+        subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                        "-fno-fast-math", "-ffp-contract=off", c_path, "-o", out_path, "-lm"],
+                       check=True, capture_output=True)
+    finally:
+        os.unlink(c_path)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _u16(a):

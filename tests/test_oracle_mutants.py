@@ -1,0 +1,119 @@
+"""Mutation test of the oracle's pins: plausible mistakes planted in a copy of
+the oracle's C source (a swapped index, a dropped term, a wrong operand or
+sign) must each make at least one pin of tests/test_oracle.py fail.
+
+Each mutant is compiled with gcc into a temporary library and its pins run
+in a subprocess (so a mutant that crashes also counts as caught).  Nothing
+here touches the GPU; the real oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+# (name, text in pgd_oracle.c, replacement, replace every occurrence?)
+MUTANTS = [
+    ("page index takes t % BS", "MB + t / BS];", "MB + t % BS];", False),
+    ("row within the page takes t / BS", "* BS + t % BS;", "* BS + t / BS;", False),
+    ("K read with KV head h % Hkv",
+     "    int G = Hq / Hkv;\n    int g = h / G;\n    const uint16_t *qh",
+     "    int G = Hq / Hkv;\n    int g = h % Hkv;\n    const uint16_t *qh", False),
+    ("V read with KV head h % Hkv",
+     "int g = h / G;\n        long L = seq_lens[s];\n        double *o = out + sh * D;",
+     "int g = h % Hkv;\n        long L = seq_lens[s];\n        double *o = out + sh * D;", False),
+    ("scale dropped", "z[t] = scale * dot;", "z[t] = dot;", False),
+    ("q . q instead of q . k",
+     "dot += g_h2d[qh[d]] * g_h2d[kt[d]];\n        z[t]",
+     "dot += g_h2d[qh[d]] * g_h2d[qh[d]];\n        z[t]", False),
+    ("softmax exponent sign flipped", "exp(z[t] - zmax)", "exp(zmax - z[t])", True),
+    ("max taken as min", "if (z[t] > zmax)", "if (z[t] < zmax)", False),
+    ("V read from the K cache",
+     "kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];",
+     "kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];", False),
+    ("partials: log2(e) dropped", "exp2(z[t] * log2e - m)", "exp2(z[t] - m)", True),
+    ("partials: output not normalised",
+     "                o[d] /= l;\n            m_out", "\n            m_out", False),
+    ("reduce: exp-sum weight dropped", "double w = l * exp2(", "double w = exp2(", False),
+    ("reduce: partial outputs unweighted", "o[d] += w * o_in[", "o[d] += o_in[", False),
+    ("online: running sum not rescaled", "l = alpha * l + p;", "l = l + p;", False),
+    ("fp16 exponent bias off by one", "expo - 25", "expo - 24", False),
+    ("page reads one past the end", "j < npages ? block_tables", "j <= npages ? block_tables",
+     False),
+    ("append row off by one", "(L - 1) % BS;", "L % BS;", False),
+]
+
+
+def _pins():
+    import test_oracle as T
+    return [
+        ("half decoding", T.test_half_decoding_matches_numpy),
+        ("hand case 0", lambda: T.test_hand_cases(0)),
+        ("hand case 1", lambda: T.test_hand_cases(1)),
+        ("sdpa 8/2 BS4", lambda: T.test_dense_sdpa_special_case(8, 2, 4)),
+        ("sdpa 6/1 BS8", lambda: T.test_dense_sdpa_special_case(6, 1, 8)),
+        ("length one", T.test_length_one_returns_v),
+        ("constant v", T.test_constant_v),
+        ("weights sum", T.test_weights_sum_to_one),
+        ("scale zero", T.test_scale_zero_gives_mean),
+        ("gqa mapping", T.test_gqa_head_mapping),
+        ("zero length", T.test_zero_length),
+        ("page permutation", T.test_page_permutation_invariance),
+        ("poison", T.test_poison_never_read),
+        ("online", T.test_online_log2_equals_definition),
+        ("split P=7", lambda: T.test_split_invariance(7)),
+        ("split P=100", lambda: T.test_split_invariance(100)),
+        ("merge empty", T.test_merge_skips_empty_partitions),
+        ("append rows", T.test_append_writes_only_the_newest_rows),
+        ("append closed forms", T.test_append_then_decode_closed_forms),
+    ]
+
+
+def _run_pins(lib_path):
+    """Subprocess body: run every pin against the library; print the failures."""
+    sys.path.insert(0, HERE)
+    sys.path.insert(0, ROOT)
+    import oracle
+    failed = []
+    with oracle.using(lib_path):
+        for name, pin in _pins():
+            try:
+                pin()
+            except Exception as e:  # an assertion or the oracle rejecting its own input
+                failed.append(f"{name}: {type(e).__name__}")
+    print("FAILED:" + "|".join(failed))
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    import oracle
+    so = oracle.compile_source(oracle.source_text(), str(tmp_path / "same.so"))
+    r = subprocess.run([sys.executable, __file__, so], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "FAILED:\n" in r.stdout or r.stdout.strip() == "FAILED:", r.stdout
+
+
+@pytest.mark.parametrize("name,find,repl,all_", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, find, repl, all_, tmp_path):
+    import oracle
+    src = oracle.source_text()
+    assert find in src, f"mutation target of '{name}' not found"
+    if not all_:
+        assert src.count(find) >= 1
+    mutated = src.replace(find, repl) if all_ else src.replace(find, repl, 1)
+    assert mutated != src
+    so = oracle.compile_source(mutated, str(tmp_path / "mutant.so"))
+    r = subprocess.run([sys.executable, __file__, so], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    if r.returncode != 0:
+        return  # the mutant crashed the pins: caught
+    line = [l for l in r.stdout.splitlines() if l.startswith("FAILED:")][-1]
+    caught = [x for x in line[len("FAILED:"):].split("|") if x]
+    assert caught, f"mutant '{name}' passed every pin"
+
+
+if __name__ == "__main__":
+    _run_pins(sys.argv[1])
