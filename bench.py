@@ -263,18 +263,32 @@ def run_ours(args):
     out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    k_new = v_new = None
     if args.append:  # the decode step with its fused KV-cache append
         gen = torch.Generator(device=dev).manual_seed(7)
         k_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
         v_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
+    if args.layout != "head_major":
+        # the same caches in another layout, through the strided entry point
+        # (the head-major copy stays for the CPU baseline)
+        strides = pgd.kv_strides(args.layout, w.Hkv, w.BS, w.D)
+        kc = w.k_cache.permute(0, 2, 1, 3).contiguous()
+        vc = w.v_cache.permute(0, 2, 1, 3).contiguous()
 
-        def step():
-            pgd.paged_gqa_decode_append(out, w.q, k_new, v_new, w.k_cache, w.v_cache,
-                                        w.block_tables, w.seq_lens, w.scale, P, stream=stream)
+        def call(q, bt, sl):
+            pgd.paged_gqa_decode_strided(out, q, kc, vc, bt, sl, w.scale, w.Hkv, w.BS, w.NB,
+                                         strides, P, k_new=k_new, v_new=v_new, stream=stream)
+    elif args.append:
+        def call(q, bt, sl):
+            pgd.paged_gqa_decode_append(out, q, k_new, v_new, w.k_cache, w.v_cache, bt, sl,
+                                        w.scale, P, stream=stream)
     else:
-        def step():
-            pgd.paged_gqa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
-                                 w.scale, P, stream=stream)
+        def call(q, bt, sl):
+            pgd.paged_gqa_decode(out, q, w.k_cache, w.v_cache, bt, sl, w.scale, P,
+                                 stream=stream)
+
+    def step():
+        call(w.q, w.block_tables, w.seq_lens)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -352,12 +366,7 @@ def run_ours(args):
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
-        if args.append:
-            pgd.paged_gqa_decode_append(out, q_d, k_new, v_new, w.k_cache, w.v_cache, bt_d,
-                                        sl_d, w.scale, P, stream=stream)
-        else:
-            pgd.paged_gqa_decode(out, q_d, w.k_cache, w.v_cache, bt_d, sl_d, w.scale, P,
-                                 stream=stream)
+        call(q_d, bt_d, sl_d)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -397,7 +406,7 @@ def run_ours(args):
                        "kv_bytes_per_step": kv_bytes, "num_blocks": w.NB,
                        "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
                        "accumulate": "fp32", "parallelism": f"replicas x{world}",
-                       "fused_kv_append": bool(args.append),
+                       "fused_kv_append": bool(args.append), "kv_layout": args.layout,
                        "ms_per_step_with_kernel_events": ms_instrumented},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -428,6 +437,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--append", action="store_true",
                     help="time the decode step with its fused KV-cache append")
+    ap.add_argument("--layout", choices=["head_major", "token_major"], default="head_major",
+                    help="K/V cache layout (token_major runs through paged_gqa_decode_strided)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -43,14 +43,15 @@
  * last page past the sequence end.  A sequence of length 0 gets an all-zero
  * output row.
  *
- * Supported: head_dim in {128, 256}; block_size in {8, 16, 32};
+ * Supported: head_dim in {64, 128, 256}; block_size in {8, 16, 32, 64, 128};
  * num_q_heads % num_kv_heads == 0 with a group of 1..8 query heads per KV
- * head (this covers the four geometries of the pages and any other group of
- * at most 8); partition_size in {256, 512} or 0 to let the library choose.
+ * head (this covers the four geometries of the pages, whose block sizes are
+ * 8/16/32 and head sizes 128/256, and any other group of at most 8);
+ * partition_size in {256, 512} or 0 to let the library choose.  Other cache
+ * layouts than the one above: paged_gqa_decode_strided.
  *
  * Memory: every array is device memory owned by the caller.  q, k_cache and
  * v_cache must be 16-byte aligned; the int32 arrays and out 4-byte aligned.
- * num_blocks * num_kv_heads * block_size must be below 2^31.
  *
  * A call with num_seqs == 0 checks the sizes, does nothing else and may pass
  * null array pointers.
@@ -180,6 +181,39 @@ pgd_status paged_gqa_decode_append(float *out, const uint16_t *q, const uint16_t
                                    int max_blocks_per_seq, int num_blocks, void *stream);
 
 /*
+ * paged_gqa_decode_strided — the decode step over a cache in any layout whose
+ * rows of head_dim halves are contiguous, with every option of the calls
+ * above.  (The pages leave the cache layout open; this is the general form.)
+ *
+ * The row of token r of physical page b, KV head g starts at element
+ *     b * page_stride + g * head_stride + r * token_stride
+ * of k_cache and of v_cache (strides in halves: positive multiples of 8,
+ * token_stride >= head_dim, each below 2^39).  Examples:
+ *   head-major  [num_blocks][num_kv_heads][block_size][head_dim] (the layout of
+ *               paged_gqa_decode): (Hkv*BS*D, BS*D, D)
+ *   token-major [num_blocks][block_size][num_kv_heads][head_dim]:
+ *               (BS*Hkv*D, D, Hkv*D)
+ *   padded pages, or K and V interleaved in one allocation: any larger page
+ *               stride, with k_cache / v_cache pointing at their first rows.
+ * Every (page, head, token) row must lie in memory the caller owns.
+ *
+ * k_new, v_new  NULL for a plain decode, or both given for the fused append of
+ *               paged_gqa_decode_append (rows written at the same strides).
+ * workspace     NULL: library scratch, as paged_gqa_decode; otherwise as for
+ *               paged_gqa_decode_ex, with workspace_bytes.
+ * page_trace    as for paged_gqa_decode_ex (NULL for none).
+ * Other arguments as for paged_gqa_decode.
+ */
+pgd_status paged_gqa_decode_strided(float *out, const uint16_t *q, const uint16_t *k_new,
+                                    const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache,
+                                    const int32_t *block_tables, const int32_t *seq_lens,
+                                    float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int partition_size,
+                                    int max_blocks_per_seq, int num_blocks, int64_t page_stride,
+                                    int64_t head_stride, int64_t token_stride, void *workspace,
+                                    size_t workspace_bytes, int32_t *page_trace, void *stream);
+
+/*
  * paged_gqa_decode_noalloc — paged_gqa_decode that allocates nothing.
  * (No counterpart on the pages: this entry point exists for callers, not
  * for the method.)
@@ -243,7 +277,8 @@ pgd_status pgd_set_timing_events(void *before, void *after);
  * assumes for (head_dim, block_size) on the current device. */
 pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas_per_sm);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch (1.1.0: strided caches,
+ * head_dim 64, block sizes 64 and 128). */
 int pgd_version(void);
 
 #ifdef __cplusplus

@@ -77,6 +77,11 @@ def _bind(lib):
     lib.oracle_page_reads.restype = I
     lib.oracle_append_kv.argtypes = [P] * 6 + [I] * 6
     lib.oracle_append_kv.restype = I
+    Lg = ctypes.c_long
+    lib.oracle_paged_gqa_decode_strided.argtypes = [P] * 6 + [D] + [I] * 7 + [Lg] * 3 + [I]
+    lib.oracle_paged_gqa_decode_strided.restype = I
+    lib.oracle_append_kv_strided.argtypes = [P] * 6 + [I] * 6 + [Lg] * 3
+    lib.oracle_append_kv_strided.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -272,6 +277,48 @@ def append_kv(k_cache, v_cache, k_new, v_new, block_tables, seq_lens):
     S, MB = bt.shape
     _check(lib.oracle_append_kv(_ptr(k), _ptr(v), _ptr(kn), _ptr(vn), _ptr(bt), _ptr(sl), S,
                                 Hkv, D, BS, MB, NB))
+    return k.view(np.float16), v.view(np.float16)
+
+
+def decode_strided(q, k_flat, v_flat, block_tables, seq_lens, scale, num_kv_heads, block_size,
+                   num_blocks, strides, threads=None):
+    """``decode`` over caches given as flat fp16 arrays whose row of token r
+    of page b, KV head g starts at element b*strides[0] + g*strides[1] +
+    r*strides[2]."""
+    lib = _load()
+    q = _u16(q)
+    k, v = _u16(np.ravel(k_flat)), _u16(np.ravel(v_flat))
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, D = q.shape
+    MB = bt.shape[1]
+    Hkv, BS, NB = int(num_kv_heads), int(block_size), int(num_blocks)
+    sp, sh, st = (int(x) for x in strides)
+    last = (NB - 1) * sp + (Hkv - 1) * sh + (BS - 1) * st + D
+    assert last <= k.size and last <= v.size, "strides address rows past the arrays"
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_paged_gqa_decode_strided(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl), float(scale), S, Hq, Hkv, D,
+        BS, MB, NB, sp, sh, st, int(threads or max_threads())))
+    return out
+
+
+def append_kv_strided(k_flat, v_flat, k_new, v_new, block_tables, seq_lens, num_kv_heads,
+                      block_size, num_blocks, strides):
+    """``append_kv`` into copies of flat caches addressed as in
+    ``decode_strided``; returns the new flat (k, v)."""
+    lib = _load()
+    k = _u16(np.ravel(k_flat)).copy()
+    v = _u16(np.ravel(v_flat)).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, MB = bt.shape
+    Hkv, BS, NB = int(num_kv_heads), int(block_size), int(num_blocks)
+    D = kn.shape[2]
+    sp, sh, st = (int(x) for x in strides)
+    last = (NB - 1) * sp + (Hkv - 1) * sh + (BS - 1) * st + D
+    assert last <= k.size and last <= v.size, "strides address rows past the arrays"
+    _check(lib.oracle_append_kv_strided(_ptr(k), _ptr(v), _ptr(kn), _ptr(vn), _ptr(bt),
+                                        _ptr(sl), S, Hkv, D, BS, MB, NB, sp, sh, st))
     return k.view(np.float16), v.view(np.float16)
 
 

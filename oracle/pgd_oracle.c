@@ -30,8 +30,8 @@
  *
  * Layouts (readings where the pages are silent):
  *   q            [S][Hq][D]           IEEE binary16 bit patterns
- *   k_cache      [NB][Hkv][BS][D]     IEEE binary16 bit patterns
- *   v_cache      [NB][Hkv][BS][D]
+ *   k_cache      [NB][Hkv][BS][D]     IEEE binary16 bit patterns (the *_strided
+ *   v_cache      [NB][Hkv][BS][D]      entry points take any row strides)
  *   block_tables [S][MB]              int32 physical page ids
  *   seq_lens     [S]                  int32, 0 <= L <= MB*BS
  *   out          [S][Hq][D]           fp64
@@ -112,18 +112,30 @@ static int check_inputs(const int32_t *block_tables, const int32_t *seq_lens,
     return ORC_OK;
 }
 
+/* Where the rows of a cache array are: the D values of token r of physical
+ * page b, KV head g start at element b*page + g*head + r*token. */
+typedef struct {
+    long page, head, token;
+} kv_strides;
+
+/* The strides of the default layout [NB][Hkv][BS][D]. */
+static kv_strides head_major(int Hkv, int BS, int D)
+{
+    kv_strides x = {(long)Hkv * BS * D, (long)BS * D, (long)D};
+    return x;
+}
+
 /* Address of row t of sequence s, KV head g: page-table lookup
  * (cf-1.com, "What is Paged Attention"). */
-static const uint16_t *kv_row(const uint16_t *cache, const int32_t *block_tables,
-                              int s, long t, int g, int Hkv, int D, int BS, int MB)
+static const uint16_t *kv_row(const uint16_t *cache, kv_strides x, const int32_t *block_tables,
+                              int s, long t, int g, int BS, int MB)
 {
     int32_t pp = block_tables[(long)s * MB + t / BS];
-    long row = ((long)pp * Hkv + g) * BS + t % BS;
-    return cache + row * D;
+    return cache + pp * x.page + g * x.head + (t % BS) * x.token;
 }
 
 /* z_t = scale * sum_d q[d] * k_t[d] for every token t < L of (s, h). */
-static void logits(double *z, const uint16_t *q, const uint16_t *k_cache,
+static void logits(double *z, const uint16_t *q, const uint16_t *k_cache, kv_strides x,
                    const int32_t *block_tables, double scale, int s, int h, long L,
                    int Hq, int Hkv, int D, int BS, int MB)
 {
@@ -131,7 +143,7 @@ static void logits(double *z, const uint16_t *q, const uint16_t *k_cache,
     int g = h / G;
     const uint16_t *qh = q + ((long)s * Hq + h) * D;
     for (long t = 0; t < L; ++t) {
-        const uint16_t *kt = kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+        const uint16_t *kt = kv_row(k_cache, x, block_tables, s, t, g, BS, MB);
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
             dot += g_h2d[qh[d]] * g_h2d[kt[d]];
@@ -144,10 +156,10 @@ static void logits(double *z, const uint16_t *q, const uint16_t *k_cache,
  * w_t = exp(z_t - max z) / sum_u exp(z_u - max z).
  * (Natural exp; equal to the log2/exp2 form of the pages mathematically.)
  */
-int oracle_paged_gqa_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
-                            const uint16_t *v_cache, const int32_t *block_tables,
-                            const int32_t *seq_lens, double scale, int S, int Hq,
-                            int Hkv, int D, int BS, int MB, int NB, int num_threads)
+static int decode(double *out, const uint16_t *q, const uint16_t *k_cache,
+                  const uint16_t *v_cache, kv_strides x, const int32_t *block_tables,
+                  const int32_t *seq_lens, double scale, int S, int Hq, int Hkv, int D, int BS,
+                  int MB, int NB, int num_threads)
 {
     int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
     if (rc)
@@ -172,7 +184,7 @@ int oracle_paged_gqa_decode(double *out, const uint16_t *q, const uint16_t *k_ca
             fail = 1;
             continue;
         }
-        logits(z, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        logits(z, q, k_cache, x, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
         double zmax = -INFINITY;
         for (long t = 0; t < L; ++t)
             if (z[t] > zmax)
@@ -182,13 +194,37 @@ int oracle_paged_gqa_decode(double *out, const uint16_t *q, const uint16_t *k_ca
             den += exp(z[t] - zmax);
         for (long t = 0; t < L; ++t) {
             double w = exp(z[t] - zmax) / den;
-            const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+            const uint16_t *vt = kv_row(v_cache, x, block_tables, s, t, g, BS, MB);
             for (int d = 0; d < D; ++d)
                 o[d] += w * g_h2d[vt[d]];
         }
         free(z);
     }
     return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
+int oracle_paged_gqa_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables,
+                            const int32_t *seq_lens, double scale, int S, int Hq,
+                            int Hkv, int D, int BS, int MB, int NB, int num_threads)
+{
+    return decode(out, q, k_cache, v_cache, head_major(Hkv, BS, D), block_tables, seq_lens,
+                  scale, S, Hq, Hkv, D, BS, MB, NB, num_threads);
+}
+
+/* The definition over caches whose rows sit at the given strides (in
+ * halves; every stride positive). */
+int oracle_paged_gqa_decode_strided(double *out, const uint16_t *q, const uint16_t *k_cache,
+                                    const uint16_t *v_cache, const int32_t *block_tables,
+                                    const int32_t *seq_lens, double scale, int S, int Hq,
+                                    int Hkv, int D, int BS, int MB, int NB, long page_stride,
+                                    long head_stride, long token_stride, int num_threads)
+{
+    if (page_stride <= 0 || head_stride <= 0 || token_stride <= 0)
+        return ORC_BAD_SHAPE;
+    kv_strides x = {page_stride, head_stride, token_stride};
+    return decode(out, q, k_cache, v_cache, x, block_tables, seq_lens, scale, S, Hq, Hkv, D,
+                  BS, MB, NB, num_threads);
 }
 
 /* Attention weights w_t of one (s, h), for the sum-to-one and closed-form
@@ -207,7 +243,8 @@ int oracle_attention_weights(double *w, const uint16_t *q, const uint16_t *k_cac
     long L = seq_lens[s];
     if (L == 0)
         return ORC_OK;
-    logits(w, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+    logits(w, q, k_cache, head_major(Hkv, BS, D), block_tables, scale, s, h, L, Hq, Hkv, D, BS,
+           MB);
     double zmax = -INFINITY;
     for (long t = 0; t < L; ++t)
         if (w[t] > zmax)
@@ -238,6 +275,7 @@ int oracle_online_log2(double *out, const uint16_t *q, const uint16_t *k_cache,
     h2d_init();
     int G = Hq / Hkv;
     const double log2e = 1.0 / log(2.0);
+    kv_strides x = head_major(Hkv, BS, D);
     long pairs = (long)S * Hq;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
     for (long sh = 0; sh < pairs; ++sh) {
@@ -252,8 +290,8 @@ int oracle_online_log2(double *out, const uint16_t *q, const uint16_t *k_cache,
         const uint16_t *qh = q + sh * D;
         double m = -INFINITY, l = 0.0;
         for (long t = 0; t < L; ++t) {
-            const uint16_t *kt = kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);
-            const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+            const uint16_t *kt = kv_row(k_cache, x, block_tables, s, t, g, BS, MB);
+            const uint16_t *vt = kv_row(v_cache, x, block_tables, s, t, g, BS, MB);
             double dot = 0.0;
             for (int d = 0; d < D; ++d)
                 dot += g_h2d[qh[d]] * g_h2d[kt[d]];
@@ -300,6 +338,7 @@ int oracle_split_partials(double *m_out, double *l_out, double *o_out,
     h2d_init();
     int G = Hq / Hkv;
     const double log2e = 1.0 / log(2.0);
+    kv_strides x = head_major(Hkv, BS, D);
     long pairs = (long)S * Hq;
     int fail = 0;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
@@ -321,7 +360,7 @@ int oracle_split_partials(double *m_out, double *l_out, double *o_out,
             fail = 1;
             continue;
         }
-        logits(z, q, k_cache, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        logits(z, q, k_cache, x, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
         long np = (L + P - 1) / P;
         for (long p = 0; p < np; ++p) {
             long t0 = p * P, t1 = t0 + P < L ? t0 + P : L;
@@ -335,7 +374,7 @@ int oracle_split_partials(double *m_out, double *l_out, double *o_out,
             double *o = o_out + (sh * NPmax + p) * D;
             for (long t = t0; t < t1; ++t) {
                 double w = exp2(z[t] * log2e - m);
-                const uint16_t *vt = kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);
+                const uint16_t *vt = kv_row(v_cache, x, block_tables, s, t, g, BS, MB);
                 for (int d = 0; d < D; ++d)
                     o[d] += w * g_h2d[vt[d]];
             }
@@ -420,7 +459,7 @@ int oracle_page_reads(int32_t *reads, const int32_t *block_tables, const int32_t
  * is Paged Attention").  The caches are modified in place.  Sequences of
  * length 0 append nothing.
  */
-int oracle_append_kv(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+static int append_kv(uint16_t *k_cache, uint16_t *v_cache, kv_strides x, const uint16_t *k_new,
                      const uint16_t *v_new, const int32_t *block_tables, const int32_t *seq_lens,
                      int S, int Hkv, int D, int BS, int MB, int NB)
 {
@@ -433,14 +472,35 @@ int oracle_append_kv(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new
             continue;
         int32_t pp = block_tables[(long)s * MB + (L - 1) / BS];
         for (int g = 0; g < Hkv; ++g) {
-            long row = ((long)pp * Hkv + g) * BS + (L - 1) % BS;
+            long row = pp * x.page + g * x.head + ((L - 1) % BS) * x.token;
             for (int d = 0; d < D; ++d) {
-                k_cache[row * D + d] = k_new[((long)s * Hkv + g) * D + d];
-                v_cache[row * D + d] = v_new[((long)s * Hkv + g) * D + d];
+                k_cache[row + d] = k_new[((long)s * Hkv + g) * D + d];
+                v_cache[row + d] = v_new[((long)s * Hkv + g) * D + d];
             }
         }
     }
     return ORC_OK;
+}
+
+int oracle_append_kv(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                     const uint16_t *v_new, const int32_t *block_tables, const int32_t *seq_lens,
+                     int S, int Hkv, int D, int BS, int MB, int NB)
+{
+    return append_kv(k_cache, v_cache, head_major(Hkv, BS, D), k_new, v_new, block_tables,
+                     seq_lens, S, Hkv, D, BS, MB, NB);
+}
+
+/* The append into caches whose rows sit at the given strides (in halves). */
+int oracle_append_kv_strided(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                             const uint16_t *v_new, const int32_t *block_tables,
+                             const int32_t *seq_lens, int S, int Hkv, int D, int BS, int MB,
+                             int NB, long page_stride, long head_stride, long token_stride)
+{
+    if (page_stride <= 0 || head_stride <= 0 || token_stride <= 0)
+        return ORC_BAD_SHAPE;
+    kv_strides x = {page_stride, head_stride, token_stride};
+    return append_kv(k_cache, v_cache, x, k_new, v_new, block_tables, seq_lens, S, Hkv, D, BS,
+                     MB, NB);
 }
 
 int oracle_max_threads(void)

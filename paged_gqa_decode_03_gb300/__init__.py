@@ -27,7 +27,7 @@ import threading
 import torch
 
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
-           "paged_gqa_decode_append", "pgd_plan", "pgd_last_partition_size",
+           "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -42,11 +42,13 @@ DEVERR_PAGE_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
 
 # Every exported symbol of include/pgd.h with its ctypes signature.
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_L = ctypes.c_int64
 SIGNATURES = {
     "paged_gqa_decode": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_ex": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
     "paged_gqa_decode_noalloc": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_append": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P]),
+    "paged_gqa_decode_strided": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_L] * 3 + [_P, _Z, _P, _P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -183,6 +185,77 @@ def paged_gqa_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables
                                      _ptr(seq_lens), float(scale), S, Hq, Hkv, D, BS,
                                      int(partition_size), MB, NB,
                                      _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def kv_strides(layout: str, num_kv_heads: int, block_size: int, head_dim: int):
+    """(page, head, token) strides in halves of a contiguous cache in
+    ``layout``: "head_major" [num_blocks, num_kv_heads, block_size, head_dim]
+    (the layout of ``paged_gqa_decode``) or "token_major" [num_blocks,
+    block_size, num_kv_heads, head_dim]."""
+    H, B, D = num_kv_heads, block_size, head_dim
+    if layout == "head_major":
+        return (H * B * D, B * D, D)
+    if layout == "token_major":
+        return (B * H * D, D, H * D)
+    raise ValueError(f"unknown layout {layout!r}")
+
+
+def _check_rows_inside(t, name, num_blocks, num_kv_heads, block_size, head_dim, strides):
+    """Every (page, head, token) row the strides address lies inside t's storage."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a float16 CUDA tensor")
+    sp, sh, st = (int(x) for x in strides)
+    if min(sp, sh, st) <= 0:
+        raise ValueError(f"strides must be positive, got {strides}")
+    last = (num_blocks - 1) * sp + (num_kv_heads - 1) * sh + (block_size - 1) * st + head_dim
+    avail = t.untyped_storage().nbytes() // 2 - t.storage_offset()
+    if last > avail:
+        raise ValueError(f"{name}: the strides address {last} halves, the tensor holds {avail}")
+
+
+def paged_gqa_decode_strided(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                             num_kv_heads: int, block_size: int, num_blocks: int, strides,
+                             partition_size: int = 0, k_new=None, v_new=None, workspace=None,
+                             page_trace=None, stream=None) -> None:
+    """Decode over caches in any layout with contiguous rows: the row of
+    token r of page b, KV head g starts at element b*strides[0] +
+    g*strides[1] + r*strides[2] of k_cache / v_cache (fp16 CUDA tensors of
+    any shape; see ``kv_strides``).  k_new / v_new (both or neither) turn on
+    the fused append; workspace and page_trace as for ``paged_gqa_decode_ex``."""
+    lib = load_library()
+    _check(q, "q", torch.float16, 3)
+    _check(out, "out", torch.float32, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    Hkv, BS, NB, MB = int(num_kv_heads), int(block_size), int(num_blocks), block_tables.shape[1]
+    if out.shape != q.shape or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes of q, out, block_tables, seq_lens")
+    _check_rows_inside(k_cache, "k_cache", NB, Hkv, BS, D, strides)
+    _check_rows_inside(v_cache, "v_cache", NB, Hkv, BS, D, strides)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new or neither")
+    if k_new is not None:
+        _check(k_new, "k_new", torch.float16, 3)
+        _check(v_new, "v_new", torch.float16, 3)
+        if tuple(k_new.shape) != (S, Hkv, D) or tuple(v_new.shape) != (S, Hkv, D):
+            raise ValueError(f"k_new / v_new must be [{S}, {Hkv}, {D}]")
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if page_trace is not None:
+        _check(page_trace, "page_trace", torch.int32, 3)
+        if tuple(page_trace.shape) != (S, Hkv, MB):
+            raise ValueError(f"page_trace must be [{S}, {Hkv}, {MB}]")
+    sp, sh, st_ = (int(x) for x in strides)
+    st = lib.paged_gqa_decode_strided(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv, D, BS,
+        int(partition_size), MB, NB, sp, sh, st_, _ptr(workspace), ws_bytes, _ptr(page_trace),
+        _stream_handle(stream, q.device))
     _raise(st)
 
 

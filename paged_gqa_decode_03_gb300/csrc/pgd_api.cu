@@ -54,7 +54,7 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_error = cudaSuccess;
     int num_sms = 0;
-    int ctas[2][3] = {};            // [D == 256][block size 8/16/32]
+    int ctas[3][5] = {};            // [head_dim 64/128/256][block size 8..128]
     unsigned *err_word = nullptr;   // address of g_device_error on this device
     std::once_flag pool_once;       // the pool is made on first library-owned scratch
     cudaError_t pool_error = cudaSuccess;
@@ -65,18 +65,35 @@ DeviceState g_dev[kMaxDevices];
 
 __device__ unsigned g_device_error;
 
-int bs_index(int bs) { return bs == 8 ? 0 : bs == 16 ? 1 : 2; }
+constexpr int kBlockSizes[5] = {8, 16, 32, 64, 128};
+
+bool supported_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
+bool supported_block_size(int BS)
+{
+    for (int b : kBlockSizes)
+        if (b == BS)
+            return true;
+    return false;
+}
+int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+int bs_index(int bs) { return bs == 8 ? 0 : bs == 16 ? 1 : bs == 32 ? 2 : bs == 64 ? 3 : 4; }
+// Tokens per pipeline stage of the partition kernel for head_dim D.
+int stage_tokens(int D)
+{
+    return D == 64 ? Shape<64>::T : D == 128 ? Shape<128>::T : Shape<256>::T;
+}
 
 cudaError_t init_device(int dev, DeviceState &st)
 {
     cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    const int sizes[3] = {8, 16, 32};
-    for (int i = 0; i < 3; ++i) {
-        if ((e = occupancy_d128(sizes[i], &st.ctas[0][i])) != cudaSuccess)
+    for (int i = 0; i < 5; ++i) {
+        if ((e = occupancy_d64(kBlockSizes[i], &st.ctas[0][i])) != cudaSuccess)
             return e;
-        if ((e = occupancy_d256(sizes[i], &st.ctas[1][i])) != cudaSuccess)
+        if ((e = occupancy_d128(kBlockSizes[i], &st.ctas[1][i])) != cudaSuccess)
+            return e;
+        if ((e = occupancy_d256(kBlockSizes[i], &st.ctas[2][i])) != cudaSuccess)
             return e;
     }
     return cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error);
@@ -151,25 +168,39 @@ pgd_status encode_fn(EncodeTiledFn *fn)
     return PGD_OK;
 }
 
-// One cache array [NB][Hkv][BS][D] viewed as a 3-D tensor
-//   (64 halves within a 128-byte slab) x (NB*Hkv*BS rows, stride D*2 bytes)
-//   x (D/64 slabs, stride 128 bytes),
-// so one copy box of 64 x box_rows x D/64 brings box_rows whole rows of a
-// page and lands in shared memory as [slab][row][128 B], each slab 128-byte
-// swizzled (the span the tensor-core operand loads read without bank
-// conflicts).
-pgd_status encode_cache_map(CUtensorMap *map, const void *base, long long rows, int D,
-                            int box_rows)
+// Geometry of one cache array: NB pages x Hkv heads x BS token rows of D
+// contiguous halves, at the given strides (in halves).
+struct CacheGeom {
+    int NB, Hkv, BS, D;
+    long long page_stride, head_stride, token_stride;
+    bool operator==(const CacheGeom &o) const
+    {
+        return NB == o.NB && Hkv == o.Hkv && BS == o.BS && D == o.D &&
+               page_stride == o.page_stride && head_stride == o.head_stride &&
+               token_stride == o.token_stride;
+    }
+};
+
+// One cache array viewed as a 5-D tensor, innermost first:
+//   64 halves within a 128-byte slab  x  BS token rows (token stride)
+//   x D/64 slabs (128 bytes)  x  Hkv heads (head stride)  x  NB pages (page stride),
+// so one copy box of 64 x box_rows x D/64 x 1 x 1 brings box_rows whole rows
+// of one (page, head) and lands in shared memory as [slab][row][128 B], each
+// slab 128-byte swizzled (the span the tensor-core operand loads read
+// without bank conflicts), whatever the layout of the array.
+pgd_status encode_cache_map(CUtensorMap *map, const void *base, const CacheGeom &g, int box_rows)
 {
     EncodeTiledFn fn;
     pgd_status st = encode_fn(&fn);
     if (st)
         return st;
-    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+    cuuint64_t dims[5] = {64, (cuuint64_t)g.BS, (cuuint64_t)(g.D / 64), (cuuint64_t)g.Hkv,
+                          (cuuint64_t)g.NB};
+    cuuint64_t strides[4] = {(cuuint64_t)g.token_stride * 2, 128, (cuuint64_t)g.head_stride * 2,
+                             (cuuint64_t)g.page_stride * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_rows, (cuuint32_t)(g.D / 64), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void *>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -259,8 +290,8 @@ void mark_counter_dirty(int slot)
 // with the same caches every step.
 struct MapCacheEntry {
     const void *k, *v;
-    long long rows;
-    int D, box, dev;
+    CacheGeom geom;
+    int box, dev;
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
 };
@@ -268,7 +299,7 @@ constexpr int kMapCache = 8;
 thread_local MapCacheEntry t_maps[kMapCache];
 thread_local int t_maps_used = 0, t_maps_next = 0;
 
-pgd_status cache_maps(const void *k, const void *v, long long rows, int D, int box,
+pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box,
                       const CUtensorMap **tk, const CUtensorMap **tv)
 {
     int dev = 0;
@@ -277,7 +308,7 @@ pgd_status cache_maps(const void *k, const void *v, long long rows, int D, int b
         return cuda_fail(e, "cudaGetDevice");
     for (int i = 0; i < t_maps_used; ++i) {
         MapCacheEntry &c = t_maps[i];
-        if (c.k == k && c.v == v && c.rows == rows && c.D == D && c.box == box && c.dev == dev) {
+        if (c.k == k && c.v == v && c.geom == geom && c.box == box && c.dev == dev) {
             *tk = &c.tk;
             *tv = &c.tv;
             return PGD_OK;
@@ -285,15 +316,14 @@ pgd_status cache_maps(const void *k, const void *v, long long rows, int D, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
-    if ((st = encode_cache_map(&c.tk, k, rows, D, box)) ||
-        (st = encode_cache_map(&c.tv, v, rows, D, box))) {
+    if ((st = encode_cache_map(&c.tk, k, geom, box)) ||
+        (st = encode_cache_map(&c.tv, v, geom, box))) {
         c.k = c.v = nullptr;
         return st;
     }
     c.k = k;
     c.v = v;
-    c.rows = rows;
-    c.D = D;
+    c.geom = geom;
     c.box = box;
     c.dev = dev;
     t_maps_next = (t_maps_next + 1) % kMapCache;
@@ -328,10 +358,10 @@ pgd_status check_sizes(int S, int Hq, int Hkv, int D, int BS, int P, int MB)
     if (Hq / Hkv > kMaxGroup)
         return fail(PGD_ERR_UNSUPPORTED, "GQA group of %d query heads exceeds %d", Hq / Hkv,
                     kMaxGroup);
-    if (D != 128 && D != 256)
-        return fail(PGD_ERR_UNSUPPORTED, "head_dim %d not in {128, 256}", D);
-    if (BS != 8 && BS != 16 && BS != 32)
-        return fail(PGD_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", BS);
+    if (!supported_head_dim(D))
+        return fail(PGD_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", D);
+    if (!supported_block_size(BS))
+        return fail(PGD_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32, 64, 128}", BS);
     if (P != 0 && P != kPartitionSmall && P != kPartitionLarge)
         return fail(PGD_ERR_INVALID_ARG, "partition_size %d not in {0, 256, 512}", P);
     if (MB <= 0)
@@ -361,7 +391,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     DeviceState *ds;
     if ((st = device_state(&ds)))
         return st;
-    const int ctas = ds->ctas[D == 256][bs_index(BS)];
+    const int ctas = ds->ctas[d_index(D)][bs_index(BS)];
     if (ctas < 1)
         return fail(PGD_ERR_UNSUPPORTED, "partition kernel does not fit on an SM");
     const int maxlen = MB * BS;
@@ -400,11 +430,35 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Strides (in halves) of the default layout [NB][Hkv][BS][D].
+struct Strides {
+    long long page, head, token;
+};
+Strides head_major(int Hkv, int BS, int D)
+{
+    return {(long long)Hkv * BS * D, (long long)BS * D, (long long)D};
+}
+
+pgd_status check_strides(const Strides &x, int D)
+{
+    const long long limit = 1ll << 39;  // the tensor copies take strides below 2^40 bytes
+    const long long v[3] = {x.page, x.head, x.token};
+    for (long long e : v)
+        if (e <= 0 || e % 8 != 0 || e >= limit)
+            return fail(PGD_ERR_INVALID_ARG,
+                        "cache strides (%lld, %lld, %lld) must be positive multiples of 8 "
+                        "halves below 2^39",
+                        x.page, x.head, x.token);
+    if (x.token < D)
+        return fail(PGD_ERR_INVALID_ARG, "token stride %lld below head_dim %d", x.token, D);
+    return PGD_OK;
+}
+
 pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
-               int Hkv, int D, int BS, int P, int MB, int NB, void *workspace, size_t ws_bytes,
-               bool own_workspace, int32_t *page_trace, void *stream_v,
-               unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
+               int Hkv, int D, int BS, int P, int MB, int NB, const Strides &kv_strides,
+               void *workspace, size_t ws_bytes, bool own_workspace, int32_t *page_trace,
+               void *stream_v, unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
                const uint16_t *v_new = nullptr)
 {
     if (S == 0) {  // nothing to read or write: only the sizes are checked
@@ -430,10 +484,8 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     pgd_status st = check_sizes(S, Hq, Hkv, D, BS, P, MB);
     if (st)
         return st;
-    const long long rows = (long long)NB * Hkv * BS;
-    if (rows >= (1ll << 31))
-        return fail(PGD_ERR_UNSUPPORTED, "num_blocks*num_kv_heads*block_size = %lld >= 2^31",
-                    rows);
+    if ((st = check_strides(kv_strides, D)))
+        return st;
     if (!own_workspace && workspace && !aligned(workspace, 256))
         return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     Plan plan;
@@ -462,11 +514,10 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
         }
     }
 
-    const int box = BS < (D == 128 ? Shape<128>::T : Shape<256>::T)
-                        ? BS
-                        : (D == 128 ? Shape<128>::T : Shape<256>::T);
+    const int box = BS < stage_tokens(D) ? BS : stage_tokens(D);
+    const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
     const CUtensorMap *tk = nullptr, *tv = nullptr;
-    if ((st = cache_maps(k_cache, v_cache, rows, D, box, &tk, &tv))) {
+    if ((st = cache_maps(k_cache, v_cache, geom, box, &tk, &tv))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
@@ -511,6 +562,9 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.v_new = reinterpret_cast<const __half *>(v_new);
     p.k_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(k_cache));
     p.v_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(v_cache));
+    p.kv_page_stride = kv_strides.page;
+    p.kv_head_stride = kv_strides.head;
+    p.kv_token_stride = kv_strides.token;
     p.err = ds->err_word;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e) folded into the scale
     p.S = S;
@@ -530,8 +584,10 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     lc.stream = stream;
     lc.ev_before = t_ev_before;
     lc.ev_after = t_ev_after;
-    e = D == 128 ? launch_decode_d128(BS, page_trace != nullptr, *tk, *tv, p, lc)
-                 : launch_decode_d256(BS, page_trace != nullptr, *tk, *tv, p, lc);
+    const bool trace = page_trace != nullptr;
+    e = D == 64    ? launch_decode_d64(BS, trace, *tk, *tv, p, lc)
+        : D == 128 ? launch_decode_d128(BS, trace, *tk, *tv, p, lc)
+                   : launch_decode_d256(BS, trace, *tk, *tv, p, lc);
     if (own_workspace && ws) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess)
@@ -592,7 +648,8 @@ pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cac
 {
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
-               num_blocks, nullptr, 0, true, nullptr, stream);
+               num_blocks, head_major(num_kv_heads, block_size, head_dim), nullptr, 0, true,
+               nullptr, stream);
 }
 
 pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_cache,
@@ -605,7 +662,8 @@ pgd_status paged_gqa_decode_ex(float *out, const uint16_t *q, const uint16_t *k_
 {
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
-               num_blocks, workspace, workspace_bytes, false, page_trace, stream);
+               num_blocks, head_major(num_kv_heads, block_size, head_dim), workspace,
+               workspace_bytes, false, page_trace, stream);
 }
 
 pgd_status paged_gqa_decode_append(float *out, const uint16_t *q, const uint16_t *k_new,
@@ -621,7 +679,28 @@ pgd_status paged_gqa_decode_append(float *out, const uint16_t *q, const uint16_t
         return fail(PGD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
-               num_blocks, nullptr, 0, true, nullptr, stream, nullptr, k_new, v_new);
+               num_blocks, head_major(num_kv_heads, block_size, head_dim), nullptr, 0, true,
+               nullptr, stream, nullptr, k_new, v_new);
+}
+
+pgd_status paged_gqa_decode_strided(float *out, const uint16_t *q, const uint16_t *k_new,
+                                    const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache,
+                                    const int32_t *block_tables, const int32_t *seq_lens,
+                                    float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int partition_size,
+                                    int max_blocks_per_seq, int num_blocks, int64_t page_stride,
+                                    int64_t head_stride, int64_t token_stride, void *workspace,
+                                    size_t workspace_bytes, int32_t *page_trace, void *stream)
+{
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(PGD_ERR_INVALID_ARG, "give both k_new and v_new or neither");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(PGD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    const bool own = workspace == nullptr;
+    return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, Strides{page_stride, head_stride, token_stride}, workspace,
+               workspace_bytes, own, page_trace, stream, nullptr, k_new, v_new);
 }
 
 pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_t *k_cache,
@@ -648,8 +727,9 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
     // [256 B: claim counter, zero at load and after every call][partials]
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
-               num_blocks, static_cast<char *>(scratch) + 256, PGD_NOALLOC_SCRATCH_BYTES - 256,
-               false, nullptr, stream, static_cast<unsigned *>(scratch));
+               num_blocks, head_major(num_kv_heads, block_size, head_dim),
+               static_cast<char *>(scratch) + 256, PGD_NOALLOC_SCRATCH_BYTES - 256, false,
+               nullptr, stream, static_cast<unsigned *>(scratch));
 }
 
 pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -704,8 +784,7 @@ pgd_status pgd_set_timing_events(void *before, void *after)
 
 pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas_per_sm)
 {
-    if ((head_dim != 128 && head_dim != 256) ||
-        (block_size != 8 && block_size != 16 && block_size != 32))
+    if (!supported_head_dim(head_dim) || !supported_block_size(block_size))
         return fail(PGD_ERR_UNSUPPORTED, "no kernel for head_dim %d, block_size %d", head_dim,
                     block_size);
     DeviceState *ds;
@@ -715,10 +794,10 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
     if (num_sms)
         *num_sms = ds->num_sms;
     if (ctas_per_sm)
-        *ctas_per_sm = ds->ctas[head_dim == 256][bs_index(block_size)];
+        *ctas_per_sm = ds->ctas[d_index(head_dim)][bs_index(block_size)];
     return PGD_OK;
 }
 
-int pgd_version(void) { return 100; }
+int pgd_version(void) { return 10100; }
 
 }  // extern "C"

@@ -33,8 +33,12 @@ constexpr int kLensCap = 256;
 constexpr int kMaxTailStages = 16;
 
 // Kernel shape per head_dim: tokens per pipeline stage (T), consumer warps
-// (NC, one 16-token tile each), stages in the shared-memory ring (NS).
+// (NC, one 16-token tile each), stages in the shared-memory ring (NS).  The
+// ring holds about 100 KB for every head_dim (two CTAs per SM).
 template <int D> struct Shape;
+template <> struct Shape<64> {
+    static constexpr int T = 64, NC = 4, NS = 6;
+};
 template <> struct Shape<128> {
     static constexpr int T = 64, NC = 4, NS = 3;
 };
@@ -67,6 +71,9 @@ struct DecodeParams {
     const __half *v_new;          // [S][Hkv][D] newest token's V
     __half *k_cache;              // caches, written at the newest token's row (append)
     __half *v_cache;
+    long long kv_page_stride;     // cache strides in halves (the copies use the
+    long long kv_head_stride;     //   same ones through the tensor maps)
+    long long kv_token_stride;
     float scale_log2;             // scale * log2(e)
     int S, Hq, Hkv, G, P, logP, MB, NB, NPmax;
     uint64_t wait_budget_ns;
@@ -79,7 +86,10 @@ struct LaunchConfig {
     cudaEvent_t ev_before, ev_after;  // optional timing hook (both or neither)
 };
 
-// Per-head_dim entry points (pgd_kernels_d128.cu / pgd_kernels_d256.cu).
+// Per-head_dim entry points (pgd_kernels_d64.cu, _d128.cu, _d256.cu).
+cudaError_t launch_decode_d64(int block_size, bool trace, const CUtensorMap &tk,
+                              const CUtensorMap &tv, const DecodeParams &p,
+                              const LaunchConfig &lc);
 cudaError_t launch_decode_d128(int block_size, bool trace, const CUtensorMap &tk,
                                const CUtensorMap &tv, const DecodeParams &p,
                                const LaunchConfig &lc);
@@ -87,12 +97,13 @@ cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk
                                const CUtensorMap &tv, const DecodeParams &p,
                                const LaunchConfig &lc);
 // Resident partition-kernel CTAs per SM for (head_dim, block_size).
+cudaError_t occupancy_d64(int block_size, int *ctas_per_sm);
 cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
 cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
 
 // Reduce kernel: one CTA per (sequence, query head); two warps suffice for
-// head_dim 128 (whose workloads have at most 16 partitions per sequence) and
-// keep every CTA resident at once, four for 256.
-template <int D> __host__ __device__ constexpr int reduce_threads() { return D == 128 ? 64 : 128; }
+// head_dim 64 and 128 (whose workloads have at most 16 partitions per
+// sequence) and keep every CTA resident at once, four for 256.
+template <int D> __host__ __device__ constexpr int reduce_threads() { return D <= 128 ? 64 : 128; }
 
 }  // namespace pgd

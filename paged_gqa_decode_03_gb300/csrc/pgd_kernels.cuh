@@ -11,10 +11,12 @@
 //      * producer warp: loads the unit's page-table entries with one
 //        coalesced warp load, broadcasts each physical page id with a warp
 //        shuffle, and issues one TMA tensor copy of the page's K rows and one
-//        of its V rows (3-D box: 64 halves x rows x 128-byte slabs, so each
-//        slab lands 128-byte swizzled; evict-first) plus one bulk copy of the
-//        group's queries, into a ring of shared-memory stages guarded by
-//        mbarriers.  Stage layout: [page][slab][row][128 B].
+//        of its V rows (5-D map over 64 halves x page rows x 128-byte slabs x
+//        KV heads x pages, strides from the caller's cache layout; box: the
+//        rows of one page and head, so each slab lands 128-byte swizzled;
+//        evict-first) plus one bulk copy of the group's queries, into a ring
+//        of shared-memory stages guarded by mbarriers.  Stage layout:
+//        [page][slab][row][128 B], whatever the layout in HBM.
 //      * consumer warps: per stage of T tokens, S^T = K Q^T on tensor cores
 //        (mma.sync m16n8k16, fp16 in, fp32 accumulate), scores exchanged
 //        through shared memory, one log2-space online-softmax update with
@@ -41,7 +43,7 @@ enum : int { kFirst = 1, kLast = 2, kDirect = 4, kAppend = 16, kTerm = 32 };
 
 struct StageHeader {
     int s, g, p, valid, flags;
-    int app_row;  // kAppend: row of the newest token in the [NB*Hkv*BS][D] cache view, -1: none
+    long long app_off;  // kAppend: element offset of the newest token's cache row, -1: none
 };
 
 template <int D, int BS, bool TRACE>
@@ -217,12 +219,13 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 const uint32_t fb = smem_addr(&full_bar[slot]);
                 // fused append: cache row of token L-1 (its page is the unit's
                 // page (L-1)/BS - pg0), published with the header
-                int app_row = -1;
+                long long app_off = -1;
                 if (app_unit && st == nst - 1) {
                     const int ja = (L - 1) / BS - pg0;
                     const int ida = __shfl_sync(~0u, ja < 32 ? id0 : id1, ja & 31);
                     if ((unsigned)ida < (unsigned)p.NB)
-                        app_row = (ida * Hkv + g) * BS + (L - 1) % BS;
+                        app_off = ida * p.kv_page_stride + g * p.kv_head_stride +
+                                  ((L - 1) % BS) * p.kv_token_stride;
                 }
                 if (lane == 0) {
                     hdr[slot].s = s;
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     hdr[slot].valid = valid;
                     hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
                                       (app_unit && st == nst - 1 ? kAppend : 0);
-                    hdr[slot].app_row = app_row;
+                    hdr[slot].app_off = app_off;
                     const uint32_t bytes = pc * PAGE_BYTES * 2 + (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
@@ -239,21 +242,20 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     const int j = pf + jj;
                     const int id = __shfl_sync(~0u, j < 32 ? id0 : id1, j & 31);
                     if (lane == 0) {
-                        int y;
-                        if ((unsigned)id < (unsigned)p.NB) {
-                            y = (id * Hkv + g) * BS + row0;
-                        } else {
+                        int c_page = id;
+                        if ((unsigned)id >= (unsigned)p.NB) {
                             atomicOr(p.err, kErrPageRange);
-                            y = -BOX;  // wholly outside the tensor: the copy reads zeros
+                            c_page = -1;  // wholly outside the tensor: the copy reads zeros
                         }
                         if (TRACE)
                             p.page_trace[((size_t)s * Hkv + g) * MB + pg0 + j] = id;
 
-                        // one copy per page for K and one for V: BOX rows x D
-                        // halves, landing as [slab][row][128 B] (swizzled)
+                        // one copy per page for K and one for V: BOX rows
+                        // from row0 of (page, KV head g), all D halves,
+                        // landing as [slab][row][128 B] (swizzled)
                         const uint32_t dk = sb + jj * PAGE_BYTES;
-                        tma_load_3d(dk, &tmap_k, 0, y, 0, fb, pol);
-                        tma_load_3d(dk + KV_BYTES, &tmap_v, 0, y, 0, fb, pol);
+                        tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
+                        tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
                     }
                 }
                 if (st == 0 && lane == 0)
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 // in the staged page (same 128-byte swizzle as the copies)
                 // and in the cache for the next steps
                 const int r = valid - 1;
-                const int app_row = hdr[slot].app_row;
+                const long long app_off = hdr[slot].app_off;
                 const size_t src = ((size_t)hs * p.Hkv + hg) * D;
                 for (int c = lane; c < D / 8; c += 32) {
                     const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + src + c * 8);
@@ -484,9 +486,9 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                                     (r % BOX) * 128 + (((c & 7) ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(sp + off) = kv;
                     *reinterpret_cast<uint4 *>(sp + KV_BYTES + off) = vv;
-                    if (app_row >= 0) {
-                        *reinterpret_cast<uint4 *>(p.k_cache + (size_t)app_row * D + c * 8) = kv;
-                        *reinterpret_cast<uint4 *>(p.v_cache + (size_t)app_row * D + c * 8) = vv;
+                    if (app_off >= 0) {
+                        *reinterpret_cast<uint4 *>(p.k_cache + app_off + c * 8) = kv;
+                        *reinterpret_cast<uint4 *>(p.v_cache + app_off + c * 8) = vv;
                     }
                 }
                 __syncwarp();
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(reduce_threads<D>())
     constexpr int kReduceThreads = reduce_threads<D>();
     constexpr int NW = kReduceThreads / 32;
     constexpr int V4 = D / 4;       // float4 per row
-    constexpr int PL = V4 / 32;     // float4 per lane
+    constexpr int PL = (V4 + 31) / 32;  // float4 per lane (lanes past V4 idle for D = 64)
     constexpr int U = 8;            // rows in flight per warp
     __shared__ float m_s[NW], den_s[NW];
     __shared__ float4 acc_s[NW][V4];
@@ -731,7 +733,8 @@ __global__ void __launch_bounds__(reduce_threads<D>())
                     const int slot = warp + NW * (src[u] + 32 * r);
 #pragma unroll
                     for (int v = 0; v < PL; ++v)
-                        x[u][v] = op[(size_t)slot * V4 + lane + 32 * v];
+                        x[u][v] = lane + 32 * v < V4 ? op[(size_t)slot * V4 + lane + 32 * v]
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
 #pragma unroll
@@ -755,7 +758,8 @@ __global__ void __launch_bounds__(reduce_threads<D>())
     }
 #pragma unroll
     for (int v = 0; v < PL; ++v)
-        acc_s[warp][lane + 32 * v] = acc[v];
+        if (lane + 32 * v < V4)
+            acc_s[warp][lane + 32 * v] = acc[v];
     __syncthreads();
     float M = m_s[0];
 #pragma unroll
@@ -844,6 +848,14 @@ cudaError_t occupancy_impl(int *ctas)
                                                          dyn_smem_bytes<D>());
 }
 
+template <int D, int BS>
+cudaError_t launch_decode_bs(bool trace, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const DecodeParams &p, const LaunchConfig &lc)
+{
+    return trace ? launch_decode_impl<D, BS, true>(tk, tv, p, lc)
+                 : launch_decode_impl<D, BS, false>(tk, tv, p, lc);
+}
+
 template <int D>
 cudaError_t launch_decode_dispatch(int block_size, bool trace, const CUtensorMap &tk,
                                    const CUtensorMap &tv, const DecodeParams &p,
@@ -851,14 +863,15 @@ cudaError_t launch_decode_dispatch(int block_size, bool trace, const CUtensorMap
 {
     switch (block_size) {
     case 8:
-        return trace ? launch_decode_impl<D, 8, true>(tk, tv, p, lc)
-                     : launch_decode_impl<D, 8, false>(tk, tv, p, lc);
+        return launch_decode_bs<D, 8>(trace, tk, tv, p, lc);
     case 16:
-        return trace ? launch_decode_impl<D, 16, true>(tk, tv, p, lc)
-                     : launch_decode_impl<D, 16, false>(tk, tv, p, lc);
+        return launch_decode_bs<D, 16>(trace, tk, tv, p, lc);
     case 32:
-        return trace ? launch_decode_impl<D, 32, true>(tk, tv, p, lc)
-                     : launch_decode_impl<D, 32, false>(tk, tv, p, lc);
+        return launch_decode_bs<D, 32>(trace, tk, tv, p, lc);
+    case 64:
+        return launch_decode_bs<D, 64>(trace, tk, tv, p, lc);
+    case 128:
+        return launch_decode_bs<D, 128>(trace, tk, tv, p, lc);
     default:
         return cudaErrorInvalidValue;
     }
@@ -874,6 +887,10 @@ cudaError_t occupancy_dispatch(int block_size, int *ctas)
         return occupancy_impl<D, 16>(ctas);
     case 32:
         return occupancy_impl<D, 32>(ctas);
+    case 64:
+        return occupancy_impl<D, 64>(ctas);
+    case 128:
+        return occupancy_impl<D, 128>(ctas);
     default:
         return cudaErrorInvalidValue;
     }

@@ -1,4 +1,4 @@
-// Instantiations of the decode kernels for head_dim 256 (block sizes 8/16/32,
+// Instantiations of the decode kernels for head_dim 256 (block sizes 8 to 128,
 // with and without the page trace).
 #include "pgd_kernels.cuh"
 

@@ -1,0 +1,19 @@
+// Instantiations of the decode kernels for head_dim 64 (block sizes 8 to 128,
+// with and without the page trace).
+#include "pgd_kernels.cuh"
+
+namespace pgd {
+
+cudaError_t launch_decode_d64(int block_size, bool trace, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const DecodeParams &p,
+                               const LaunchConfig &lc)
+{
+    return launch_decode_dispatch<64>(block_size, trace, tk, tv, p, lc);
+}
+
+cudaError_t occupancy_d64(int block_size, int *ctas_per_sm)
+{
+    return occupancy_dispatch<64>(block_size, ctas_per_sm);
+}
+
+}  // namespace pgd

@@ -61,13 +61,12 @@ def test_null_arrays_rejected(lib, i):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(D=64), UNSUPPORTED), (dict(D=192), UNSUPPORTED),
-    (dict(BS=4), UNSUPPORTED), (dict(BS=64), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=192), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
+    (dict(BS=4), UNSUPPORTED), (dict(BS=48), UNSUPPORTED), (dict(BS=256), UNSUPPORTED),
     (dict(P=128), INVALID), (dict(P=1024), INVALID), (dict(P=-1), INVALID),
     (dict(Hq=30, Hkv=8), INVALID), (dict(Hq=0), INVALID), (dict(Hkv=0), INVALID),
     (dict(Hq=32, Hkv=2), UNSUPPORTED),      # 16 query heads per KV head > 8
     (dict(MB=0), INVALID), (dict(S=-1), INVALID), (dict(NB=0), INVALID),
-    (dict(NB=1 << 27, Hkv=8, BS=16), UNSUPPORTED),   # rows >= 2^31
     (dict(scale=math.inf), INVALID), (dict(scale=math.nan), INVALID),
 ])
 def test_bad_sizes_rejected(lib, kw, status):
@@ -110,7 +109,8 @@ def test_timing_events_need_both(lib):
 
 def test_device_info_rejects_unbuilt_shapes(lib):
     n, c = ctypes.c_int(0), ctypes.c_int(0)
-    assert lib.pgd_device_info(64, 16, ctypes.byref(n), ctypes.byref(c)) == UNSUPPORTED
+    assert lib.pgd_device_info(96, 16, ctypes.byref(n), ctypes.byref(c)) == UNSUPPORTED
+    assert lib.pgd_device_info(128, 256, ctypes.byref(n), ctypes.byref(c)) == UNSUPPORTED
 
 
 def test_binding_rejects_cpu_tensors():
@@ -124,3 +124,41 @@ def test_binding_rejects_cpu_tensors():
         pgd.paged_gqa_decode(out, q, k, k, bt, sl, 0.1)
     with pytest.raises(TypeError):
         pgd.paged_gqa_decode(out, q.float(), k, k, bt, sl, 0.1)
+
+
+def call_strided(lib, strides=(8 * 16 * 128, 16 * 128, 128), new=(A, A), D=128, ws=None,
+                 ws_bytes=0):
+    return lib.paged_gqa_decode_strided(
+        A, A, new[0], new[1], A, A, A, A, ctypes.c_float(0.1), 4, 32, 8, D, 16, 512, 64, 1024,
+        *strides, ws or ctypes.c_void_p(0), ws_bytes, ctypes.c_void_p(0), ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("strides", [
+    (8 * 16 * 128, 16 * 128, 0),          # zero token stride
+    (8 * 16 * 128, -16 * 128, 128),       # negative
+    (8 * 16 * 128 + 4, 16 * 128, 128),    # not a multiple of 8 halves (16 bytes)
+    (8 * 16 * 128, 16 * 128, 120),        # rows overlap: token stride < head_dim
+    (1 << 39, 16 * 128, 128),             # beyond what a tensor copy can stride
+])
+def test_strided_bad_strides_rejected(lib, strides):
+    assert call_strided(lib, strides=strides) == INVALID
+    assert "stride" in lib.pgd_last_error().decode()
+
+
+def test_strided_append_needs_both_rows(lib):
+    assert call_strided(lib, new=(A, ctypes.c_void_p(0))) == INVALID
+    assert call_strided(lib, new=(ctypes.c_void_p(0), A)) == INVALID
+    assert call_strided(lib, new=(ctypes.c_void_p((1 << 20) + 8), A)) == INVALID
+
+
+def test_strided_workspace_alignment_rejected(lib):
+    assert call_strided(lib, new=(ctypes.c_void_p(0), ctypes.c_void_p(0)),
+                        ws=ctypes.c_void_p((1 << 20) + 16), ws_bytes=1 << 20) == INVALID
+
+
+def test_kv_strides_helper():
+    assert pgd.kv_strides("head_major", 8, 16, 128) == (8 * 16 * 128, 16 * 128, 128)
+    assert pgd.kv_strides("token_major", 8, 16, 128) == (16 * 8 * 128, 128, 8 * 128)
+    with pytest.raises(ValueError):
+        pgd.kv_strides("page_major", 8, 16, 128)
+

@@ -361,3 +361,62 @@ def test_append_then_decode_closed_forms():
                              inp["block_tables"], inp["seq_lens"], w.scale)
     b = oracle.decode(inp["q"], k2, v2, inp["block_tables"], inp["seq_lens"], w.scale)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- cache layouts
+def _layouts(inp):
+    """The same cache in three layouts, as (name, k_flat, v_flat, strides):
+    token-major [NB][BS][Hkv][D] (a numpy transpose), pages padded with NaN
+    between them, and rows padded with NaN to D + 8 halves."""
+    k, v = inp["k_cache"], inp["v_cache"]
+    NB, Hkv, BS, D = k.shape
+    tm = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3))
+    pad_page = 24
+
+    def padded_pages(a):
+        b = np.full((NB, Hkv * BS * D + pad_page), np.float16("nan"), dtype=np.float16)
+        b[:, :Hkv * BS * D] = a.reshape(NB, -1)
+        return b
+
+    def padded_rows(a):
+        b = np.full((NB, Hkv, BS, D + 8), np.float16("nan"), dtype=np.float16)
+        b[..., :D] = a
+        return b
+
+    return [
+        ("token_major", tm(k), tm(v), (BS * Hkv * D, D, Hkv * D)),
+        ("padded_pages", padded_pages(k), padded_pages(v), (Hkv * BS * D + pad_page, BS * D, D)),
+        ("padded_rows", padded_rows(k), padded_rows(v),
+         (Hkv * BS * (D + 8), BS * (D + 8), D + 8)),
+        ("head_major", k, v, (Hkv * BS * D, BS * D, D)),
+    ]
+
+
+def test_strided_layouts_equal_head_major():
+    """The strided form reads the same numbers whatever the layout: bitwise
+    equal to the head-major decode (layouts built by numpy, not the oracle;
+    a swapped head/token stride or a read of the padding fails here)."""
+    w = _small(seed=31, Hq=8, Hkv=2, D=16, BS=4, lens=(0, 1, 7, 13, 16))
+    inp = _np(w)
+    ref = oracle.decode(**inp, scale=w.scale)
+    NB, Hkv, BS, D = inp["k_cache"].shape
+    for name, kf, vf, strides in _layouts(inp):
+        out = oracle.decode_strided(inp["q"], kf, vf, inp["block_tables"], inp["seq_lens"],
+                                    w.scale, Hkv, BS, NB, strides)
+        assert np.array_equal(out, ref), name
+
+
+def test_strided_append_equals_head_major_append():
+    w = _small(seed=32, lens=(0, 1, 8, 13), BS=4)
+    inp = _np(w)
+    kn, vn = _new_kv(w, 4)
+    k_ref, v_ref = oracle.append_kv(inp["k_cache"], inp["v_cache"], kn, vn,
+                                    inp["block_tables"], inp["seq_lens"])
+    NB, Hkv, BS, D = inp["k_cache"].shape
+    kf, vf = (np.ascontiguousarray(a.transpose(0, 2, 1, 3)) for a in (inp["k_cache"],
+                                                                      inp["v_cache"]))
+    k2, v2 = oracle.append_kv_strided(kf, vf, kn, vn, inp["block_tables"], inp["seq_lens"], Hkv,
+                                      BS, NB, (BS * Hkv * D, D, Hkv * D))
+    back = lambda a: np.ascontiguousarray(a.reshape(NB, BS, Hkv, D).transpose(0, 2, 1, 3))
+    assert np.array_equal(back(k2).view(np.uint16), k_ref.view(np.uint16))
+    assert np.array_equal(back(v2).view(np.uint16), v_ref.view(np.uint16))

@@ -18,7 +18,9 @@ ROOT = os.path.dirname(HERE)
 # (name, text in pgd_oracle.c, replacement, replace every occurrence?)
 MUTANTS = [
     ("page index takes t % BS", "MB + t / BS];", "MB + t % BS];", False),
-    ("row within the page takes t / BS", "* BS + t % BS;", "* BS + t / BS;", False),
+    ("row within the page takes t / BS", "(t % BS) * x.token", "(t / BS) * x.token", False),
+    ("head and token strides swapped", "g * x.head + (t % BS) * x.token",
+     "g * x.token + (t % BS) * x.head", False),
     ("K read with KV head h % Hkv",
      "    int G = Hq / Hkv;\n    int g = h / G;\n    const uint16_t *qh",
      "    int G = Hq / Hkv;\n    int g = h % Hkv;\n    const uint16_t *qh", False),
@@ -32,8 +34,8 @@ MUTANTS = [
     ("softmax exponent sign flipped", "exp(z[t] - zmax)", "exp(zmax - z[t])", True),
     ("max taken as min", "if (z[t] > zmax)", "if (z[t] < zmax)", False),
     ("V read from the K cache",
-     "kv_row(v_cache, block_tables, s, t, g, Hkv, D, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];",
-     "kv_row(k_cache, block_tables, s, t, g, Hkv, D, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];", False),
+     "kv_row(v_cache, x, block_tables, s, t, g, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];",
+     "kv_row(k_cache, x, block_tables, s, t, g, BS, MB);\n            for (int d = 0; d < D; ++d)\n                o[d] += w * g_h2d[vt[d]];", False),
     ("partials: log2(e) dropped", "exp2(z[t] * log2e - m)", "exp2(z[t] - m)", True),
     ("partials: output not normalised",
      "                o[d] /= l;\n            m_out", "\n            m_out", False),
@@ -43,7 +45,7 @@ MUTANTS = [
     ("fp16 exponent bias off by one", "expo - 25", "expo - 24", False),
     ("page reads one past the end", "j < npages ? block_tables", "j <= npages ? block_tables",
      False),
-    ("append row off by one", "(L - 1) % BS;", "L % BS;", False),
+    ("append row off by one", "((L - 1) % BS) * x.token", "(L % BS) * x.token", False),
 ]
 
 
@@ -69,6 +71,8 @@ def _pins():
         ("merge empty", T.test_merge_skips_empty_partitions),
         ("append rows", T.test_append_writes_only_the_newest_rows),
         ("append closed forms", T.test_append_then_decode_closed_forms),
+        ("strided layouts", T.test_strided_layouts_equal_head_major),
+        ("strided append", T.test_strided_append_equals_head_major_append),
     ]
 
 
