@@ -82,6 +82,8 @@ def _bind(lib):
     lib.oracle_paged_gqa_decode_strided.restype = I
     lib.oracle_append_kv_strided.argtypes = [P] * 6 + [I] * 6 + [Lg] * 3
     lib.oracle_append_kv_strided.restype = I
+    lib.oracle_paged_varlen.argtypes = [P] * 7 + [D] + [I] * 7 + [Lg] * 3 + [I]
+    lib.oracle_paged_varlen.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -320,6 +322,37 @@ def append_kv_strided(k_flat, v_flat, k_new, v_new, block_tables, seq_lens, num_
     _check(lib.oracle_append_kv_strided(_ptr(k), _ptr(v), _ptr(kn), _ptr(vn), _ptr(bt),
                                         _ptr(sl), S, Hkv, D, BS, MB, NB, sp, sh, st))
     return k.view(np.float16), v.view(np.float16)
+
+
+def varlen(q, cu_seqlens_q, k_cache, v_cache, block_tables, seq_lens, scale, layout=None,
+           threads=None):
+    """out[total_q, Hq, D] (fp64): causal attention of every query row over
+    its sequence's cached tokens up to its own position (query i of
+    sequence s sits at seq_lens[s] - n_s + i).  k_cache / v_cache are
+    head-major [NB, Hkv, BS, D], or flat arrays with
+    ``layout = (num_kv_heads, block_size, num_blocks, strides)``."""
+    lib = _load()
+    q = _u16(q)
+    cu = _i32(cu_seqlens_q)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    T, Hq, D = q.shape
+    S, MB = bt.shape
+    if layout is None:
+        NB, Hkv, BS, D2 = np.shape(k_cache)
+        assert D2 == D
+        strides = (Hkv * BS * D, BS * D, D)
+    else:
+        Hkv, BS, NB, strides = layout
+    k, v = _u16(np.ravel(k_cache)), _u16(np.ravel(v_cache))
+    sp, sh, st = (int(x) for x in strides)
+    last = (NB - 1) * sp + (Hkv - 1) * sh + (BS - 1) * st + D
+    assert last <= k.size and last <= v.size, "strides address rows past the arrays"
+    assert cu.shape == (S + 1,) and int(cu[-1]) == T, "cu_seqlens_q must be [S+1], ending at total_q"
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    _check(lib.oracle_paged_varlen(_ptr(out), _ptr(q), _ptr(cu), _ptr(k), _ptr(v), _ptr(bt),
+                                   _ptr(sl), float(scale), S, Hq, int(Hkv), D, int(BS), MB,
+                                   int(NB), sp, sh, st, int(threads or max_threads())))
+    return out
 
 
 def decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, scale,

@@ -134,14 +134,12 @@ static const uint16_t *kv_row(const uint16_t *cache, kv_strides x, const int32_t
     return cache + pp * x.page + g * x.head + (t % BS) * x.token;
 }
 
-/* z_t = scale * sum_d q[d] * k_t[d] for every token t < L of (s, h). */
-static void logits(double *z, const uint16_t *q, const uint16_t *k_cache, kv_strides x,
-                   const int32_t *block_tables, double scale, int s, int h, long L,
-                   int Hq, int Hkv, int D, int BS, int MB)
+/* z_t = scale * sum_d qh[d] * k_t[d] for every token t < L of sequence s,
+ * KV head g (qh: one query row of D values). */
+static void logits(double *z, const uint16_t *qh, const uint16_t *k_cache, kv_strides x,
+                   const int32_t *block_tables, double scale, int s, int g, long L, int D,
+                   int BS, int MB)
 {
-    int G = Hq / Hkv;
-    int g = h / G;
-    const uint16_t *qh = q + ((long)s * Hq + h) * D;
     for (long t = 0; t < L; ++t) {
         const uint16_t *kt = kv_row(k_cache, x, block_tables, s, t, g, BS, MB);
         double dot = 0.0;
@@ -184,7 +182,7 @@ static int decode(double *out, const uint16_t *q, const uint16_t *k_cache,
             fail = 1;
             continue;
         }
-        logits(z, q, k_cache, x, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        logits(z, q + sh * D, k_cache, x, block_tables, scale, s, g, L, D, BS, MB);
         double zmax = -INFINITY;
         for (long t = 0; t < L; ++t)
             if (z[t] > zmax)
@@ -227,6 +225,81 @@ int oracle_paged_gqa_decode_strided(double *out, const uint16_t *q, const uint16
                   BS, MB, NB, num_threads);
 }
 
+/*
+ * Paged attention with several query tokens per sequence: the unified paged
+ * variable-length attention of "vllm-metal" (introduction and "Three Metal
+ * kernels": one kernel for prefill chunks, decode and the verification step
+ * of speculative decoding).  Sequence s owns query rows cu_q[s] ..
+ * cu_q[s+1]-1 of q ([total_q][Hq][D], total_q = cu_q[S]); its
+ * n_s = cu_q[s+1] - cu_q[s] query tokens are the newest n_s of its
+ * L_s = seq_lens[s] cached tokens (their K/V already in the cache), so query
+ * i (0 <= i < n_s) sits at position L_s - n_s + i and attends every cached
+ * token up to and including that position (causal).  For every query row r
+ * and head h, with z_t = scale * q[r][h] . k_t over t = 0 .. pos:
+ *   out[r][h] = sum_t w_t v_t,   w_t = exp(z_t - max z) / sum_u exp(z_u - max z).
+ * A decode step is the case n_s = 1 for every sequence.  Caches are
+ * addressed through strides as in oracle_paged_gqa_decode_strided.
+ */
+int oracle_paged_varlen(double *out, const uint16_t *q, const int32_t *cu_q,
+                        const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, double scale,
+                        int S, int Hq, int Hkv, int D, int BS, int MB, int NB, long page_stride,
+                        long head_stride, long token_stride, int num_threads)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    if (page_stride <= 0 || head_stride <= 0 || token_stride <= 0 || cu_q[0] != 0)
+        return ORC_BAD_SHAPE;
+    for (int s = 0; s < S; ++s) {
+        long n = (long)cu_q[s + 1] - cu_q[s];
+        if (n < 0 || n > seq_lens[s])
+            return ORC_BAD_LENGTH;
+    }
+    h2d_init();
+    kv_strides x = {page_stride, head_stride, token_stride};
+    int G = Hq / Hkv;
+    long rows = (long)cu_q[S] * Hq;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+    for (long rh = 0; rh < rows; ++rh) {
+        long r = rh / Hq;
+        int h = (int)(rh % Hq);
+        int g = h / G;
+        int s = 0;
+        while (cu_q[s + 1] <= r) /* the sequence owning query row r */
+            ++s;
+        long n = (long)cu_q[s + 1] - cu_q[s];
+        long pos = (long)seq_lens[s] - n + (r - cu_q[s]);
+        long count = pos + 1; /* tokens 0 .. pos */
+        double *o = out + rh * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        double *z = (double *)malloc(sizeof(double) * (size_t)count);
+        if (!z) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        logits(z, q + rh * D, k_cache, x, block_tables, scale, s, g, count, D, BS, MB);
+        double zmax = -INFINITY;
+        for (long t = 0; t < count; ++t)
+            if (z[t] > zmax)
+                zmax = z[t];
+        double den = 0.0;
+        for (long t = 0; t < count; ++t)
+            den += exp(z[t] - zmax);
+        for (long t = 0; t < count; ++t) {
+            double w = exp(z[t] - zmax) / den;
+            const uint16_t *vt = kv_row(v_cache, x, block_tables, s, t, g, BS, MB);
+            for (int d = 0; d < D; ++d)
+                o[d] += w * g_h2d[vt[d]];
+        }
+        free(z);
+    }
+    return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
 /* Attention weights w_t of one (s, h), for the sum-to-one and closed-form
  * pins.  w must hold seq_lens[s] doubles. */
 int oracle_attention_weights(double *w, const uint16_t *q, const uint16_t *k_cache,
@@ -243,8 +316,8 @@ int oracle_attention_weights(double *w, const uint16_t *q, const uint16_t *k_cac
     long L = seq_lens[s];
     if (L == 0)
         return ORC_OK;
-    logits(w, q, k_cache, head_major(Hkv, BS, D), block_tables, scale, s, h, L, Hq, Hkv, D, BS,
-           MB);
+    logits(w, q + ((long)s * Hq + h) * D, k_cache, head_major(Hkv, BS, D), block_tables, scale,
+           s, h / (Hq / Hkv), L, D, BS, MB);
     double zmax = -INFINITY;
     for (long t = 0; t < L; ++t)
         if (w[t] > zmax)
@@ -360,7 +433,7 @@ int oracle_split_partials(double *m_out, double *l_out, double *o_out,
             fail = 1;
             continue;
         }
-        logits(z, q, k_cache, x, block_tables, scale, s, h, L, Hq, Hkv, D, BS, MB);
+        logits(z, q + sh * D, k_cache, x, block_tables, scale, s, g, L, D, BS, MB);
         long np = (L + P - 1) / P;
         for (long p = 0; p < np; ++p) {
             long t0 = p * P, t1 = t0 + P < L ? t0 + P : L;

@@ -252,3 +252,103 @@ def make_workload(name: str, seed: int | None = None, device="cuda", poison=True
                        NB=spec.get("NB"), seed=seed, device=device,
                        std=spec.get("std", 1.0), peaky=spec.get("peaky", 0.0),
                        poison=poison, pool_bytes=spec.get("pool_bytes"), name=name)
+
+
+# ---------------------------------------------------------------- several query tokens
+# Workloads of the variable-length form (query tokens per sequence n_s >= 1,
+# the newest n_s of its L_s cached tokens):
+#   chunked_prefill  8 seqs, (32,8,128), BS 16, a 512-token chunk after a
+#                    context of U{0..8192} tokens (L = context + 512)
+#   spec_verify      64 seqs, (32,8,128), BS 16, 4 query tokens (the verification
+#                    step of speculative decoding) after U{512..4096} tokens
+#   prefill          4 seqs, (32,8,128), BS 16, whole 2048-token prompts (n = L)
+VARLEN_WORKLOADS = ["chunked_prefill", "spec_verify", "prefill"]
+
+_VARLEN_SPECS = {
+    "chunked_prefill": dict(S=8, Hq=32, Hkv=8, D=128, BS=16, ctx=("uniform", 0, 8192),
+                            n=("fixed", 512)),
+    "spec_verify": dict(S=64, Hq=32, Hkv=8, D=128, BS=16, ctx=("uniform", 512, 4096),
+                        n=("fixed", 4)),
+    "prefill": dict(S=4, Hq=32, Hkv=8, D=128, BS=16, ctx=("fixed", 0), n=("fixed", 2048)),
+}
+
+
+@dataclass
+class VarlenWorkload:
+    name: str
+    base: Workload                # caches, page tables, total lengths L_s (its q unused)
+    q: torch.Tensor               # fp16 [total_q, Hq, D]
+    cu_seqlens_q: torch.Tensor    # int32 [S+1]
+    q_lens: np.ndarray            # int64 [S]
+    max_q_len: int
+
+    def __getattr__(self, k):     # S, Hq, Hkv, D, BS, MB, NB, scale, caches ... of the base
+        if k == "base":
+            raise AttributeError(k)
+        return getattr(self.base, k)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q_lens.sum())
+
+    def positions(self) -> np.ndarray:
+        """Position of every query row (L_s - n_s + i)."""
+        L = self.base.lens
+        return np.concatenate([np.arange(L[s] - n, L[s]) for s, n in enumerate(self.q_lens)]
+                              or [np.zeros(0, dtype=np.int64)]).astype(np.int64)
+
+    def flops(self) -> int:
+        """4 * D * Hq per (query row, attended token): QK and PV multiply-adds."""
+        return int((self.positions() + 1).sum()) * 4 * self.D * self.Hq
+
+    def compact(self, seqs=None) -> dict:
+        """Numpy inputs of the listed sequences (see Workload.compact)."""
+        if seqs is None:
+            seqs = list(range(self.S))
+        c = self.base.compact(seqs)
+        cu = self.cu_seqlens_q.cpu().numpy()
+        rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs]).astype(np.int64)
+        q = self.q.index_select(0, torch.from_numpy(rows).to(self.q.device)).cpu().numpy()
+        n = self.q_lens[seqs]
+        cu_c = np.zeros(len(seqs) + 1, dtype=np.int32)
+        cu_c[1:] = np.cumsum(n)
+        c.update(q=q, cu_seqlens_q=cu_c)
+        return c
+
+
+def make_varlen(*, S, Hq, Hkv, D, BS, ctx, n, seed=0, device="cpu", std=1.0, poison=True,
+                scale=None, MB=None, NB=None, name="varlen") -> VarlenWorkload:
+    """Caches holding L_s = context_s + n_s tokens per sequence and n_s query
+    rows per sequence.  ``ctx`` and ``n`` are lists or length specs as in
+    make_custom."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 31337)
+    C = _draw_lens(ctx, S, g) if isinstance(ctx, tuple) else np.asarray(ctx, dtype=np.int64)
+    N = _draw_lens(n, S, g) if isinstance(n, tuple) else np.asarray(n, dtype=np.int64)
+    L = C + N
+    if MB is None:
+        MB = max(1, int(((L + BS - 1) // BS).max()) if S else 1)
+    base = make_custom(S=S, Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=list(L), MB=MB, NB=NB, seed=seed,
+                       device=device, std=std, poison=poison, scale=scale, name=name)
+    dev = torch.device(device)
+    gq = torch.Generator(device=dev)
+    gq.manual_seed(seed + 104729)
+    total = int(N.sum())
+    q = (torch.randn((total, Hq, D), generator=gq, device=dev, dtype=torch.float32) * std
+         ).to(torch.float16)
+    cu = np.zeros(S + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(N)
+    return VarlenWorkload(name=name, base=base, q=q, cu_seqlens_q=torch.from_numpy(cu).to(dev),
+                          q_lens=N, max_q_len=int(N.max()) if S else 0)
+
+
+def make_varlen_workload(name: str, seed: int | None = None, device="cuda", poison=True,
+                         **overrides) -> VarlenWorkload:
+    spec = dict(_VARLEN_SPECS[name])
+    spec.update(overrides)
+    if seed is None:
+        seed = 2000 + VARLEN_WORKLOADS.index(name)
+    return make_varlen(S=spec["S"], Hq=spec["Hq"], Hkv=spec["Hkv"], D=spec["D"], BS=spec["BS"],
+                       ctx=spec["ctx"], n=spec["n"], seed=seed, device=device, poison=poison,
+                       name=name)
+

@@ -46,11 +46,19 @@ MUTANTS = [
     ("page reads one past the end", "j < npages ? block_tables", "j <= npages ? block_tables",
      False),
     ("append row off by one", "((L - 1) % BS) * x.token", "(L % BS) * x.token", False),
+    ("varlen: position one early", "- n + (r - cu_q[s]);", "- n + (r - cu_q[s]) - 1;", False),
+    ("varlen: causal bound dropped", "long count = pos + 1;", "long count = seq_lens[s];",
+     False),
+    ("varlen: query row of the sequence, not of the token", "logits(z, q + rh * D,",
+     "logits(z, q + ((long)s * Hq + h) * D,", False),
+    ("varlen: owner of a row off by one", "while (cu_q[s + 1] <= r)", "while (cu_q[s + 1] < r)",
+     False),
 ]
 
 
 def _pins():
     import test_oracle as T
+    import test_oracle_varlen as V
     return [
         ("half decoding", T.test_half_decoding_matches_numpy),
         ("hand case 0", lambda: T.test_hand_cases(0)),
@@ -73,6 +81,12 @@ def _pins():
         ("append closed forms", T.test_append_then_decode_closed_forms),
         ("strided layouts", T.test_strided_layouts_equal_head_major),
         ("strided append", T.test_strided_append_equals_head_major_append),
+        ("varlen hand case", V.test_hand_case),
+        ("varlen sdpa", lambda: V.test_dense_causal_sdpa(8, 2, 4)),
+        ("varlen prefix decode", V.test_each_row_is_a_decode_of_its_prefix),
+        ("varlen n = 1", V.test_single_token_rows_equal_decode),
+        ("varlen prompt row 0", V.test_prompt_first_row_is_v0),
+        ("varlen permutation", V.test_page_permutation_invariance),
     ]
 
 
