@@ -189,6 +189,24 @@ def test_weights_sum_to_one():
             assert abs(wt.sum() - 1.0) <= 1e-12
 
 
+def test_weights_match_dense_softmax():
+    """The weights of every (sequence, query head) against a numpy softmax of
+    the densely gathered keys of KV head h / G."""
+    w = _small(seed=19, Hq=8, Hkv=2, lens=(1, 9, 23))
+    inp = _np(w)
+    K, _ = _dense(w)
+    G = w.Hq // w.Hkv
+    q = w.q.numpy().astype(np.float64)
+    for s in range(w.S):
+        L = int(w.lens[s])
+        for h in range(w.Hq):
+            z = w.scale * (K[s, h // G, :L] @ q[s, h])
+            e = np.exp(z - z.max())
+            ours = oracle.weights(inp["q"], inp["k_cache"], inp["block_tables"], inp["seq_lens"],
+                                  w.scale, s, h)
+            np.testing.assert_allclose(ours, e / e.sum(), rtol=0, atol=1e-13)
+
+
 def test_scale_zero_gives_mean():
     w = _small(seed=6, lens=(2, 11, 29), scale=0.0)
     out = oracle.decode(**_np(w), scale=0.0)

@@ -21,10 +21,9 @@ MUTANTS = [
     ("row within the page takes t / BS", "(t % BS) * x.token", "(t / BS) * x.token", False),
     ("head and token strides swapped", "g * x.head + (t % BS) * x.token",
      "g * x.token + (t % BS) * x.head", False),
-    ("K read with KV head h % Hkv",
-     "    int G = Hq / Hkv;\n    int g = h / G;\n    const uint16_t *qh",
-     "    int G = Hq / Hkv;\n    int g = h % Hkv;\n    const uint16_t *qh", False),
-    ("V read with KV head h % Hkv",
+    ("weights: KV head h % Hkv", "s, h / (Hq / Hkv), L, D, BS, MB);", "s, h % Hkv, L, D, BS, MB);",
+     False),
+    ("decode: KV head h % Hkv",
      "int g = h / G;\n        long L = seq_lens[s];\n        double *o = out + sh * D;",
      "int g = h % Hkv;\n        long L = seq_lens[s];\n        double *o = out + sh * D;", False),
     ("scale dropped", "z[t] = scale * dot;", "z[t] = dot;", False),
@@ -68,6 +67,7 @@ def _pins():
         ("length one", T.test_length_one_returns_v),
         ("constant v", T.test_constant_v),
         ("weights sum", T.test_weights_sum_to_one),
+        ("weights dense", T.test_weights_match_dense_softmax),
         ("scale zero", T.test_scale_zero_gives_mean),
         ("gqa mapping", T.test_gqa_head_mapping),
         ("zero length", T.test_zero_length),
