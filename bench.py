@@ -16,6 +16,10 @@ aggregate: value = N * bytes / max-over-ranks time.
 
 ``--impl reference`` times the CPU oracle (fp64, all host cores) on a
 bounded sample of the same workload instead, as the reference arm.
+
+``--workload chunked_prefill | spec_verify | prefill`` times the
+several-query-token path (paged_gqa_varlen) instead: TFLOP/s against the
+tensor-core roofline where the work is compute-bound, KV GB/s otherwise.
 """
 from __future__ import annotations
 
@@ -427,6 +431,201 @@ def run_ours(args):
     return 0
 
 
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor-core TFLOP/s from MEASURED_PEAKS.json (fp16 runs
+    at the bf16 rate on this part), burst and sustained."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_varlen_bench(args):
+    """Several query tokens per sequence (paged_gqa_varlen): one step is one
+    call over the whole workload.  Compute-bound workloads report TFLOP/s
+    against the tensor roofline, the others KV GB/s against HBM."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_gqa_decode_03_gb300 as pgd
+    from paged_gqa_decode_03_gb300.workloads import make_varlen_workload
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    pgd.load_library()
+
+    w = make_varlen_workload(args.workload, device=dev)
+    flops = w.flops()
+    kv_bytes = w.kv_bytes()
+    alg_bytes = kv_bytes + w.total_q * w.Hq * w.D * (2 + 4)
+    out = torch.empty((w.total_q, w.Hq, w.D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kvp = args.partition or 0
+
+    def call(q, cu, bt, sl):
+        pgd.paged_gqa_varlen(out, q, cu, w.k_cache, w.v_cache, bt, sl, w.scale, w.max_q_len,
+                             kv_partition=kvp, stream=stream)
+
+    def step():
+        call(w.q, w.cu_seqlens_q, w.block_tables, w.seq_lens)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pgd.pgd_check_device_error(stream) == 0
+    PK = pgd.pgd_last_partition_size()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for _ in range(max(args.warmup, 3)):
+            step()
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+        for i in range(args.steps):  # per-call events (kernel time incl. its reduce if any)
+            kb[i].record(stream)
+            step()
+            ka[i].record(stream)
+        barrier()
+    clocks = clk.summary()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(args.steps))
+    tflops = flops * world / (ms * 1e-3) / 1e12
+    kv_gbs = kv_bytes * world / (ms * 1e-3) / 1e9
+    peak_t, peak_t_sus, peak_kind = measured_tensor_peak()
+    peak_b, _ = measured_peaks()
+    intensity = flops / alg_bytes
+    tensor_bound = intensity > peak_t * 1e12 / (peak_b * 1e9)
+
+    # e2e: per step the step's inputs (q, cu_seqlens_q, block_tables, seq_lens)
+    # host -> device in one packed pinned copy, the call, the output back
+    def _align(x):
+        return (x + 255) // 256 * 256
+    parts = [(w.q, torch.float16), (w.cu_seqlens_q, torch.int32), (w.block_tables, torch.int32),
+             (w.seq_lens, torch.int32)]
+    offs, nin = [], 0
+    for t, _ in parts:
+        offs.append(nin)
+        nin += _align(t.numel() * t.element_size())
+    h_in = torch.empty(nin, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nin, dtype=torch.uint8, device=dev)
+    views = []
+    for (t, dt), o in zip(parts, offs):
+        nb = t.numel() * t.element_size()
+        h_in[o:o + nb].view(dt).copy_(t.cpu().view(-1))
+        views.append(d_in[o:o + nb].view(dt).view(t.shape))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t, _ in parts)
+    d2h = out_h.numel() * 4
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        call(*views)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    barrier()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) / e2e_steps * 1e3, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        seqs = [0]
+        c = w.compact(seqs)
+        rows = int(w.q_lens[0])
+        sub_flops = int((w.positions()[:rows] + 1).sum()) * 4 * w.D * w.Hq
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.varlen(c["q"], c["cu_seqlens_q"], c["k_cache"], c["v_cache"],
+                          c["block_tables"], c["seq_lens"], c["scale"])
+            reps += 1
+            if time.perf_counter() - t0 >= args.cpu_seconds:
+                break
+        sec = (time.perf_counter() - t0) / reps
+        cpu = {"value": sub_flops / sec / 1e12 if tensor_bound else
+                        int(c["seq_lens"][0]) * w.Hkv * w.D * 4 / sec / 1e9,
+               "unit": "TFLOP/s" if tensor_bound else "GB/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"sequence 0 of {args.workload} ({rows} query rows), {reps} reps, "
+                         f"fp64 C oracle, {sec * 1e3:.1f} ms per call"}
+
+    if rank == 0:
+        if tensor_bound:
+            metric = "paged varlen attention (several query tokens per sequence): TFLOP/s"
+            value, unit = tflops, "TFLOP/s"
+            achieved = flops / (kern_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                    "frac": achieved / peak_t, "frac_of_sustained": achieved / peak_t_sus,
+                    "traffic": None,
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS bf16_tflops; fp16 at the bf16 rate)",
+                    "algorithmic_flops_per_launch": flops}
+            e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+        else:
+            metric = "paged varlen attention (several query tokens per sequence): KV-cache GB/s"
+            value, unit = kv_gbs, "GB/s"
+            achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peak_b, "unit": "GB/s",
+                    "frac": achieved / peak_b, "traffic": None,
+                    "peak_source": "measured (MEASURED_PEAKS hbm_gbs)",
+                    "algorithmic_bytes_per_launch": alg_bytes}
+            e2e_val = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
+        roof.update(kernel="paged_varlen_kernel", kernel_ms=kern_ms)
+        line = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "us_per_call": ms * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "tflops": tflops, "kv_gbs": kv_gbs,
+            "config": {"workload": args.workload, "num_seqs": w.S, "total_q": w.total_q,
+                       "max_q_len": w.max_q_len, "gqa": [w.Hq, w.Hkv, w.D],
+                       "block_size": w.BS, "kv_partition": PK,
+                       "flops_per_step": flops, "kv_bytes_per_step": kv_bytes,
+                       "l2": "no flush: K/V + q + out per step exceed the 129 MB L2"
+                             if alg_bytes > 129e6 else "K/V bytes fit L2: warm-cache figure",
+                       "accumulate": "fp32 (tcgen05, tensor memory)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,6 +644,13 @@ def main():
     ap.add_argument("--ref-sample-bytes", type=float, default=1.6e8)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()
+    from paged_gqa_decode_03_gb300.workloads import VARLEN_WORKLOADS
+    if args.workload in VARLEN_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the reference arm times the decode workloads only"}))
+            return 0
+        return run_varlen_bench(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

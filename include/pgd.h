@@ -250,6 +250,55 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                                     int block_size, int partition_size, int max_blocks_per_seq,
                                     int num_blocks, void *stream);
 
+/*
+ * paged_gqa_varlen — attention for several query tokens per sequence over the
+ * paged cache: the unified paged variable-length form of "vllm-metal"
+ * (introduction and "Three Metal kernels": prefill chunks, decode steps and
+ * the verification step of speculative decoding in one call).  A decode step
+ * is the case of one query token per sequence.
+ *
+ * Sequence s has n_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] query tokens, rows
+ * cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 of q; they are its newest n_s cached
+ * tokens (their K and V already written to the cache), so query i sits at
+ * position seq_lens[s] - n_s + i and attends every cached token t up to and
+ * including that position (causal).  For every query row r and head h:
+ *     out[r][h][:] = softmax( q[r][h] . K^T * scale over t <= pos ) . V
+ *
+ * q             [total_q][num_q_heads][head_dim] fp16, 16-byte aligned
+ * cu_seqlens_q  [num_seqs + 1] int32, cu[0] = 0, non-decreasing, cu[S] = total_q
+ * out           [total_q][num_q_heads][head_dim] fp32, written
+ * max_q_len     bound on every n_s (sizes the launch)
+ * cache arrays, strides, block_tables, seq_lens, scale: as for
+ *               paged_gqa_decode_strided.
+ * kv_partition  tokens per split-KV partition: 0 lets the library choose
+ *               (no split when the query tiles alone fill the GPU), else a
+ *               multiple of 128 (head_dim 64, 128) or 64 (head_dim 256).
+ * workspace     NULL: library scratch; else at least pgd_varlen_plan's bytes,
+ *               256-byte aligned.
+ *
+ * Supported: head_dim 64/128/256, block sizes 8..128, groups of up to 128
+ * query heads per KV head.  Runs on the tcgen05 tensor cores.  Device-side
+ * checks as for the decode: a sequence whose n_s is negative, above its
+ * length or above max_q_len sets PGD_DEVERR_QUERY_LEN and is skipped (its
+ * output rows are not written).
+ */
+#define PGD_DEVERR_QUERY_LEN 8u
+
+pgd_status paged_gqa_varlen(float *out, const uint16_t *q, const int32_t *cu_seqlens_q,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                            int num_seqs, int total_q, int max_q_len, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_blocks, int64_t page_stride,
+                            int64_t head_stride, int64_t token_stride, int kv_partition,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* The KV partition a paged_gqa_varlen call with these sizes would use and the
+ * scratch bytes it needs (0: no partials).  Does not launch. */
+pgd_status pgd_varlen_plan(int num_seqs, int total_q, int max_q_len, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                           int kv_partition, int *chosen_kv_partition, size_t *workspace_bytes);
+
 /* Partition size used by this thread's last successful call (0 if none);
  * the diagnostic of the pages' "Hands-on" section. */
 int pgd_last_partition_size(void);
@@ -278,7 +327,8 @@ pgd_status pgd_set_timing_events(void *before, void *after);
 pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas_per_sm);
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: strided caches,
- * head_dim 64, block sizes 64 and 128). */
+ * head_dim 64, block sizes 64 and 128; 1.2.0: several query tokens per
+ * sequence). */
 int pgd_version(void);
 
 #ifdef __cplusplus

@@ -27,7 +27,8 @@ import threading
 import torch
 
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
-           "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides", "pgd_plan", "pgd_last_partition_size",
+           "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
+           "paged_gqa_varlen", "pgd_varlen_plan", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -38,7 +39,7 @@ _lib = None
 
 STATUS_NAMES = {0: "PGD_OK", 1: "PGD_ERR_INVALID_ARG", 2: "PGD_ERR_UNSUPPORTED",
                 3: "PGD_ERR_WORKSPACE", 4: "PGD_ERR_CUDA", 5: "PGD_ERR_DEVICE"}
-DEVERR_PAGE_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_PAGE_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_QUERY_LEN = 1, 2, 4, 8
 
 # Every exported symbol of include/pgd.h with its ctypes signature.
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -49,6 +50,8 @@ SIGNATURES = {
     "paged_gqa_decode_noalloc": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_append": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_strided": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_L] * 3 + [_P, _Z, _P, _P]),
+    "paged_gqa_varlen": (_I, [_P] * 7 + [_F] + [_I] * 9 + [_L] * 3 + [_I, _P, _Z, _P]),
+    "pgd_varlen_plan": (_I, [_I] * 9 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -257,6 +260,60 @@ def paged_gqa_decode_strided(out, q, k_cache, v_cache, block_tables, seq_lens, s
         int(partition_size), MB, NB, sp, sh, st_, _ptr(workspace), ws_bytes, _ptr(page_trace),
         _stream_handle(stream, q.device))
     _raise(st)
+
+
+def paged_gqa_varlen(out, q, cu_seqlens_q, k_cache, v_cache, block_tables, seq_lens, scale,
+                     max_q_len: int, kv_partition: int = 0, layout=None, workspace=None,
+                     stream=None) -> None:
+    """Causal attention of several query tokens per sequence (q, out:
+    [total_q, Hq, D]; sequence s owns rows cu_seqlens_q[s]..cu_seqlens_q[s+1]-1,
+    its newest tokens).  Caches head-major [NB, Hkv, BS, D], or any tensors
+    with ``layout = (num_kv_heads, block_size, num_blocks, strides)``."""
+    lib = load_library()
+    _check(q, "q", torch.float16, 3)
+    _check(out, "out", torch.float32, 3)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    T, Hq, D = q.shape
+    S = seq_lens.shape[0]
+    if out.shape != q.shape or cu_seqlens_q.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise ValueError("inconsistent shapes of q, out, cu_seqlens_q, block_tables, seq_lens")
+    if layout is None:
+        _check(k_cache, "k_cache", torch.float16, 4)
+        _check(v_cache, "v_cache", torch.float16, 4)
+        NB, Hkv, BS, D2 = k_cache.shape
+        if v_cache.shape != k_cache.shape or D2 != D:
+            raise ValueError("k_cache / v_cache shapes")
+        strides = kv_strides("head_major", Hkv, BS, D)
+    else:
+        Hkv, BS, NB, strides = layout
+    _check_rows_inside(k_cache, "k_cache", NB, Hkv, BS, D, strides)
+    _check_rows_inside(v_cache, "v_cache", NB, Hkv, BS, D, strides)
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    sp, sh, st_ = (int(x) for x in strides)
+    st = lib.paged_gqa_varlen(
+        _ptr(out), _ptr(q), _ptr(cu_seqlens_q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(seq_lens), float(scale), S, T, int(max_q_len), Hq, int(Hkv), D, int(BS),
+        block_tables.shape[1], int(NB), sp, sh, st_, int(kv_partition), _ptr(workspace),
+        ws_bytes, _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def pgd_varlen_plan(num_seqs, total_q, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                    block_size, max_blocks_per_seq, kv_partition=0):
+    """(KV partition used, scratch bytes needed) of a paged_gqa_varlen call."""
+    lib = load_library()
+    pk = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    _raise(lib.pgd_varlen_plan(num_seqs, total_q, max_q_len, num_q_heads, num_kv_heads,
+                               head_dim, block_size, max_blocks_per_seq, kv_partition,
+                               ctypes.byref(pk), ctypes.byref(b)))
+    return pk.value, b.value
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # PGD_NOALLOC_SCRATCH_BYTES of include/pgd.h

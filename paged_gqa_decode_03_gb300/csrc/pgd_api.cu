@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -606,6 +607,204 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     return PGD_OK;
 }
 
+// ------------------------------------------------------------------ several query tokens
+// q [total_q][Hq][D] viewed as a 4-D tensor, innermost first: 64 halves x Hq
+// heads (D*2 bytes apart) x total_q tokens (Hq*D*2 apart) x D/64 slabs (128
+// bytes apart); a box of 64 x G x TQ x 1 is one slab of a 128-row tile (TQ
+// tokens x the G heads of a group), landing row-major as [token][head][128 B].
+pgd_status encode_q_map(CUtensorMap *map, const void *q, int total_q, int Hq, int D, int G,
+                        int TQ)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    cuuint64_t dims[4] = {64, (cuuint64_t)Hq, (cuuint64_t)total_q, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2, 128};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)TQ, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (CUresult %d)", (int)r);
+    return PGD_OK;
+}
+
+struct VarlenPlan {
+    int G, TQ, QT, PK, NP, NT;
+    long long grid;
+    size_t ws_bytes, off_l, off_o;
+};
+
+int varlen_tokens_per_stage(int D) { return D == 64 ? VShape<64>::NT : D == 128 ? VShape<128>::NT : VShape<256>::NT; }
+
+// Work split of the multi-token path: 128-row tiles of (query token, head)
+// per (sequence, KV head); the KV range is cut into partitions of PK tokens
+// only when the tiles alone (counted at max_q_len) would not give every SM
+// two units.  Scratch (partials) only when some row spans two partitions.
+pgd_status make_varlen_plan(int S, int total_q, int max_q, int Hq, int Hkv, int D, int BS,
+                            int MB, int kv_partition, VarlenPlan *vp)
+{
+    pgd_status st;
+    if (S < 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_seqs %d < 0", S);
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return fail(PGD_ERR_INVALID_ARG, "head counts %d / %d", Hq, Hkv);
+    if (Hq / Hkv > 128)
+        return fail(PGD_ERR_UNSUPPORTED, "GQA group of %d query heads exceeds 128", Hq / Hkv);
+    if (!supported_head_dim(D))
+        return fail(PGD_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", D);
+    if (!supported_block_size(BS))
+        return fail(PGD_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32, 64, 128}", BS);
+    if (MB <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", MB);
+    if ((long long)MB * BS > (1ll << 30))
+        return fail(PGD_ERR_UNSUPPORTED, "length bound %lld above 2^30", (long long)MB * BS);
+    if (total_q < 0 || max_q < 0 || (total_q > 0 && max_q < 1))
+        return fail(PGD_ERR_INVALID_ARG, "total_q %d / max_q_len %d", total_q, max_q);
+    vp->NT = varlen_tokens_per_stage(D);
+    if (kv_partition < 0 || (kv_partition > 0 && kv_partition % vp->NT != 0))
+        return fail(PGD_ERR_INVALID_ARG, "kv_partition %d: 0 or a positive multiple of %d",
+                    kv_partition, vp->NT);
+    DeviceState *ds;
+    if ((st = device_state(&ds)))
+        return st;
+    vp->G = Hq / Hkv;
+    vp->TQ = 128 / vp->G;
+    vp->QT = (max_q + vp->TQ - 1) / vp->TQ;
+    const long long maxlen = (long long)MB * BS;
+    const long long whole = (maxlen + vp->NT - 1) / vp->NT * vp->NT;
+    const long long tiles = (long long)S * Hkv * vp->QT;
+    const size_t rows = (size_t)total_q * Hq;
+    auto ws_for = [&](int NP) -> size_t {
+        if (NP <= 1)
+            return 0;
+        return align256(rows * NP * 4) * 2 + align256(rows * NP * D * 4);
+    };
+    long long PK;
+    if (kv_partition > 0) {
+        PK = kv_partition;
+    } else {
+        const long long target = 2ll * ds->num_sms;
+        PK = whole;
+        if (tiles > 0 && tiles < target) {
+            const long long want = (target + tiles - 1) / tiles;
+            PK = std::max<long long>(4ll * vp->NT, ((maxlen + want - 1) / want + vp->NT - 1) /
+                                                       vp->NT * vp->NT);
+        }
+        while (PK < whole && ws_for((int)((maxlen + PK - 1) / PK)) > kMaxWorkspaceBytes)
+            PK *= 2;
+    }
+    if (PK > whole)
+        PK = whole > 0 ? whole : vp->NT;
+    vp->PK = (int)PK;
+    vp->NP = (int)((maxlen + PK - 1) / PK);
+    if (vp->NP < 1)
+        vp->NP = 1;
+    vp->ws_bytes = ws_for(vp->NP);
+    vp->off_l = align256(rows * vp->NP * 4);
+    vp->off_o = 2 * vp->off_l;
+    if (vp->ws_bytes > kMaxWorkspaceBytes)
+        return fail(PGD_ERR_WORKSPACE, "partials need %zu bytes, above the %zu-byte cap",
+                    vp->ws_bytes, kMaxWorkspaceBytes);
+    vp->grid = tiles * vp->NP;
+    if (vp->grid >= (1ll << 31))
+        return fail(PGD_ERR_UNSUPPORTED, "%lld work units", vp->grid);
+    return PGD_OK;
+}
+
+pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const uint16_t *k_cache,
+                      const uint16_t *v_cache, const int32_t *block_tables,
+                      const int32_t *seq_lens, float scale, int S, int total_q, int max_q, int Hq,
+                      int Hkv, int D, int BS, int MB, int NB, const Strides &kv_strides,
+                      int kv_partition, void *workspace, size_t ws_bytes, void *stream_v)
+{
+    VarlenPlan vp;
+    pgd_status st = make_varlen_plan(S, total_q, max_q, Hq, Hkv, D, BS, MB, kv_partition, &vp);
+    if (st)
+        return st;
+    if (S == 0 || total_q == 0) {
+        t_last_error.clear();
+        return PGD_OK;
+    }
+    if (!out || !q || !cu_q || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return fail(PGD_ERR_INVALID_ARG, "null array argument");
+    if (!std::isfinite(scale))
+        return fail(PGD_ERR_INVALID_ARG, "scale is not finite");
+    if (NB <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_blocks %d <= 0", NB);
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return fail(PGD_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(cu_q, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return fail(PGD_ERR_INVALID_ARG, "int32 arrays must be 4-byte aligned");
+    if ((st = check_strides(kv_strides, D)))
+        return st;
+    DeviceState *ds;
+    if ((st = device_state(&ds)))
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaError_t e;
+    char *ws = static_cast<char *>(workspace);
+    const bool own = workspace == nullptr;
+    if (vp.ws_bytes) {
+        if (own) {
+            cudaMemPool_t pool;
+            if ((st = device_pool(*ds, &pool)))
+                return st;
+            if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), vp.ws_bytes, pool,
+                                             stream)) != cudaSuccess)
+                return cuda_fail(e, "scratch allocation");
+        } else if (ws_bytes < vp.ws_bytes || !aligned(ws, 256)) {
+            return fail(PGD_ERR_WORKSPACE, "workspace of %zu bytes (256-byte aligned) given, %zu needed",
+                        ws_bytes, vp.ws_bytes);
+        }
+    }
+    CUtensorMap tq;
+    const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
+    const CUtensorMap *tk = nullptr, *tv = nullptr;
+    if ((st = encode_q_map(&tq, q, total_q, Hq, D, vp.G, vp.TQ)) ||
+        (st = cache_maps(k_cache, v_cache, geom, 8, &tk, &tv))) {
+        if (own && ws)
+            cudaFreeAsync(ws, stream);
+        return st;
+    }
+    VarlenParams p = {};
+    p.out = out;
+    p.cu_q = cu_q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.ws_m = vp.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr;
+    p.ws_l = vp.ws_bytes ? reinterpret_cast<float *>(ws + vp.off_l) : nullptr;
+    p.ws_o = vp.ws_bytes ? reinterpret_cast<float *>(ws + vp.off_o) : nullptr;
+    p.err = ds->err_word;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.S = S;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = vp.G;
+    p.TQ = vp.TQ;
+    p.QT = vp.QT;
+    p.NP = vp.NP;
+    p.PK = vp.PK;
+    p.MB = MB;
+    p.NB = NB;
+    p.BS = BS;
+    p.max_q = max_q;
+    p.wait_budget_ns = kWaitBudgetNs;
+    e = launch_varlen(D, tq, *tk, *tv, p, (int)vp.grid, vp.NP > 1 ? total_q * Hq : 0, stream);
+    if (own && ws) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess)
+            e = e2;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kernel launch");
+    t_last_partition = vp.PK;
+    t_last_error.clear();
+    return PGD_OK;
+}
+
 // Device address of pgd_noalloc_scratch, looked up once per device (with
 // that device current) on the first paged_gqa_decode_noalloc call there.
 struct NoAllocScratch {
@@ -732,6 +931,38 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                nullptr, stream, static_cast<unsigned *>(scratch));
 }
 
+pgd_status paged_gqa_varlen(float *out, const uint16_t *q, const int32_t *cu_seqlens_q,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                            int num_seqs, int total_q, int max_q_len, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_blocks, int64_t page_stride,
+                            int64_t head_stride, int64_t token_stride, int kv_partition,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    return run_varlen(out, q, cu_seqlens_q, k_cache, v_cache, block_tables, seq_lens, scale,
+                      num_seqs, total_q, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks,
+                      Strides{page_stride, head_stride, token_stride}, kv_partition, workspace,
+                      workspace_bytes, stream);
+}
+
+pgd_status pgd_varlen_plan(int num_seqs, int total_q, int max_q_len, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                           int kv_partition, int *chosen_kv_partition, size_t *workspace_bytes)
+{
+    VarlenPlan vp;
+    pgd_status st = make_varlen_plan(num_seqs, total_q, max_q_len, num_q_heads, num_kv_heads,
+                                     head_dim, block_size, max_blocks_per_seq, kv_partition, &vp);
+    if (st)
+        return st;
+    if (chosen_kv_partition)
+        *chosen_kv_partition = vp.PK;
+    if (workspace_bytes)
+        *workspace_bytes = vp.ws_bytes;
+    return PGD_OK;
+}
+
 pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                     int block_size, int partition_size, int max_blocks_per_seq,
                     int *chosen_partition_size, size_t *workspace_bytes)
@@ -798,6 +1029,6 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
     return PGD_OK;
 }
 
-int pgd_version(void) { return 10100; }
+int pgd_version(void) { return 10200; }
 
 }  // extern "C"

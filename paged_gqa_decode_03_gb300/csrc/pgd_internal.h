@@ -106,4 +106,47 @@ cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
 // sequence) and keep every CTA resident at once, four for 256.
 template <int D> __host__ __device__ constexpr int reduce_threads() { return D <= 128 ? 64 : 128; }
 
+// ---------------------------------------------------------------- several query tokens
+// Paged attention with n_s >= 1 query tokens per sequence (pgd_varlen.cu).
+// A work unit is 128 rows of one (sequence, KV head): TQ = 128 / G query
+// tokens x the G heads of the group, over one KV partition of PK tokens.
+constexpr unsigned kErrQueryLen = 8u;  // a query count < 0, > its length or > max_q_len
+
+// KV tokens per pipeline stage (NT) and stages (NSTG) per head_dim; the
+// 128-row tiles and both score buffers live in 512 tensor-memory columns.
+template <int D> struct VShape;
+template <> struct VShape<64> {
+    static constexpr int NT = 128, NSTG = 3;
+};
+template <> struct VShape<128> {
+    static constexpr int NT = 128, NSTG = 2;
+};
+template <> struct VShape<256> {
+    static constexpr int NT = 64, NSTG = 2;
+};
+template <int D> __host__ __device__ constexpr size_t varlen_smem_bytes()
+{
+    // Q tile + stages of K and V + the fp16 P tile + alignment slack
+    return size_t(128) * D * 2 + size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 +
+           size_t(128) * VShape<D>::NT * 2 + 1024;
+}
+constexpr int kVarlenThreads = 192;   // producer warp, MMA warp, 4 softmax warps
+constexpr uint32_t kVarlenTmemCols = 512;
+
+struct VarlenParams {
+    float *out;                   // [total_q][Hq][D]
+    const int32_t *cu_q;          // [S+1]
+    const int32_t *block_tables;  // [S][MB]
+    const int32_t *seq_lens;      // [S]
+    float *ws_m, *ws_l, *ws_o;    // [total_q*Hq][NP] (m, l), [total_q*Hq][NP][D]
+    unsigned *err;
+    float scale_log2;
+    int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, max_q;
+    uint64_t wait_budget_ns;
+};
+
+cudaError_t launch_varlen(int head_dim, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,
+                          cudaStream_t stream);
+
 }  // namespace pgd

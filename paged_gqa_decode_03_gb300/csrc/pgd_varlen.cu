@@ -1,0 +1,492 @@
+// Paged attention with several query tokens per sequence on the 5th-generation
+// tensor cores (sm_103a): the unified paged variable-length attention of
+// "vllm-metal" (introduction and "Three Metal kernels": prefill chunks, decode
+// and the verification step of speculative decoding in one kernel).  Query
+// token i of sequence s sits at position seq_lens[s] - n_s + i and attends
+// every cached token up to it (causal).
+//
+// paged_varlen_kernel<D> — one CTA per work unit: 128 rows (TQ = 128 / G query
+// tokens x the G query heads of one KV head; the group shares every K/V page,
+// "Metal parallel model") over one KV partition.
+//   * warp 0, producer: the Q tile (one 4-D tensor copy per 64-wide slab of
+//     head_dim) and, per stage of NT tokens, the K and V rows of the pages in
+//     the stage as 8-row tensor copies through the cache's 5-D map, landing
+//     as [8-row group][slab][row][128 B] (128-byte swizzle) — a K-major
+//     operand for S = Q K^T and an MN-major one for O += P V.
+//   * warp 1, MMA: one thread issues tcgen05.mma (fp16 in, fp32 in tensor
+//     memory): S_j = Q K_j^T into one of two score buffers, then, once the
+//     softmax has written P_{j-1}, O += P_{j-1} V_{j-1}; completion is
+//     signalled through mbarriers with tcgen05.commit.
+//   * warps 2-5, softmax: thread r owns row r.  Per stage it reads its 128
+//     (64) scores from tensor memory, masks them causally, and runs the
+//     log2-space online softmax with exp2 ("Four speed-up tricks", 1); the
+//     reference max only moves when a score exceeds it by more than 2^8
+//     (p <= 256 stays exact in fp16), and only then is the row of O rescaled
+//     in tensor memory.  P goes to shared memory as fp16 (K-major, swizzled).
+//     At the end: out = O / l, or the partition partial (log2-space max,
+//     exp-sum, normalised output, "Four speed-up tricks", 4).
+// paged_varlen_reduce_kernel<D> — merges the partials of rows that span more
+//   than one KV partition.
+#include "pgd_device.cuh"
+#include "pgd_internal.h"
+
+namespace pgd {
+
+template <int D>
+__global__ void __launch_bounds__(kVarlenThreads, 1)
+    paged_varlen_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const VarlenParams p)
+{
+    constexpr int NT = VShape<D>::NT, NSTG = VShape<D>::NSTG;
+    constexpr int SLABS = D / 64;
+    constexpr int GROUP = SLABS * 1024;     // one 8-row group of K or V, all slabs
+    constexpr int KV_TILE = NT * D * 2;     // K (or V) of one stage
+    constexpr int Q_SLAB = 128 * 128;       // one 64-wide slab of the 128-row Q / P tile
+    constexpr uint32_t S_COL = 0, O_COL = 2 * NT;  // tensor-memory columns
+    static_assert(O_COL + D <= kVarlenTmemCols, "tensor memory");
+    constexpr uint32_t IDESC_S = tc_idesc_f16(128, NT, 0, 0);
+    constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, 0, 1);
+
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t q_full, kv_full[NSTG], kv_empty[NSTG], s_full[2], p_full,
+        o_done, mma_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag;
+
+    // ---- the unit: (sequence, KV head, query tile, KV partition); query
+    // tiles in decreasing order so the longest causal ranges start first
+    int u = blockIdx.x;
+    const int part = u % p.NP;
+    u /= p.NP;
+    const int qt = p.QT - 1 - u % p.QT;
+    u /= p.QT;
+    const int g = u % p.Hkv;
+    const int s = u / p.Hkv;
+    const int maxlen = p.MB * p.BS;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > maxlen ? maxlen : L);
+    const int row0 = __ldg(p.cu_q + s);
+    int n = __ldg(p.cu_q + s + 1) - row0;
+    if (n < 0 || n > L || n > p.max_q) {
+        if (qt == p.QT - 1 && g == 0 && part == 0 && threadIdx.x == 0)
+            atomicOr(p.err, kErrQueryLen);
+        n = 0;
+    }
+    const int i0 = qt * p.TQ;
+    if (i0 >= n)
+        return;
+    const int ni = min(p.TQ, n - i0);
+    const int kv_lo = part * p.PK;
+    const int kv_hi = min(kv_lo + p.PK, L - n + i0 + ni);
+    if (kv_lo >= kv_hi)
+        return;
+    const int j0 = kv_lo / NT;
+    const int ntiles = (kv_hi + NT - 1) / NT - j0;
+
+    const uint32_t dyn_base = smem_addr(dyn_smem);
+    const uint32_t base = (dyn_base + 1023u) & ~1023u;
+    uint8_t *const base_ptr = dyn_smem + (base - dyn_base);
+    const uint32_t q_s = base;
+    const uint32_t kv_s = q_s + 128 * D * 2;              // stage st: K at +st*2*KV_TILE, V after
+    const uint32_t p_s = kv_s + NSTG * 2 * KV_TILE;
+    uint8_t *const kv_ptr = base_ptr + 128 * D * 2;
+    uint8_t *const p_ptr = base_ptr + 128 * D * 2 + NSTG * 2 * KV_TILE;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&q_full), 1);
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(smem_addr(&kv_full[i]), 1);
+            mbar_init(smem_addr(&kv_empty[i]), 1);
+        }
+        mbar_init(smem_addr(&s_full[0]), 1);
+        mbar_init(smem_addr(&s_full[1]), 1);
+        mbar_init(smem_addr(&p_full), 4);
+        mbar_init(smem_addr(&o_done), 1);
+        mbar_init(smem_addr(&mma_done), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1)
+        tc_alloc(smem_addr(&tmem_base_s), kVarlenTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    griddep_launch_dependents();
+
+    auto give_up = [&]() {
+        if (!abort_flag)
+            atomicOr(p.err, kErrTimeout);
+        abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ============================================================ producer
+        const uint64_t pol = l2_evict_first_policy();
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_q);
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+            mbar_arrive_expect_tx(smem_addr(&q_full), SLABS * p.TQ * p.G * 128);
+            for (int sl = 0; sl < SLABS; ++sl)
+                tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
+                            smem_addr(&q_full));
+        }
+        const int npages = (L + p.BS - 1) / p.BS;
+        const int32_t *bt = p.block_tables + (size_t)s * p.MB;
+        int issued = 0;
+        for (int jj = 0; jj < ntiles; ++jj, ++issued) {
+            const int st = jj % NSTG;
+            bool w = true;
+            if (lane == 0)
+                w = mbar_wait_bounded(smem_addr(&kv_empty[st]), ((jj / NSTG) & 1) ^ 1,
+                                      &abort_flag, p.wait_budget_ns);
+            if (!__shfl_sync(~0u, w, 0)) {
+                if (lane == 0)
+                    give_up();
+                break;
+            }
+            const int t0 = (j0 + jj) * NT;
+            // page ids of the stage, one per lane (at most NT / 8 pages)
+            const int pg0 = t0 / p.BS;
+            const int pg = pg0 + lane;
+            int id = -1;
+            if (lane < NT / 8 && pg < npages) {
+                id = __ldg(bt + pg);
+                if ((unsigned)id >= (unsigned)p.NB) {
+                    atomicOr(p.err, kErrPageRange);
+                    id = -1;  // wholly outside the tensor: the copies read zeros
+                }
+            }
+            const uint32_t fb = smem_addr(&kv_full[st]);
+            if (lane == 0)
+                mbar_arrive_expect_tx(fb, 2 * KV_TILE);
+            const uint32_t ks = kv_s + st * 2 * KV_TILE;
+#pragma unroll 1
+            for (int gi = 0; gi < NT / 8; ++gi) {
+                const int tt = t0 + 8 * gi;
+                const int cid = __shfl_sync(~0u, id, tt / p.BS - pg0);
+                if (lane == 0) {
+                    const int r0 = tt % p.BS;
+                    tma_load_5d(ks + gi * GROUP, &tmap_k, 0, r0, 0, g, cid, fb, pol);
+                    tma_load_5d(ks + KV_TILE + gi * GROUP, &tmap_v, 0, r0, 0, g, cid, fb, pol);
+                }
+            }
+        }
+        if (abort_flag && lane == 0) {
+            // let this CTA's copies in flight land before it exits
+            mbar_wait_bounded(smem_addr(&q_full), 0, nullptr, p.wait_budget_ns);
+            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i)
+                mbar_wait_bounded(smem_addr(&kv_full[i % NSTG]), (i / NSTG) & 1, nullptr,
+                                  p.wait_budget_ns);
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issue
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, &abort_flag, p.wait_budget_ns);
+            auto issue_pv = [&](int jj) -> bool {
+                if (!mbar_wait_bounded(smem_addr(&p_full), jj & 1, &abort_flag, p.wait_budget_ns))
+                    return false;
+                tc_fence_after();
+                const int st = jj % NSTG;
+                const uint32_t vs = kv_s + st * 2 * KV_TILE + KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < NT / 16; ++kk) {
+                    const uint64_t a = tc_sdesc(p_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
+                    const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
+                    tc_mma(tmem + O_COL, a, b, IDESC_O, jj > 0 || kk > 0);
+                }
+                tc_commit(smem_addr(&o_done));
+                tc_commit(smem_addr(&kv_empty[st]));
+                return true;
+            };
+            for (int jj = 0; ok && jj < ntiles; ++jj) {
+                const int st = jj % NSTG;
+                if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (jj / NSTG) & 1, &abort_flag,
+                                       p.wait_budget_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ks = kv_s + st * 2 * KV_TILE;
+                const uint32_t sd = tmem + S_COL + (jj & 1) * NT;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = tc_sdesc(q_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
+                    const uint64_t b = tc_sdesc(ks + (kk / 4) * 1024 + (kk % 4) * 32, 16, GROUP);
+                    tc_mma(sd, a, b, IDESC_S, kk > 0);
+                }
+                tc_commit(smem_addr(&s_full[jj & 1]));
+                if (jj > 0 && !issue_pv(jj - 1))
+                    ok = false;
+            }
+            if (ok)
+                ok = issue_pv(ntiles - 1);
+            if (!ok)
+                give_up();
+            // every MMA issued here has completed before the memory is freed
+            tc_commit(smem_addr(&mma_done));
+            mbar_wait_bounded(smem_addr(&mma_done), 0, nullptr, p.wait_budget_ns);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ softmax
+        const int quarter = warp & 3;                 // tensor-memory lanes 32*quarter ..
+        const int r = 32 * quarter + lane;            // this thread's row
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * quarter) << 16);
+        const int ti = r / p.G, hj = r - ti * p.G;
+        const bool row_ok = r < p.TQ * p.G && ti < ni;
+        const int pos = row_ok ? L - n + i0 + ti : -1;
+        const int lim = min(pos, kv_hi - 1);          // last token this row sees here
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        const int last_page_end = ((L + p.BS - 1) / p.BS) * p.BS;
+        for (int jj = 0; jj < ntiles; ++jj) {
+            const int t0 = (j0 + jj) * NT;
+            if (!mbar_wait_bounded(smem_addr(&s_full[jj & 1]), (jj >> 1) & 1, &abort_flag,
+                                   p.wait_budget_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[NT];
+#pragma unroll
+            for (int c = 0; c < NT / 32; ++c) {
+                float v[32];
+                tc_ld32(t_lane + S_COL + (jj & 1) * NT + 32 * c, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[32 * c + i] = v[i];
+            }
+            tc_wait_ld();
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < NT; ++c) {
+                x[c] = t0 + c <= lim ? x[c] * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, x[c]);
+            }
+            // lazy reference max: moves only by more than 8 (log2 units)
+            bool rescale = false;
+            float alpha = 1.f;
+            if (mt > m_ref + 8.f) {
+                rescale = m_ref != -INFINITY;
+                alpha = rescale ? ex2(m_ref - mt) : 1.f;
+                m_ref = mt;
+            }
+            uint32_t pk[NT / 2];
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < NT; c += 2) {
+                const float a = m_ref == -INFINITY ? 0.f : ex2(x[c] - m_ref);
+                const float b = m_ref == -INFINITY ? 0.f : ex2(x[c + 1] - m_ref);
+                pk[c / 2] = pack_half2(a, b);
+                const float2 f = unpack_half2(pk[c / 2]);
+                sum += f.x + f.y;
+            }
+            l = l * alpha + sum;
+            // the previous P V has finished: O may be rescaled, P overwritten
+            if (jj > 0) {
+                if (!mbar_wait_bounded(smem_addr(&o_done), (jj - 1) & 1, &abort_flag,
+                                       p.wait_budget_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(~0u, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float v[32];
+                        tc_ld32(t_lane + O_COL + 32 * c, v);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] *= alpha;
+                        tc_st32(t_lane + O_COL + 32 * c, v);
+                    }
+                    tc_wait_st();
+                }
+            }
+            // rows of the stage past the sequence end inside its last page may
+            // hold anything: zero them in V (pages past it were copied as zeros)
+            if (L < t0 + NT && t0 < last_page_end && last_page_end > L) {
+                const int st = jj % NSTG;
+                mbar_wait_bounded(smem_addr(&kv_full[st]), (jj / NSTG) & 1, nullptr,
+                                  p.wait_budget_ns);
+                uint8_t *vs = kv_ptr + st * 2 * KV_TILE + KV_TILE;
+                const int za = max(L, t0) - t0, zb = min(last_page_end, t0 + NT) - t0;
+                for (int idx = r; idx < (zb - za) * SLABS * 8; idx += 128) {
+                    const int row = za + idx / (SLABS * 8), c = idx % (SLABS * 8);
+                    *reinterpret_cast<uint4 *>(vs + (row / 8) * GROUP + (c >> 3) * 1024 +
+                                               (row % 8) * 128 + (c & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            // P row r: K-major, 128-byte swizzled, 64 tokens per slab
+#pragma unroll
+            for (int c16 = 0; c16 < NT / 8; ++c16) {
+                uint8_t *dst = p_ptr + (c16 / 8) * Q_SLAB + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) =
+                    make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&p_full));
+        }
+        // ---- epilogue
+        if (ok)
+            ok = mbar_wait_bounded(smem_addr(&o_done), (ntiles - 1) & 1, &abort_flag,
+                                   p.wait_budget_ns);
+        if (!ok) {
+            if (lane == 0)
+                give_up();
+        } else {
+            tc_fence_after();
+            // rows that see no token of this partition write nothing: a row
+            // within the first partition is written (directly) by that unit
+            const bool has = row_ok && lim >= kv_lo;
+            const bool direct = p.NP == 1 || pos < p.PK;
+            const size_t rowh = ((size_t)(row0 + i0 + ti) * p.Hq + (size_t)g * p.G + hj);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *dst = direct ? p.out + rowh * D : p.ws_o + (rowh * p.NP + part) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tc_ld32(t_lane + O_COL + 32 * c, v);
+                tc_wait_ld();
+                if (has) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + 32 * c + i) =
+                            make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+                }
+            }
+            if (has && !direct) {
+                p.ws_m[rowh * p.NP + part] = m_ref;
+                p.ws_l[rowh * p.NP + part] = l;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, kVarlenTmemCols);
+    }
+}
+
+// One CTA per (query row, head) whose causal range spans more than one KV
+// partition: out = sum_i w_i o_i / sum_i w_i with w_i = l_i * exp2(m_i - max m).
+template <int D>
+__global__ void __launch_bounds__(128) paged_varlen_reduce_kernel(const VarlenParams p)
+{
+    const int rowh = blockIdx.x;
+    const int r = rowh / p.Hq;
+    int lo = 0, hi = p.S - 1;  // the sequence owning query row r
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.cu_q + mid) <= r)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int s = lo;
+    const int maxlen = p.MB * p.BS;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > maxlen ? maxlen : L);
+    const int row0 = __ldg(p.cu_q + s);
+    const int n = __ldg(p.cu_q + s + 1) - row0;
+    const bool bad = n < 0 || n > L || n > p.max_q;
+    const int pos = L - n + (r - row0);
+    const int np = bad ? 1 : pos / p.PK + 1;
+    griddep_wait();
+    if (np == 1)
+        return;
+    const float *mp = p.ws_m + (size_t)rowh * p.NP;
+    const float *lp = p.ws_l + (size_t)rowh * p.NP;
+    float M = -INFINITY;
+    for (int i = 0; i < np; ++i)
+        if (lp[i] > 0.f)
+            M = fmaxf(M, mp[i]);
+    float den = 0.f;
+    float acc[(D + 127) / 128];
+#pragma unroll
+    for (int k = 0; k < (D + 127) / 128; ++k)
+        acc[k] = 0.f;
+    for (int i = 0; i < np; ++i) {
+        const float li = lp[i];
+        if (!(li > 0.f))
+            continue;
+        const float w = li * ex2(mp[i] - M);
+        den += w;
+        const float *o = p.ws_o + ((size_t)rowh * p.NP + i) * D;
+#pragma unroll
+        for (int k = 0; k < (D + 127) / 128; ++k)
+            if (threadIdx.x + 128 * k < D)
+                acc[k] += w * o[threadIdx.x + 128 * k];
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int k = 0; k < (D + 127) / 128; ++k)
+        if (threadIdx.x + 128 * k < D)
+            p.out[(size_t)rowh * D + threadIdx.x + 128 * k] = acc[k] * inv;
+}
+
+template <int D>
+cudaError_t launch_varlen_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const VarlenParams &p, int grid, int reduce_rows,
+                               cudaStream_t stream)
+{
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (!attr_done[dev & 63]) {
+        e = cudaFuncSetAttribute(paged_varlen_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)varlen_smem_bytes<D>());
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev & 63] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kVarlenThreads);
+    cfg.dynamicSmemBytes = varlen_smem_bytes<D>();
+    cfg.stream = stream;
+    if ((e = cudaLaunchKernelEx(&cfg, paged_varlen_kernel<D>, tq, tk, tv, p)) != cudaSuccess)
+        return e;
+    if (reduce_rows <= 0)
+        return cudaSuccess;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3(reduce_rows);
+    rcfg.blockDim = dim3(128);
+    rcfg.stream = stream;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&rcfg, paged_varlen_reduce_kernel<D>, p);
+}
+
+cudaError_t launch_varlen(int head_dim, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,
+                          cudaStream_t stream)
+{
+    switch (head_dim) {
+    case 64:
+        return launch_varlen_impl<64>(tq, tk, tv, p, grid, reduce_rows, stream);
+    case 128:
+        return launch_varlen_impl<128>(tq, tk, tv, p, grid, reduce_rows, stream);
+    case 256:
+        return launch_varlen_impl<256>(tq, tk, tv, p, grid, reduce_rows, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pgd
