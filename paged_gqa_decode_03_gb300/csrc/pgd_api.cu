@@ -790,6 +790,7 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     p.MB = MB;
     p.NB = NB;
     p.BS = BS;
+    p.log2BS = BS == 8 ? 3 : BS == 16 ? 4 : BS == 32 ? 5 : BS == 64 ? 6 : 7;
     p.max_q = max_q;
     p.wait_budget_ns = kWaitBudgetNs;
     e = launch_varlen(D, tq, *tk, *tv, p, (int)vp.grid, vp.NP > 1 ? total_q * Hq : 0, stream);

@@ -141,7 +141,7 @@ struct VarlenParams {
     float *ws_m, *ws_l, *ws_o;    // [total_q*Hq][NP] (m, l), [total_q*Hq][NP][D]
     unsigned *err;
     float scale_log2;
-    int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, max_q;
+    int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, log2BS, max_q;
     uint64_t wait_budget_ns;
 };
 

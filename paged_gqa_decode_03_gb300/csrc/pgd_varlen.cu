@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, 0, 1);
 
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ __align__(8) uint64_t q_full, kv_full[NSTG], kv_empty[NSTG], s_full[2], p_full,
-        o_done, mma_done;
+    __shared__ __align__(8) uint64_t q_full, k_full[NSTG], v_full[NSTG], kv_empty[NSTG], s_full[2],
+        p_full, o_done, mma_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
 
@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&q_full), 1);
         for (int i = 0; i < NSTG; ++i) {
-            mbar_init(smem_addr(&kv_full[i]), 1);
+            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&v_full[i]), 1);
             mbar_init(smem_addr(&kv_empty[i]), 1);
         }
         mbar_init(smem_addr(&s_full[0]), 1);
@@ -134,11 +135,30 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
                             smem_addr(&q_full));
         }
-        const int npages = (L + p.BS - 1) / p.BS;
+        const int npages = (L + p.BS - 1) >> p.log2BS;
         const int32_t *bt = p.block_tables + (size_t)s * p.MB;
+        // page id of 8-row group `lane` (< NT / 8) of stage jj, -1 past the
+        // sequence's last page (those rows are copied as zeros)
+        auto group_id = [&](int jj) -> int {
+            const int tt = (j0 + jj) * NT + 8 * lane;
+            const int pg = tt >> p.log2BS;
+            int id = -1;
+            if (lane < NT / 8 && pg < npages) {
+                id = __ldg(bt + pg);
+                if ((unsigned)id >= (unsigned)p.NB) {
+                    atomicOr(p.err, kErrPageRange);
+                    id = -1;  // wholly outside the tensor: the copies read zeros
+                }
+            }
+            return id;
+        };
         int issued = 0;
+        int id_next = group_id(0);
         for (int jj = 0; jj < ntiles; ++jj, ++issued) {
             const int st = jj % NSTG;
+            const int id = id_next;
+            if (jj + 1 < ntiles)
+                id_next = group_id(jj + 1);  // in flight while this stage waits
             bool w = true;
             if (lane == 0)
                 w = mbar_wait_bounded(smem_addr(&kv_empty[st]), ((jj / NSTG) & 1) ^ 1,
@@ -148,49 +168,41 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                     give_up();
                 break;
             }
-            const int t0 = (j0 + jj) * NT;
-            // page ids of the stage, one per lane (at most NT / 8 pages)
-            const int pg0 = t0 / p.BS;
-            const int pg = pg0 + lane;
-            int id = -1;
-            if (lane < NT / 8 && pg < npages) {
-                id = __ldg(bt + pg);
-                if ((unsigned)id >= (unsigned)p.NB) {
-                    atomicOr(p.err, kErrPageRange);
-                    id = -1;  // wholly outside the tensor: the copies read zeros
-                }
+            const uint32_t kb = smem_addr(&k_full[st]), vb = smem_addr(&v_full[st]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(kb, KV_TILE);
+                mbar_arrive_expect_tx(vb, KV_TILE);
             }
-            const uint32_t fb = smem_addr(&kv_full[st]);
-            if (lane == 0)
-                mbar_arrive_expect_tx(fb, 2 * KV_TILE);
+            __syncwarp();
+            // lane gi copies 8-row group gi of K, then of V
             const uint32_t ks = kv_s + st * 2 * KV_TILE;
-#pragma unroll 1
-            for (int gi = 0; gi < NT / 8; ++gi) {
-                const int tt = t0 + 8 * gi;
-                const int cid = __shfl_sync(~0u, id, tt / p.BS - pg0);
-                if (lane == 0) {
-                    const int r0 = tt % p.BS;
-                    tma_load_5d(ks + gi * GROUP, &tmap_k, 0, r0, 0, g, cid, fb, pol);
-                    tma_load_5d(ks + KV_TILE + gi * GROUP, &tmap_v, 0, r0, 0, g, cid, fb, pol);
-                }
+            if (lane < NT / 8) {
+                const int r0 = ((j0 + jj) * NT + 8 * lane) & (p.BS - 1);
+                tma_load_5d(ks + lane * GROUP, &tmap_k, 0, r0, 0, g, id, kb, pol);
+                tma_load_5d(ks + KV_TILE + lane * GROUP, &tmap_v, 0, r0, 0, g, id, vb, pol);
             }
         }
         if (abort_flag && lane == 0) {
             // let this CTA's copies in flight land before it exits
             mbar_wait_bounded(smem_addr(&q_full), 0, nullptr, p.wait_budget_ns);
-            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i)
-                mbar_wait_bounded(smem_addr(&kv_full[i % NSTG]), (i / NSTG) & 1, nullptr,
+            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i) {
+                mbar_wait_bounded(smem_addr(&k_full[i % NSTG]), (i / NSTG) & 1, nullptr,
                                   p.wait_budget_ns);
+                mbar_wait_bounded(smem_addr(&v_full[i % NSTG]), (i / NSTG) & 1, nullptr,
+                                  p.wait_budget_ns);
+            }
         }
     } else if (warp == 1) {
         // ============================================================ MMA issue
         if (lane == 0) {
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, &abort_flag, p.wait_budget_ns);
             auto issue_pv = [&](int jj) -> bool {
-                if (!mbar_wait_bounded(smem_addr(&p_full), jj & 1, &abort_flag, p.wait_budget_ns))
+                const int st = jj % NSTG;
+                if (!mbar_wait_bounded(smem_addr(&p_full), jj & 1, &abort_flag, p.wait_budget_ns) ||
+                    !mbar_wait_bounded(smem_addr(&v_full[st]), (jj / NSTG) & 1, &abort_flag,
+                                       p.wait_budget_ns))
                     return false;
                 tc_fence_after();
-                const int st = jj % NSTG;
                 const uint32_t vs = kv_s + st * 2 * KV_TILE + KV_TILE;
 #pragma unroll
                 for (int kk = 0; kk < NT / 16; ++kk) {
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             };
             for (int jj = 0; ok && jj < ntiles; ++jj) {
                 const int st = jj % NSTG;
-                if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (jj / NSTG) & 1, &abort_flag,
+                if (!mbar_wait_bounded(smem_addr(&k_full[st]), (jj / NSTG) & 1, &abort_flag,
                                        p.wait_budget_ns)) {
                     ok = false;
                     break;
@@ -261,12 +273,30 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                     x[32 * c + i] = v[i];
             }
             tc_wait_ld();
-            float mt = -INFINITY;
+            // causal / partition mask only where the stage reaches past this
+            // row's last token.  The extreme is taken on raw scores: the max
+            // for a scale >= 0, the min for a negative one, with masked
+            // scores set to the value that scales to -inf.
+            const float sc = p.scale_log2;
+            const bool neg = sc < 0.f;
+            const float masked = neg ? INFINITY : -INFINITY;
+            const bool masked_tile = t0 + NT - 1 > lim;
+            if (masked_tile) {
 #pragma unroll
-            for (int c = 0; c < NT; ++c) {
-                x[c] = t0 + c <= lim ? x[c] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[c]);
+                for (int c = 0; c < NT; ++c)
+                    x[c] = t0 + c <= lim ? x[c] : masked;
             }
+            float e = masked;
+            if (!neg) {
+#pragma unroll
+                for (int c = 0; c < NT; ++c)
+                    e = fmaxf(e, x[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < NT; ++c)
+                    e = fminf(e, x[c]);
+            }
+            const float mt = e == masked ? -INFINITY : e * sc;
             // lazy reference max: moves only by more than 8 (log2 units)
             bool rescale = false;
             float alpha = 1.f;
@@ -277,13 +307,26 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
             uint32_t pk[NT / 2];
             float sum = 0.f;
+            // p = exp2(x * scale_log2 - m_ref); a row with nothing seen yet
+            // has m_ref = -inf and only masked scores: offset by a finite
+            // value there (every p is then 0) instead of -inf + inf
+            const float off = m_ref == -INFINITY ? 0.f : -m_ref;
+            if (masked_tile) {  // masked scores give 0 whatever the scale (0 included)
 #pragma unroll
-            for (int c = 0; c < NT; c += 2) {
-                const float a = m_ref == -INFINITY ? 0.f : ex2(x[c] - m_ref);
-                const float b = m_ref == -INFINITY ? 0.f : ex2(x[c + 1] - m_ref);
-                pk[c / 2] = pack_half2(a, b);
-                const float2 f = unpack_half2(pk[c / 2]);
-                sum += f.x + f.y;
+                for (int c = 0; c < NT; c += 2) {
+                    const float a = x[c] == masked ? 0.f : ex2(fmaf(x[c], sc, off));
+                    const float b = x[c + 1] == masked ? 0.f : ex2(fmaf(x[c + 1], sc, off));
+                    pk[c / 2] = pack_half2(a, b);
+                    const float2 f = unpack_half2(pk[c / 2]);
+                    sum += f.x + f.y;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NT; c += 2) {
+                    pk[c / 2] = pack_half2(ex2(fmaf(x[c], sc, off)), ex2(fmaf(x[c + 1], sc, off)));
+                    const float2 f = unpack_half2(pk[c / 2]);
+                    sum += f.x + f.y;
+                }
             }
             l = l * alpha + sum;
             // the previous P V has finished: O may be rescaled, P overwritten
@@ -312,7 +355,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // hold anything: zero them in V (pages past it were copied as zeros)
             if (L < t0 + NT && t0 < last_page_end && last_page_end > L) {
                 const int st = jj % NSTG;
-                mbar_wait_bounded(smem_addr(&kv_full[st]), (jj / NSTG) & 1, nullptr,
+                mbar_wait_bounded(smem_addr(&v_full[st]), (jj / NSTG) & 1, nullptr,
                                   p.wait_budget_ns);
                 uint8_t *vs = kv_ptr + st * 2 * KV_TILE + KV_TILE;
                 const int za = max(L, t0) - t0, zb = min(last_page_end, t0 + NT) - t0;

@@ -89,6 +89,16 @@ def test_single_token_rows_match_decode():
     assert_parity(out.cpu().numpy(), oracle_varlen(w), "n=1")
 
 
+@pytest.mark.parametrize("scale", [-0.07, 0.0, 0.3])
+def test_any_scale(scale):
+    """The softmax takes the scale's sign into account (and scale 0 gives
+    the mean over the causal range)."""
+    w = make_varlen(S=3, Hq=16, Hkv=4, D=128, BS=16, ctx=[0, 200, 31], n=[70, 5, 130], seed=8,
+                    device=DEV)
+    w.base.scale = scale
+    assert_parity(run_varlen(w).cpu().numpy(), oracle_varlen(w), f"scale {scale}")
+
+
 def test_token_major_bit_equal():
     w = make_varlen(S=4, Hq=32, Hkv=8, D=128, BS=16, ctx=[0, 50, 400, 1000], n=[64, 9, 100, 3],
                     seed=4, device=DEV)
