@@ -209,6 +209,58 @@ pgd_status encode_cache_map(CUtensorMap *map, const void *base, const CacheGeom 
     return PGD_OK;
 }
 
+// The cache viewed for the multi-token kernel, innermost first:
+//   64 halves x 8 token rows (token stride) x D/64 slabs (128 bytes)
+//   x BS/8 row groups (8 token strides) x blocks (u halves),
+// where u = gcd(page stride, head stride) and (page b, head g) is block
+// b * page_stride/u + g * head_stride/u.  A box of 64 x 8 x D/64 x groups x 1
+// lands a page's rows as [group][slab][row][128 B] (128-byte swizzle): the
+// layout the tensor cores read K (K-major) and V (MN-major) in.
+long long gcd_ll(long long a, long long b)
+{
+    while (b) {
+        const long long t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+pgd_status group_blocks(const CacheGeom &g, long long *u, long long *blocks)
+{
+    *u = gcd_ll(g.page_stride, g.head_stride);
+    *blocks = (g.NB - 1) * (g.page_stride / *u) + (g.Hkv - 1) * (g.head_stride / *u) + 1;
+    if (*blocks >= (1ll << 31))
+        return fail(PGD_ERR_UNSUPPORTED,
+                    "cache strides (%lld, %lld) give %lld page/head blocks (limit 2^31)",
+                    g.page_stride, g.head_stride, *blocks);
+    return PGD_OK;
+}
+
+pgd_status encode_cache_map_groups(CUtensorMap *map, const void *base, const CacheGeom &g,
+                                   int box_groups)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    long long u, blocks;
+    if ((st = group_blocks(g, &u, &blocks)))
+        return st;
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)(g.D / 64), (cuuint64_t)(g.BS / 8), (cuuint64_t)blocks};
+    cuuint64_t strides[4] = {(cuuint64_t)g.token_stride * 2, 128, (cuuint64_t)g.token_stride * 16,
+                             (cuuint64_t)u * 2};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)(g.D / 64), (cuuint32_t)box_groups, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (page groups) failed (CUresult %d)",
+                    (int)r);
+    return PGD_OK;
+}
+
 // ------------------------------------------------------------------ claim counters
 // The partition kernel hands out work units with a 4-byte counter that must
 // read 0 at launch; the reduce kernel zeroes it at the end of every call.
@@ -292,7 +344,7 @@ void mark_counter_dirty(int slot)
 struct MapCacheEntry {
     const void *k, *v;
     CacheGeom geom;
-    int box, dev;
+    int box, kind, dev;
     alignas(64) CUtensorMap tk;
     alignas(64) CUtensorMap tv;
 };
@@ -300,7 +352,9 @@ constexpr int kMapCache = 8;
 thread_local MapCacheEntry t_maps[kMapCache];
 thread_local int t_maps_used = 0, t_maps_next = 0;
 
-pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box,
+// kind 0: the decode view (box = rows per copy); kind 1: the page-group view
+// (box = 8-row groups per copy).
+pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box, int kind,
                       const CUtensorMap **tk, const CUtensorMap **tv)
 {
     int dev = 0;
@@ -309,7 +363,8 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
         return cuda_fail(e, "cudaGetDevice");
     for (int i = 0; i < t_maps_used; ++i) {
         MapCacheEntry &c = t_maps[i];
-        if (c.k == k && c.v == v && c.geom == geom && c.box == box && c.dev == dev) {
+        if (c.k == k && c.v == v && c.geom == geom && c.box == box && c.kind == kind &&
+            c.dev == dev) {
             *tk = &c.tk;
             *tv = &c.tv;
             return PGD_OK;
@@ -317,8 +372,10 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
-    if ((st = encode_cache_map(&c.tk, k, geom, box)) ||
-        (st = encode_cache_map(&c.tv, v, geom, box))) {
+    if (kind == 0 ? ((st = encode_cache_map(&c.tk, k, geom, box)) ||
+                     (st = encode_cache_map(&c.tv, v, geom, box)))
+                  : ((st = encode_cache_map_groups(&c.tk, k, geom, box)) ||
+                     (st = encode_cache_map_groups(&c.tv, v, geom, box)))) {
         c.k = c.v = nullptr;
         return st;
     }
@@ -326,6 +383,7 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     c.v = v;
     c.geom = geom;
     c.box = box;
+    c.kind = kind;
     c.dev = dev;
     t_maps_next = (t_maps_next + 1) % kMapCache;
     if (t_maps_used < kMapCache)
@@ -518,7 +576,7 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     const int box = BS < stage_tokens(D) ? BS : stage_tokens(D);
     const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
     const CUtensorMap *tk = nullptr, *tv = nullptr;
-    if ((st = cache_maps(k_cache, v_cache, geom, box, &tk, &tv))) {
+    if ((st = cache_maps(k_cache, v_cache, geom, box, 0, &tk, &tv))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
@@ -763,8 +821,11 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     CUtensorMap tq;
     const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
     const CUtensorMap *tk = nullptr, *tv = nullptr;
-    if ((st = encode_q_map(&tq, q, total_q, Hq, D, vp.G, vp.TQ)) ||
-        (st = cache_maps(k_cache, v_cache, geom, 8, &tk, &tv))) {
+    long long blk_u, blk_n;
+    const int box_groups = (BS <= vp.NT ? BS : vp.NT) / 8;
+    if ((st = group_blocks(geom, &blk_u, &blk_n)) ||
+        (st = encode_q_map(&tq, q, total_q, Hq, D, vp.G, vp.TQ)) ||
+        (st = cache_maps(k_cache, v_cache, geom, box_groups, 1, &tk, &tv))) {
         if (own && ws)
             cudaFreeAsync(ws, stream);
         return st;
@@ -791,6 +852,8 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     p.NB = NB;
     p.BS = BS;
     p.log2BS = BS == 8 ? 3 : BS == 16 ? 4 : BS == 32 ? 5 : BS == 64 ? 6 : 7;
+    p.blk_page = (int)(kv_strides.page / blk_u);
+    p.blk_head = (int)(kv_strides.head / blk_u);
     p.max_q = max_q;
     p.wait_budget_ns = kWaitBudgetNs;
     e = launch_varlen(D, tq, *tk, *tv, p, (int)vp.grid, vp.NP > 1 ? total_q * Hq : 0, stream);

@@ -142,6 +142,7 @@ struct VarlenParams {
     unsigned *err;
     float scale_log2;
     int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, log2BS, max_q;
+    int blk_page, blk_head;       // (page, KV head) -> block coordinate of the K/V maps
     uint64_t wait_budget_ns;
 };
 

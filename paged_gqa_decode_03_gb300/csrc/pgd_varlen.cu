@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, 0, 1);
 
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ __align__(8) uint64_t q_full, k_full[NSTG], v_full[NSTG], kv_empty[NSTG], s_full[2],
-        p_full, o_done, mma_done;
+    __shared__ __align__(8) uint64_t q_full, k_full[NSTG], v_full[NSTG], k_empty[NSTG],
+        v_empty[NSTG], s_full[2], p_full, o_done, mma_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
 
@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         for (int i = 0; i < NSTG; ++i) {
             mbar_init(smem_addr(&k_full[i]), 1);
             mbar_init(smem_addr(&v_full[i]), 1);
-            mbar_init(smem_addr(&kv_empty[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), 1);
         }
         mbar_init(smem_addr(&s_full[0]), 1);
         mbar_init(smem_addr(&s_full[1]), 1);
@@ -137,31 +138,34 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         }
         const int npages = (L + p.BS - 1) >> p.log2BS;
         const int32_t *bt = p.block_tables + (size_t)s * p.MB;
-        // page id of 8-row group `lane` (< NT / 8) of stage jj, -1 past the
-        // sequence's last page (those rows are copied as zeros)
-        auto group_id = [&](int jj) -> int {
-            const int tt = (j0 + jj) * NT + 8 * lane;
-            const int pg = tt >> p.log2BS;
-            int id = -1;
-            if (lane < NT / 8 && pg < npages) {
-                id = __ldg(bt + pg);
-                if ((unsigned)id >= (unsigned)p.NB) {
-                    atomicOr(p.err, kErrPageRange);
-                    id = -1;  // wholly outside the tensor: the copies read zeros
-                }
+        // one copy per page of the stage (a piece of NT rows when pages are
+        // longer): lane c issues copy c, of the 8-row groups of that page
+        const int copies = p.BS <= NT ? NT >> p.log2BS : 1;
+        const int groups = (p.BS <= NT ? p.BS : NT) / 8;
+        auto block_of = [&](int jj) -> int {  // block coordinate of lane's page, -1: none
+            const int pg = (((j0 + jj) * NT) >> p.log2BS) + lane;
+            int b = -1;
+            if (lane < copies && pg < npages) {
+                const int id = __ldg(bt + pg);
+                if ((unsigned)id < (unsigned)p.NB)
+                    b = id * p.blk_page + g * p.blk_head;
+                else
+                    atomicOr(p.err, kErrPageRange);  // wholly outside: the copy reads zeros
             }
-            return id;
+            return b;
         };
         int issued = 0;
-        int id_next = group_id(0);
+        int blk_next = block_of(0);
         for (int jj = 0; jj < ntiles; ++jj, ++issued) {
             const int st = jj % NSTG;
-            const int id = id_next;
+            const int blk = blk_next;
             if (jj + 1 < ntiles)
-                id_next = group_id(jj + 1);  // in flight while this stage waits
+                blk_next = block_of(jj + 1);  // in flight while this stage waits
+            const int grp0 = p.BS <= NT ? 0 : (((j0 + jj) * NT) & (p.BS - 1)) >> 3;
+            const uint32_t dst = kv_s + st * 2 * KV_TILE + lane * groups * GROUP;
             bool w = true;
             if (lane == 0)
-                w = mbar_wait_bounded(smem_addr(&kv_empty[st]), ((jj / NSTG) & 1) ^ 1,
+                w = mbar_wait_bounded(smem_addr(&k_empty[st]), ((jj / NSTG) & 1) ^ 1,
                                       &abort_flag, p.wait_budget_ns);
             if (!__shfl_sync(~0u, w, 0)) {
                 if (lane == 0)
@@ -169,18 +173,24 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 break;
             }
             const uint32_t kb = smem_addr(&k_full[st]), vb = smem_addr(&v_full[st]);
-            if (lane == 0) {
+            if (lane == 0)
                 mbar_arrive_expect_tx(kb, KV_TILE);
-                mbar_arrive_expect_tx(vb, KV_TILE);
-            }
             __syncwarp();
-            // lane gi copies 8-row group gi of K, then of V
-            const uint32_t ks = kv_s + st * 2 * KV_TILE;
-            if (lane < NT / 8) {
-                const int r0 = ((j0 + jj) * NT + 8 * lane) & (p.BS - 1);
-                tma_load_5d(ks + lane * GROUP, &tmap_k, 0, r0, 0, g, id, kb, pol);
-                tma_load_5d(ks + KV_TILE + lane * GROUP, &tmap_v, 0, r0, 0, g, id, vb, pol);
+            if (lane < copies)
+                tma_load_5d(dst, &tmap_k, 0, 0, 0, grp0, blk, kb, pol);
+            if (lane == 0)
+                w = mbar_wait_bounded(smem_addr(&v_empty[st]), ((jj / NSTG) & 1) ^ 1,
+                                      &abort_flag, p.wait_budget_ns);
+            if (!__shfl_sync(~0u, w, 0)) {
+                if (lane == 0)
+                    give_up();
+                break;
             }
+            if (lane == 0)
+                mbar_arrive_expect_tx(vb, KV_TILE);
+            __syncwarp();
+            if (lane < copies)
+                tma_load_5d(dst + KV_TILE, &tmap_v, 0, 0, 0, grp0, blk, vb, pol);
         }
         if (abort_flag && lane == 0) {
             // let this CTA's copies in flight land before it exits
@@ -196,46 +206,63 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // ============================================================ MMA issue
         if (lane == 0) {
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, &abort_flag, p.wait_budget_ns);
-            auto issue_pv = [&](int jj) -> bool {
-                const int st = jj % NSTG;
-                if (!mbar_wait_bounded(smem_addr(&p_full), jj & 1, &abort_flag, p.wait_budget_ns) ||
-                    !mbar_wait_bounded(smem_addr(&v_full[st]), (jj / NSTG) & 1, &abort_flag,
-                                       p.wait_budget_ns))
-                    return false;
-                tc_fence_after();
-                const uint32_t vs = kv_s + st * 2 * KV_TILE + KV_TILE;
+            // Two streams of work, issued as soon as each is ready: S_ns = Q K^T
+            // once K of stage ns has landed (and its score buffer was read,
+            // i.e. P_{ns-2} is done), and O += P V for the oldest tile whose
+            // P and V are ready.
+            int ns = 0, npv = 0;
+            uint64_t idle_since = 0;
+            while (ok && npv < ntiles) {
+                bool did = false;
+                if (ns < ntiles && ns < npv + 2) {
+                    const int st = ns % NSTG;
+                    if (mbar_test_wait(smem_addr(&k_full[st]), (ns / NSTG) & 1)) {
+                        tc_fence_after();
+                        const uint32_t ks = kv_s + st * 2 * KV_TILE;
+                        const uint32_t sd = tmem + S_COL + (ns & 1) * NT;
 #pragma unroll
-                for (int kk = 0; kk < NT / 16; ++kk) {
-                    const uint64_t a = tc_sdesc(p_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
-                    const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
-                    tc_mma(tmem + O_COL, a, b, IDESC_O, jj > 0 || kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t a =
+                                tc_sdesc(q_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
+                            const uint64_t b =
+                                tc_sdesc(ks + (kk / 4) * 1024 + (kk % 4) * 32, 16, GROUP);
+                            tc_mma(sd, a, b, IDESC_S, kk > 0);
+                        }
+                        tc_commit(smem_addr(&s_full[ns & 1]));
+                        tc_commit(smem_addr(&k_empty[st]));
+                        ++ns;
+                        did = true;
+                    }
                 }
-                tc_commit(smem_addr(&o_done));
-                tc_commit(smem_addr(&kv_empty[st]));
-                return true;
-            };
-            for (int jj = 0; ok && jj < ntiles; ++jj) {
-                const int st = jj % NSTG;
-                if (!mbar_wait_bounded(smem_addr(&k_full[st]), (jj / NSTG) & 1, &abort_flag,
-                                       p.wait_budget_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ks = kv_s + st * 2 * KV_TILE;
-                const uint32_t sd = tmem + S_COL + (jj & 1) * NT;
+                if (npv < ns) {
+                    const int st = npv % NSTG;
+                    if (mbar_test_wait(smem_addr(&p_full), npv & 1) &&
+                        mbar_test_wait(smem_addr(&v_full[st]), (npv / NSTG) & 1)) {
+                        tc_fence_after();
+                        const uint32_t vs = kv_s + st * 2 * KV_TILE + KV_TILE;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc_sdesc(q_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
-                    const uint64_t b = tc_sdesc(ks + (kk / 4) * 1024 + (kk % 4) * 32, 16, GROUP);
-                    tc_mma(sd, a, b, IDESC_S, kk > 0);
+                        for (int kk = 0; kk < NT / 16; ++kk) {
+                            const uint64_t a =
+                                tc_sdesc(p_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
+                            const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
+                            tc_mma(tmem + O_COL, a, b, IDESC_O, npv > 0 || kk > 0);
+                        }
+                        tc_commit(smem_addr(&o_done));
+                        tc_commit(smem_addr(&v_empty[st]));
+                        ++npv;
+                        did = true;
+                    }
                 }
-                tc_commit(smem_addr(&s_full[jj & 1]));
-                if (jj > 0 && !issue_pv(jj - 1))
-                    ok = false;
+                if (did) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_ns();
+                    if (idle_since == 0)
+                        idle_since = now;
+                    else if (now - idle_since > p.wait_budget_ns || abort_flag)
+                        ok = false;
+                }
             }
-            if (ok)
-                ok = issue_pv(ntiles - 1);
             if (!ok)
                 give_up();
             // every MMA issued here has completed before the memory is freed
@@ -281,13 +308,15 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             const bool neg = sc < 0.f;
             const float masked = neg ? INFINITY : -INFINITY;
             const bool masked_tile = t0 + NT - 1 > lim;
-            if (masked_tile) {
+            const bool none = lim < t0;  // this row sees no token of the stage
+            if (masked_tile && !none) {
 #pragma unroll
                 for (int c = 0; c < NT; ++c)
                     x[c] = t0 + c <= lim ? x[c] : masked;
             }
             float e = masked;
-            if (!neg) {
+            if (none) {
+            } else if (!neg) {
 #pragma unroll
                 for (int c = 0; c < NT; ++c)
                     e = fmaxf(e, x[c]);
@@ -311,7 +340,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // has m_ref = -inf and only masked scores: offset by a finite
             // value there (every p is then 0) instead of -inf + inf
             const float off = m_ref == -INFINITY ? 0.f : -m_ref;
-            if (masked_tile) {  // masked scores give 0 whatever the scale (0 included)
+            if (none) {
+#pragma unroll
+                for (int c = 0; c < NT / 2; ++c)
+                    pk[c] = 0u;
+            } else if (masked_tile) {  // masked scores give 0 whatever the scale (0 included)
 #pragma unroll
                 for (int c = 0; c < NT; c += 2) {
                     const float a = x[c] == masked ? 0.f : ex2(fmaf(x[c], sc, off));
