@@ -130,7 +130,8 @@ template <int D> __host__ __device__ constexpr size_t varlen_smem_bytes()
     return size_t(128) * D * 2 + size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 +
            size_t(128) * VShape<D>::NT * 2 + 1024;
 }
-constexpr int kVarlenThreads = 192;   // producer warp, MMA warp, 4 softmax warps
+constexpr int kVarlenThreads = 352;   // K producer, MMA, 8 softmax warps, V producer
+constexpr int kVWarp = 10;            // the V producer warp
 constexpr uint32_t kVarlenTmemCols = 512;
 
 struct VarlenParams {

@@ -17,8 +17,10 @@
 //     memory): S_j = Q K_j^T into one of two score buffers, then, once the
 //     softmax has written P_{j-1}, O += P_{j-1} V_{j-1}; completion is
 //     signalled through mbarriers with tcgen05.commit.
-//   * warps 2-5, softmax: thread r owns row r.  Per stage it reads its 128
-//     (64) scores from tensor memory, masks them causally, and runs the
+//   * warps 2-9, softmax: row r belongs to one thread in each of two
+//     warpgroups, one per half of the stage's columns.  Per stage a thread
+//     reads its 64 (32) scores from tensor memory, masks them causally, the
+//     pair combines the row's extreme through shared memory, and each runs the
 //     log2-space online softmax with exp2 ("Four speed-up tricks", 1); the
 //     reference max only moves when a score exceeds it by more than 2^8
 //     (p <= 256 stays exact in fp16), and only then is the row of O rescaled
@@ -31,6 +33,14 @@
 #include "pgd_internal.h"
 
 namespace pgd {
+
+// Exponentials of the softmax: one column in four on the FMA pipe
+// (exp2_poly), the rest on the special-function unit, whose 16 results per
+// clock and SM would otherwise take as long as the tile's matrix products.
+__device__ __forceinline__ float exp2_split(int c, float x)
+{
+    return ex2(x);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
@@ -53,6 +63,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         v_empty[NSTG], s_full[2], p_full, o_done, mma_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
+    __shared__ float pair_red[2][2][128];  // [tile parity][half][row]: softmax pair exchange
 
     // ---- the unit: (sequence, KV head, query tile, KV partition); query
     // tiles in decreasing order so the longest causal ranges start first
@@ -104,7 +115,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         }
         mbar_init(smem_addr(&s_full[0]), 1);
         mbar_init(smem_addr(&s_full[1]), 1);
-        mbar_init(smem_addr(&p_full), 4);
+        mbar_init(smem_addr(&p_full), 8);
         mbar_init(smem_addr(&o_done), 1);
         mbar_init(smem_addr(&mma_done), 1);
         abort_flag = 0;
@@ -124,18 +135,26 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         abort_flag = 1;
     };
 
-    if (warp == 0) {
-        // ============================================================ producer
+    if (warp == 0 || warp == kVWarp) {
+        // ============================================================ producers
+        // warp 0: the Q tile, then K of every stage; warp 10: V of every
+        // stage (the two rings refill independently: K is free again after
+        // S, V only after P V)
+        const bool is_v = warp == kVWarp;
         const uint64_t pol = l2_evict_first_policy();
         if (lane == 0) {
-            prefetch_tensormap(&tmap_q);
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-            mbar_arrive_expect_tx(smem_addr(&q_full), SLABS * p.TQ * p.G * 128);
-            for (int sl = 0; sl < SLABS; ++sl)
-                tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
-                            smem_addr(&q_full));
+            prefetch_tensormap(is_v ? &tmap_v : &tmap_k);
+            if (!is_v) {
+                prefetch_tensormap(&tmap_q);
+                mbar_arrive_expect_tx(smem_addr(&q_full), SLABS * p.TQ * p.G * 128);
+                for (int sl = 0; sl < SLABS; ++sl)
+                    tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
+                                smem_addr(&q_full));
+            }
         }
+        const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
+        uint64_t *full = is_v ? v_full : k_full;
+        uint64_t *empty = is_v ? v_empty : k_empty;
         const int npages = (L + p.BS - 1) >> p.log2BS;
         const int32_t *bt = p.block_tables + (size_t)s * p.MB;
         // one copy per page of the stage (a piece of NT rows when pages are
@@ -149,7 +168,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 const int id = __ldg(bt + pg);
                 if ((unsigned)id < (unsigned)p.NB)
                     b = id * p.blk_page + g * p.blk_head;
-                else
+                else if (!is_v)
                     atomicOr(p.err, kErrPageRange);  // wholly outside: the copy reads zeros
             }
             return b;
@@ -162,45 +181,31 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (jj + 1 < ntiles)
                 blk_next = block_of(jj + 1);  // in flight while this stage waits
             const int grp0 = p.BS <= NT ? 0 : (((j0 + jj) * NT) & (p.BS - 1)) >> 3;
-            const uint32_t dst = kv_s + st * 2 * KV_TILE + lane * groups * GROUP;
+            const uint32_t dst =
+                kv_s + st * 2 * KV_TILE + (is_v ? KV_TILE : 0) + lane * groups * GROUP;
             bool w = true;
             if (lane == 0)
-                w = mbar_wait_bounded(smem_addr(&k_empty[st]), ((jj / NSTG) & 1) ^ 1,
-                                      &abort_flag, p.wait_budget_ns);
+                w = mbar_wait_bounded(smem_addr(&empty[st]), ((jj / NSTG) & 1) ^ 1, &abort_flag,
+                                      p.wait_budget_ns);
             if (!__shfl_sync(~0u, w, 0)) {
                 if (lane == 0)
                     give_up();
                 break;
             }
-            const uint32_t kb = smem_addr(&k_full[st]), vb = smem_addr(&v_full[st]);
+            const uint32_t fb = smem_addr(&full[st]);
             if (lane == 0)
-                mbar_arrive_expect_tx(kb, KV_TILE);
+                mbar_arrive_expect_tx(fb, KV_TILE);
             __syncwarp();
             if (lane < copies)
-                tma_load_5d(dst, &tmap_k, 0, 0, 0, grp0, blk, kb, pol);
-            if (lane == 0)
-                w = mbar_wait_bounded(smem_addr(&v_empty[st]), ((jj / NSTG) & 1) ^ 1,
-                                      &abort_flag, p.wait_budget_ns);
-            if (!__shfl_sync(~0u, w, 0)) {
-                if (lane == 0)
-                    give_up();
-                break;
-            }
-            if (lane == 0)
-                mbar_arrive_expect_tx(vb, KV_TILE);
-            __syncwarp();
-            if (lane < copies)
-                tma_load_5d(dst + KV_TILE, &tmap_v, 0, 0, 0, grp0, blk, vb, pol);
+                tma_load_5d(dst, map, 0, 0, 0, grp0, blk, fb, pol);
         }
         if (abort_flag && lane == 0) {
-            // let this CTA's copies in flight land before it exits
-            mbar_wait_bounded(smem_addr(&q_full), 0, nullptr, p.wait_budget_ns);
-            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i) {
-                mbar_wait_bounded(smem_addr(&k_full[i % NSTG]), (i / NSTG) & 1, nullptr,
+            // let this warp's copies in flight land before the CTA exits
+            if (!is_v)
+                mbar_wait_bounded(smem_addr(&q_full), 0, nullptr, p.wait_budget_ns);
+            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i)
+                mbar_wait_bounded(smem_addr(&full[i % NSTG]), (i / NSTG) & 1, nullptr,
                                   p.wait_budget_ns);
-                mbar_wait_bounded(smem_addr(&v_full[i % NSTG]), (i / NSTG) & 1, nullptr,
-                                  p.wait_budget_ns);
-            }
         }
     } else if (warp == 1) {
         // ============================================================ MMA issue
@@ -212,6 +217,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // P and V are ready.
             int ns = 0, npv = 0;
             uint64_t idle_since = 0;
+            uint32_t spins = 0;
             while (ok && npv < ntiles) {
                 bool did = false;
                 if (ns < ntiles && ns < npv + 2) {
@@ -255,7 +261,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 }
                 if (did) {
                     idle_since = 0;
-                } else {
+                    spins = 0;
+                } else if ((++spins & 255u) == 0) {  // the clock only now and then
                     const uint64_t now = global_ns();
                     if (idle_since == 0)
                         idle_since = now;
@@ -272,61 +279,81 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         __syncwarp();
     } else {
         // ============================================================ softmax
-        const int quarter = warp & 3;                 // tensor-memory lanes 32*quarter ..
+        // Two warpgroups share every stage: warps 2-5 take the first half of
+        // its columns (tokens), warps 6-9 the second half, for the same rows
+        // (warps w and w+4 read tensor-memory lane quarter w & 3).  They
+        // combine each row's extreme through shared memory, keep their own
+        // part of the exp-sum, and own their half of P and of O.
+        constexpr int HC = NT / 2, HD = D / 2;
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;            // this thread's row
         const uint32_t t_lane = tmem + ((uint32_t)(32 * quarter) << 16);
+        const uint32_t pair_bar = 1 + quarter;        // named barrier of the warp pair
         const int ti = r / p.G, hj = r - ti * p.G;
         const bool row_ok = r < p.TQ * p.G && ti < ni;
         const int pos = row_ok ? L - n + i0 + ti : -1;
         const int lim = min(pos, kv_hi - 1);          // last token this row sees here
+        const float sc = p.scale_log2;
+        const bool neg = sc < 0.f;
+        const float masked = neg ? INFINITY : -INFINITY;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         const int last_page_end = ((L + p.BS - 1) / p.BS) * p.BS;
         for (int jj = 0; jj < ntiles; ++jj) {
             const int t0 = (j0 + jj) * NT;
-            if (!mbar_wait_bounded(smem_addr(&s_full[jj & 1]), (jj >> 1) & 1, &abort_flag,
-                                   p.wait_budget_ns)) {
+            const int c0 = t0 + half * HC;            // first token of this half
+            // after a failed wait the loop keeps running without doing work,
+            // so the two warps of a pair meet at every named barrier
+            if (ok && !mbar_wait_bounded(smem_addr(&s_full[jj & 1]), (jj >> 1) & 1, &abort_flag,
+                                         p.wait_budget_ns)) {
                 ok = false;
-                break;
+                give_up();
             }
-            tc_fence_after();
-            float x[NT];
+            float x[HC];
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < NT / 32; ++c) {
-                float v[32];
-                tc_ld32(t_lane + S_COL + (jj & 1) * NT + 32 * c, v);
+                for (int c = 0; c < HC / 32; ++c) {
+                    float v[32];
+                    tc_ld32(t_lane + S_COL + (jj & 1) * NT + half * HC + 32 * c, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    x[32 * c + i] = v[i];
+                    for (int i = 0; i < 32; ++i)
+                        x[32 * c + i] = v[i];
+                }
+                tc_wait_ld();
             }
-            tc_wait_ld();
-            // causal / partition mask only where the stage reaches past this
+            // causal / partition mask only where this half reaches past the
             // row's last token.  The extreme is taken on raw scores: the max
             // for a scale >= 0, the min for a negative one, with masked
             // scores set to the value that scales to -inf.
-            const float sc = p.scale_log2;
-            const bool neg = sc < 0.f;
-            const float masked = neg ? INFINITY : -INFINITY;
-            const bool masked_tile = t0 + NT - 1 > lim;
-            const bool none = lim < t0;  // this row sees no token of the stage
+            const bool masked_tile = c0 + HC - 1 > lim;
+            const bool none = lim < c0;  // this row sees no token of this half
             if (masked_tile && !none) {
 #pragma unroll
-                for (int c = 0; c < NT; ++c)
-                    x[c] = t0 + c <= lim ? x[c] : masked;
+                for (int c = 0; c < HC; ++c)
+                    x[c] = c0 + c <= lim ? x[c] : masked;
             }
             float e = masked;
-            if (none) {
+            if (none || !ok) {
             } else if (!neg) {
 #pragma unroll
-                for (int c = 0; c < NT; ++c)
+                for (int c = 0; c < HC; ++c)
                     e = fmaxf(e, x[c]);
             } else {
 #pragma unroll
-                for (int c = 0; c < NT; ++c)
+                for (int c = 0; c < HC; ++c)
                     e = fminf(e, x[c]);
             }
+            pair_red[jj & 1][half][r] = e;
+            named_barrier_sync(pair_bar, 64);
+            const float e2 = pair_red[jj & 1][half ^ 1][r];
+            if (!ok)
+                continue;
+            e = neg ? fminf(e, e2) : fmaxf(e, e2);
             const float mt = e == masked ? -INFINITY : e * sc;
-            // lazy reference max: moves only by more than 8 (log2 units)
+            // lazy reference max (same decision in both halves): moves only
+            // by more than 8 (log2 units)
             bool rescale = false;
             float alpha = 1.f;
             if (mt > m_ref + 8.f) {
@@ -334,7 +361,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 alpha = rescale ? ex2(m_ref - mt) : 1.f;
                 m_ref = mt;
             }
-            uint32_t pk[NT / 2];
+            uint32_t pk[HC / 2];
             float sum = 0.f;
             // p = exp2(x * scale_log2 - m_ref); a row with nothing seen yet
             // has m_ref = -inf and only masked scores: offset by a finite
@@ -342,44 +369,47 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             const float off = m_ref == -INFINITY ? 0.f : -m_ref;
             if (none) {
 #pragma unroll
-                for (int c = 0; c < NT / 2; ++c)
+                for (int c = 0; c < HC / 2; ++c)
                     pk[c] = 0u;
             } else if (masked_tile) {  // masked scores give 0 whatever the scale (0 included)
 #pragma unroll
-                for (int c = 0; c < NT; c += 2) {
-                    const float a = x[c] == masked ? 0.f : ex2(fmaf(x[c], sc, off));
-                    const float b = x[c + 1] == masked ? 0.f : ex2(fmaf(x[c + 1], sc, off));
+                for (int c = 0; c < HC; c += 2) {
+                    const float a = x[c] == masked ? 0.f : exp2_split(c, fmaf(x[c], sc, off));
+                    const float b =
+                        x[c + 1] == masked ? 0.f : exp2_split(c + 1, fmaf(x[c + 1], sc, off));
                     pk[c / 2] = pack_half2(a, b);
-                    const float2 f = unpack_half2(pk[c / 2]);
-                    sum += f.x + f.y;
+                    sum += a + b;
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < NT; c += 2) {
-                    pk[c / 2] = pack_half2(ex2(fmaf(x[c], sc, off)), ex2(fmaf(x[c + 1], sc, off)));
-                    const float2 f = unpack_half2(pk[c / 2]);
-                    sum += f.x + f.y;
+                for (int c = 0; c < HC; c += 2) {
+                    const float a = exp2_split(c, fmaf(x[c], sc, off));
+                    const float b = exp2_split(c + 1, fmaf(x[c + 1], sc, off));
+                    pk[c / 2] = pack_half2(a, b);
+                    sum += a + b;
                 }
             }
             l = l * alpha + sum;
-            // the previous P V has finished: O may be rescaled, P overwritten
+            // the previous P V has finished: this half of O may be rescaled,
+            // P overwritten
             if (jj > 0) {
                 if (!mbar_wait_bounded(smem_addr(&o_done), (jj - 1) & 1, &abort_flag,
                                        p.wait_budget_ns)) {
                     ok = false;
-                    break;
+                    give_up();
+                    continue;
                 }
                 tc_fence_after();
                 if (__any_sync(~0u, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < HD / 32; ++c) {
                         float v[32];
-                        tc_ld32(t_lane + O_COL + 32 * c, v);
+                        tc_ld32(t_lane + O_COL + half * HD + 32 * c, v);
                         tc_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             v[i] *= alpha;
-                        tc_st32(t_lane + O_COL + 32 * c, v);
+                        tc_st32(t_lane + O_COL + half * HD + 32 * c, v);
                     }
                     tc_wait_st();
                 }
@@ -392,17 +422,18 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                                   p.wait_budget_ns);
                 uint8_t *vs = kv_ptr + st * 2 * KV_TILE + KV_TILE;
                 const int za = max(L, t0) - t0, zb = min(last_page_end, t0 + NT) - t0;
-                for (int idx = r; idx < (zb - za) * SLABS * 8; idx += 128) {
+                for (int idx = half * 128 + r; idx < (zb - za) * SLABS * 8; idx += 256) {
                     const int row = za + idx / (SLABS * 8), c = idx % (SLABS * 8);
                     *reinterpret_cast<uint4 *>(vs + (row / 8) * GROUP + (c >> 3) * 1024 +
                                                (row % 8) * 128 + (c & 7) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
             }
-            // P row r: K-major, 128-byte swizzled, 64 tokens per slab
+            // this half of P row r: K-major, 128-byte swizzled, 64 tokens per slab
 #pragma unroll
-            for (int c16 = 0; c16 < NT / 8; ++c16) {
-                uint8_t *dst = p_ptr + (c16 / 8) * Q_SLAB + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+            for (int c16 = 0; c16 < HC / 8; ++c16) {
+                const int g16 = half * (HC / 8) + c16;
+                uint8_t *dst = p_ptr + (g16 >> 3) * Q_SLAB + r * 128 + (((g16 & 7) ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) =
                     make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
             }
@@ -412,13 +443,16 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             if (lane == 0)
                 mbar_arrive(smem_addr(&p_full));
         }
-        // ---- epilogue
+        // ---- epilogue: the row's exp-sum from both halves, then each half
+        // writes its columns
         if (ok)
             ok = mbar_wait_bounded(smem_addr(&o_done), (ntiles - 1) & 1, &abort_flag,
                                    p.wait_budget_ns);
+        pair_red[ntiles & 1][half][r] = l;
+        named_barrier_sync(pair_bar, 64);
+        const float lt = l + pair_red[ntiles & 1][half ^ 1][r];
         if (!ok) {
-            if (lane == 0)
-                give_up();
+            give_up();
         } else {
             tc_fence_after();
             // rows that see no token of this partition write nothing: a row
@@ -426,12 +460,12 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             const bool has = row_ok && lim >= kv_lo;
             const bool direct = p.NP == 1 || pos < p.PK;
             const size_t rowh = ((size_t)(row0 + i0 + ti) * p.Hq + (size_t)g * p.G + hj);
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float *dst = direct ? p.out + rowh * D : p.ws_o + (rowh * p.NP + part) * D;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            float *dst = (direct ? p.out + rowh * D : p.ws_o + (rowh * p.NP + part) * D) + half * HD;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
                 float v[32];
-                tc_ld32(t_lane + O_COL + 32 * c, v);
+                tc_ld32(t_lane + O_COL + half * HD + 32 * c, v);
                 tc_wait_ld();
                 if (has) {
 #pragma unroll
@@ -440,9 +474,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                             make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
                 }
             }
-            if (has && !direct) {
+            if (has && !direct && half == 0) {
                 p.ws_m[rowh * p.NP + part] = m_ref;
-                p.ws_l[rowh * p.NP + part] = l;
+                p.ws_l[rowh * p.NP + part] = lt;
             }
         }
     }
