@@ -301,27 +301,6 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// 2^x on the FMA and integer pipes (for x <= 8; x below -127 gives a value
-// that rounds to 0 in fp16): x = n + f with n = round(x) and f in [-0.5, 0.5],
-// 2^f from a degree-4 polynomial, 2^n added to the exponent field.  The
-// coefficients are a least-squares fit of 2^f in relative error at 4097
-// Chebyshev nodes of [-0.5, 0.5]; evaluated in fp32 (Horner) the relative
-// error stays below 3e-6 over the interval, far under the 2^-11 rounding of
-// the fp16 weights it feeds.  Adding 1.5 * 2^23 rounds x to an integer held
-// in the low mantissa bits of t; those bits shifted by 23 are n in the
-// exponent position (two's complement wraps for n < 0).
-__device__ __forceinline__ float exp2_poly(float x)
-{
-    x = fmaxf(x, -127.f);
-    const float t = x + 12582912.f;
-    const float f = x - (t - 12582912.f);
-    float p = fmaf(0.009560510516166687f, f, 0.05591703951358795f);
-    p = fmaf(p, f, 0.24024981260299683f);
-    p = fmaf(p, f, 0.6931219696998596f);
-    p = fmaf(p, f, 0.9999991655349731f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 // Transpose of an 8x8 matrix of 16-bit elements held as mma fragments
 // (thread t: row t/4, columns 2(t%4), 2(t%4)+1).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)

@@ -34,14 +34,6 @@
 
 namespace pgd {
 
-// Exponentials of the softmax: one column in four on the FMA pipe
-// (exp2_poly), the rest on the special-function unit, whose 16 results per
-// clock and SM would otherwise take as long as the tile's matrix products.
-__device__ __forceinline__ float exp2_split(int c, float x)
-{
-    return ex2(x);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
     paged_varlen_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -374,17 +366,17 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             } else if (masked_tile) {  // masked scores give 0 whatever the scale (0 included)
 #pragma unroll
                 for (int c = 0; c < HC; c += 2) {
-                    const float a = x[c] == masked ? 0.f : exp2_split(c, fmaf(x[c], sc, off));
+                    const float a = x[c] == masked ? 0.f : ex2(fmaf(x[c], sc, off));
                     const float b =
-                        x[c + 1] == masked ? 0.f : exp2_split(c + 1, fmaf(x[c + 1], sc, off));
+                        x[c + 1] == masked ? 0.f : ex2(fmaf(x[c + 1], sc, off));
                     pk[c / 2] = pack_half2(a, b);
                     sum += a + b;
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < HC; c += 2) {
-                    const float a = exp2_split(c, fmaf(x[c], sc, off));
-                    const float b = exp2_split(c + 1, fmaf(x[c + 1], sc, off));
+                    const float a = ex2(fmaf(x[c], sc, off));
+                    const float b = ex2(fmaf(x[c + 1], sc, off));
                     pk[c / 2] = pack_half2(a, b);
                     sum += a + b;
                 }
