@@ -41,22 +41,34 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# partition kernel from one ncu capture (profiles/), valid only for the
-# kernel sources they were taken on (hash of csrc/ below).
+# dominant kernel from one ncu capture (profiles/), valid only for the kernel
+# sources they were taken on (hash of csrc/ below), keyed by (workload,
+# partition size).
 TRAFFIC = {
-    "5b2a9b24854f33e7": {("batch_decode", 512): 633_325_568 + 5_516_800},
+    # decode kernels (hash without pgd_varlen.cu)
+    "87a5f486f84e3b04": {("batch_decode", 512): 633_313_024 + 5_209_600},
+    # the several-query-token kernel (hash of all sources)
+    "eae0f9a91e51ed3d": {("chunked_prefill", 8320): 231_608_576 + 13_471_744},
 }
 
 
-def kernel_source_hash():
+def kernel_source_hash(exclude=()):
+    """Hash of the CUDA sources (csrc/), less the files in `exclude`: the
+    decode kernels do not include pgd_varlen.cu, so their traffic figure
+    stays valid while only that file changes."""
     import glob
     import hashlib
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "paged_gqa_decode_03_gb300", "csrc", "*"))):
+        if os.path.basename(f) in exclude:
+            continue
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+DECODE_HASH_EXCLUDE = ("pgd_varlen.cu",)
 
 
 def measured_peaks():
@@ -397,7 +409,7 @@ def run_ours(args):
 
     if rank == 0:
         achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-        traffic = TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, P_used))
+        traffic = TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get((args.workload, P_used))
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -585,7 +597,7 @@ def run_varlen_bench(args):
             achieved = flops / (kern_ms * 1e-3) / 1e12
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t, "frac_of_sustained": achieved / peak_t_sus,
-                    "traffic": None,
+                    "traffic": TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, PK)),
                     "peak_source": f"{peak_kind} (MEASURED_PEAKS bf16_tflops; fp16 at the bf16 rate)",
                     "algorithmic_flops_per_launch": flops}
             e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
@@ -594,7 +606,8 @@ def run_varlen_bench(args):
             value, unit = kv_gbs, "GB/s"
             achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peak_b, "unit": "GB/s",
-                    "frac": achieved / peak_b, "traffic": None,
+                    "frac": achieved / peak_b,
+                    "traffic": TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, PK)),
                     "peak_source": "measured (MEASURED_PEAKS hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg_bytes}
             e2e_val = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
