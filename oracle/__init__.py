@@ -84,6 +84,12 @@ def _bind(lib):
     lib.oracle_append_kv_strided.restype = I
     lib.oracle_paged_varlen.argtypes = [P] * 7 + [D] + [I] * 7 + [Lg] * 3 + [I]
     lib.oracle_paged_varlen.restype = I
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = D
+    lib.oracle_dequant_affine.argtypes = [P, P, P, Lg, I]
+    lib.oracle_dequant_affine.restype = I
+    lib.oracle_paged_gqa_decode_q8.argtypes = [P] * 8 + [D] + [I] * 8
+    lib.oracle_paged_gqa_decode_q8.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -352,6 +358,45 @@ def varlen(q, cu_seqlens_q, k_cache, v_cache, block_tables, seq_lens, scale, lay
     _check(lib.oracle_paged_varlen(_ptr(out), _ptr(q), _ptr(cu), _ptr(k), _ptr(v), _ptr(bt),
                                    _ptr(sl), float(scale), S, Hq, int(Hkv), D, int(BS), MB,
                                    int(NB), sp, sh, st, int(threads or max_threads())))
+    return out
+
+
+def bf16_to_double(bits):
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.oracle_bf16_to_double(int(b)) for b in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+def dequant_affine(codes, meta, group=64):
+    """w = scale * code + bias per group (codes uint8 [n], meta bf16 bits
+    [n / group, 2] = (scale, bias))."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    m = np.ascontiguousarray(meta, dtype=np.uint16)
+    w = np.empty(c.size, dtype=np.float64)
+    _check(lib.oracle_dequant_affine(_ptr(w), _ptr(c), _ptr(m), int(c.size), int(group)))
+    return w.reshape(np.shape(codes))
+
+
+def decode_q8(q, k_codes, k_meta, v_codes, v_meta, block_tables, seq_lens, scale, threads=None):
+    """``decode`` over quantised caches: codes uint8 [NB, Hkv, BS, D], meta
+    bf16 bits [NB, Hkv, BS, D/64, 2] (scale, bias)."""
+    lib = _load()
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    km = np.ascontiguousarray(k_meta, dtype=np.uint16)
+    vm = np.ascontiguousarray(v_meta, dtype=np.uint16)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, D = q.shape
+    NB, Hkv, BS, D2 = kc.shape
+    assert D2 == D and km.shape == (NB, Hkv, BS, D // 64, 2), (kc.shape, km.shape)
+    MB = bt.shape[1]
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_paged_gqa_decode_q8(_ptr(out), _ptr(q), _ptr(kc), _ptr(km), _ptr(vc),
+                                          _ptr(vm), _ptr(bt), _ptr(sl), float(scale), S, Hq,
+                                          Hkv, D, BS, MB, NB, int(threads or max_threads())))
     return out
 
 

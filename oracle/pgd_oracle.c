@@ -576,6 +576,106 @@ int oracle_append_kv_strided(uint16_t *k_cache, uint16_t *v_cache, const uint16_
                      MB, NB);
 }
 
+/*
+ * Quantised KV pages in the affine group format of the Kapitsa series
+ * (blog.hacking.pub, "权重怎样存储: 4-bit 编码与额外的量化参数"): a value is
+ * approximated as scale * q + bias, with an unsigned integer code q and one
+ * (scale, bias) pair per group of consecutive values, both stored as bf16.
+ * Here the codes are 8-bit, a group is 64 consecutive head_dim elements of
+ * one token row, and the pairs are stored [NB][Hkv][BS][D/64][2] next to the
+ * codes [NB][Hkv][BS][D].
+ */
+
+/* bf16 -> double: the bf16 bits are the upper half of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* w[i] = scale_g * codes[i] + bias_g for n values in groups of `group`
+ * (meta: [n / group][2] bf16 pairs (scale, bias)). */
+int oracle_dequant_affine(double *w, const uint8_t *codes, const uint16_t *meta, long n,
+                          int group)
+{
+    if (n < 0 || group <= 0 || n % group != 0)
+        return ORC_BAD_SHAPE;
+    for (long i = 0; i < n; ++i) {
+        long gidx = i / group;
+        w[i] = oracle_bf16_to_double(meta[2 * gidx]) * codes[i] +
+               oracle_bf16_to_double(meta[2 * gidx + 1]);
+    }
+    return ORC_OK;
+}
+
+/* The decode definition over quantised caches: every K/V row is first
+ * dequantised (oracle_dequant_affine), then attention as in
+ * oracle_paged_gqa_decode (natural exp, fp64). */
+int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_codes,
+                               const uint16_t *k_meta, const uint8_t *v_codes,
+                               const uint16_t *v_meta, const int32_t *block_tables,
+                               const int32_t *seq_lens, double scale, int S, int Hq, int Hkv,
+                               int D, int BS, int MB, int NB, int num_threads)
+{
+    int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
+    if (rc)
+        return rc;
+    if (D % 64 != 0)
+        return ORC_BAD_SHAPE;
+    h2d_init();
+    int G = Hq / Hkv;
+    long pairs = (long)S * Hq;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+    for (long sh = 0; sh < pairs; ++sh) {
+        int s = (int)(sh / Hq), h = (int)(sh % Hq);
+        int g = h / G;
+        long L = seq_lens[s];
+        double *o = out + sh * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        if (L == 0)
+            continue;
+        double *z = (double *)malloc(sizeof(double) * (size_t)L);
+        double *row = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!z || !row) {
+            free(z);
+            free(row);
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        const uint16_t *qh = q + sh * D;
+        for (long t = 0; t < L; ++t) {
+            long r = ((long)block_tables[(long)s * MB + t / BS] * Hkv + g) * BS + t % BS;
+            oracle_dequant_affine(row, k_codes + r * D, k_meta + r * (D / 64) * 2, D, 64);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += g_h2d[qh[d]] * row[d];
+            z[t] = scale * dot;
+        }
+        double zmax = -INFINITY;
+        for (long t = 0; t < L; ++t)
+            if (z[t] > zmax)
+                zmax = z[t];
+        double den = 0.0;
+        for (long t = 0; t < L; ++t)
+            den += exp(z[t] - zmax);
+        for (long t = 0; t < L; ++t) {
+            double w = exp(z[t] - zmax) / den;
+            long r = ((long)block_tables[(long)s * MB + t / BS] * Hkv + g) * BS + t % BS;
+            oracle_dequant_affine(row, v_codes + r * D, v_meta + r * (D / 64) * 2, D, 64);
+            for (int d = 0; d < D; ++d)
+                o[d] += w * row[d];
+        }
+        free(z);
+        free(row);
+    }
+    return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -352,3 +352,47 @@ def make_varlen_workload(name: str, seed: int | None = None, device="cuda", pois
                        ctx=spec["ctx"], n=spec["n"], seed=seed, device=device, poison=poison,
                        name=name)
 
+
+# ---------------------------------------------------------------- quantised pages
+@dataclass
+class Q8Caches:
+    """K and V of a workload as 8-bit codes with one bf16 (scale, bias) pair
+    per 64 head_dim values of a row (the affine group format): codes uint8
+    [NB, Hkv, BS, D], meta int16 (bf16 bits) [NB, Hkv, BS, D/64, 2]."""
+    k_codes: torch.Tensor
+    k_meta: torch.Tensor
+    v_codes: torch.Tensor
+    v_meta: torch.Tensor
+
+    def bytes_per_token_head(self, D: int) -> int:
+        return 2 * (D + (D // 64) * 4)
+
+
+def make_q8(w: Workload, seed: int | None = None) -> Q8Caches:
+    """Seeded codes and metadata over the page placement of ``w``: codes
+    drawn around 128 with spread 40, scales near 1/40 and biases near -128
+    scale (values of order one), all random draws, nothing quantised.  Where
+    ``w``'s caches hold poison (rows past a sequence's end, unowned pages)
+    the scale is NaN."""
+    dev = w.k_cache.device
+    g = torch.Generator(device=dev)
+    g.manual_seed((w.meta.get("seed", 0) if seed is None else seed) + 424242)
+    NB, Hkv, BS, D = w.k_cache.shape
+    out = []
+    for cache in (w.k_cache, w.v_cache):
+        codes = torch.empty((NB, Hkv, BS, D), dtype=torch.uint8, device=dev)
+        meta = torch.empty((NB, Hkv, BS, D // 64, 2), dtype=torch.bfloat16, device=dev)
+        chunk = 1 << 14
+        for a in range(0, NB, chunk):
+            b = min(NB, a + chunk)
+            c = torch.randn((b - a, Hkv, BS, D), generator=g, device=dev) * 40 + 128
+            codes[a:b] = c.round().clamp_(0, 255).to(torch.uint8)
+            sc = (1 + 0.2 * (torch.rand((b - a, Hkv, BS, D // 64), generator=g, device=dev) - 0.5)) / 40
+            bi = -128 * sc + 0.05 * torch.randn((b - a, Hkv, BS, D // 64), generator=g, device=dev)
+            poison = torch.isnan(cache[a:b].view(b - a, Hkv, BS, D // 64, 64).float()).any(-1)
+            sc = torch.where(poison, torch.full_like(sc, float("nan")), sc)
+            meta[a:b, ..., 0] = sc.to(torch.bfloat16)
+            meta[a:b, ..., 1] = bi.to(torch.bfloat16)
+        out += [codes, meta.view(torch.int16)]
+    return Q8Caches(*out)
+

@@ -52,12 +52,18 @@ MUTANTS = [
      "logits(z, q + ((long)s * Hq + h) * D,", False),
     ("varlen: owner of a row off by one", "while (cu_q[s + 1] <= r)", "while (cu_q[s + 1] < r)",
      False),
+    ("q8: scale and bias swapped", "meta[2 * gidx]) * codes[i] +\n               oracle_bf16_to_double(meta[2 * gidx + 1]);",
+     "meta[2 * gidx + 1]) * codes[i] +\n               oracle_bf16_to_double(meta[2 * gidx]);", False),
+    ("q8: V dequantised with the K metadata", "v_codes + r * D, v_meta + r", "v_codes + r * D, k_meta + r",
+     False),
+    ("q8: bf16 bits shifted by 15", "(uint32_t)h << 16", "(uint32_t)h << 15", False),
 ]
 
 
 def _pins():
     import test_oracle as T
     import test_oracle_varlen as V
+    import test_oracle_q8 as Q
     return [
         ("half decoding", T.test_half_decoding_matches_numpy),
         ("hand case 0", lambda: T.test_hand_cases(0)),
@@ -87,6 +93,10 @@ def _pins():
         ("varlen n = 1", V.test_single_token_rows_equal_decode),
         ("varlen prompt row 0", V.test_prompt_first_row_is_v0),
         ("varlen permutation", V.test_page_permutation_invariance),
+        ("q8 worked example", Q.test_worked_example),
+        ("q8 bf16", Q.test_bf16_decoding_matches_torch),
+        ("q8 exact fp16", Q.test_equals_fp16_decode_on_exact_values),
+        ("q8 sdpa", lambda: Q.test_dense_sdpa_on_dequantised_values(8, 2, 8)),
     ]
 
 
