@@ -280,11 +280,23 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     k_new = v_new = None
+    q8 = None
+    if args.kv == "q8":  # the same workload over quantised pages (codes + bf16 pairs)
+        from paged_gqa_decode_03_gb300.workloads import make_q8
+        if args.append or args.layout != "head_major":
+            raise SystemExit("--kv q8 runs the plain decode over head-major pages only")
+        q8 = make_q8(w)
+        kv_bytes = int(w.lens.sum()) * w.Hkv * 2 * (w.D + (w.D // 64) * 4)
+        alg_bytes = kv_bytes + w.S * w.Hq * w.D * (2 + 4) + int(w.page_offsets[-1]) * 4
     if args.append:  # the decode step with its fused KV-cache append
         gen = torch.Generator(device=dev).manual_seed(7)
         k_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
         v_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
-    if args.layout != "head_major":
+    if q8 is not None:
+        def call(q, bt, sl):
+            pgd.paged_gqa_decode_q8(out, q, q8.k_codes, q8.k_meta, q8.v_codes, q8.v_meta, bt, sl,
+                                    w.scale, P, stream=stream)
+    elif args.layout != "head_major":
         # the same caches in another layout, through the strided entry point
         # (the head-major copy stays for the CPU baseline)
         strides = pgd.kv_strides(args.layout, w.Hkv, w.BS, w.D)
@@ -399,7 +411,7 @@ def run_ours(args):
 
     # ---- CPU baseline: the oracle on this host (rank 0, N == 1 only)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and q8 is None:
         seqs = list(range(w.S))
         sec, kv_s, threads, reps = oracle_time(w, seqs, min_seconds=args.cpu_seconds)
         cpu = {"value": kv_s / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -409,7 +421,8 @@ def run_ours(args):
 
     if rank == 0:
         achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-        traffic = TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get((args.workload, P_used))
+        traffic = TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get(
+            (args.workload + ("_q8" if q8 is not None else ""), P_used))
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -423,6 +436,8 @@ def run_ours(args):
                        "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
                        "accumulate": "fp32", "parallelism": f"replicas x{world}",
                        "fused_kv_append": bool(args.append), "kv_layout": args.layout,
+                       "kv_format": "8-bit codes + bf16 (scale, bias) per 64" if q8 is not None
+                       else "fp16",
                        "ms_per_step_with_kernel_events": ms_instrumented},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -651,6 +666,8 @@ def main():
                     help="time the decode step with its fused KV-cache append")
     ap.add_argument("--layout", choices=["head_major", "token_major"], default="head_major",
                     help="K/V cache layout (token_major runs through paged_gqa_decode_strided)")
+    ap.add_argument("--kv", choices=["fp16", "q8"], default="fp16",
+                    help="cache format: fp16 rows, or quantised pages (paged_gqa_decode_q8)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -251,6 +251,35 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                                     int num_blocks, void *stream);
 
 /*
+ * paged_gqa_decode_q8 — the decode step over quantised pages: the affine
+ * group format of the Kapitsa series (blog.hacking.pub, part 02, "how
+ * weights are stored": a value is scale * q + bias with an unsigned integer
+ * code q and one bf16 (scale, bias) pair per group of values), with 8-bit
+ * codes and groups of 64 consecutive head_dim values of one token row.
+ * About 53 % of the fp16 bytes at head_dim 128.
+ *
+ * k_codes, v_codes  [num_blocks][num_kv_heads][block_size][head_dim] uint8,
+ *                   16-byte aligned
+ * k_meta, v_meta    [num_blocks][num_kv_heads][block_size][head_dim / 64][2]
+ *                   bf16 bit patterns (scale, bias), 16-byte aligned
+ * The row of token t is dequantised as scale_g * code + bias_g for element d
+ * in group g = d / 64; the decode is then that of paged_gqa_decode over the
+ * dequantised rows (the affine map is applied in fp32 around exact fp16
+ * tensor-core products of the codes; nothing is rounded to fp16 that the
+ * fp16 path does not round).  Other arguments as for paged_gqa_decode_ex
+ * (workspace NULL: library scratch).  head_dim 128 or 256 only; no fused
+ * append.
+ */
+pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_codes,
+                               const uint16_t *k_meta, const uint8_t *v_codes,
+                               const uint16_t *v_meta, const int32_t *block_tables,
+                               const int32_t *seq_lens, float scale, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int partition_size, int max_blocks_per_seq, int num_blocks,
+                               void *workspace, size_t workspace_bytes, int32_t *page_trace,
+                               void *stream);
+
+/*
  * paged_gqa_varlen — attention for several query tokens per sequence over the
  * paged cache: the unified paged variable-length form of "vllm-metal"
  * (introduction and "Three Metal kernels": prefill chunks, decode steps and
@@ -328,7 +357,7 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: strided caches,
  * head_dim 64, block sizes 64 and 128; 1.2.0: several query tokens per
- * sequence). */
+ * sequence; 1.3.0: quantised pages). */
 int pgd_version(void);
 
 #ifdef __cplusplus

@@ -28,7 +28,7 @@ import torch
 
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
            "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
-           "paged_gqa_varlen", "pgd_varlen_plan", "pgd_plan", "pgd_last_partition_size",
+           "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -52,6 +52,7 @@ SIGNATURES = {
     "paged_gqa_decode_strided": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_L] * 3 + [_P, _Z, _P, _P]),
     "paged_gqa_varlen": (_I, [_P] * 7 + [_F] + [_I] * 9 + [_L] * 3 + [_I, _P, _Z, _P]),
     "pgd_varlen_plan": (_I, [_I] * 9 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
+    "paged_gqa_decode_q8": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -314,6 +315,44 @@ def pgd_varlen_plan(num_seqs, total_q, max_q_len, num_q_heads, num_kv_heads, hea
                                head_dim, block_size, max_blocks_per_seq, kv_partition,
                                ctypes.byref(pk), ctypes.byref(b)))
     return pk.value, b.value
+
+
+def paged_gqa_decode_q8(out, q, k_codes, k_meta, v_codes, v_meta, block_tables, seq_lens, scale,
+                        partition_size: int = 0, workspace=None, page_trace=None,
+                        stream=None) -> None:
+    """Decode over quantised pages: codes uint8 [NB, Hkv, BS, D], meta int16
+    (bf16 bits) [NB, Hkv, BS, D/64, 2] = (scale, bias) per 64 values."""
+    lib = load_library()
+    _check(q, "q", torch.float16, 3)
+    _check(out, "out", torch.float32, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _check(t, n, torch.uint8, 4)
+    for t, n in ((k_meta, "k_meta"), (v_meta, "v_meta")):
+        _check(t, n, torch.int16, 5)
+    S, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_codes.shape
+    if (v_codes.shape != k_codes.shape or D2 != D or out.shape != q.shape
+            or tuple(k_meta.shape) != (NB, Hkv, BS, D // 64, 2) or v_meta.shape != k_meta.shape):
+        raise ValueError("inconsistent shapes of q, codes, meta, out")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens do not have num_seqs rows")
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if page_trace is not None:
+        _check(page_trace, "page_trace", torch.int32, 3)
+        if tuple(page_trace.shape) != (S, Hkv, block_tables.shape[1]):
+            raise ValueError("page_trace must be [num_seqs, num_kv_heads, max_blocks_per_seq]")
+    st = lib.paged_gqa_decode_q8(
+        _ptr(out), _ptr(q), _ptr(k_codes), _ptr(k_meta), _ptr(v_codes), _ptr(v_meta),
+        _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv, D, BS, int(partition_size),
+        block_tables.shape[1], NB, _ptr(workspace), ws_bytes, _ptr(page_trace),
+        _stream_handle(stream, q.device))
+    _raise(st)
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # PGD_NOALLOC_SCRATCH_BYTES of include/pgd.h

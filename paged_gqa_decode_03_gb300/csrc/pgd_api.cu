@@ -55,7 +55,7 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_error = cudaSuccess;
     int num_sms = 0;
-    int ctas[3][5] = {};            // [head_dim 64/128/256][block size 8..128]
+    int ctas[2][3][5] = {};         // [quantised pages][head_dim 64/128/256][block size 8..128]
     unsigned *err_word = nullptr;   // address of g_device_error on this device
     std::once_flag pool_once;       // the pool is made on first library-owned scratch
     cudaError_t pool_error = cudaSuccess;
@@ -89,14 +89,15 @@ cudaError_t init_device(int dev, DeviceState &st)
     cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    for (int i = 0; i < 5; ++i) {
-        if ((e = occupancy_d64(kBlockSizes[i], &st.ctas[0][i])) != cudaSuccess)
-            return e;
-        if ((e = occupancy_d128(kBlockSizes[i], &st.ctas[1][i])) != cudaSuccess)
-            return e;
-        if ((e = occupancy_d256(kBlockSizes[i], &st.ctas[2][i])) != cudaSuccess)
-            return e;
-    }
+    for (int q8 = 0; q8 < 2; ++q8)
+        for (int i = 0; i < 5; ++i) {
+            if ((e = occupancy_d64(kBlockSizes[i], q8, &st.ctas[q8][0][i])) != cudaSuccess)
+                return e;
+            if ((e = occupancy_d128(kBlockSizes[i], q8, &st.ctas[q8][1][i])) != cudaSuccess)
+                return e;
+            if ((e = occupancy_d256(kBlockSizes[i], q8, &st.ctas[q8][2][i])) != cudaSuccess)
+                return e;
+        }
     return cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error);
 }
 
@@ -206,6 +207,50 @@ pgd_status encode_cache_map(CUtensorMap *map, const void *base, const CacheGeom 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PGD_OK;
+}
+
+// Quantised pages (head-major): the 8-bit codes [NB][Hkv][BS][D] viewed as
+// 128 bytes x BS rows x D/128 slabs x Hkv x NB (same box and landing order
+// as the fp16 rows), and their (scale, bias) pairs [NB][Hkv][BS][D/64] as
+// 32-bit elements: BS*D/64 per (page, head) x Hkv x NB, a box being the
+// pairs of box_rows rows.
+pgd_status encode_code_map(CUtensorMap *map, const void *base, const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    cuuint64_t dims[5] = {128, (cuuint64_t)g.BS, (cuuint64_t)(g.D / 128), (cuuint64_t)g.Hkv,
+                          (cuuint64_t)g.NB};
+    cuuint64_t strides[4] = {(cuuint64_t)g.D, 128, (cuuint64_t)g.BS * g.D,
+                             (cuuint64_t)g.Hkv * g.BS * g.D};
+    cuuint32_t box[5] = {128, (cuuint32_t)box_rows, (cuuint32_t)(g.D / 128), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (codes) failed (CUresult %d)", (int)r);
+    return PGD_OK;
+}
+
+pgd_status encode_meta_map(CUtensorMap *map, const void *base, const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    const int ng = g.D / kQuantGroup;
+    cuuint64_t dims[3] = {(cuuint64_t)g.BS * ng, (cuuint64_t)g.Hkv, (cuuint64_t)g.NB};
+    cuuint64_t strides[2] = {(cuuint64_t)g.BS * ng * 4, (cuuint64_t)g.Hkv * g.BS * ng * 4};
+    cuuint32_t box[3] = {(cuuint32_t)(box_rows * ng), 1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (CUresult %d)", (int)r);
     return PGD_OK;
 }
 
@@ -353,7 +398,8 @@ thread_local MapCacheEntry t_maps[kMapCache];
 thread_local int t_maps_used = 0, t_maps_next = 0;
 
 // kind 0: the decode view (box = rows per copy); kind 1: the page-group view
-// (box = 8-row groups per copy).
+// (box = 8-row groups per copy); kind 2: quantised codes, kind 3: their
+// (scale, bias) pairs (box = rows per copy).
 pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box, int kind,
                       const CUtensorMap **tk, const CUtensorMap **tv)
 {
@@ -372,10 +418,19 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
-    if (kind == 0 ? ((st = encode_cache_map(&c.tk, k, geom, box)) ||
-                     (st = encode_cache_map(&c.tv, v, geom, box)))
-                  : ((st = encode_cache_map_groups(&c.tk, k, geom, box)) ||
-                     (st = encode_cache_map_groups(&c.tv, v, geom, box)))) {
+    auto enc = [&](CUtensorMap *m, const void *base) -> pgd_status {
+        switch (kind) {
+        case 0:
+            return encode_cache_map(m, base, geom, box);
+        case 1:
+            return encode_cache_map_groups(m, base, geom, box);
+        case 2:
+            return encode_code_map(m, base, geom, box);
+        default:
+            return encode_meta_map(m, base, geom, box);
+        }
+    };
+    if ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v))) {
         c.k = c.v = nullptr;
         return st;
     }
@@ -442,7 +497,8 @@ int choose_partition(int S, int Hkv, int maxlen, int num_sms, int ctas_per_sm)
     return full512 >= target ? kPartitionLarge : kPartitionSmall;
 }
 
-pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan *plan)
+pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan *plan,
+                     bool q8 = false)
 {
     pgd_status st = check_sizes(S, Hq, Hkv, D, BS, P, MB);
     if (st)
@@ -450,7 +506,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     DeviceState *ds;
     if ((st = device_state(&ds)))
         return st;
-    const int ctas = ds->ctas[d_index(D)][bs_index(BS)];
+    const int ctas = ds->ctas[q8][d_index(D)][bs_index(BS)];
     if (ctas < 1)
         return fail(PGD_ERR_UNSUPPORTED, "partition kernel does not fit on an SM");
     const int maxlen = MB * BS;
@@ -513,24 +569,36 @@ pgd_status check_strides(const Strides &x, int D)
     return PGD_OK;
 }
 
-pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+// q8: the caches hold 8-bit codes (head-major) and k_meta / v_meta their
+// (scale, bias) pairs.
+pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
                int Hkv, int D, int BS, int P, int MB, int NB, const Strides &kv_strides,
                void *workspace, size_t ws_bytes, bool own_workspace, int32_t *page_trace,
                void *stream_v, unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
-               const uint16_t *v_new = nullptr)
+               const uint16_t *v_new = nullptr, bool q8 = false, const void *k_meta = nullptr,
+               const void *v_meta = nullptr)
 {
+    if (q8) {
+        if (D % 128 != 0)
+            return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d", D);
+        if (k_new || v_new)
+            return fail(PGD_ERR_UNSUPPORTED, "no fused append into quantised pages");
+    }
     if (S == 0) {  // nothing to read or write: only the sizes are checked
         Plan plan;
-        pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan);
+        pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, q8);
         if (st0)
             return st0;
         t_last_partition = plan.P;
         t_last_error.clear();
         return PGD_OK;
     }
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens ||
+        (q8 && (!k_meta || !v_meta)))
         return fail(PGD_ERR_INVALID_ARG, "null array argument");
+    if (q8 && (!aligned(k_meta, 16) || !aligned(v_meta, 16)))
+        return fail(PGD_ERR_INVALID_ARG, "k_meta and v_meta must be 16-byte aligned");
     if (!std::isfinite(scale))
         return fail(PGD_ERR_INVALID_ARG, "scale is not finite");
     if (NB <= 0)
@@ -548,7 +616,7 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     if (!own_workspace && workspace && !aligned(workspace, 256))
         return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     Plan plan;
-    if ((st = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan)))
+    if ((st = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, q8)))
         return st;
     DeviceState *ds;
     if ((st = device_state(&ds)))
@@ -575,12 +643,14 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
 
     const int box = BS < stage_tokens(D) ? BS : stage_tokens(D);
     const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
-    const CUtensorMap *tk = nullptr, *tv = nullptr;
-    if ((st = cache_maps(k_cache, v_cache, geom, box, 0, &tk, &tv))) {
+    const CUtensorMap *tk = nullptr, *tv = nullptr, *tkm = nullptr, *tvm = nullptr;
+    if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? 2 : 0, &tk, &tv)) ||
+        (q8 && (st = cache_maps(k_meta, v_meta, geom, box, 3, &tkm, &tvm)))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
     }
+    const KVMaps maps = {tk, tv, q8 ? tkm : tk, q8 ? tvm : tv};
 
     // claim counter: given (static scratch), this stream's, or a per-call one
     int slot = -1;
@@ -619,8 +689,8 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     p.counter = counter;
     p.k_new = reinterpret_cast<const __half *>(k_new);
     p.v_new = reinterpret_cast<const __half *>(v_new);
-    p.k_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(k_cache));
-    p.v_cache = reinterpret_cast<__half *>(const_cast<uint16_t *>(v_cache));
+    p.k_cache = reinterpret_cast<__half *>(const_cast<void *>(k_cache));
+    p.v_cache = reinterpret_cast<__half *>(const_cast<void *>(v_cache));
     p.kv_page_stride = kv_strides.page;
     p.kv_head_stride = kv_strides.head;
     p.kv_token_stride = kv_strides.token;
@@ -644,9 +714,9 @@ pgd_status run(float *out, const uint16_t *q, const uint16_t *k_cache, const uin
     lc.ev_before = t_ev_before;
     lc.ev_after = t_ev_after;
     const bool trace = page_trace != nullptr;
-    e = D == 64    ? launch_decode_d64(BS, trace, *tk, *tv, p, lc)
-        : D == 128 ? launch_decode_d128(BS, trace, *tk, *tv, p, lc)
-                   : launch_decode_d256(BS, trace, *tk, *tv, p, lc);
+    e = D == 64    ? launch_decode_d64(BS, trace, q8, maps, p, lc)
+        : D == 128 ? launch_decode_d128(BS, trace, q8, maps, p, lc)
+                   : launch_decode_d256(BS, trace, q8, maps, p, lc);
     if (own_workspace && ws) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess)
@@ -995,6 +1065,26 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                nullptr, stream, static_cast<unsigned *>(scratch));
 }
 
+pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_codes,
+                               const uint16_t *k_meta, const uint8_t *v_codes,
+                               const uint16_t *v_meta, const int32_t *block_tables,
+                               const int32_t *seq_lens, float scale, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int partition_size, int max_blocks_per_seq, int num_blocks,
+                               void *workspace, size_t workspace_bytes, int32_t *page_trace,
+                               void *stream)
+{
+    if (num_seqs > 0 && (!k_meta || !v_meta))
+        return fail(PGD_ERR_INVALID_ARG, "null k_meta / v_meta");
+    const bool own = workspace == nullptr;
+    // the codes' strides in elements (bytes): head-major [NB][Hkv][BS][D]
+    return run(out, q, k_codes, v_codes, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, head_major(num_kv_heads, block_size, head_dim), workspace,
+               workspace_bytes, own, page_trace, stream, nullptr, nullptr, nullptr, true, k_meta,
+               v_meta);
+}
+
 pgd_status paged_gqa_varlen(float *out, const uint16_t *q, const int32_t *cu_seqlens_q,
                             const uint16_t *k_cache, const uint16_t *v_cache,
                             const int32_t *block_tables, const int32_t *seq_lens, float scale,
@@ -1089,10 +1179,10 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
     if (num_sms)
         *num_sms = ds->num_sms;
     if (ctas_per_sm)
-        *ctas_per_sm = ds->ctas[d_index(head_dim)][bs_index(block_size)];
+        *ctas_per_sm = ds->ctas[0][d_index(head_dim)][bs_index(block_size)];
     return PGD_OK;
 }
 
-int pgd_version(void) { return 10200; }
+int pgd_version(void) { return 10300; }
 
 }  // extern "C"

@@ -108,6 +108,17 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 5-D tiled tensor copy global -> shared, completion counted on `bar`.
 // Coordinates innermost first.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -308,6 +319,31 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
     uint32_t d;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
+}
+
+// Two 8-bit codes (bytes 0,1 of `w`, or 2,3 when `hi`) as an exact fp16
+// pair: each byte b becomes the fp16 bit pattern 0x64bb = 1024 + b, and 1024
+// is subtracted (both steps exact).
+__device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, bool hi)
+{
+    const uint32_t t = __byte_perm(w, 0x64646464u, hi ? 0x4342u : 0x4140u);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
+{
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// (scale, bias) of one quantisation group: a bf16 pair, scale in the low
+// half-word; bf16 bits are the upper half of an fp32.
+__device__ __forceinline__ float2 bf16_pair(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)

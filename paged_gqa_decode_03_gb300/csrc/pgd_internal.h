@@ -36,24 +36,53 @@ constexpr int kMaxTailStages = 16;
 // (NC, one 16-token tile each), stages in the shared-memory ring (NS).  The
 // ring holds about 100 KB for every head_dim (two CTAs per SM).
 template <int D> struct Shape;
+// NS8: stages for quantised pages (8-bit codes: half the bytes per stage,
+// more stages for the same bytes in flight).
 template <> struct Shape<64> {
-    static constexpr int T = 64, NC = 4, NS = 6;
+    static constexpr int T = 64, NC = 4, NS = 6, NS8 = 6;
 };
 template <> struct Shape<128> {
-    static constexpr int T = 64, NC = 4, NS = 3;
+    static constexpr int T = 64, NC = 4, NS = 3, NS8 = 5;
 };
 template <> struct Shape<256> {
-    static constexpr int T = 32, NC = 2, NS = 3;
+    static constexpr int T = 32, NC = 2, NS = 3, NS8 = 5;
 };
 
-template <int D> __host__ __device__ constexpr int stage_kv_bytes() { return Shape<D>::T * D * 2; }  // K or V
+// Quantised pages: 8-bit codes plus one (scale, bias) bf16 pair per 64
+// values of a row.
+constexpr int kQuantGroup = 64;
+
+// Bytes of K (or V) codes / values of one stage, of their (scale, bias)
+// pairs, and of a whole stage (K, V, their pairs, the group's queries).
+template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_kv_bytes()
+{
+    return Shape<D>::T * D * (Q8 ? 1 : 2);
+}
+// (scale, bias) pairs of one copied page piece, padded so every piece lands
+// 128-byte aligned (a tensor-copy requirement); the stage reserves room for
+// the worst case, 8-row pages.
+__host__ __device__ constexpr int meta_slot_bytes(int rows, int D)
+{
+    return (rows * (D / kQuantGroup) * 4 + 127) / 128 * 128;
+}
+template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_meta_bytes()
+{
+    return Q8 ? (Shape<D>::T / 8) * meta_slot_bytes(8, D) : 0;
+}
 template <int D> __host__ __device__ constexpr int stage_q_bytes() { return kMaxGroup * D * 2; }
-template <int D> __host__ __device__ constexpr int stage_bytes() { return 2 * stage_kv_bytes<D>() + stage_q_bytes<D>(); }
+template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_bytes()
+{
+    return 2 * stage_kv_bytes<D, Q8>() + 2 * stage_meta_bytes<D, Q8>() + stage_q_bytes<D>();
+}
+template <int D, bool Q8 = false> __host__ __device__ constexpr int ring_stages()
+{
+    return Q8 ? Shape<D>::NS8 : Shape<D>::NS;
+}
 // Dynamic shared memory: the ring plus slack to align it to 1024 bytes
 // (required by the 128-byte swizzle of the tensor copies).
-template <int D> __host__ __device__ constexpr size_t dyn_smem_bytes()
+template <int D, bool Q8 = false> __host__ __device__ constexpr size_t dyn_smem_bytes()
 {
-    return size_t(Shape<D>::NS) * stage_bytes<D>() + 1024;
+    return size_t(ring_stages<D, Q8>()) * stage_bytes<D, Q8>() + 1024;
 }
 
 struct DecodeParams {
@@ -86,20 +115,25 @@ struct LaunchConfig {
     cudaEvent_t ev_before, ev_after;  // optional timing hook (both or neither)
 };
 
+// The tensor maps of one decode launch: K and V (fp16 rows, or 8-bit codes),
+// and for quantised pages the maps of their (scale, bias) pairs (otherwise
+// K and V again, unused).
+struct KVMaps {
+    const CUtensorMap *k, *v, *km, *vm;
+};
+
 // Per-head_dim entry points (pgd_kernels_d64.cu, _d128.cu, _d256.cu).
-cudaError_t launch_decode_d64(int block_size, bool trace, const CUtensorMap &tk,
-                              const CUtensorMap &tv, const DecodeParams &p,
-                              const LaunchConfig &lc);
-cudaError_t launch_decode_d128(int block_size, bool trace, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const DecodeParams &p,
-                               const LaunchConfig &lc);
-cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const DecodeParams &p,
-                               const LaunchConfig &lc);
-// Resident partition-kernel CTAs per SM for (head_dim, block_size).
-cudaError_t occupancy_d64(int block_size, int *ctas_per_sm);
-cudaError_t occupancy_d128(int block_size, int *ctas_per_sm);
-cudaError_t occupancy_d256(int block_size, int *ctas_per_sm);
+cudaError_t launch_decode_d64(int block_size, bool trace, bool q8, const KVMaps &m,
+                              const DecodeParams &p, const LaunchConfig &lc);
+cudaError_t launch_decode_d128(int block_size, bool trace, bool q8, const KVMaps &m,
+                               const DecodeParams &p, const LaunchConfig &lc);
+cudaError_t launch_decode_d256(int block_size, bool trace, bool q8, const KVMaps &m,
+                               const DecodeParams &p, const LaunchConfig &lc);
+// Resident partition-kernel CTAs per SM for (head_dim, block_size, page kind);
+// 0 where no kernel is built (quantised pages at head_dim 64).
+cudaError_t occupancy_d64(int block_size, bool q8, int *ctas_per_sm);
+cudaError_t occupancy_d128(int block_size, bool q8, int *ctas_per_sm);
+cudaError_t occupancy_d256(int block_size, bool q8, int *ctas_per_sm);
 
 // Reduce kernel: one CTA per (sequence, query head); two warps suffice for
 // head_dim 64 and 128 (whose workloads have at most 16 partitions per

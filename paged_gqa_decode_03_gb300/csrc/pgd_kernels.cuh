@@ -46,24 +46,39 @@ struct StageHeader {
     long long app_off;  // kAppend: element offset of the newest token's cache row, -1: none
 };
 
-template <int D, int BS, bool TRACE>
+// Q8: the cache holds 8-bit codes with a bf16 (scale, bias) pair per 64
+// values of a row (tmap_km / tmap_vm: the pairs); the affine map is applied
+// in fp32 around exact fp16 tensor-core products of the codes:
+//   s = sum_g scale_g (q_g . code_g) + bias_g sum(q_g)            (QK)
+//   O += sum_t (p_t scale_g(t)) code_t + sum_t p_t bias_g(t)      (PV)
+template <int D, int BS, bool TRACE, bool Q8>
 __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     paged_gqa_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
+                             const __grid_constant__ CUtensorMap tmap_km,
+                             const __grid_constant__ CUtensorMap tmap_vm,
                              const DecodeParams p)
 {
-    constexpr int T = Shape<D>::T, NC = Shape<D>::NC, NS = Shape<D>::NS;
-    constexpr int SLABS = D / 64;          // 128-byte column slabs of a row
+    constexpr int T = Shape<D>::T, NC = Shape<D>::NC, NS = ring_stages<D, Q8>();
+    constexpr int ROWB = D * (Q8 ? 1 : 2); // bytes of one cached row
+    constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
-    constexpr int PAGE_BYTES = BOX * D * 2;  // one copy: BOX rows of one page, all slabs
+    constexpr int PAGE_BYTES = BOX * ROWB; // one copy: BOX rows of one page, all slabs
+    constexpr int NGRP = D / kQuantGroup;  // quantisation groups of a row
+    constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
+    constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
     constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
-    constexpr int KV_BYTES = stage_kv_bytes<D>();
-    constexpr int STAGE = stage_bytes<D>();
+    constexpr int KV_BYTES = stage_kv_bytes<D, Q8>();
+    constexpr int META_BYTES = stage_meta_bytes<D, Q8>();
+    constexpr int Q_OFF = 2 * KV_BYTES + 2 * META_BYTES;  // the group's queries in a stage
+    constexpr int STAGE = stage_bytes<D, Q8>();
     constexpr int OST = D + 4;             // merge buffer row stride (floats)
     static_assert(NC * 16 == T, "one 16-token tile per consumer warp per stage");
     static_assert(BS <= T ? (T % BS == 0) : (BS % T == 0), "stage/page sizes");
     static_assert(STAGE % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle alignment");
     static_assert(NC * kMaxGroup * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
+    static_assert(!Q8 || (D % 128 == 0), "quantised pages: rows of whole 128-byte slabs");
+    static_assert(!Q8 || (T / BOX) * META_SLOT <= META_BYTES, "scale slots fit the stage");
 
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[NS];
@@ -162,6 +177,10 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
         if (lane == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
+            if (Q8) {
+                prefetch_tensormap(&tmap_km);
+                prefetch_tensormap(&tmap_vm);
+            }
         }
         const uint64_t pol = l2_evict_first_policy();
         const int S = p.S, Hkv = p.Hkv, P = p.P, G = p.G, MB = p.MB;
@@ -235,7 +254,8 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
                                       (app_unit && st == nst - 1 ? kAppend : 0);
                     hdr[slot].app_off = app_off;
-                    const uint32_t bytes = pc * PAGE_BYTES * 2 + (st == 0 ? G * D * 2 : 0);
+                    const uint32_t bytes =
+                        pc * (PAGE_BYTES + PAGE_META) * 2 + (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
                 for (int jj = 0; jj < pc; ++jj) {
@@ -256,10 +276,16 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         const uint32_t dk = sb + jj * PAGE_BYTES;
                         tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
                         tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
+                        if (Q8) {  // the rows' (scale, bias) pairs: [row][group]
+                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT;
+                            tma_load_3d(dm, &tmap_km, row0 * NGRP, g, c_page, fb, pol);
+                            tma_load_3d(dm + META_BYTES, &tmap_vm, row0 * NGRP, g, c_page, fb,
+                                        pol);
+                        }
                     }
                 }
                 if (st == 0 && lane == 0)
-                    bulk_load(sb + 2 * KV_BYTES, p.q + ((size_t)s * p.Hq + (size_t)g * G) * D,
+                    bulk_load(sb + Q_OFF, p.q + ((size_t)s * p.Hq + (size_t)g * G) * D,
                               G * D * 2, fb);
             }
             return true;
@@ -407,13 +433,20 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
     const int tq = (lane & 3) * 2;       // C-fragment columns: query heads tq, tq+1
     const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix index, row in it
     const int t0 = 16 * w;               // this warp's tile within a stage
-    float o[KT][4];                      // O^T[D x 8]: row 16 i + gb (+8), columns tq, tq+1
+    float o[KT][4];                      // O^T[D x 8]: 16-row tile i, columns tq, tq+1
     uint32_t qf[KT][2];                  // Q^T B-fragments
+    // Q8: rows of O^T are interleaved: tile i, fragment rows gb / gb+8 hold
+    // d = 16i + 2gb / 16i + 2gb + 1 (the order the byte codes of V load in)
+    float qsum[NGRP > 0 ? NGRP : 1][2];  // Q8: sum of q over each group, heads tq, tq+1
+    float beta[NGRP > 0 ? NGRP : 1][2];  // Q8: sum_t p_t bias_g(t), this lane's tokens
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         qf[i][0] = qf[i][1] = 0u;
     }
+#pragma unroll
+    for (int gi = 0; gi < (NGRP > 0 ? NGRP : 1); ++gi)
+        qsum[gi][0] = qsum[gi][1] = beta[gi][0] = beta[gi][1] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads tq, tq+1 (log2 units)
     float l0 = 0.f, l1 = 0.f;              // this lane's share of the running exp2-sums
     uint32_t msync = 0;                    // merge-barrier phases passed
@@ -448,54 +481,83 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
         if (flags & kFirst) {
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
-            const uint8_t *qs = sp + 2 * KV_BYTES;
+            const uint8_t *qs = sp + Q_OFF;
             const bool live = gb < p.G;
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
                 o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-                const uint8_t *qrow = qs + (gb * D + i * 16 + tq) * 2;
-                qf[i][0] = live ? *reinterpret_cast<const uint32_t *>(qrow) : 0u;
-                qf[i][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16) : 0u;
+                // fp16 pages: k slots tq, tq+1 | tq+8, tq+9 are d = 16i + tq.. | +8..;
+                // Q8: they are d = 16i + 2tq, +1 | 16i + 2tq + 2, +3 (the bytes one
+                // ldmatrix row piece gives a lane)
+                const int d0 = Q8 ? i * 16 + 2 * tq : i * 16 + tq;
+                const int d1 = Q8 ? d0 + 2 : d0 + 8;
+                qf[i][0] = live ? *reinterpret_cast<const uint32_t *>(qs + (gb * D + d0) * 2) : 0u;
+                qf[i][1] = live ? *reinterpret_cast<const uint32_t *>(qs + (gb * D + d1) * 2) : 0u;
+            }
+            if constexpr (Q8) {
+                // sum of q over each group for head gb (four lanes hold its
+                // d's), then each lane takes heads tq, tq+1
+#pragma unroll
+                for (int gi = 0; gi < NGRP; ++gi) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int i = gi * 4; i < gi * 4 + 4; ++i) {
+                        const float2 a = unpack_half2(qf[i][0]), b = unpack_half2(qf[i][1]);
+                        sum += (a.x + a.y) + (b.x + b.y);
+                    }
+                    sum += __shfl_xor_sync(~0u, sum, 1);
+                    sum += __shfl_xor_sync(~0u, sum, 2);
+                    qsum[gi][0] = __shfl_sync(~0u, sum, tq * 4);
+                    qsum[gi][1] = __shfl_sync(~0u, sum, (tq + 1) * 4);
+                    beta[gi][0] = beta[gi][1] = 0.f;
+                }
             }
         }
         if (t0 < valid) {
-            if (t0 + 16 > valid) {
-                // rows of this tile past the unit's end: zero V so that
-                // zero weights never meet stale or NaN rows
-                const int r_lo = valid, nrow = t0 + 16 - valid;
-                for (int idx = lane; idx < nrow * SLABS * 8; idx += 32) {
-                    const int r = r_lo + idx / (SLABS * 8), c = idx % (SLABS * 8);
-                    *reinterpret_cast<uint4 *>(sp + KV_BYTES + (r / BOX) * PAGE_BYTES +
-                                               (c >> 3) * (BOX * 128) + (r % BOX) * 128 +
-                                               (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-                }
-                __syncwarp();
-            }
-            if ((flags & kAppend) && valid - 1 >= t0 && valid - 1 < t0 + 16) {
-                // fused append: the newest token (row valid-1 of the stage,
-                // in this warp's tile) takes its K and V from k_new / v_new,
-                // in the staged page (same 128-byte swizzle as the copies)
-                // and in the cache for the next steps
-                const int r = valid - 1;
-                const long long app_off = hdr[slot].app_off;
-                const size_t src = ((size_t)hs * p.Hkv + hg) * D;
-                for (int c = lane; c < D / 8; c += 32) {
-                    const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + src + c * 8);
-                    const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src + c * 8);
-                    const int off = (r / BOX) * PAGE_BYTES + (c >> 3) * (BOX * 128) +
-                                    (r % BOX) * 128 + (((c & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sp + off) = kv;
-                    *reinterpret_cast<uint4 *>(sp + KV_BYTES + off) = vv;
-                    if (app_off >= 0) {
-                        *reinterpret_cast<uint4 *>(p.k_cache + app_off + c * 8) = kv;
-                        *reinterpret_cast<uint4 *>(p.v_cache + app_off + c * 8) = vv;
+            if constexpr (!Q8) {
+                if (t0 + 16 > valid) {
+                    // rows of this tile past the unit's end: zero V so that
+                    // zero weights never meet stale or NaN rows
+                    const int r_lo = valid, nrow = t0 + 16 - valid;
+                    for (int idx = lane; idx < nrow * SLABS * 8; idx += 32) {
+                        const int r = r_lo + idx / (SLABS * 8), c = idx % (SLABS * 8);
+                        *reinterpret_cast<uint4 *>(sp + KV_BYTES + (r / BOX) * PAGE_BYTES +
+                                                   (c >> 3) * (BOX * 128) + (r % BOX) * 128 +
+                                                   (c & 7) * 16) = make_uint4(0, 0, 0, 0);
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
+                if ((flags & kAppend) && valid - 1 >= t0 && valid - 1 < t0 + 16) {
+                    // fused append: the newest token (row valid-1 of the stage,
+                    // in this warp's tile) takes its K and V from k_new / v_new,
+                    // in the staged page (same 128-byte swizzle as the copies)
+                    // and in the cache for the next steps
+                    const int r = valid - 1;
+                    const long long app_off = hdr[slot].app_off;
+                    const size_t src = ((size_t)hs * p.Hkv + hg) * D;
+                    for (int c = lane; c < D / 8; c += 32) {
+                        const uint4 kv = *reinterpret_cast<const uint4 *>(p.k_new + src + c * 8);
+                        const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src + c * 8);
+                        const int off = (r / BOX) * PAGE_BYTES + (c >> 3) * (BOX * 128) +
+                                        (r % BOX) * 128 + (((c & 7) ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(sp + off) = kv;
+                        *reinterpret_cast<uint4 *>(sp + KV_BYTES + off) = vv;
+                        if (app_off >= 0) {
+                            *reinterpret_cast<uint4 *>(p.k_cache + app_off + c * 8) = kv;
+                            *reinterpret_cast<uint4 *>(p.v_cache + app_off + c * 8) = vv;
+                        }
+                    }
+                    __syncwarp();
+                }
             }
-            // S^T[16 tokens x 8 heads] = K[tile] . Q^T
-            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-            {
+            // S^T[16 tokens x 8 heads] = K[tile] . Q^T (Q8: one accumulator
+            // per quantisation group, combined with the groups' scales below)
+            constexpr int NACC = Q8 ? NGRP : 2;
+            float c[NACC][4];
+#pragma unroll
+            for (int a = 0; a < NACC; ++a)
+                c[a][0] = c[a][1] = c[a][2] = c[a][3] = 0.f;
+            if constexpr (!Q8) {
                 const int tok = t0 + r8 + (mi & 1) * 8;
                 const uint32_t rowaddr = sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
                 const int sw = tok & 7;
@@ -506,18 +568,58 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                         rowaddr + (dim >> 6) * (BOX * 128) + ((((dim & 63) >> 3) ^ sw) << 4);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(addr, a0, a1, a2, a3);
-                    if (kk & 1)
-                        mma_16816(c1, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                    else
-                        mma_16816(c0, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                    mma_16816(c[kk & 1], a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                }
+            } else {
+                // K codes: 16 bytes (one k-step) per ldmatrix row piece;
+                // matrices: rows 0-7 / 8-15 of the tile, k-steps kk / kk+1
+                const int tok = t0 + r8 + (mi & 1) * 8;
+                const uint32_t rowaddr = sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                const int sw = tok & 7;
+#pragma unroll
+                for (int kk = 0; kk < KT; kk += 2) {
+                    const int chunk = kk + (mi >> 1);  // 16-byte chunk of the row
+                    const uint32_t addr =
+                        rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(addr, r0, r1, r2, r3);
+                    mma_16816(c[kk / 4], codes_to_half2(r0, false), codes_to_half2(r1, false),
+                              codes_to_half2(r0, true), codes_to_half2(r1, true), qf[kk][0],
+                              qf[kk][1]);
+                    mma_16816(c[(kk + 1) / 4], codes_to_half2(r2, false), codes_to_half2(r3, false),
+                              codes_to_half2(r2, true), codes_to_half2(r3, true), qf[kk + 1][0],
+                              qf[kk + 1][1]);
                 }
             }
             const float sc = p.scale_log2;
             const bool va = t0 + gb < valid, vb = t0 + gb + 8 < valid;
-            const float x0 = va ? (c0[0] + c1[0]) * sc : -INFINITY;  // token gb,   head tq
-            const float x1 = va ? (c0[1] + c1[1]) * sc : -INFINITY;  // token gb,   head tq+1
-            const float x2 = vb ? (c0[2] + c1[2]) * sc : -INFINITY;  // token gb+8, head tq
-            const float x3 = vb ? (c0[3] + c1[3]) * sc : -INFINITY;  // token gb+8, head tq+1
+            float d0, d1, d2, d3;  // token gb / gb+8, head tq / tq+1
+            if constexpr (!Q8) {
+                d0 = c[0][0] + c[1][0];
+                d1 = c[0][1] + c[1][1];
+                d2 = c[0][2] + c[1][2];
+                d3 = c[0][3] + c[1][3];
+            } else {
+                const uint8_t *kmeta = sp + 2 * KV_BYTES;
+                const int ra = t0 + gb, rb = ra + 8;
+                const uint32_t *kma = reinterpret_cast<const uint32_t *>(
+                    kmeta + (ra / BOX) * META_SLOT + (ra % BOX) * NGRP * 4);
+                const uint32_t *kmb = reinterpret_cast<const uint32_t *>(
+                    kmeta + (rb / BOX) * META_SLOT + (rb % BOX) * NGRP * 4);
+                d0 = d1 = d2 = d3 = 0.f;
+#pragma unroll
+                for (int gi = 0; gi < NGRP; ++gi) {
+                    const float2 ea = bf16_pair(kma[gi]), eb = bf16_pair(kmb[gi]);
+                    d0 += fmaf(ea.x, c[gi][0], ea.y * qsum[gi][0]);
+                    d1 += fmaf(ea.x, c[gi][1], ea.y * qsum[gi][1]);
+                    d2 += fmaf(eb.x, c[gi][2], eb.y * qsum[gi][0]);
+                    d3 += fmaf(eb.x, c[gi][3], eb.y * qsum[gi][1]);
+                }
+            }
+            const float x0 = va ? d0 * sc : -INFINITY;  // token gb,   head tq
+            const float x1 = va ? d1 * sc : -INFINITY;  // token gb,   head tq+1
+            const float x2 = vb ? d2 * sc : -INFINITY;  // token gb+8, head tq
+            const float x3 = vb ? d3 * sc : -INFINITY;  // token gb+8, head tq+1
             // ---- one online-softmax step over the tile (token 0 of the tile is valid,
             // so every column max is finite)
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -530,8 +632,9 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
             m0 = mn0;
             m1 = mn1;
-            const uint32_t pa = pack_half2(ex2(x0 - mn0), ex2(x1 - mn1));  // P[gb][tq..tq+1]
-            const uint32_t pb = pack_half2(ex2(x2 - mn0), ex2(x3 - mn1));  // P[gb+8][..]
+            const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);  // P[gb][tq..tq+1]
+            const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);  // P[gb+8][..]
+            const uint32_t pa = pack_half2(p0, p1), pb = pack_half2(p2, p3);
             const float2 fa = unpack_half2(pa), fb = unpack_half2(pb);
             l0 = l0 * al0 + (fa.x + fb.x);
             l1 = l1 * al1 + (fa.y + fb.y);
@@ -542,9 +645,9 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                 o[i][2] *= al0;
                 o[i][3] *= al1;
             }
-            // P^T as the B operand of O^T += V^T . P^T: register transpose
-            const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
-            {
+            if constexpr (!Q8) {
+                // P^T as the B operand of O^T += V^T . P^T: register transpose
+                const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
                 const int tok = t0 + r8 + (mi >> 1) * 8;
                 const int sw = tok & 7;
                 const uint32_t rowaddr =
@@ -557,6 +660,56 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     uint32_t v0, v1, v2, v3;
                     ldsm_x4_t(addr, v0, v1, v2, v3);
                     mma_16816(o[i], v0, v1, v2, v3, b0, b1);
+                }
+            } else {
+                // per group: P scaled by the V rows' scales as the B operand,
+                // the biases into beta; V^T fragments from two codes
+                // (d = 16i + 2gb, +1) of tokens tq, tq+1, tq+8, tq+9
+                const uint8_t *vmeta = sp + 2 * KV_BYTES + META_BYTES;
+                const int ra = t0 + gb, rb = ra + 8;
+                const uint32_t *vma = reinterpret_cast<const uint32_t *>(
+                    vmeta + (ra / BOX) * META_SLOT + (ra % BOX) * NGRP * 4);
+                const uint32_t *vmb = reinterpret_cast<const uint32_t *>(
+                    vmeta + (rb / BOX) * META_SLOT + (rb % BOX) * NGRP * 4);
+                uint32_t bf[NGRP][2];
+#pragma unroll
+                for (int gi = 0; gi < NGRP; ++gi) {
+                    float2 ea = bf16_pair(vma[gi]), eb = bf16_pair(vmb[gi]);
+                    if (!va)  // rows past the unit's end: their pairs may be anything
+                        ea = make_float2(0.f, 0.f);
+                    if (!vb)
+                        eb = make_float2(0.f, 0.f);
+                    bf[gi][0] = movmatrix_trans(pack_half2(p0 * ea.x, p1 * ea.x));
+                    bf[gi][1] = movmatrix_trans(pack_half2(p2 * eb.x, p3 * eb.x));
+                    beta[gi][0] = beta[gi][0] * al0 + (p0 * ea.y + p2 * eb.y);
+                    beta[gi][1] = beta[gi][1] * al1 + (p1 * ea.y + p3 * eb.y);
+                }
+                const uint32_t vrow = sb + KV_BYTES;
+                uint32_t rowoff[4];  // tokens tq, tq+1, tq+8, tq+9 of the tile
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = t0 + tq + (j & 1) + (j >> 1) * 8;
+                    rowoff[j] = (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                }
+#pragma unroll
+                for (int i = 0; i < KT; ++i) {
+                    const int byte = i * 16 + 2 * gb;   // d of fragment row gb
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int tok = t0 + tq + (j & 1) + (j >> 1) * 8;
+                        wv[j] = ld_shared_u16(vrow + rowoff[j] + (byte >> 7) * (BOX * 128) +
+                                              ((((byte & 127) >> 4) ^ (tok & 7)) << 4) + (byte & 15));
+                    }
+                    // bytes [v(t, d), v(t, d+1)] of tokens tq / tq+1 -> A rows
+                    // gb (d) and gb+8 (d+1), k slots tq, tq+1 (and +8, +9)
+                    // [v(tq,d), v(tq+1,d), v(tq,d+1), v(tq+1,d+1)] and the same for
+                    // tokens tq+8, tq+9
+                    const uint32_t lo = __byte_perm(wv[0], wv[1], 0x5140);
+                    const uint32_t hi = __byte_perm(wv[2], wv[3], 0x5140);
+                    mma_16816(o[i], codes_to_half2(lo, false), codes_to_half2(lo, true),
+                              codes_to_half2(hi, false), codes_to_half2(hi, true), bf[i / 4][0],
+                              bf[i / 4][1]);
                 }
             }
         }
@@ -580,6 +733,25 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             lt0 += __shfl_xor_sync(~0u, lt0, off);
             lt1 += __shfl_xor_sync(~0u, lt1, off);
         }
+        if constexpr (Q8) {
+            // the biases' part of O: the same for every d of a group
+#pragma unroll
+            for (int gi = 0; gi < NGRP; ++gi) {
+                float b0 = beta[gi][0], b1 = beta[gi][1];
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    b0 += __shfl_xor_sync(~0u, b0, off);
+                    b1 += __shfl_xor_sync(~0u, b1, off);
+                }
+#pragma unroll
+                for (int i = gi * 4; i < gi * 4 + 4; ++i) {
+                    o[i][0] += b0;
+                    o[i][1] += b1;
+                    o[i][2] += b0;
+                    o[i][3] += b1;
+                }
+            }
+        }
         if (!consumers_sync())  // every warp is done reading the stage
             break;
         if (gb == 0) {
@@ -592,11 +764,12 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
             float *ow = mg_o + w * kMaxGroup * OST;
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
-                const int d = i * 16 + gb;
+                const int d = Q8 ? i * 16 + 2 * gb : i * 16 + gb;   // fragment row gb
+                const int d8 = Q8 ? d + 1 : d + 8;                  // fragment row gb+8
                 ow[tq * OST + d] = o[i][0];
                 ow[(tq + 1) * OST + d] = o[i][1];
-                ow[tq * OST + d + 8] = o[i][2];
-                ow[(tq + 1) * OST + d + 8] = o[i][3];
+                ow[tq * OST + d8] = o[i][2];
+                ow[(tq + 1) * OST + d8] = o[i][3];
             }
         }
         if (!consumers_sync())  // all states written
@@ -788,7 +961,7 @@ __global__ void __launch_bounds__(reduce_threads<D>())
 // ---------------------------------------------------------------- launch
 // Raises the partition kernel's dynamic shared-memory limit, once per
 // device and instantiation.
-template <int D, int BS, bool TRACE>
+template <int D, int BS, bool TRACE, bool Q8>
 cudaError_t ensure_smem_attribute()
 {
     static std::atomic<unsigned long long> done{0};  // bit per device ordinal < 64
@@ -799,29 +972,29 @@ cudaError_t ensure_smem_attribute()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem_bytes<D>());
+    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn_smem_bytes<D, Q8>());
     if (e == cudaSuccess)
         done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 
-template <int D, int BS, bool TRACE>
-cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv,
-                               const DecodeParams &p, const LaunchConfig &lc)
+template <int D, int BS, bool TRACE, bool Q8>
+cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const LaunchConfig &lc)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, TRACE>;
-    cudaError_t e = ensure_smem_attribute<D, BS, TRACE>();
+    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8>;
+    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(lc.grid);
     cfg.blockDim = dim3((Shape<D>::NC + 1) * 32);
-    cfg.dynamicSmemBytes = dyn_smem_bytes<D>();
+    cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8>();
     cfg.stream = lc.stream;
     if (lc.ev_before && (e = cudaEventRecord(lc.ev_before, lc.stream)) != cudaSuccess)
         return e;
-    if ((e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, kern, *m.k, *m.v, *m.km, *m.vm, p)) != cudaSuccess)
         return e;
     if (lc.ev_after && (e = cudaEventRecord(lc.ev_after, lc.stream)) != cudaSuccess)
         return e;
@@ -837,63 +1010,82 @@ cudaError_t launch_decode_impl(const CUtensorMap &tk, const CUtensorMap &tv,
     return cudaLaunchKernelEx(&rcfg, paged_gqa_reduce_kernel<D>, p, p.MB * BS);
 }
 
-template <int D, int BS>
+template <int D, int BS, bool Q8>
 cudaError_t occupancy_impl(int *ctas)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, false>;
-    cudaError_t e = ensure_smem_attribute<D, BS, false>();
+    auto kern = paged_gqa_partial_kernel<D, BS, false, Q8>;
+    cudaError_t e = ensure_smem_attribute<D, BS, false, Q8>();
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, (Shape<D>::NC + 1) * 32,
-                                                         dyn_smem_bytes<D>());
+                                                         dyn_smem_bytes<D, Q8>());
 }
 
 template <int D, int BS>
-cudaError_t launch_decode_bs(bool trace, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const DecodeParams &p, const LaunchConfig &lc)
+cudaError_t launch_decode_bs(bool trace, bool q8, const KVMaps &m, const DecodeParams &p,
+                             const LaunchConfig &lc)
 {
-    return trace ? launch_decode_impl<D, BS, true>(tk, tv, p, lc)
-                 : launch_decode_impl<D, BS, false>(tk, tv, p, lc);
+    if constexpr (D % 128 == 0) {
+        if (q8)
+            return trace ? launch_decode_impl<D, BS, true, true>(m, p, lc)
+                         : launch_decode_impl<D, BS, false, true>(m, p, lc);
+    } else if (q8) {
+        return cudaErrorInvalidValue;
+    }
+    return trace ? launch_decode_impl<D, BS, true, false>(m, p, lc)
+                 : launch_decode_impl<D, BS, false, false>(m, p, lc);
 }
 
 template <int D>
-cudaError_t launch_decode_dispatch(int block_size, bool trace, const CUtensorMap &tk,
-                                   const CUtensorMap &tv, const DecodeParams &p,
-                                   const LaunchConfig &lc)
+cudaError_t launch_decode_dispatch(int block_size, bool trace, bool q8, const KVMaps &m,
+                                   const DecodeParams &p, const LaunchConfig &lc)
 {
     switch (block_size) {
     case 8:
-        return launch_decode_bs<D, 8>(trace, tk, tv, p, lc);
+        return launch_decode_bs<D, 8>(trace, q8, m, p, lc);
     case 16:
-        return launch_decode_bs<D, 16>(trace, tk, tv, p, lc);
+        return launch_decode_bs<D, 16>(trace, q8, m, p, lc);
     case 32:
-        return launch_decode_bs<D, 32>(trace, tk, tv, p, lc);
+        return launch_decode_bs<D, 32>(trace, q8, m, p, lc);
     case 64:
-        return launch_decode_bs<D, 64>(trace, tk, tv, p, lc);
+        return launch_decode_bs<D, 64>(trace, q8, m, p, lc);
     case 128:
-        return launch_decode_bs<D, 128>(trace, tk, tv, p, lc);
+        return launch_decode_bs<D, 128>(trace, q8, m, p, lc);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+template <int D, bool Q8>
+cudaError_t occupancy_bs(int block_size, int *ctas)
+{
+    switch (block_size) {
+    case 8:
+        return occupancy_impl<D, 8, Q8>(ctas);
+    case 16:
+        return occupancy_impl<D, 16, Q8>(ctas);
+    case 32:
+        return occupancy_impl<D, 32, Q8>(ctas);
+    case 64:
+        return occupancy_impl<D, 64, Q8>(ctas);
+    case 128:
+        return occupancy_impl<D, 128, Q8>(ctas);
     default:
         return cudaErrorInvalidValue;
     }
 }
 
 template <int D>
-cudaError_t occupancy_dispatch(int block_size, int *ctas)
+cudaError_t occupancy_dispatch(int block_size, bool q8, int *ctas)
 {
-    switch (block_size) {
-    case 8:
-        return occupancy_impl<D, 8>(ctas);
-    case 16:
-        return occupancy_impl<D, 16>(ctas);
-    case 32:
-        return occupancy_impl<D, 32>(ctas);
-    case 64:
-        return occupancy_impl<D, 64>(ctas);
-    case 128:
-        return occupancy_impl<D, 128>(ctas);
-    default:
-        return cudaErrorInvalidValue;
+    if constexpr (D % 128 == 0) {
+        if (q8)
+            return occupancy_bs<D, true>(block_size, ctas);
+    } else if (q8) {
+        *ctas = 0;
+        return cudaSuccess;
     }
+    return occupancy_bs<D, false>(block_size, ctas);
 }
 
 }  // namespace pgd

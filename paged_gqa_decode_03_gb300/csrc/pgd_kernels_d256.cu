@@ -1,19 +1,17 @@
-// Instantiations of the decode kernels for head_dim 256 (block sizes 8 to 128,
-// with and without the page trace).
+// Instantiations of the decode kernels for head_dim 256 (block sizes 8 to 128, with and without the page trace, fp16 and quantised pages).
 #include "pgd_kernels.cuh"
 
 namespace pgd {
 
-cudaError_t launch_decode_d256(int block_size, bool trace, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const DecodeParams &p,
-                               const LaunchConfig &lc)
+cudaError_t launch_decode_d256(int block_size, bool trace, bool q8, const KVMaps &m,
+                              const DecodeParams &p, const LaunchConfig &lc)
 {
-    return launch_decode_dispatch<256>(block_size, trace, tk, tv, p, lc);
+    return launch_decode_dispatch<256>(block_size, trace, q8, m, p, lc);
 }
 
-cudaError_t occupancy_d256(int block_size, int *ctas_per_sm)
+cudaError_t occupancy_d256(int block_size, bool q8, int *ctas_per_sm)
 {
-    return occupancy_dispatch<256>(block_size, ctas_per_sm);
+    return occupancy_dispatch<256>(block_size, q8, ctas_per_sm);
 }
 
 }  // namespace pgd

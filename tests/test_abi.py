@@ -162,3 +162,15 @@ def test_kv_strides_helper():
     with pytest.raises(ValueError):
         pgd.kv_strides("page_major", 8, 16, 128)
 
+
+
+def call_q8(lib, D=128, metas=(A, A), S=4):
+    return lib.paged_gqa_decode_q8(A, A, A, metas[0], A, metas[1], A, A, ctypes.c_float(0.1), S,
+                                   32, 8, D, 16, 512, 64, 1024, ctypes.c_void_p(0), 0,
+                                   ctypes.c_void_p(0), ctypes.c_void_p(0))
+
+
+def test_q8_validation(lib):
+    assert call_q8(lib, D=64) == UNSUPPORTED             # codes need whole 128-byte rows
+    assert call_q8(lib, metas=(ctypes.c_void_p(0), A)) == INVALID
+    assert call_q8(lib, metas=(A, ctypes.c_void_p((1 << 20) + 8))) == INVALID
