@@ -641,7 +641,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
         }
     }
 
-    const int box = BS < stage_tokens(D) ? BS : stage_tokens(D);
+    const int stage_t = q8 ? (D == 128 ? Shape<128>::T8 : Shape<256>::T8) : stage_tokens(D);
+    const int box = BS < stage_t ? BS : stage_t;
     const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
     const CUtensorMap *tk = nullptr, *tv = nullptr, *tkm = nullptr, *tvm = nullptr;
     if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? 2 : 0, &tk, &tv)) ||

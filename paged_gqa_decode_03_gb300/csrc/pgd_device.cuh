@@ -332,11 +332,14 @@ __device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, bool hi)
     return r;
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
+// Bytes 0 and 2 (or 1 and 3 when `odd`) of `w` as an exact fp16 pair (see
+// codes_to_half2).
+__device__ __forceinline__ uint32_t codes_to_half2_strided(uint32_t w, bool odd)
 {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
+    const uint32_t t = __byte_perm(w, 0x64646464u, odd ? 0x4341u : 0x4240u);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
+    return r;
 }
 
 // (scale, bias) of one quantisation group: a bf16 pair, scale in the low

@@ -36,17 +36,20 @@ constexpr int kMaxTailStages = 16;
 // (NC, one 16-token tile each), stages in the shared-memory ring (NS).  The
 // ring holds about 100 KB for every head_dim (two CTAs per SM).
 template <int D> struct Shape;
-// NS8: stages for quantised pages (8-bit codes: half the bytes per stage,
-// more stages for the same bytes in flight).
+// T8 / NC8 / NS8: the same for quantised pages, whose consumers do more work
+// per byte (code conversion, the affine terms): twice the tokens and
+// consumer warps per stage, fewer stages (about the same bytes in flight).
 template <> struct Shape<64> {
-    static constexpr int T = 64, NC = 4, NS = 6, NS8 = 6;
+    static constexpr int T = 64, NC = 4, NS = 6, T8 = 64, NC8 = 4, NS8 = 6;
 };
 template <> struct Shape<128> {
-    static constexpr int T = 64, NC = 4, NS = 3, NS8 = 5;
+    static constexpr int T = 64, NC = 4, NS = 3, T8 = 128, NC8 = 8, NS8 = 2;
 };
 template <> struct Shape<256> {
-    static constexpr int T = 32, NC = 2, NS = 3, NS8 = 5;
+    static constexpr int T = 32, NC = 2, NS = 3, T8 = 64, NC8 = 4, NS8 = 2;
 };
+template <int D, bool Q8> __host__ __device__ constexpr int stage_tokens_of() { return Q8 ? Shape<D>::T8 : Shape<D>::T; }
+template <int D, bool Q8> __host__ __device__ constexpr int consumer_warps() { return Q8 ? Shape<D>::NC8 : Shape<D>::NC; }
 
 // Quantised pages: 8-bit codes plus one (scale, bias) bf16 pair per 64
 // values of a row.
@@ -56,7 +59,7 @@ constexpr int kQuantGroup = 64;
 // pairs, and of a whole stage (K, V, their pairs, the group's queries).
 template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_kv_bytes()
 {
-    return Shape<D>::T * D * (Q8 ? 1 : 2);
+    return stage_tokens_of<D, Q8>() * D * (Q8 ? 1 : 2);
 }
 // (scale, bias) pairs of one copied page piece, padded so every piece lands
 // 128-byte aligned (a tensor-copy requirement); the stage reserves room for
@@ -67,7 +70,7 @@ __host__ __device__ constexpr int meta_slot_bytes(int rows, int D)
 }
 template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_meta_bytes()
 {
-    return Q8 ? (Shape<D>::T / 8) * meta_slot_bytes(8, D) : 0;
+    return Q8 ? (stage_tokens_of<D, Q8>() / 8) * meta_slot_bytes(8, D) : 0;
 }
 template <int D> __host__ __device__ constexpr int stage_q_bytes() { return kMaxGroup * D * 2; }
 template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_bytes()

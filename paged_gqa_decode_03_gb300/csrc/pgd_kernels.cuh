@@ -52,14 +52,15 @@ struct StageHeader {
 //   s = sum_g scale_g (q_g . code_g) + bias_g sum(q_g)            (QK)
 //   O += sum_t (p_t scale_g(t)) code_t + sum_t p_t bias_g(t)      (PV)
 template <int D, int BS, bool TRACE, bool Q8>
-__global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
+__global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     paged_gqa_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ CUtensorMap tmap_km,
                              const __grid_constant__ CUtensorMap tmap_vm,
                              const DecodeParams p)
 {
-    constexpr int T = Shape<D>::T, NC = Shape<D>::NC, NS = ring_stages<D, Q8>();
+    constexpr int T = stage_tokens_of<D, Q8>(), NC = consumer_warps<D, Q8>();
+    constexpr int NS = ring_stages<D, Q8>();
     constexpr int ROWB = D * (Q8 ? 1 : 2); // bytes of one cached row
     constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
@@ -684,32 +685,28 @@ __global__ void __launch_bounds__((Shape<D>::NC + 1) * 32, 2)
                     beta[gi][0] = beta[gi][0] * al0 + (p0 * ea.y + p2 * eb.y);
                     beta[gi][1] = beta[gi][1] * al1 + (p1 * ea.y + p3 * eb.y);
                 }
-                const uint32_t vrow = sb + KV_BYTES;
-                uint32_t rowoff[4];  // tokens tq, tq+1, tq+8, tq+9 of the tile
+                // V codes by ldmatrix.trans on 16-byte row pieces (16 d): lane
+                // gets bytes [v(tq, d), v(tq, d+1), v(tq+1, d), v(tq+1, d+1)] with
+                // d = 16i + 2gb, i.e. A rows gb (d) and gb+8 (d+1), k slots
+                // tq, tq+1; matrices: tokens 0-7 / 8-15, pieces i / i+1
+                const int tok = t0 + r8 + (mi & 1) * 8;
+                const uint32_t rowaddr =
+                    sb + KV_BYTES + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                const int sw = tok & 7;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tok = t0 + tq + (j & 1) + (j >> 1) * 8;
-                    rowoff[j] = (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
-                }
-#pragma unroll
-                for (int i = 0; i < KT; ++i) {
-                    const int byte = i * 16 + 2 * gb;   // d of fragment row gb
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int tok = t0 + tq + (j & 1) + (j >> 1) * 8;
-                        wv[j] = ld_shared_u16(vrow + rowoff[j] + (byte >> 7) * (BOX * 128) +
-                                              ((((byte & 127) >> 4) ^ (tok & 7)) << 4) + (byte & 15));
-                    }
-                    // bytes [v(t, d), v(t, d+1)] of tokens tq / tq+1 -> A rows
-                    // gb (d) and gb+8 (d+1), k slots tq, tq+1 (and +8, +9)
-                    // [v(tq,d), v(tq+1,d), v(tq,d+1), v(tq+1,d+1)] and the same for
-                    // tokens tq+8, tq+9
-                    const uint32_t lo = __byte_perm(wv[0], wv[1], 0x5140);
-                    const uint32_t hi = __byte_perm(wv[2], wv[3], 0x5140);
-                    mma_16816(o[i], codes_to_half2(lo, false), codes_to_half2(lo, true),
-                              codes_to_half2(hi, false), codes_to_half2(hi, true), bf[i / 4][0],
-                              bf[i / 4][1]);
+                for (int i = 0; i < KT; i += 2) {
+                    const int chunk = i + (mi >> 1);
+                    const uint32_t addr =
+                        rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(addr, r0, r1, r2, r3);
+                    mma_16816(o[i], codes_to_half2_strided(r0, false),
+                              codes_to_half2_strided(r0, true), codes_to_half2_strided(r1, false),
+                              codes_to_half2_strided(r1, true), bf[i / 4][0], bf[i / 4][1]);
+                    mma_16816(o[i + 1], codes_to_half2_strided(r2, false),
+                              codes_to_half2_strided(r2, true), codes_to_half2_strided(r3, false),
+                              codes_to_half2_strided(r3, true), bf[(i + 1) / 4][0],
+                              bf[(i + 1) / 4][1]);
                 }
             }
         }
@@ -989,7 +986,7 @@ cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const Lau
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(lc.grid);
-    cfg.blockDim = dim3((Shape<D>::NC + 1) * 32);
+    cfg.blockDim = dim3((consumer_warps<D, Q8>() + 1) * 32);
     cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8>();
     cfg.stream = lc.stream;
     if (lc.ev_before && (e = cudaEventRecord(lc.ev_before, lc.stream)) != cudaSuccess)
@@ -1017,8 +1014,8 @@ cudaError_t occupancy_impl(int *ctas)
     cudaError_t e = ensure_smem_attribute<D, BS, false, Q8>();
     if (e != cudaSuccess)
         return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, (Shape<D>::NC + 1) * 32,
-                                                         dyn_smem_bytes<D, Q8>());
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        ctas, kern, (consumer_warps<D, Q8>() + 1) * 32, dyn_smem_bytes<D, Q8>());
 }
 
 template <int D, int BS>
