@@ -46,7 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "87a5f486f84e3b04": {("batch_decode", 512): 633_313_024 + 5_209_600},
+    "b0bc01d644b2e91f": {("batch_decode", 512): 633_327_872 + 5_126_400,
+                         ("batch_decode_q8", 512): 336_795_904 + 5_142_784},
     # the several-query-token kernel (hash of all sources)
     "eae0f9a91e51ed3d": {("chunked_prefill", 8320): 231_608_576 + 13_471_744},
 }
