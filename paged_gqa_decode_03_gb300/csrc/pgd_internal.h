@@ -153,19 +153,18 @@ constexpr unsigned kErrQueryLen = 8u;  // a query count < 0, > its length or > m
 // 128-row tiles and both score buffers live in 512 tensor-memory columns.
 template <int D> struct VShape;
 template <> struct VShape<64> {
-    static constexpr int NT = 128, NSTG = 3;
+    static constexpr int NT = 128, NSTG = 4;
 };
 template <> struct VShape<128> {
-    static constexpr int NT = 128, NSTG = 2;
+    static constexpr int NT = 128, NSTG = 2;  // a third stage would pass the 227 KB limit
 };
 template <> struct VShape<256> {
     static constexpr int NT = 64, NSTG = 2;
 };
 template <int D> __host__ __device__ constexpr size_t varlen_smem_bytes()
 {
-    // Q tile + stages of K and V + the fp16 P tile + alignment slack
-    return size_t(128) * D * 2 + size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 +
-           size_t(128) * VShape<D>::NT * 2 + 1024;
+    // Q tile + stages of K and V + alignment slack (P lives in tensor memory)
+    return size_t(128) * D * 2 + size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 + 1024;
 }
 constexpr int kVarlenThreads = 352;   // K producer, MMA, 8 softmax warps, V producer
 constexpr int kVWarp = 10;            // the V producer warp

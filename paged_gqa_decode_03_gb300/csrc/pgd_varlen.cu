@@ -24,7 +24,8 @@
 //     log2-space online softmax with exp2 ("Four speed-up tricks", 1); the
 //     reference max only moves when a score exceeds it by more than 2^8
 //     (p <= 256 stays exact in fp16), and only then is the row of O rescaled
-//     in tensor memory.  P goes to shared memory as fp16 (K-major, swizzled).
+//     in tensor memory.  P (fp16) overwrites the scores it came from in
+//     tensor memory, the A operand of P V.
 //     At the end: out = O / l, or the partition partial (log2-space max,
 //     exp-sum, normalised output, "Four speed-up tricks", 4).
 // paged_varlen_reduce_kernel<D> — merges the partials of rows that span more
@@ -92,9 +93,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     uint8_t *const base_ptr = dyn_smem + (base - dyn_base);
     const uint32_t q_s = base;
     const uint32_t kv_s = q_s + 128 * D * 2;              // stage st: K at +st*2*KV_TILE, V after
-    const uint32_t p_s = kv_s + NSTG * 2 * KV_TILE;
     uint8_t *const kv_ptr = base_ptr + 128 * D * 2;
-    uint8_t *const p_ptr = base_ptr + 128 * D * 2 + NSTG * 2 * KV_TILE;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -238,12 +237,13 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                         mbar_test_wait(smem_addr(&v_full[st]), (npv / NSTG) & 1)) {
                         tc_fence_after();
                         const uint32_t vs = kv_s + st * 2 * KV_TILE + KV_TILE;
+                        // P_npv in the columns of its score buffer: 16 tokens
+                        // per instruction = 8 columns
+                        const uint32_t pt = tmem + S_COL + (npv & 1) * NT;
 #pragma unroll
                         for (int kk = 0; kk < NT / 16; ++kk) {
-                            const uint64_t a =
-                                tc_sdesc(p_s + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
                             const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
-                            tc_mma(tmem + O_COL, a, b, IDESC_O, npv > 0 || kk > 0);
+                            tc_mma_ta(tmem + O_COL, pt + kk * 8, b, IDESC_O, npv > 0 || kk > 0);
                         }
                         tc_commit(smem_addr(&o_done));
                         tc_commit(smem_addr(&v_empty[st]));
@@ -408,7 +408,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             }
             // rows of the stage past the sequence end inside its last page may
             // hold anything: zero them in V (pages past it were copied as zeros)
-            if (L < t0 + NT && t0 < last_page_end && last_page_end > L) {
+            const bool zero_v = L < t0 + NT && t0 < last_page_end && last_page_end > L;
+            if (zero_v) {
                 const int st = jj % NSTG;
                 mbar_wait_bounded(smem_addr(&v_full[st]), (jj / NSTG) & 1, nullptr,
                                   p.wait_budget_ns);
@@ -421,15 +422,21 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                         make_uint4(0, 0, 0, 0);
                 }
             }
-            // this half of P row r: K-major, 128-byte swizzled, 64 tokens per slab
-#pragma unroll
-            for (int c16 = 0; c16 < HC / 8; ++c16) {
-                const int g16 = half * (HC / 8) + c16;
-                uint8_t *dst = p_ptr + (g16 >> 3) * Q_SLAB + r * 128 + (((g16 & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) =
-                    make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+            // this half of P row r into the score buffer it came from (both
+            // halves have read their scores: the pair met at the barrier
+            // above), two fp16 per column, as the A operand of P V
+            {
+                const uint32_t pt = t_lane + S_COL + (jj & 1) * NT + half * (HC / 2);
+                if constexpr (HC / 2 == 32) {
+                    tc_st32u(pt, pk);
+                } else {
+                    static_assert(HC / 2 == 16, "P columns per half");
+                    tc_st16u(pt, pk);
+                }
+                tc_wait_st();
             }
-            fence_proxy_async_smem();
+            if (zero_v)
+                fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
