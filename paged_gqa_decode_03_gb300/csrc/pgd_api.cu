@@ -692,6 +692,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.v_new = reinterpret_cast<const __half *>(v_new);
     p.k_cache = reinterpret_cast<__half *>(const_cast<void *>(k_cache));
     p.v_cache = reinterpret_cast<__half *>(const_cast<void *>(v_cache));
+    p.k_meta = q8 ? static_cast<const uint16_t *>(k_meta) : nullptr;
+    p.v_meta = q8 ? static_cast<const uint16_t *>(v_meta) : nullptr;
     p.kv_page_stride = kv_strides.page;
     p.kv_head_stride = kv_strides.head;
     p.kv_token_stride = kv_strides.token;

@@ -143,6 +143,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared on the load path (not the
+// tensor-copy unit); src_bytes 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Adds one pending arrival to the barrier's current phase now and performs
+// it once this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -357,25 +373,19 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
     return d;
 }
 
-// Two 8-bit codes (bytes 0,1 of `w`, or 2,3 when `hi`) as an exact fp16
-// pair: each byte b becomes the fp16 bit pattern 0x64bb = 1024 + b, and 1024
-// is subtracted (both steps exact).
-__device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, bool hi)
+// Two 8-bit codes (bytes 0,1 of `w`, or 2,3 when `hi`) as an fp16 pair
+// (1024 + b0, 1024 + b1): each byte b becomes the fp16 bit pattern 0x64bb,
+// exact (fp16 holds every integer up to 2048).  One byte permute; the caller
+// takes the 1024 back out of its sums.
+__device__ __forceinline__ uint32_t codes_to_half2_offset(uint32_t w, bool hi)
 {
-    const uint32_t t = __byte_perm(w, 0x64646464u, hi ? 0x4342u : 0x4140u);
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
-    return r;
+    return __byte_perm(w, 0x64646464u, hi ? 0x4342u : 0x4140u);
 }
 
-// Bytes 0 and 2 (or 1 and 3 when `odd`) of `w` as an exact fp16 pair (see
-// codes_to_half2).
-__device__ __forceinline__ uint32_t codes_to_half2_strided(uint32_t w, bool odd)
+// Bytes 0 and 2 (or 1 and 3 when `odd`) of `w` in the same form.
+__device__ __forceinline__ uint32_t codes_to_half2_strided_offset(uint32_t w, bool odd)
 {
-    const uint32_t t = __byte_perm(w, 0x64646464u, odd ? 0x4341u : 0x4240u);
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
-    return r;
+    return __byte_perm(w, 0x64646464u, odd ? 0x4341u : 0x4240u);
 }
 
 // (scale, bias) of one quantisation group: a bf16 pair, scale in the low

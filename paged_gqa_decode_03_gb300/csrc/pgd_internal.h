@@ -103,6 +103,8 @@ struct DecodeParams {
     const __half *v_new;          // [S][Hkv][D] newest token's V
     __half *k_cache;              // caches, written at the newest token's row (append)
     __half *v_cache;
+    const uint16_t *k_meta;       // quantised pages: [NB][Hkv][BS][D/64][2] bf16
+    const uint16_t *v_meta;       //   (scale, bias) pairs, or null
     long long kv_page_stride;     // cache strides in halves (the copies use the
     long long kv_head_stride;     //   same ones through the tensor maps)
     long long kv_token_stride;

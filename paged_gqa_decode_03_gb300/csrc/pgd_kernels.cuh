@@ -68,6 +68,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     constexpr int NGRP = D / kQuantGroup;  // quantisation groups of a row
     constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
     constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
+    // runs of 512 bytes and more go by tensor copy, shorter ones on the load path
+    constexpr bool META_BY_TMA = PAGE_META >= 512;
     constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
     constexpr int KV_BYTES = stage_kv_bytes<D, Q8>();
     constexpr int META_BYTES = stage_meta_bytes<D, Q8>();
@@ -247,6 +249,36 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         app_off = ida * p.kv_page_stride + g * p.kv_head_stride +
                                   ((L - 1) % BS) * p.kv_token_stride;
                 }
+                if constexpr (Q8 && !META_BY_TMA) {
+                    // the rows' (scale, bias) pairs, [row][group] per page
+                    // piece: one contiguous run per (page, KV head) of under
+                    // 512 bytes, copied by the lanes in 16-byte pieces on the
+                    // load path (the tensor-copy unit takes about as long per
+                    // copy whatever its size, and at 16-row pages these
+                    // copies would double its count); a page outside the
+                    // pool reads as zeros.  Each lane's arrival on the
+                    // stage's barrier waits for its copies.
+                    constexpr int CH = PAGE_META / 16;  // pieces per page
+                    static_assert(PAGE_META % 16 == 0, "16-byte pieces");
+                    for (int r0 = 0; r0 < pc * CH; r0 += 32) {
+                        const int idx = r0 + lane;
+                        const int jj = min(idx / CH, pc - 1), c = idx % CH;
+                        const int j = pf + jj;
+                        const int ida = __shfl_sync(~0u, id0, j & 31);
+                        const int idb = __shfl_sync(~0u, id1, j & 31);
+                        const int id = j < 32 ? ida : idb;
+                        if (idx < pc * CH) {
+                            const bool in = (unsigned)id < (unsigned)p.NB;
+                            const size_t off =
+                                in ? ((((size_t)id * Hkv + g) * BS + row0) * NGRP * 2 + c * 8) : 0;
+                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT + c * 16;
+                            cp_async_16(dm, p.k_meta + off, in ? 16u : 0u);
+                            cp_async_16(dm + META_BYTES, p.v_meta + off, in ? 16u : 0u);
+                        }
+                    }
+                    cp_async_mbar_arrive(fb);
+                    __syncwarp();  // every lane's arrival counted before the producer's own
+                }
                 if (lane == 0) {
                     hdr[slot].s = s;
                     hdr[slot].g = g;
@@ -255,8 +287,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                     hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
                                       (app_unit && st == nst - 1 ? kAppend : 0);
                     hdr[slot].app_off = app_off;
-                    const uint32_t bytes =
-                        pc * (PAGE_BYTES + PAGE_META) * 2 + (st == 0 ? G * D * 2 : 0);
+                    const uint32_t bytes = pc * (PAGE_BYTES + (META_BY_TMA ? PAGE_META : 0)) * 2 +
+                                           (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
                 for (int jj = 0; jj < pc; ++jj) {
@@ -277,7 +309,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         const uint32_t dk = sb + jj * PAGE_BYTES;
                         tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
                         tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
-                        if (Q8) {  // the rows' (scale, bias) pairs: [row][group]
+                        if (Q8 && META_BY_TMA) {  // the rows' (scale, bias) pairs
                             const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT;
                             tma_load_3d(dm, &tmap_km, row0 * NGRP, g, c_page, fb, pol);
                             tma_load_3d(dm + META_BYTES, &tmap_vm, row0 * NGRP, g, c_page, fb,
@@ -439,7 +471,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     // Q8: rows of O^T are interleaved: tile i, fragment rows gb / gb+8 hold
     // d = 16i + 2gb / 16i + 2gb + 1 (the order the byte codes of V load in)
     float qsum[NGRP > 0 ? NGRP : 1][2];  // Q8: sum of q over each group, heads tq, tq+1
-    float beta[NGRP > 0 ? NGRP : 1][2];  // Q8: sum_t p_t bias_g(t), this lane's tokens
+    // Q8: sum_t p_t bias_g(t) - 1024 P'_t over this lane's tokens.  Codes
+    // enter the products as 1024 + code (one byte permute per pair): for K
+    // the offset is folded into the bias term of the scores, for V taken out
+    // here with the fp16 P'_t = p_t scale_g(t) the products use
+    float beta[NGRP > 0 ? NGRP : 1][2];
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -584,12 +620,12 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(addr, r0, r1, r2, r3);
-                    mma_16816(c[kk / 4], codes_to_half2(r0, false), codes_to_half2(r1, false),
-                              codes_to_half2(r0, true), codes_to_half2(r1, true), qf[kk][0],
-                              qf[kk][1]);
-                    mma_16816(c[(kk + 1) / 4], codes_to_half2(r2, false), codes_to_half2(r3, false),
-                              codes_to_half2(r2, true), codes_to_half2(r3, true), qf[kk + 1][0],
-                              qf[kk + 1][1]);
+                    mma_16816(c[kk / 4], codes_to_half2_offset(r0, false),
+                              codes_to_half2_offset(r1, false), codes_to_half2_offset(r0, true),
+                              codes_to_half2_offset(r1, true), qf[kk][0], qf[kk][1]);
+                    mma_16816(c[(kk + 1) / 4], codes_to_half2_offset(r2, false),
+                              codes_to_half2_offset(r3, false), codes_to_half2_offset(r2, true),
+                              codes_to_half2_offset(r3, true), qf[kk + 1][0], qf[kk + 1][1]);
                 }
             }
             const float sc = p.scale_log2;
@@ -610,11 +646,13 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 d0 = d1 = d2 = d3 = 0.f;
 #pragma unroll
                 for (int gi = 0; gi < NGRP; ++gi) {
+                    // scale * (c - 1024 qsum) + bias * qsum (c over 1024 + code)
                     const float2 ea = bf16_pair(kma[gi]), eb = bf16_pair(kmb[gi]);
-                    d0 += fmaf(ea.x, c[gi][0], ea.y * qsum[gi][0]);
-                    d1 += fmaf(ea.x, c[gi][1], ea.y * qsum[gi][1]);
-                    d2 += fmaf(eb.x, c[gi][2], eb.y * qsum[gi][0]);
-                    d3 += fmaf(eb.x, c[gi][3], eb.y * qsum[gi][1]);
+                    const float ba = fmaf(-1024.f, ea.x, ea.y), bb = fmaf(-1024.f, eb.x, eb.y);
+                    d0 += fmaf(ea.x, c[gi][0], ba * qsum[gi][0]);
+                    d1 += fmaf(ea.x, c[gi][1], ba * qsum[gi][1]);
+                    d2 += fmaf(eb.x, c[gi][2], bb * qsum[gi][0]);
+                    d3 += fmaf(eb.x, c[gi][3], bb * qsum[gi][1]);
                 }
             }
             const float x0 = va ? d0 * sc : -INFINITY;  // token gb,   head tq
@@ -639,12 +677,15 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             const float2 fa = unpack_half2(pa), fb = unpack_half2(pb);
             l0 = l0 * al0 + (fa.x + fb.x);
             l1 = l1 * al1 + (fa.y + fb.y);
+            // (Q8: skipped when neither head's max moved, al = 1 exactly)
+            if (!Q8 || __any_sync(~0u, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
-            for (int i = 0; i < KT; ++i) {
-                o[i][0] *= al0;
-                o[i][1] *= al1;
-                o[i][2] *= al0;
-                o[i][3] *= al1;
+                for (int i = 0; i < KT; ++i) {
+                    o[i][0] *= al0;
+                    o[i][1] *= al1;
+                    o[i][2] *= al0;
+                    o[i][3] *= al1;
+                }
             }
             if constexpr (!Q8) {
                 // P^T as the B operand of O^T += V^T . P^T: register transpose
@@ -680,10 +721,13 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         ea = make_float2(0.f, 0.f);
                     if (!vb)
                         eb = make_float2(0.f, 0.f);
-                    bf[gi][0] = movmatrix_trans(pack_half2(p0 * ea.x, p1 * ea.x));
-                    bf[gi][1] = movmatrix_trans(pack_half2(p2 * eb.x, p3 * eb.x));
-                    beta[gi][0] = beta[gi][0] * al0 + (p0 * ea.y + p2 * eb.y);
-                    beta[gi][1] = beta[gi][1] * al1 + (p1 * ea.y + p3 * eb.y);
+                    const uint32_t ha = pack_half2(p0 * ea.x, p1 * ea.x);
+                    const uint32_t hb = pack_half2(p2 * eb.x, p3 * eb.x);
+                    bf[gi][0] = movmatrix_trans(ha);
+                    bf[gi][1] = movmatrix_trans(hb);
+                    const float2 fa = unpack_half2(ha), fb = unpack_half2(hb);
+                    beta[gi][0] = beta[gi][0] * al0 + (fmaf(-1024.f, fa.x + fb.x, p0 * ea.y) + p2 * eb.y);
+                    beta[gi][1] = beta[gi][1] * al1 + (fmaf(-1024.f, fa.y + fb.y, p1 * ea.y) + p3 * eb.y);
                 }
                 // V codes by ldmatrix.trans on 16-byte row pieces (16 d): lane
                 // gets bytes [v(tq, d), v(tq, d+1), v(tq+1, d), v(tq+1, d+1)] with
@@ -700,12 +744,14 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4_t(addr, r0, r1, r2, r3);
-                    mma_16816(o[i], codes_to_half2_strided(r0, false),
-                              codes_to_half2_strided(r0, true), codes_to_half2_strided(r1, false),
-                              codes_to_half2_strided(r1, true), bf[i / 4][0], bf[i / 4][1]);
-                    mma_16816(o[i + 1], codes_to_half2_strided(r2, false),
-                              codes_to_half2_strided(r2, true), codes_to_half2_strided(r3, false),
-                              codes_to_half2_strided(r3, true), bf[(i + 1) / 4][0],
+                    mma_16816(o[i], codes_to_half2_strided_offset(r0, false),
+                              codes_to_half2_strided_offset(r0, true),
+                              codes_to_half2_strided_offset(r1, false),
+                              codes_to_half2_strided_offset(r1, true), bf[i / 4][0], bf[i / 4][1]);
+                    mma_16816(o[i + 1], codes_to_half2_strided_offset(r2, false),
+                              codes_to_half2_strided_offset(r2, true),
+                              codes_to_half2_strided_offset(r3, false),
+                              codes_to_half2_strided_offset(r3, true), bf[(i + 1) / 4][0],
                               bf[(i + 1) / 4][1]);
                 }
             }
@@ -731,7 +777,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             lt1 += __shfl_xor_sync(~0u, lt1, off);
         }
         if constexpr (Q8) {
-            // the biases' part of O: the same for every d of a group
+            // the biases' part of O and the code offset's correction: the
+            // same for every d of a group
 #pragma unroll
             for (int gi = 0; gi < NGRP; ++gi) {
                 float b0 = beta[gi][0], b1 = beta[gi][1];

@@ -296,9 +296,11 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             const int t0 = (j0 + jj) * NT;
             const int c0 = t0 + half * HC;            // first token of this half
             // after a failed wait the loop keeps running without doing work,
-            // so the two warps of a pair meet at every named barrier
-            if (ok && !mbar_wait_bounded(smem_addr(&s_full[jj & 1]), (jj >> 1) & 1, &abort_flag,
-                                         p.wait_budget_ns)) {
+            // so the two warps of a pair meet at every named barrier; wait
+            // outcomes are made warp-uniform (the tensor-memory loads and
+            // stores after them are warp-collective)
+            if (ok && !__all_sync(~0u, mbar_wait_bounded(smem_addr(&s_full[jj & 1]), (jj >> 1) & 1,
+                                                         &abort_flag, p.wait_budget_ns))) {
                 ok = false;
                 give_up();
             }
@@ -385,8 +387,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             // the previous P V has finished: this half of O may be rescaled,
             // P overwritten
             if (jj > 0) {
-                if (!mbar_wait_bounded(smem_addr(&o_done), (jj - 1) & 1, &abort_flag,
-                                       p.wait_budget_ns)) {
+                if (!__all_sync(~0u, mbar_wait_bounded(smem_addr(&o_done), (jj - 1) & 1,
+                                                       &abort_flag, p.wait_budget_ns))) {
                     ok = false;
                     give_up();
                     continue;
@@ -445,8 +447,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         // ---- epilogue: the row's exp-sum from both halves, then each half
         // writes its columns
         if (ok)
-            ok = mbar_wait_bounded(smem_addr(&o_done), (ntiles - 1) & 1, &abort_flag,
-                                   p.wait_budget_ns);
+            ok = __all_sync(~0u, mbar_wait_bounded(smem_addr(&o_done), (ntiles - 1) & 1,
+                                                   &abort_flag, p.wait_budget_ns));
         pair_red[ntiles & 1][half][r] = l;
         named_barrier_sync(pair_bar, 64);
         const float lt = l + pair_red[ntiles & 1][half ^ 1][r];
