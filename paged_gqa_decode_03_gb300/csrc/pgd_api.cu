@@ -763,7 +763,8 @@ pgd_status encode_q_map(CUtensorMap *map, const void *q, int total_q, int Hq, in
 }
 
 struct VarlenPlan {
-    int G, TQ, QT, PK, NP, NT;
+    int G, TQ, QT, QP, PK, NP, NT;
+    bool pairs;  // two query tiles per CTA
     long long grid;
     size_t ws_bytes, off_l, off_o;
 };
@@ -804,9 +805,14 @@ pgd_status make_varlen_plan(int S, int total_q, int max_q, int Hq, int Hkv, int 
     vp->G = Hq / Hkv;
     vp->TQ = 128 / vp->G;
     vp->QT = (max_q + vp->TQ - 1) / vp->TQ;
+    // two query tiles per CTA where they fit in tensor memory and the
+    // sequences can have more than one tile of query rows
+    vp->pairs = (D == 64 ? varlen_pairs<64>() : D == 128 ? varlen_pairs<128>() : varlen_pairs<256>()) &&
+                vp->QT >= 2;
+    vp->QP = vp->pairs ? (vp->QT + 1) / 2 : vp->QT;  // query-tile units per (sequence, KV head)
     const long long maxlen = (long long)MB * BS;
     const long long whole = (maxlen + vp->NT - 1) / vp->NT * vp->NT;
-    const long long tiles = (long long)S * Hkv * vp->QT;
+    const long long tiles = (long long)S * Hkv * vp->QP;
     const size_t rows = (size_t)total_q * Hq;
     auto ws_for = [&](int NP) -> size_t {
         if (NP <= 1)
@@ -919,6 +925,7 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     p.G = vp.G;
     p.TQ = vp.TQ;
     p.QT = vp.QT;
+    p.QP = vp.QP;
     p.NP = vp.NP;
     p.PK = vp.PK;
     p.MB = MB;
@@ -929,7 +936,8 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     p.blk_head = (int)(kv_strides.head / blk_u);
     p.max_q = max_q;
     p.wait_budget_ns = kWaitBudgetNs;
-    e = launch_varlen(D, tq, *tk, *tv, p, (int)vp.grid, vp.NP > 1 ? total_q * Hq : 0, stream);
+    e = launch_varlen(D, vp.pairs, tq, *tk, *tv, p, (int)vp.grid, vp.NP > 1 ? total_q * Hq : 0,
+                      stream);
     if (own && ws) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess)

@@ -163,10 +163,16 @@ template <> struct VShape<128> {
 template <> struct VShape<256> {
     static constexpr int NT = 64, NSTG = 2;
 };
-template <int D> __host__ __device__ constexpr size_t varlen_smem_bytes()
+// head_dim 64 and 128 can run two query tiles per CTA
+// (paged_varlen_pair_kernel): two score buffers and two O accumulators fit in
+// tensor memory.  Calls whose sequences have at most one tile of query rows
+// use the one-tile kernel.
+template <int D> __host__ __device__ constexpr bool varlen_pairs() { return 2 * VShape<D>::NT + 2 * D <= 512; }
+template <int D> __host__ __device__ constexpr size_t varlen_smem_bytes(bool pairs)
 {
-    // Q tile + stages of K and V + alignment slack (P lives in tensor memory)
-    return size_t(128) * D * 2 + size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 + 1024;
+    // Q tile(s) + stages of K and V + alignment slack (P lives in tensor memory)
+    return size_t(pairs ? 2 : 1) * 128 * D * 2 +
+           size_t(VShape<D>::NSTG) * 2 * VShape<D>::NT * D * 2 + 1024;
 }
 constexpr int kVarlenThreads = 352;   // K producer, MMA, 8 softmax warps, V producer
 constexpr int kVWarp = 10;            // the V producer warp
@@ -181,11 +187,13 @@ struct VarlenParams {
     unsigned *err;
     float scale_log2;
     int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, log2BS, max_q;
+    int QP;                       // query-tile units per (sequence, KV head): QT, or
+                                  //   ceil(QT / 2) pairs (paged_varlen_pair_kernel)
     int blk_page, blk_head;       // (page, KV head) -> block coordinate of the K/V maps
     uint64_t wait_budget_ns;
 };
 
-cudaError_t launch_varlen(int head_dim, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_varlen(int head_dim, bool pairs, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,
                           cudaStream_t stream);
 

@@ -489,6 +489,459 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     }
 }
 
+// paged_varlen_pair_kernel<D> (head_dim 64 and 128) — one CTA per pair of
+// consecutive 128-row query tiles (A: query tokens i0 .. i0+TQ-1, B: the next
+// TQ) of one (sequence, KV head) over one KV partition.  Both tiles use every
+// K and V stage the producers bring in, which halves the copies per matrix
+// product against one tile per CTA.  Tensor memory holds a score buffer and
+// an O accumulator per tile (2 * NT + 2 * D <= 512 columns).
+//   * warp 0 / warp 10, producers: both Q tiles, then K (warp 0) and V
+//     (warp 10) rings exactly as in paged_varlen_kernel.
+//   * warp 1, MMA: per tile the chain S_j -> softmax -> P_j V_j -> S_{j+1}
+//     (S_{j+1} overwrites the columns P_j V_j reads; the tensor pipe runs one
+//     thread's MMAs in issue order).  The issue order alternates between the
+//     tiles, PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), so that one tile's matrix
+//     products run while the other tile's softmax works.
+//   * warps 2-5 softmax of tile A, warps 6-9 of tile B: thread = row of the
+//     tile, every column of the stage.  Per stage: the row's extreme from
+//     tensor memory (pass 1), then p = exp2(s * scale_log2 - m) written back
+//     as fp16 over the scores (pass 2), the same lazy reference max as
+//     paged_varlen_kernel; S_j completing implies P_{j-1} V_{j-1} completed,
+//     so O may be rescaled then without another wait.
+template <int D>
+__global__ void __launch_bounds__(kVarlenThreads, 1)
+    paged_varlen_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                             const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const VarlenParams p)
+{
+    constexpr int NT = VShape<D>::NT, NSTG = VShape<D>::NSTG;
+    constexpr int SLABS = D / 64;
+    constexpr int GROUP = SLABS * 1024;     // one 8-row group of K or V, all slabs
+    constexpr int KV_TILE = NT * D * 2;     // K (or V) of one stage
+    constexpr int Q_SLAB = 128 * 128;       // one 64-wide slab of a 128-row Q tile
+    constexpr int Q_TILE = 128 * D * 2;
+    // tensor-memory columns: scores (then P) of tile x at x * NT, O at O_COL + x * D
+    constexpr uint32_t O_COL = 2 * NT;
+    static_assert(O_COL + 2 * D <= kVarlenTmemCols, "tensor memory");
+    constexpr uint32_t IDESC_S = tc_idesc_f16(128, NT, 0, 0);
+    constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, 0, 1);
+
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t q_full, k_full[NSTG], v_full[NSTG], k_empty[NSTG],
+        v_empty[NSTG], s_full[2], p_full[2], o_done[2], mma_done;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag;
+
+    // ---- the unit: (sequence, KV head, query-tile pair, KV partition);
+    // pairs in decreasing order so the longest causal ranges start first
+    int u = blockIdx.x;
+    const int part = u % p.NP;
+    u /= p.NP;
+    const int qp = p.QP - 1 - u % p.QP;
+    u /= p.QP;
+    const int g = u % p.Hkv;
+    const int s = u / p.Hkv;
+    const int maxlen = p.MB * p.BS;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > maxlen ? maxlen : L);
+    const int row0 = __ldg(p.cu_q + s);
+    int n = __ldg(p.cu_q + s + 1) - row0;
+    if (n < 0 || n > L || n > p.max_q) {
+        if (qp == p.QP - 1 && g == 0 && part == 0 && threadIdx.x == 0)
+            atomicOr(p.err, kErrQueryLen);
+        n = 0;
+    }
+    const int kv_lo = part * p.PK;
+    int i0[2], ni[2], kv_hi[2], nt[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        i0[x] = (2 * qp + x) * p.TQ;
+        ni[x] = max(0, min(p.TQ, n - i0[x]));
+        kv_hi[x] = ni[x] > 0 ? min(kv_lo + p.PK, L - n + i0[x] + ni[x]) : kv_lo;
+        nt[x] = kv_hi[x] > kv_lo ? (kv_hi[x] + NT - 1) / NT - kv_lo / NT : 0;
+    }
+    // tile B's range contains tile A's whenever B has rows: B then takes
+    // part in every stage and is the last user of each K and V stage
+    const int ntiles = max(nt[0], nt[1]);
+    if (ntiles == 0)
+        return;
+    const int j0 = kv_lo / NT;
+    const int last = nt[1] > 0 ? 1 : 0;
+
+    const uint32_t dyn_base = smem_addr(dyn_smem);
+    const uint32_t base = (dyn_base + 1023u) & ~1023u;
+    uint8_t *const base_ptr = dyn_smem + (base - dyn_base);
+    const uint32_t q_s = base;                    // tile x at q_s + x * Q_TILE
+    const uint32_t kv_s = q_s + 2 * Q_TILE;       // stage st: K at +st*2*KV_TILE, V after
+    uint8_t *const kv_ptr = base_ptr + 2 * Q_TILE;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&q_full), 1);
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&v_full[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(smem_addr(&s_full[x]), 1);
+            mbar_init(smem_addr(&p_full[x]), 4);
+            mbar_init(smem_addr(&o_done[x]), 1);
+        }
+        mbar_init(smem_addr(&mma_done), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1)
+        tc_alloc(smem_addr(&tmem_base_s), kVarlenTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    griddep_launch_dependents();
+
+    auto give_up = [&]() {
+        if (!abort_flag)
+            atomicOr(p.err, kErrTimeout);
+        abort_flag = 1;
+    };
+
+    if (warp == 0 || warp == kVWarp) {
+        // ============================================================ producers
+        const bool is_v = warp == kVWarp;
+        const uint64_t pol = l2_evict_first_policy();
+        if (lane == 0) {
+            prefetch_tensormap(is_v ? &tmap_v : &tmap_k);
+            if (!is_v) {
+                prefetch_tensormap(&tmap_q);
+                const int ntq = ni[1] > 0 ? 2 : 1;  // tile B only when it has rows
+                mbar_arrive_expect_tx(smem_addr(&q_full), ntq * SLABS * p.TQ * p.G * 128);
+                for (int x = 0; x < ntq; ++x)
+                    for (int sl = 0; sl < SLABS; ++sl)
+                        tma_load_4d(q_s + x * Q_TILE + sl * Q_SLAB, &tmap_q, 0, g * p.G,
+                                    row0 + i0[x], sl, smem_addr(&q_full));
+            }
+        }
+        const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
+        uint64_t *full = is_v ? v_full : k_full;
+        uint64_t *empty = is_v ? v_empty : k_empty;
+        const int npages = (L + p.BS - 1) >> p.log2BS;
+        const int32_t *bt = p.block_tables + (size_t)s * p.MB;
+        // one copy per page of the stage (a piece of NT rows when pages are
+        // longer): lane c issues copy c, of the 8-row groups of that page
+        const int copies = p.BS <= NT ? NT >> p.log2BS : 1;
+        const int groups = (p.BS <= NT ? p.BS : NT) / 8;
+        auto block_of = [&](int jj) -> int {  // block coordinate of lane's page, -1: none
+            const int pg = (((j0 + jj) * NT) >> p.log2BS) + lane;
+            int b = -1;
+            if (lane < copies && pg < npages) {
+                const int id = __ldg(bt + pg);
+                if ((unsigned)id < (unsigned)p.NB)
+                    b = id * p.blk_page + g * p.blk_head;
+                else if (!is_v)
+                    atomicOr(p.err, kErrPageRange);  // wholly outside: the copy reads zeros
+            }
+            return b;
+        };
+        int issued = 0;
+        int blk_next = block_of(0);
+        for (int jj = 0; jj < ntiles; ++jj, ++issued) {
+            const int st = jj % NSTG;
+            const int blk = blk_next;
+            if (jj + 1 < ntiles)
+                blk_next = block_of(jj + 1);  // in flight while this stage waits
+            const int grp0 = p.BS <= NT ? 0 : (((j0 + jj) * NT) & (p.BS - 1)) >> 3;
+            const uint32_t dst =
+                kv_s + st * 2 * KV_TILE + (is_v ? KV_TILE : 0) + lane * groups * GROUP;
+            bool w = true;
+            if (lane == 0)
+                w = mbar_wait_bounded(smem_addr(&empty[st]), ((jj / NSTG) & 1) ^ 1, &abort_flag,
+                                      p.wait_budget_ns);
+            if (!__shfl_sync(~0u, w, 0)) {
+                if (lane == 0)
+                    give_up();
+                break;
+            }
+            const uint32_t fb = smem_addr(&full[st]);
+            if (lane == 0)
+                mbar_arrive_expect_tx(fb, KV_TILE);
+            __syncwarp();
+            if (lane < copies)
+                tma_load_5d(dst, map, 0, 0, 0, grp0, blk, fb, pol);
+        }
+        if (abort_flag && lane == 0) {
+            // let this warp's copies in flight land before the CTA exits
+            if (!is_v)
+                mbar_wait_bounded(smem_addr(&q_full), 0, nullptr, p.wait_budget_ns);
+            for (int i = issued > NSTG ? issued - NSTG : 0; i < issued; ++i)
+                mbar_wait_bounded(smem_addr(&full[i % NSTG]), (i / NSTG) & 1, nullptr,
+                                  p.wait_budget_ns);
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issue
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, &abort_flag, p.wait_budget_ns);
+            auto wait = [&](uint64_t *bar, int parity) {
+                if (ok && !mbar_wait_bounded(smem_addr(bar), parity, &abort_flag, p.wait_budget_ns))
+                    ok = false;
+                return ok;
+            };
+            // S_x(j) = Q_x K_j^T into tile x's score columns
+            auto issue_s = [&](int x, int j) {
+                const uint32_t ks = kv_s + (j % NSTG) * 2 * KV_TILE;
+                const uint32_t qx = q_s + x * Q_TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = tc_sdesc(qx + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
+                    const uint64_t b = tc_sdesc(ks + (kk / 4) * 1024 + (kk % 4) * 32, 16, GROUP);
+                    tc_mma(tmem + x * NT, a, b, IDESC_S, kk > 0);
+                }
+                tc_commit(smem_addr(&s_full[x]));
+            };
+            // O_x += P_x(j) V_j, P in the score columns (16 tokens = 8 columns
+            // per instruction)
+            auto issue_pv = [&](int x, int j) {
+                const uint32_t vs = kv_s + (j % NSTG) * 2 * KV_TILE + KV_TILE;
+#pragma unroll
+                for (int kk = 0; kk < NT / 16; ++kk) {
+                    const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
+                    tc_mma_ta(tmem + O_COL + x * D, tmem + x * NT + kk * 8, b, IDESC_O,
+                              j > 0 || kk > 0);
+                }
+            };
+            if (wait(&k_full[0], 0)) {
+                tc_fence_after();
+                for (int x = 0; x < 2; ++x)
+                    if (nt[x] > 0)
+                        issue_s(x, 0);
+                tc_commit(smem_addr(&k_empty[0]));
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int st = j % NSTG;
+                bool v_ready = false, k_ready = false;
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (j >= nt[x])
+                        continue;
+                    if (!wait(&p_full[x], j & 1))
+                        break;
+                    if (!v_ready && !wait(&v_full[st], (j / NSTG) & 1))
+                        break;
+                    v_ready = true;
+                    tc_fence_after();
+                    issue_pv(x, j);
+                    if (x == last)
+                        tc_commit(smem_addr(&v_empty[st]));
+                    if (j + 1 < nt[x]) {
+                        const int sn = (j + 1) % NSTG;
+                        if (!k_ready && !wait(&k_full[sn], ((j + 1) / NSTG) & 1))
+                            break;
+                        k_ready = true;
+                        tc_fence_after();
+                        issue_s(x, j + 1);
+                        if (x == last)
+                            tc_commit(smem_addr(&k_empty[sn]));
+                    } else {
+                        tc_commit(smem_addr(&o_done[x]));
+                    }
+                }
+            }
+            if (!ok)
+                give_up();
+            // every MMA issued here has completed before the memory is freed
+            tc_commit(smem_addr(&mma_done));
+            mbar_wait_bounded(smem_addr(&mma_done), 0, nullptr, p.wait_budget_ns);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ softmax
+        // warps 2-5: tile A, warps 6-9: tile B; warp w reads tensor-memory
+        // lane quarter w & 3, thread = row r of its tile
+        const int x = (warp - 2) >> 2;
+        // this tile's bounds as scalars (no per-thread indexing of the arrays)
+        const int i0x = x ? i0[1] : i0[0], nix = x ? ni[1] : ni[0];
+        const int kv_hix = x ? kv_hi[1] : kv_hi[0], ntx = x ? nt[1] : nt[0];
+        const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * quarter) << 16);
+        const uint32_t s_col = x * NT, o_col = O_COL + x * D;
+        const int ti = r / p.G, hj = r - ti * p.G;
+        const bool row_ok = r < p.TQ * p.G && ti < nix;
+        const int pos = row_ok ? L - n + i0x + ti : -1;
+        const int lim = min(pos, kv_hix - 1);  // last token this row sees here
+        // a scale of 0 runs as 1e-30: every score then gives exp2 of a value
+        // below 2^-25, which is 1 in fp32 (the mean over the range, as for 0),
+        // while the masked scores (infinite) still give exp2(-inf) = 0
+        const float sc = p.scale_log2 == 0.f ? 1e-30f : p.scale_log2;
+        const bool neg = sc < 0.f;
+        const float masked = neg ? INFINITY : -INFINITY;
+        const float2 sc2 = make_float2(sc, sc);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        const int last_page_end = ((L + p.BS - 1) / p.BS) * p.BS;
+        for (int jj = 0; jj < ntx; ++jj) {
+            const int t0 = (j0 + jj) * NT;
+            // wait outcomes are warp-uniform: tensor-memory loads and stores
+            // are warp-collective
+            if (!__all_sync(~0u, mbar_wait_bounded(smem_addr(&s_full[x]), jj & 1, &abort_flag,
+                                                   p.wait_budget_ns))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // pass 1: the row's extreme over the scores it sees (the max for
+            // a scale >= 0, the min for a negative one; masked scores count as
+            // the value that scales to -inf), 64 scores per tensor-memory wait;
+            // the second half stays in registers for pass 2
+            static_assert(NT == 128, "two 64-token halves per stage");
+            const bool masked_tile = t0 + NT - 1 > lim;
+            float e = masked;
+            float v[2][32];
+            auto load_half = [&](int h) {
+                tc_ld32(t_lane + s_col + 64 * h, v[0]);
+                tc_ld32(t_lane + s_col + 64 * h + 32, v[1]);
+                tc_wait_ld();
+                tc_ld_ready(v[0]);
+                tc_ld_ready(v[1]);
+                if (masked_tile) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[c][i] = t0 + 64 * h + 32 * c + i > lim ? masked : v[c][i];
+                }
+            };
+            auto extreme = [&]() {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        e = neg ? fmin3(e, v[c][i], v[c][i + 1]) : fmax3(e, v[c][i], v[c][i + 1]);
+            };
+            load_half(0);
+            extreme();
+            load_half(1);
+            extreme();
+            const float mt = e == masked ? -INFINITY : e * sc;
+            // lazy reference max: moves only by more than 8 (log2 units), so
+            // every p <= 256 stays exact enough in fp16
+            bool rescale = false;
+            float alpha = 1.f;
+            if (mt > m_ref + 8.f) {
+                rescale = m_ref != -INFINITY;
+                alpha = rescale ? ex2(m_ref - mt) : 1.f;
+                m_ref = mt;
+            }
+            // pass 2: p = exp2(s * scale_log2 - m_ref) (offset 0 while the row
+            // has seen nothing: its scores are all masked, every p is 0; masked
+            // scores are infinite with the sign that scales to -inf), as fp16 pairs;
+            // half h goes to columns 32h .. 32h+31, the A operand of P V.  The
+            // second half is still in registers; the first is read again
+            // before P of the second overwrites its last 32 scores.
+            const float off = m_ref == -INFINITY ? 0.f : -m_ref;
+            const float2 off2 = make_float2(off, off);
+            float2 sum2 = make_float2(0.f, 0.f);
+            uint32_t pk[32];
+            auto exp_half = [&](int h) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float2 a = ffma2(make_float2(v[c][i], v[c][i + 1]), sc2, off2);
+                        a.x = ex2(a.x);
+                        a.y = ex2(a.y);
+                        pk[16 * c + i / 2] = pack_half2(a.x, a.y);
+                        sum2 = fadd2(sum2, a);
+                    }
+            };
+            exp_half(1);
+            tc_ld_ready(pk);  // half 1 done before half 0's scores come back
+            load_half(0);
+            tc_st32u(t_lane + s_col + 32, pk);
+            exp_half(0);
+            tc_st32u(t_lane + s_col, pk);
+            l = l * alpha + (sum2.x + sum2.y);
+            // this tile's previous P V has completed (S_jj was issued after
+            // it): its O may be rescaled
+            if (jj > 0 && __any_sync(~0u, rescale)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+                    tc_ld32(t_lane + o_col + 32 * c, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] *= alpha;
+                    tc_st32(t_lane + o_col + 32 * c, v);
+                }
+            }
+            // rows of the stage past the sequence end inside its last page may
+            // hold anything: the first tile to use the stage zeroes them in V
+            // (pages past it were copied as zeros)
+            const bool zero_v = (x == 0 || jj >= nt[0]) && L < t0 + NT && t0 < last_page_end &&
+                                last_page_end > L;
+            if (zero_v) {
+                const int st = jj % NSTG;
+                mbar_wait_bounded(smem_addr(&v_full[st]), (jj / NSTG) & 1, nullptr,
+                                  p.wait_budget_ns);
+                uint8_t *vs = kv_ptr + st * 2 * KV_TILE + KV_TILE;
+                const int za = max(L, t0) - t0, zb = min(last_page_end, t0 + NT) - t0;
+                for (int idx = r; idx < (zb - za) * SLABS * 8; idx += 128) {
+                    const int row = za + idx / (SLABS * 8), c = idx % (SLABS * 8);
+                    *reinterpret_cast<uint4 *>(vs + (row / 8) * GROUP + (c >> 3) * 1024 +
+                                               (row % 8) * 128 + (c & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            tc_wait_st();
+            if (zero_v)
+                fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&p_full[x]));
+        }
+        // ---- epilogue: out = O / l, or the partition's partial
+        if (ok && ntx > 0)
+            ok = __all_sync(~0u, mbar_wait_bounded(smem_addr(&o_done[x]), 0, &abort_flag,
+                                                   p.wait_budget_ns));
+        if (!ok) {
+            give_up();
+        } else if (ntx > 0) {
+            tc_fence_after();
+            // rows that see no token of this partition write nothing: a row
+            // within the first partition is written (directly) by that unit
+            const bool has = row_ok && lim >= kv_lo;
+            const bool direct = p.NP == 1 || pos < p.PK;
+            const size_t rowh = ((size_t)(row0 + i0x + ti) * p.Hq + (size_t)g * p.G + hj);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *dst = direct ? p.out + rowh * D : p.ws_o + (rowh * p.NP + part) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tc_ld32(t_lane + o_col + 32 * c, v);
+                tc_wait_ld();
+                if (has) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + 32 * c + i) =
+                            make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+                }
+            }
+            if (has && !direct) {
+                p.ws_m[rowh * p.NP + part] = m_ref;
+                p.ws_l[rowh * p.NP + part] = l;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tc_dealloc(tmem, kVarlenTmemCols);
+    }
+}
+
 // One CTA per (query row, head) whose causal range spans more than one KV
 // partition: out = sum_i w_i o_i / sum_i w_i with w_i = l_i * exp2(m_i - max m).
 template <int D>
@@ -547,28 +1000,34 @@ __global__ void __launch_bounds__(128) paged_varlen_reduce_kernel(const VarlenPa
 }
 
 template <int D>
-cudaError_t launch_varlen_impl(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const VarlenParams &p, int grid, int reduce_rows,
-                               cudaStream_t stream)
+cudaError_t launch_varlen_impl(bool pairs, const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const VarlenParams &p, int grid,
+                               int reduce_rows, cudaStream_t stream)
 {
-    static bool attr_done[64] = {};
+    // head_dim 256 has one kernel (two tiles' scores and outputs would not
+    // fit in tensor memory)
+    auto kernel = paged_varlen_kernel<D>;
+    if constexpr (varlen_pairs<D>())
+        if (pairs)
+            kernel = paged_varlen_pair_kernel<D>;
+    const size_t smem = varlen_smem_bytes<D>(pairs && varlen_pairs<D>());
+    static bool attr_done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (!attr_done[dev & 63]) {
-        e = cudaFuncSetAttribute(paged_varlen_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)varlen_smem_bytes<D>());
+    if (!attr_done[pairs][dev & 63]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        attr_done[dev & 63] = true;
+        attr_done[pairs][dev & 63] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kVarlenThreads);
-    cfg.dynamicSmemBytes = varlen_smem_bytes<D>();
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    if ((e = cudaLaunchKernelEx(&cfg, paged_varlen_kernel<D>, tq, tk, tv, p)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p)) != cudaSuccess)
         return e;
     if (reduce_rows <= 0)
         return cudaSuccess;
@@ -584,17 +1043,17 @@ cudaError_t launch_varlen_impl(const CUtensorMap &tq, const CUtensorMap &tk, con
     return cudaLaunchKernelEx(&rcfg, paged_varlen_reduce_kernel<D>, p);
 }
 
-cudaError_t launch_varlen(int head_dim, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_varlen(int head_dim, bool pairs, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,
                           cudaStream_t stream)
 {
     switch (head_dim) {
     case 64:
-        return launch_varlen_impl<64>(tq, tk, tv, p, grid, reduce_rows, stream);
+        return launch_varlen_impl<64>(pairs, tq, tk, tv, p, grid, reduce_rows, stream);
     case 128:
-        return launch_varlen_impl<128>(tq, tk, tv, p, grid, reduce_rows, stream);
+        return launch_varlen_impl<128>(pairs, tq, tk, tv, p, grid, reduce_rows, stream);
     case 256:
-        return launch_varlen_impl<256>(tq, tk, tv, p, grid, reduce_rows, stream);
+        return launch_varlen_impl<256>(pairs, tq, tk, tv, p, grid, reduce_rows, stream);
     default:
         return cudaErrorInvalidValue;
     }
