@@ -323,7 +323,10 @@ pgd_status paged_gqa_varlen(float *out, const uint16_t *q, const int32_t *cu_seq
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /* The KV partition a paged_gqa_varlen call with these sizes would use and the
- * scratch bytes it needs (0: no partials).  Does not launch. */
+ * scratch bytes it needs: the split-KV partials, and when the work units are
+ * pairs of query tiles (head_dim 64/128, max_q_len above one tile of
+ * 128/G tokens) and outnumber the SMs, a 4-byte entry per unit for their
+ * longest-first order (0: no scratch).  Does not launch. */
 pgd_status pgd_varlen_plan(int num_seqs, int total_q, int max_q_len, int num_q_heads,
                            int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                            int kv_partition, int *chosen_kv_partition, size_t *workspace_bytes);

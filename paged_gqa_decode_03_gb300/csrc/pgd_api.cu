@@ -764,9 +764,10 @@ pgd_status encode_q_map(CUtensorMap *map, const void *q, int total_q, int Hq, in
 
 struct VarlenPlan {
     int G, TQ, QT, QP, PK, NP, NT;
-    bool pairs;  // two query tiles per CTA
+    bool pairs;    // two query tiles per CTA
+    bool ordered;  // units sorted longest first on the device (more than one wave)
     long long grid;
-    size_t ws_bytes, off_l, off_o;
+    size_t ws_bytes, off_l, off_o, off_order;
 };
 
 int varlen_tokens_per_stage(int D) { return D == 64 ? VShape<64>::NT : D == 128 ? VShape<128>::NT : VShape<256>::NT; }
@@ -839,15 +840,21 @@ pgd_status make_varlen_plan(int S, int total_q, int max_q, int Hq, int Hkv, int 
     vp->NP = (int)((maxlen + PK - 1) / PK);
     if (vp->NP < 1)
         vp->NP = 1;
-    vp->ws_bytes = ws_for(vp->NP);
     vp->off_l = align256(rows * vp->NP * 4);
     vp->off_o = 2 * vp->off_l;
-    if (vp->ws_bytes > kMaxWorkspaceBytes)
-        return fail(PGD_ERR_WORKSPACE, "partials need %zu bytes, above the %zu-byte cap",
-                    vp->ws_bytes, kMaxWorkspaceBytes);
     vp->grid = tiles * vp->NP;
     if (vp->grid >= (1ll << 31))
         return fail(PGD_ERR_UNSUPPORTED, "%lld work units", vp->grid);
+    // pairs of query tiles (compute-bound) and more units than SMs: a unit
+    // order (longest first) after the partials.  One-tile calls (decode and
+    // speculative verification: HBM-bound, units of similar cost per byte)
+    // measured slower with the extra sorting launch.
+    vp->ordered = vp->pairs && vp->grid > ds->num_sms;
+    vp->off_order = ws_for(vp->NP);
+    vp->ws_bytes = vp->off_order + (vp->ordered ? align256((size_t)vp->grid * 4) : 0);
+    if (vp->ws_bytes > kMaxWorkspaceBytes)
+        return fail(PGD_ERR_WORKSPACE, "scratch of %zu bytes needed, above the %zu-byte cap",
+                    vp->ws_bytes, kMaxWorkspaceBytes);
     return PGD_OK;
 }
 
@@ -914,9 +921,10 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     p.cu_q = cu_q;
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
-    p.ws_m = vp.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr;
-    p.ws_l = vp.ws_bytes ? reinterpret_cast<float *>(ws + vp.off_l) : nullptr;
-    p.ws_o = vp.ws_bytes ? reinterpret_cast<float *>(ws + vp.off_o) : nullptr;
+    p.ws_m = vp.NP > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+    p.ws_l = vp.NP > 1 ? reinterpret_cast<float *>(ws + vp.off_l) : nullptr;
+    p.ws_o = vp.NP > 1 ? reinterpret_cast<float *>(ws + vp.off_o) : nullptr;
+    p.order = vp.ordered ? reinterpret_cast<const int *>(ws + vp.off_order) : nullptr;
     p.err = ds->err_word;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.S = S;

@@ -189,6 +189,8 @@ struct VarlenParams {
     int S, Hq, Hkv, G, TQ, QT, NP, PK, MB, NB, BS, log2BS, max_q;
     int QP;                       // query-tile units per (sequence, KV head): QT, or
                                   //   ceil(QT / 2) pairs (paged_varlen_pair_kernel)
+    const int *order;             // [grid] unit of each block, longest first; null:
+                                  //   block index order
     int blk_page, blk_head;       // (page, KV head) -> block coordinate of the K/V maps
     uint64_t wait_budget_ns;
 };
@@ -196,5 +198,6 @@ struct VarlenParams {
 cudaError_t launch_varlen(int head_dim, bool pairs, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,
                           cudaStream_t stream);
+constexpr int kVarlenOrderKeys = 1024;  // stage counts the unit sort tells apart
 
 }  // namespace pgd

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
     // ---- the unit: (sequence, KV head, query tile, KV partition); query
     // tiles in decreasing order so the longest causal ranges start first
-    int u = blockIdx.x;
+    int u = p.order ? __ldg(p.order + blockIdx.x) : (int)blockIdx.x;
     const int part = u % p.NP;
     u /= p.NP;
     const int qt = p.QT - 1 - u % p.QT;
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
     // ---- the unit: (sequence, KV head, query-tile pair, KV partition);
     // pairs in decreasing order so the longest causal ranges start first
-    int u = blockIdx.x;
+    int u = p.order ? __ldg(p.order + blockIdx.x) : (int)blockIdx.x;
     const int part = u % p.NP;
     u /= p.NP;
     const int qp = p.QP - 1 - u % p.QP;
@@ -942,6 +942,77 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     }
 }
 
+// The units of a varlen call in decreasing order of their KV stages (a
+// counting sort, stage counts capped at kVarlenOrderKeys - 1; ties in any
+// order): the block scheduler starts blocks in index order as SMs free up, so
+// the longest units start first and the short ones fill in at the end.  One
+// CTA of kVarlenOrderKeys threads; the keys are those of the unit decoding
+// in the two kernels (rows = query tokens per unit: TQ, or 2 TQ for pairs).
+template <int NT>
+__global__ void __launch_bounds__(kVarlenOrderKeys)
+    paged_varlen_order_kernel(const VarlenParams p, int units, int rows, int *order)
+{
+    __shared__ int cnt[kVarlenOrderKeys];
+    __shared__ int warp_tot[kVarlenOrderKeys / 32];
+    const int t = threadIdx.x;
+    cnt[t] = 0;
+    __syncthreads();
+    const int maxlen = p.MB * p.BS;
+    auto key = [&](int u) -> int {
+        const int part = u % p.NP;
+        u /= p.NP;
+        const int qi = p.QP - 1 - u % p.QP;
+        u /= p.QP;
+        const int s = u / p.Hkv;
+        int L = __ldg(p.seq_lens + s);
+        L = L < 0 ? 0 : (L > maxlen ? maxlen : L);
+        const int row0 = __ldg(p.cu_q + s);
+        int n = __ldg(p.cu_q + s + 1) - row0;
+        if (n < 0 || n > L || n > p.max_q)
+            n = 0;
+        const int i0 = qi * rows;
+        if (i0 >= n)
+            return 0;
+        const int kv_lo = part * p.PK;
+        const int kv_hi = min(kv_lo + p.PK, L - n + min(n, i0 + rows));
+        if (kv_hi <= kv_lo)
+            return 0;
+        return min((kv_hi + NT - 1) / NT - kv_lo / NT, kVarlenOrderKeys - 1);
+    };
+    for (int u = t; u < units; u += kVarlenOrderKeys)
+        atomicAdd(&cnt[key(u)], 1);
+    __syncthreads();
+    // exclusive prefix sum over the keys from the largest down: thread t owns
+    // key kVarlenOrderKeys - 1 - t
+    const int k = kVarlenOrderKeys - 1 - t, lane = t & 31, w = t >> 5;
+    const int c = cnt[k];
+    int inc = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(~0u, inc, off);
+        if (lane >= off)
+            inc += y;
+    }
+    if (lane == 31)
+        warp_tot[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        int x = warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(~0u, x, off);
+            if (lane >= off)
+                x += y;
+        }
+        warp_tot[lane] = x - warp_tot[lane];  // exclusive
+    }
+    __syncthreads();
+    cnt[k] = warp_tot[w] + inc - c;
+    __syncthreads();
+    for (int u = t; u < units; u += kVarlenOrderKeys)
+        order[atomicAdd(&cnt[key(u)], 1)] = u;
+}
+
 // One CTA per (query row, head) whose causal range spans more than one KV
 // partition: out = sum_i w_i o_i / sum_i w_i with w_i = l_i * exp2(m_i - max m).
 template <int D>
@@ -1021,6 +1092,12 @@ cudaError_t launch_varlen_impl(bool pairs, const CUtensorMap &tq, const CUtensor
         if (e != cudaSuccess)
             return e;
         attr_done[pairs][dev & 63] = true;
+    }
+    if (p.order) {
+        paged_varlen_order_kernel<VShape<D>::NT><<<1, kVarlenOrderKeys, 0, stream>>>(
+            p, grid, pairs && varlen_pairs<D>() ? 2 * p.TQ : p.TQ, const_cast<int *>(p.order));
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
