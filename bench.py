@@ -46,10 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "b0bc01d644b2e91f": {("batch_decode", 512): 633_327_872 + 5_126_400,
-                         ("batch_decode_q8", 512): 336_795_904 + 5_142_784},
-    # the several-query-token kernel (hash of all sources)
-    "eae0f9a91e51ed3d": {("chunked_prefill", 8320): 231_608_576 + 13_471_744},
+    "efd15f02f6df6b52": {("batch_decode_q8", 512): 336_721_920 + 4_054_016},
+    # the several-query-token kernels (hash of all sources)
+    "b3aa7256cb0eaa62": {("chunked_prefill", 8320): 280_806_144 + 13_987_840},
 }
 
 
