@@ -235,6 +235,32 @@ pgd_status encode_code_map(CUtensorMap *map, const void *base, const CacheGeom &
     return PGD_OK;
 }
 
+// Both quantised code arrays in one map (head-major caches): 128 bytes x rows
+// x D/128 slabs x (page, head) blocks (page * Hkv + head) x 2 arrays, the
+// array stride being the distance between them (`lo` the lower one); a box
+// of 128 x rows x slabs x 1 x 2 lands a page's codes of both arrays as
+// [array][slab][row][128 B] (128-byte swizzle).
+pgd_status encode_code_pair_map(CUtensorMap *map, const void *lo, long long pair_stride,
+                                const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    cuuint64_t dims[5] = {128, (cuuint64_t)g.BS, (cuuint64_t)(g.D / 128),
+                          (cuuint64_t)g.NB * g.Hkv, 2};
+    cuuint64_t strides[4] = {(cuuint64_t)g.D, 128, (cuuint64_t)g.BS * g.D,
+                             (cuuint64_t)pair_stride};
+    cuuint32_t box[5] = {128, (cuuint32_t)box_rows, (cuuint32_t)(g.D / 128), 1, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(lo), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (code pair) failed (CUresult %d)", (int)r);
+    return PGD_OK;
+}
+
 pgd_status encode_meta_map(CUtensorMap *map, const void *base, const CacheGeom &g, int box_rows)
 {
     EncodeTiledFn fn;
@@ -399,7 +425,8 @@ thread_local int t_maps_used = 0, t_maps_next = 0;
 
 // kind 0: the decode view (box = rows per copy); kind 1: the page-group view
 // (box = 8-row groups per copy); kind 2: quantised codes, kind 3: their
-// (scale, bias) pairs (box = rows per copy).
+// (scale, bias) pairs (box = rows per copy); kind 4: both code arrays in one
+// map (*tk = *tv, based at the lower array).
 pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box, int kind,
                       const CUtensorMap **tk, const CUtensorMap **tv)
 {
@@ -418,6 +445,15 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
+    if (kind == 4) {
+        const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
+        const long long stride = (long long)(ka < va ? va - ka : ka - va);
+        if ((st = encode_code_pair_map(&c.tk, ka < va ? k : v, stride, geom, box))) {
+            c.k = c.v = nullptr;
+            return st;
+        }
+        c.tv = c.tk;
+    }
     auto enc = [&](CUtensorMap *m, const void *base) -> pgd_status {
         switch (kind) {
         case 0:
@@ -430,7 +466,7 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
             return encode_meta_map(m, base, geom, box);
         }
     };
-    if ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v))) {
+    if (kind != 4 && ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v)))) {
         c.k = c.v = nullptr;
         return st;
     }
@@ -645,7 +681,19 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     const int box = BS < stage_t ? BS : stage_t;
     const CacheGeom geom = {NB, Hkv, BS, D, kv_strides.page, kv_strides.head, kv_strides.token};
     const CUtensorMap *tk = nullptr, *tv = nullptr, *tkm = nullptr, *tvm = nullptr;
-    if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? 2 : 0, &tk, &tv)) ||
+    // quantised pages with page pieces of up to 4 KB (the kernel then keeps a
+    // piece's K and V codes side by side): one copy per page for both code
+    // arrays when their distance fits a tensor-map stride (a multiple of 16
+    // bytes below 2^40) and the (page, head) blocks fit a coordinate
+    const uintptr_t k_at = reinterpret_cast<uintptr_t>(k_cache),
+                    v_at = reinterpret_cast<uintptr_t>(v_cache);
+    const long long code_gap = !q8 ? 0
+                               : v_at >= k_at ? (long long)(v_at - k_at)
+                                              : -(long long)(k_at - v_at);
+    const long long gap_abs = code_gap < 0 ? -code_gap : code_gap;
+    const bool q8_pair = q8 && box * D <= 4096 && gap_abs > 0 && gap_abs % 16 == 0 &&
+                         gap_abs < (1ll << 40) && (long long)NB * Hkv < (1ll << 31);
+    if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? (q8_pair ? 4 : 2) : 0, &tk, &tv)) ||
         (q8 && (st = cache_maps(k_meta, v_meta, geom, box, 3, &tkm, &tvm)))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
@@ -694,6 +742,9 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.v_cache = reinterpret_cast<__half *>(const_cast<void *>(v_cache));
     p.k_meta = q8 ? static_cast<const uint16_t *>(k_meta) : nullptr;
     p.v_meta = q8 ? static_cast<const uint16_t *>(v_meta) : nullptr;
+    p.q8_pair = q8_pair ? 1 : 0;
+    p.q8_koff = q8_pair && code_gap < 0 ? box * D : 0;  // the lower array lands first
+    p.q8_voff = q8_pair && code_gap < 0 ? 0 : box * D;   // (used for pieces of <= 4 KB)
     p.kv_page_stride = kv_strides.page;
     p.kv_head_stride = kv_strides.head;
     p.kv_token_stride = kv_strides.token;

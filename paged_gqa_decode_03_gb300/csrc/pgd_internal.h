@@ -105,6 +105,9 @@ struct DecodeParams {
     __half *v_cache;
     const uint16_t *k_meta;       // quantised pages: [NB][Hkv][BS][D/64][2] bf16
     const uint16_t *v_meta;       //   (scale, bias) pairs, or null
+    int q8_pair;                  // quantised pages: 1 = one tensor copy brings a page's
+                                  //   K and V codes (tmap_k spans both arrays)
+    int q8_koff, q8_voff;         //   bytes of K / V codes within a page's pair of slots
     long long kv_page_stride;     // cache strides in halves (the copies use the
     long long kv_head_stride;     //   same ones through the tensor maps)
     long long kv_token_stride;

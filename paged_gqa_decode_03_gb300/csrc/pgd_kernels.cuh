@@ -65,6 +65,12 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
     constexpr int PAGE_BYTES = BOX * ROWB; // one copy: BOX rows of one page, all slabs
+    // Q8 with page pieces of up to 4 KB: a piece's K and V codes sit side by
+    // side (K at q8_koff, V at q8_voff within 2 PAGE_BYTES), so that one
+    // tensor copy can bring both; otherwise K pieces from the stage start, V
+    // pieces KV_BYTES after (larger pieces measured faster that way)
+    constexpr bool PAIRED = Q8 && PAGE_BYTES <= 4096;
+    constexpr int PSTR = PAIRED ? 2 * PAGE_BYTES : PAGE_BYTES;  // page piece to page piece
     constexpr int NGRP = D / kQuantGroup;  // quantisation groups of a row
     constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
     constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
@@ -305,10 +311,20 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
 
                         // one copy per page for K and one for V: BOX rows
                         // from row0 of (page, KV head g), all D halves,
-                        // landing as [slab][row][128 B] (swizzled)
-                        const uint32_t dk = sb + jj * PAGE_BYTES;
-                        tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
-                        tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
+                        // landing as [slab][row][128 B] (swizzled); Q8
+                        // with both code arrays in one map: one copy of
+                        // [array][slab][row][128 B] for the pair of slots
+                        const uint32_t dk = sb + jj * PSTR;
+                        if (PAIRED && p.q8_pair) {
+                            tma_load_5d(dk, &tmap_k, 0, row0, 0, c_page < 0 ? -1 : c_page * Hkv + g,
+                                        0, fb, pol);
+                        } else if (PAIRED) {
+                            tma_load_5d(dk + p.q8_koff, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
+                            tma_load_5d(dk + p.q8_voff, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
+                        } else {
+                            tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
+                            tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
+                        }
                         if (Q8 && META_BY_TMA) {  // the rows' (scale, bias) pairs
                             const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT;
                             tma_load_3d(dm, &tmap_km, row0 * NGRP, g, c_page, fb, pol);
@@ -611,7 +627,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 // K codes: 16 bytes (one k-step) per ldmatrix row piece;
                 // matrices: rows 0-7 / 8-15 of the tile, k-steps kk / kk+1
                 const int tok = t0 + r8 + (mi & 1) * 8;
-                const uint32_t rowaddr = sb + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                const uint32_t rowaddr =
+                    sb + (PAIRED ? p.q8_koff : 0) + (tok / BOX) * PSTR + (tok % BOX) * 128;
                 const int sw = tok & 7;
 #pragma unroll
                 for (int kk = 0; kk < KT; kk += 2) {
@@ -735,7 +752,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 // tq, tq+1; matrices: tokens 0-7 / 8-15, pieces i / i+1
                 const int tok = t0 + r8 + (mi & 1) * 8;
                 const uint32_t rowaddr =
-                    sb + KV_BYTES + (tok / BOX) * PAGE_BYTES + (tok % BOX) * 128;
+                    sb + (PAIRED ? p.q8_voff : KV_BYTES) + (tok / BOX) * PSTR + (tok % BOX) * 128;
                 const int sw = tok & 7;
 #pragma unroll
                 for (int i = 0; i < KT; i += 2) {

@@ -1,5 +1,7 @@
 """GPU parity of the decode over quantised pages (8-bit codes, bf16 (scale,
 bias) per 64 values) against the oracle's dequantising decode."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -90,3 +92,26 @@ def test_repeated_calls_identical():
     a, _ = run_q8(w, c)
     for _ in range(3):
         assert torch.equal(run_q8(w, c)[0], a)
+
+
+def test_code_arrays_in_either_order_or_shared():
+    """One tensor copy brings a page's K and V codes when both arrays fit one
+    map: with V below K in memory the codes land in the other order; with K
+    and V the same array they cannot share a map and go by two copies."""
+    w = make_custom(S=len(LENS), Hq=32, Hkv=8, D=128, BS=16, lens=LENS, seed=77, device=DEV,
+                    MB=(1600 + 15) // 16)
+    c = make_q8(w)
+    ref = oracle_q8(w, c)
+    n = c.k_codes.numel()
+    buf = torch.empty(2 * n, dtype=torch.uint8, device=DEV)
+    buf[:n].copy_(c.v_codes.reshape(-1))
+    buf[n:].copy_(c.k_codes.reshape(-1))
+    c_swapped = dataclasses.replace(c, k_codes=buf[n:].view(c.k_codes.shape),
+                                    v_codes=buf[:n].view(c.v_codes.shape))
+    out, _ = run_q8(w, c_swapped)
+    assert_parity(out.cpu().numpy(), ref, "q8 V codes below K codes")
+    shared = dataclasses.replace(c, v_codes=c.k_codes, v_meta=c.k_meta)
+    ref_shared = oracle_q8(w, shared)
+    out, _ = run_q8(w, shared)
+    assert_parity(out.cpu().numpy(), ref_shared, "q8 K and V one array")
+    assert pgd.pgd_check_device_error() == 0
