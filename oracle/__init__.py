@@ -90,6 +90,12 @@ def _bind(lib):
     lib.oracle_dequant_affine.restype = I
     lib.oracle_paged_gqa_decode_q8.argtypes = [P] * 8 + [D] + [I] * 8
     lib.oracle_paged_gqa_decode_q8.restype = I
+    lib.oracle_quantise_affine.argtypes = [P, P, P, Lg, I]
+    lib.oracle_quantise_affine.restype = I
+    lib.oracle_quantise_rows.argtypes = [P] * 4 + [I] * 5
+    lib.oracle_quantise_rows.restype = I
+    lib.oracle_append_kv_q8.argtypes = [P] * 8 + [I] * 6
+    lib.oracle_append_kv_q8.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -377,6 +383,51 @@ def dequant_affine(codes, meta, group=64):
     w = np.empty(c.size, dtype=np.float64)
     _check(lib.oracle_dequant_affine(_ptr(w), _ptr(c), _ptr(m), int(c.size), int(group)))
     return w.reshape(np.shape(codes))
+
+
+def quantise_affine(x, group=64):
+    """Binary16 values x ([n], n a multiple of group) -> (codes uint8 [n],
+    pairs bf16 bits [n / group, 2] = (scale, bias)): bias = bf16(min),
+    scale = bf16((max - min) / 255), code = clamp(rint((x - bias) / scale))."""
+    lib = _load()
+    xb = _u16(x).ravel()
+    codes = np.empty(xb.size, dtype=np.uint8)
+    pairs = np.empty((xb.size // group, 2), dtype=np.uint16)
+    _check(lib.oracle_quantise_affine(_ptr(codes), _ptr(pairs), _ptr(xb), int(xb.size),
+                                      int(group)))
+    return codes, pairs
+
+
+def quantise_rows(codes, meta, src, slots):
+    """Copies of the quantised caches (codes uint8 [NB, Hkv, BS, D], meta bf16
+    bits [NB, Hkv, BS, D/64, 2]) with rows src [N, Hkv, D] (binary16) written
+    at cache rows slots[n] = page * BS + row (negative: skipped)."""
+    lib = _load()
+    c = np.array(codes, dtype=np.uint8, copy=True, order="C")
+    m = np.array(meta, dtype=np.uint16, copy=True, order="C")
+    x = _u16(src)
+    sl = _i32(slots)
+    NB, Hkv, BS, D = c.shape
+    _check(lib.oracle_quantise_rows(_ptr(c), _ptr(m), _ptr(x), _ptr(sl), int(sl.size), Hkv, D,
+                                    BS, NB))
+    return c, m
+
+
+def append_kv_q8(k_codes, k_meta, v_codes, v_meta, k_new, v_new, block_tables, seq_lens):
+    """Copies of the four quantised arrays with k_new / v_new [S, Hkv, D]
+    quantised into the row of token seq_lens[s] - 1 of each sequence."""
+    lib = _load()
+    kc = np.array(k_codes, dtype=np.uint8, copy=True, order="C")
+    km = np.array(k_meta, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_codes, dtype=np.uint8, copy=True, order="C")
+    vm = np.array(v_meta, dtype=np.uint16, copy=True, order="C")
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    NB, Hkv, BS, D = kc.shape
+    S, MB = bt.shape
+    _check(lib.oracle_append_kv_q8(_ptr(kc), _ptr(km), _ptr(vc), _ptr(vm), _ptr(kn), _ptr(vn),
+                                   _ptr(bt), _ptr(sl), S, Hkv, D, BS, MB, NB))
+    return kc, km, vc, vm
 
 
 def decode_q8(q, k_codes, k_meta, v_codes, v_meta, block_tables, seq_lens, scale, threads=None):

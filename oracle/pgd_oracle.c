@@ -676,6 +676,144 @@ int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_
     return fail ? ORC_NO_MEMORY : ORC_OK;
 }
 
+/* ---------------------------------------------------------------- quantiser
+ * Writing rows into quantised pages.  The pages give the affine format from
+ * the reading side only (Kapitsa part 02, the affine group-64 weight format:
+ * w ~ scale * q + bias, worked example scale 0.25, bias -1, q = [0, 3, 8, 15]
+ * -> [-1, -0.25, 1, 2.75]); how scale and bias are chosen is not stated.  The
+ * plainest reading for unsigned 8-bit codes: per group of 64 values the bias
+ * is the group's minimum and the scale spreads the range over 255 steps,
+ * both rounded to bf16 (nearest, ties to even) as they are stored, and each
+ * code is the nearest step from the stored bias:
+ *     mn = min x,  mx = max x                       (binary32)
+ *     S  = bf16((mx - mn) / 255),  B = bf16(mn)
+ *     q  = S > 0 ? clamp(rint((x - B) / S), 0, 255) : 0
+ * Every step is one correctly rounded binary32 operation (this file is built
+ * without contraction into fused multiply-adds), so any implementation that
+ * takes the same steps in binary32 decides the same codes.
+ */
+
+/* binary32 -> bf16, round to nearest, ties to even (the upper 16 bits after
+ * adding half an ulp of the result, plus one when the kept lsb is odd). */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a (quiet) NaN */
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* One group of n binary16 values -> n codes and the (scale, bias) pair. */
+static void quantise_group(uint8_t *codes, uint16_t *pair, const uint16_t *x, int n)
+{
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+        float v = (float)g_h2d[x[i]]; /* exact: binary16 values are binary32 values */
+        if (v < mn)
+            mn = v;
+        if (v > mx)
+            mx = v;
+    }
+    float range = mx - mn;
+    uint16_t sb = f32_to_bf16_rne(range / 255.0f), bb = f32_to_bf16_rne(mn);
+    float S = bf16_to_f32(sb), B = bf16_to_f32(bb);
+    for (int i = 0; i < n; ++i) {
+        int q = 0;
+        if (S > 0.0f) {
+            float diff = (float)g_h2d[x[i]] - B;
+            float t = rintf(diff / S);
+            q = t < 0.0f ? 0 : (t > 255.0f ? 255 : (int)t);
+        }
+        codes[i] = (uint8_t)q;
+    }
+    pair[0] = sb;
+    pair[1] = bb;
+}
+
+/* n binary16 values (n a multiple of `group`) -> codes [n] and pairs
+ * [n / group][2] (scale, bias). */
+int oracle_quantise_affine(uint8_t *codes, uint16_t *pairs, const uint16_t *x, long n, int group)
+{
+    if (n < 0 || group <= 0 || n % group != 0)
+        return ORC_BAD_SHAPE;
+    h2d_init();
+    for (long gi = 0; gi < n / group; ++gi)
+        quantise_group(codes + gi * group, pairs + 2 * gi, x + gi * group, group);
+    return ORC_OK;
+}
+
+/* Rows src[n][h][:] (binary16, [N][Hkv][D]) written into the quantised
+ * head-major cache at cache row slots[n] (page * BS + row; negative: row
+ * skipped): codes [NB][Hkv][BS][D], pairs [NB][Hkv][BS][D/64][2]. */
+int oracle_quantise_rows(uint8_t *codes, uint16_t *meta, const uint16_t *src,
+                         const int32_t *slots, int N, int Hkv, int D, int BS, int NB)
+{
+    if (N < 0 || Hkv <= 0 || D <= 0 || D % 64 != 0 || BS <= 0 || NB <= 0)
+        return ORC_BAD_SHAPE;
+    h2d_init();
+    for (int n = 0; n < N; ++n) {
+        if (slots[n] < 0)
+            continue;
+        long page = slots[n] / BS, row = slots[n] % BS;
+        if (page >= NB)
+            return ORC_BAD_PAGE;
+        for (int h = 0; h < Hkv; ++h) {
+            long r = (page * Hkv + h) * BS + row;
+            for (int g = 0; g < D / 64; ++g)
+                quantise_group(codes + r * D + g * 64, meta + (r * (D / 64) + g) * 2,
+                               src + ((long)n * Hkv + h) * D + g * 64, 64);
+        }
+    }
+    return ORC_OK;
+}
+
+/* The decode step's append into quantised pages: sequence s's newest token
+ * (position L_s - 1, L_s > 0) gets k_new[s] / v_new[s] ([S][Hkv][D]
+ * binary16) written, quantised, into its row of page
+ * block_tables[s][(L_s - 1) / BS]; the decode then reads them like every
+ * other row (oracle_paged_gqa_decode_q8). */
+int oracle_append_kv_q8(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta,
+                        const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_tables,
+                        const int32_t *seq_lens, int S, int Hkv, int D, int BS, int MB, int NB)
+{
+    if (S < 0 || MB <= 0)
+        return ORC_BAD_SHAPE;
+    int32_t *slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(S > 0 ? S : 1));
+    if (!slots)
+        return ORC_NO_MEMORY;
+    int rc = ORC_OK;
+    for (int s = 0; s < S && !rc; ++s) {
+        long L = seq_lens[s];
+        if (L < 0 || L > (long)MB * BS)
+            rc = ORC_BAD_LENGTH;
+        else if (L == 0)
+            slots[s] = -1;
+        else {
+            int32_t page = block_tables[(long)s * MB + (L - 1) / BS];
+            if (page < 0 || page >= NB)
+                rc = ORC_BAD_PAGE;
+            else
+                slots[s] = (int32_t)(page * (long)BS + (L - 1) % BS);
+        }
+    }
+    if (!rc)
+        rc = oracle_quantise_rows(k_codes, k_meta, k_new, slots, S, Hkv, D, BS, NB);
+    if (!rc)
+        rc = oracle_quantise_rows(v_codes, v_meta, v_new, slots, S, Hkv, D, BS, NB);
+    free(slots);
+    return rc;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -57,6 +57,20 @@ MUTANTS = [
     ("q8: V dequantised with the K metadata", "v_codes + r * D, v_meta + r", "v_codes + r * D, k_meta + r",
      False),
     ("q8: bf16 bits shifted by 15", "(uint32_t)h << 16", "(uint32_t)h << 15", False),
+    ("quantiser: codes truncated", "float t = rintf(diff / S);", "float t = truncf(diff / S);",
+     False),
+    ("quantiser: ties rounded up", "float t = rintf(diff / S);", "float t = floorf(diff / S + 0.5f);",
+     False),
+    ("quantiser: 256 steps", "range / 255.0f", "range / 256.0f", False),
+    ("quantiser: bias from the maximum", "bb = f32_to_bf16_rne(mn)", "bb = f32_to_bf16_rne(mx)",
+     False),
+    ("quantiser: bf16 truncated", "    u += 0x7FFFu + ((u >> 16) & 1u);\n", "", False),
+    ("quantiser: codes from the unrounded bias", "float diff = (float)g_h2d[x[i]] - B;",
+     "float diff = (float)g_h2d[x[i]] - mn;", False),
+    ("quantiser: row within the page off by one", "long r = (page * Hkv + h) * BS + row;",
+     "long r = (page * Hkv + h) * BS + (row + 1) % BS;", False),
+    ("append q8: newest row one late", "(int32_t)(page * (long)BS + (L - 1) % BS)",
+     "(int32_t)(page * (long)BS + L % BS)", False),
 ]
 
 
@@ -64,6 +78,7 @@ def _pins():
     import test_oracle as T
     import test_oracle_varlen as V
     import test_oracle_q8 as Q
+    import test_oracle_quantise as Z
     return [
         ("half decoding", T.test_half_decoding_matches_numpy),
         ("hand case 0", lambda: T.test_hand_cases(0)),
@@ -97,6 +112,15 @@ def _pins():
         ("q8 bf16", Q.test_bf16_decoding_matches_torch),
         ("q8 exact fp16", Q.test_equals_fp16_decode_on_exact_values),
         ("q8 sdpa", lambda: Q.test_dense_sdpa_on_dequantised_values(8, 2, 8)),
+        ("quantise example", Z.test_worked_example_inverted),
+        ("quantise grid", Z.test_exact_grid),
+        ("quantise ties", Z.test_ties_go_to_even),
+        ("quantise constant", Z.test_constant_group),
+        ("quantise bound", Z.test_round_trip_bound),
+        ("quantise pair", Z.test_pair_is_bf16_of_min_and_step),
+        ("quantise rows", Z.test_rows_land_at_their_slots),
+        ("quantise append", Z.test_append_is_the_newest_row),
+        ("quantise stored bias", Z.test_codes_count_from_the_stored_bias),
     ]
 
 
