@@ -267,8 +267,8 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
  * dequantised rows (the affine map is applied in fp32 around exact fp16
  * tensor-core products of the codes; nothing is rounded to fp16 that the
  * fp16 path does not round).  Other arguments as for paged_gqa_decode_ex
- * (workspace NULL: library scratch).  head_dim 128 or 256 only; no fused
- * append.
+ * (workspace NULL: library scratch).  head_dim 128 or 256 only; the fused
+ * append is paged_gqa_decode_q8_append.
  */
 pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_codes,
                                const uint16_t *k_meta, const uint8_t *v_codes,
@@ -278,6 +278,45 @@ pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_c
                                int partition_size, int max_blocks_per_seq, int num_blocks,
                                void *workspace, size_t workspace_bytes, int32_t *page_trace,
                                void *stream);
+
+/*
+ * paged_kv_quantize — writes fp16 rows into quantised pages (the format of
+ * paged_gqa_decode_q8).  The pages show the affine format only from the
+ * reading side (Kapitsa part 02: value = scale * q + bias); the quantiser
+ * here is the plainest reading for unsigned 8-bit codes, per group of 64
+ * values of a row, every step one correctly rounded binary32 operation:
+ *     bias  = bf16(min),  scale = bf16((max - min) / 255)   (nearest, ties even)
+ *     code  = scale > 0 ? clamp(rint((x - bias) / scale), 0, 255) : 0
+ * src    [num_rows][num_kv_heads][head_dim] fp16, 16-byte aligned (read)
+ * slots  [num_rows] int32: cache row page * block_size + row of each source
+ *        row (all KV heads); negative: the row is skipped
+ * codes  [num_blocks][num_kv_heads][block_size][head_dim] uint8 (written)
+ * meta   [num_blocks][num_kv_heads][block_size][head_dim / 64][2] bf16 (written)
+ * Asynchronous on `stream`.  A slot whose page is at or past num_blocks is
+ * skipped and sets PGD_DEVERR_PAGE_RANGE.  Call once for K, once for V.
+ */
+pgd_status paged_kv_quantize(uint8_t *codes, uint16_t *meta, const uint16_t *src,
+                             const int32_t *slots, int num_rows, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, void *stream);
+
+/*
+ * paged_gqa_decode_q8_append — paged_gqa_decode_q8 with the step's new K/V
+ * fused in: k_new / v_new [num_seqs][num_kv_heads][head_dim] fp16 (16-byte
+ * aligned) are the newest token of each sequence (position seq_lens[s] - 1,
+ * in page block_tables[s][(seq_lens[s] - 1) / block_size]).  The kernel
+ * quantises them (paged_kv_quantize's steps), uses them in this step's
+ * attention and writes their codes and (scale, bias) pairs into the caches
+ * for the next steps.  Other arguments as paged_gqa_decode_q8 (library
+ * scratch, no page trace).
+ */
+pgd_status paged_gqa_decode_q8_append(float *out, const uint16_t *q, const uint16_t *k_new,
+                                      const uint16_t *v_new, uint8_t *k_codes, uint16_t *k_meta,
+                                      uint8_t *v_codes, uint16_t *v_meta,
+                                      const int32_t *block_tables, const int32_t *seq_lens,
+                                      float scale, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int partition_size, int max_blocks_per_seq, int num_blocks,
+                                      void *stream);
 
 /*
  * paged_gqa_varlen — attention for several query tokens per sequence over the

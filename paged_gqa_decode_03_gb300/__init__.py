@@ -28,7 +28,8 @@ import torch
 
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
            "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
-           "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8", "pgd_plan", "pgd_last_partition_size",
+           "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8",
+           "paged_gqa_decode_q8_append", "paged_kv_quantize", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -53,6 +54,8 @@ SIGNATURES = {
     "paged_gqa_varlen": (_I, [_P] * 7 + [_F] + [_I] * 9 + [_L] * 3 + [_I, _P, _Z, _P]),
     "pgd_varlen_plan": (_I, [_I] * 9 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "paged_gqa_decode_q8": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
+    "paged_gqa_decode_q8_append": (_I, [_P] * 10 + [_F] + [_I] * 8 + [_P]),
+    "paged_kv_quantize": (_I, [_P] * 4 + [_I] * 5 + [_P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -352,6 +355,68 @@ def paged_gqa_decode_q8(out, q, k_codes, k_meta, v_codes, v_meta, block_tables, 
         _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq, Hkv, D, BS, int(partition_size),
         block_tables.shape[1], NB, _ptr(workspace), ws_bytes, _ptr(page_trace),
         _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def _check_q8(k_codes, k_meta, v_codes, v_meta):
+    for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _check(t, n, torch.uint8, 4)
+    for t, n in ((k_meta, "k_meta"), (v_meta, "v_meta")):
+        _check(t, n, torch.int16, 5)
+    NB, Hkv, BS, D = k_codes.shape
+    if (v_codes.shape != k_codes.shape or tuple(k_meta.shape) != (NB, Hkv, BS, D // 64, 2)
+            or v_meta.shape != k_meta.shape):
+        raise ValueError("inconsistent shapes of codes and meta")
+    return NB, Hkv, BS, D
+
+
+def paged_gqa_decode_q8_append(out, q, k_new, v_new, k_codes, k_meta, v_codes, v_meta,
+                               block_tables, seq_lens, scale, partition_size: int = 0,
+                               stream=None) -> None:
+    """Quantises each sequence's newest K/V row (k_new, v_new: fp16
+    [num_seqs, num_kv_heads, head_dim]) into the quantised caches at token
+    seq_lens[s] - 1 and decodes over all seq_lens[s] tokens, in one launch."""
+    lib = load_library()
+    _check(q, "q", torch.float16, 3)
+    _check(out, "out", torch.float32, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    NB, Hkv, BS, D = _check_q8(k_codes, k_meta, v_codes, v_meta)
+    S, Hq, D2 = q.shape
+    if D2 != D or out.shape != q.shape:
+        raise ValueError("inconsistent shapes of q, codes, out")
+    if block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables / seq_lens do not have num_seqs rows")
+    _check(k_new, "k_new", torch.float16, 3)
+    _check(v_new, "v_new", torch.float16, 3)
+    if tuple(k_new.shape) != (S, Hkv, D) or tuple(v_new.shape) != (S, Hkv, D):
+        raise ValueError(f"k_new / v_new must be [{S}, {Hkv}, {D}]")
+    st = lib.paged_gqa_decode_q8_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(k_meta),
+        _ptr(v_codes), _ptr(v_meta), _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq,
+        Hkv, D, BS, int(partition_size), block_tables.shape[1], NB,
+        _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def paged_kv_quantize(codes, meta, src, slots, stream=None) -> None:
+    """Writes fp16 rows src [N, num_kv_heads, head_dim] into the quantised
+    cache (codes uint8 [NB, Hkv, BS, D], meta int16 bf16 bits [NB, Hkv, BS,
+    D/64, 2]) at cache rows slots[n] = page * block_size + row (int32 [N];
+    negative: skipped)."""
+    lib = load_library()
+    _check(codes, "codes", torch.uint8, 4)
+    _check(meta, "meta", torch.int16, 5)
+    _check(src, "src", torch.float16, 3)
+    _check(slots, "slots", torch.int32, 1)
+    NB, Hkv, BS, D = codes.shape
+    if tuple(meta.shape) != (NB, Hkv, BS, D // 64, 2):
+        raise ValueError("meta must be [NB, Hkv, BS, D/64, 2]")
+    N = src.shape[0]
+    if tuple(src.shape) != (N, Hkv, D) or slots.shape[0] != N:
+        raise ValueError(f"src must be [N, {Hkv}, {D}] with one slot per row")
+    st = lib.paged_kv_quantize(_ptr(codes), _ptr(meta), _ptr(src), _ptr(slots), N, Hkv, D, BS,
+                               NB, _stream_handle(stream, src.device))
     _raise(st)
 
 

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpgd.so")
-SOURCES = ["pgd_api.cu", "pgd_kernels_d64.cu", "pgd_kernels_d128.cu", "pgd_kernels_d256.cu",
+SOURCES = ["pgd_api.cu", "pgd_kernels_d64.cu", "pgd_kernels_d128.cu", "pgd_kernels_d256.cu", "pgd_quantize.cu",
            "pgd_varlen.cu"]
 HEADERS = ["pgd_device.cuh", "pgd_internal.h", "pgd_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

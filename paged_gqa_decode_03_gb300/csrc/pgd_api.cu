@@ -615,12 +615,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                const uint16_t *v_new = nullptr, bool q8 = false, const void *k_meta = nullptr,
                const void *v_meta = nullptr)
 {
-    if (q8) {
-        if (D % 128 != 0)
-            return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d", D);
-        if (k_new || v_new)
-            return fail(PGD_ERR_UNSUPPORTED, "no fused append into quantised pages");
-    }
+    if (q8 && D % 128 != 0)
+        return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d", D);
     if (S == 0) {  // nothing to read or write: only the sizes are checked
         Plan plan;
         pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, q8);
@@ -740,8 +736,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.v_new = reinterpret_cast<const __half *>(v_new);
     p.k_cache = reinterpret_cast<__half *>(const_cast<void *>(k_cache));
     p.v_cache = reinterpret_cast<__half *>(const_cast<void *>(v_cache));
-    p.k_meta = q8 ? static_cast<const uint16_t *>(k_meta) : nullptr;
-    p.v_meta = q8 ? static_cast<const uint16_t *>(v_meta) : nullptr;
+    p.k_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(k_meta)) : nullptr;
+    p.v_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(v_meta)) : nullptr;
     p.q8_pair = q8_pair ? 1 : 0;
     p.q8_koff = q8_pair && code_gap < 0 ? box * D : 0;  // the lower array lands first
     p.q8_voff = q8_pair && code_gap < 0 ? 0 : box * D;   // (used for pieces of <= 4 KB)
@@ -1153,6 +1149,58 @@ pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_c
                num_blocks, head_major(num_kv_heads, block_size, head_dim), workspace,
                workspace_bytes, own, page_trace, stream, nullptr, nullptr, nullptr, true, k_meta,
                v_meta);
+}
+
+pgd_status paged_gqa_decode_q8_append(float *out, const uint16_t *q, const uint16_t *k_new,
+                                      const uint16_t *v_new, uint8_t *k_codes, uint16_t *k_meta,
+                                      uint8_t *v_codes, uint16_t *v_meta,
+                                      const int32_t *block_tables, const int32_t *seq_lens,
+                                      float scale, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int partition_size, int max_blocks_per_seq, int num_blocks,
+                                      void *stream)
+{
+    if (num_seqs > 0 && (!k_new || !v_new || !k_meta || !v_meta))
+        return fail(PGD_ERR_INVALID_ARG, "null k_new / v_new / k_meta / v_meta");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(PGD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    return run(out, q, k_codes, v_codes, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, head_major(num_kv_heads, block_size, head_dim), nullptr, 0, true,
+               nullptr, stream, nullptr, k_new, v_new, true, k_meta, v_meta);
+}
+
+pgd_status paged_kv_quantize(uint8_t *codes, uint16_t *meta, const uint16_t *src,
+                             const int32_t *slots, int num_rows, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, void *stream)
+{
+    if (num_rows < 0 || num_kv_heads <= 0 || num_blocks <= 0 || block_size <= 0)
+        return fail(PGD_ERR_INVALID_ARG, "num_rows %d, num_kv_heads %d, num_blocks %d, block_size %d",
+                    num_rows, num_kv_heads, num_blocks, block_size);
+    if (head_dim != 128 && head_dim != 256)
+        return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d",
+                    head_dim);
+    if ((long long)num_blocks * num_kv_heads * block_size >= (1ll << 40))
+        return fail(PGD_ERR_UNSUPPORTED, "cache of %lld rows", (long long)num_blocks * num_kv_heads * block_size);
+    if (num_rows == 0) {
+        t_last_error.clear();
+        return PGD_OK;
+    }
+    if (!codes || !meta || !src || !slots)
+        return fail(PGD_ERR_INVALID_ARG, "null array argument");
+    if (!aligned(codes, 16) || !aligned(meta, 16) || !aligned(src, 16) || !aligned(slots, 4))
+        return fail(PGD_ERR_INVALID_ARG, "codes, meta and src must be 16-byte aligned, slots 4");
+    DeviceState *ds;
+    pgd_status st;
+    if ((st = device_state(&ds)))
+        return st;
+    const cudaError_t e = launch_quantize(head_dim, codes, meta, src, slots, num_rows,
+                                          num_kv_heads, block_size, num_blocks, ds->err_word,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kernel launch");
+    t_last_error.clear();
+    return PGD_OK;
 }
 
 pgd_status paged_gqa_varlen(float *out, const uint16_t *q, const int32_t *cu_seqlens_q,

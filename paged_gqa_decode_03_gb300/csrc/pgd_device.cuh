@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace pgd {
@@ -161,6 +162,13 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses to the same memory.
+// Orders this thread's generic-proxy global-memory writes before later
+// async-proxy (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -464,6 +472,74 @@ __device__ __forceinline__ float2 unpack_half2(uint32_t v)
 {
     __half2 h = *reinterpret_cast<__half2 *>(&v);
     return __half22float2(h);
+}
+
+// ---------------------------------------------------------------- quantiser
+// One D-value fp16 row into 8-bit codes with a bf16 (scale, bias) pair per
+// group of 64, by one warp: lane l holds values VPL*l .. VPL*l+VPL-1 (VPL =
+// D/32) and gets their codes packed (byte i = value i) and its group's pair
+// (scale in the low half).  Per group: bias = bf16(min), scale =
+// bf16((max - min) / 255), code = clamp(rint((x - bias) / scale), 0, 255)
+// (0 when the scale is 0), each step one correctly rounded binary32
+// operation, so the codes are those of any binary32 implementation of
+// these steps.
+template <int D> struct QuantRow {
+    uint32_t codes[D / 128];
+    uint32_t pair;
+};
+
+template <int D>
+__device__ __forceinline__ QuantRow<D> quantise_row_warp(const __half *row, int lane)
+{
+    constexpr int VPL = D / 32;   // values per lane
+    constexpr int LPG = 64 / VPL; // lanes per group
+    static_assert(D == 128 || D == 256, "rows of 128 or 256 values");
+    float x[VPL];
+    uint32_t w[VPL / 2];
+    if constexpr (VPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(row + VPL * lane);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + VPL * lane);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL / 2; ++i) {
+        const float2 f = unpack_half2(w[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < VPL; ++i) {
+        mn = fminf(mn, x[i]);
+        mx = fmaxf(mx, x[i]);
+    }
+#pragma unroll
+    for (int off = 1; off < LPG; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(~0u, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, off));
+    }
+    const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 255.f));
+    const __nv_bfloat16 bb = __float2bfloat16_rn(mn);
+    const float S = __bfloat162float(sb), B = __bfloat162float(bb);
+    QuantRow<D> q;
+#pragma unroll
+    for (int j = 0; j < D / 128; ++j)
+        q.codes[j] = 0u;
+    if (S > 0.f) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const float t = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[i], B), S)), 0.f), 255.f);
+            q.codes[i / 4] |= (uint32_t)t << (8 * (i % 4));
+        }
+    }
+    q.pair = (uint32_t)__bfloat16_as_ushort(sb) | ((uint32_t)__bfloat16_as_ushort(bb) << 16);
+    return q;
 }
 
 }  // namespace pgd

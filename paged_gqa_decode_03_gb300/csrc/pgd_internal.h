@@ -103,8 +103,9 @@ struct DecodeParams {
     const __half *v_new;          // [S][Hkv][D] newest token's V
     __half *k_cache;              // caches, written at the newest token's row (append)
     __half *v_cache;
-    const uint16_t *k_meta;       // quantised pages: [NB][Hkv][BS][D/64][2] bf16
-    const uint16_t *v_meta;       //   (scale, bias) pairs, or null
+    uint16_t *k_meta;             // quantised pages: [NB][Hkv][BS][D/64][2] bf16
+    uint16_t *v_meta;             //   (scale, bias) pairs (written by the fused
+                                  //   append), or null
     int q8_pair;                  // quantised pages: 1 = one tensor copy brings a page's
                                   //   K and V codes (tmap_k spans both arrays)
     int q8_koff, q8_voff;         //   bytes of K / V codes within a page's pair of slots
@@ -197,6 +198,11 @@ struct VarlenParams {
     int blk_page, blk_head;       // (page, KV head) -> block coordinate of the K/V maps
     uint64_t wait_budget_ns;
 };
+
+// Quantiser of rows into quantised pages (pgd_quantize.cu).
+cudaError_t launch_quantize(int head_dim, uint8_t *codes, uint16_t *meta, const uint16_t *src,
+                            const int32_t *slots, int rows, int Hkv, int BS, int NB,
+                            unsigned *err, cudaStream_t stream);
 
 cudaError_t launch_varlen(int head_dim, bool pairs, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, const VarlenParams &p, int grid, int reduce_rows,

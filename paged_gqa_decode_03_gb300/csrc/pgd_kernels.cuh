@@ -46,12 +46,45 @@ struct StageHeader {
     long long app_off;  // kAppend: element offset of the newest token's cache row, -1: none
 };
 
+// Fused append into quantised pages, by the producer warp before it copies
+// the stage that holds the newest token: the warp quantises the token's K and
+// V rows (quantise_row_warp, the library's quantiser) and writes codes and
+// (scale, bias) pairs into the cache at app_off (bytes of the row's codes;
+// head-major pairs at row app_off / D); the stage's copies then bring them
+// like every other row.  Each lane orders its writes before the warp's later
+// tensor copies (proxy fence) and load-path copies (the caller's __syncwarp).
+template <int D>
+__device__ __forceinline__ void q8_append_to_cache(long long app_off, const __half *k_new,
+                                                   const __half *v_new, void *k_cache,
+                                                   void *v_cache, uint16_t *k_meta,
+                                                   uint16_t *v_meta, int lane)
+{
+    constexpr int VPL = D / 32, LPG = 64 / VPL, NGRP = D / kQuantGroup;
+    const QuantRow<D> qk = quantise_row_warp<D>(k_new, lane);
+    const QuantRow<D> qv = quantise_row_warp<D>(v_new, lane);
+    uint8_t *kg = static_cast<uint8_t *>(k_cache) + app_off + VPL * lane;
+    uint8_t *vg = static_cast<uint8_t *>(v_cache) + app_off + VPL * lane;
+    if constexpr (VPL == 4) {
+        *reinterpret_cast<uint32_t *>(kg) = qk.codes[0];
+        *reinterpret_cast<uint32_t *>(vg) = qv.codes[0];
+    } else {
+        *reinterpret_cast<uint2 *>(kg) = make_uint2(qk.codes[0], qk.codes[1]);
+        *reinterpret_cast<uint2 *>(vg) = make_uint2(qv.codes[0], qv.codes[1]);
+    }
+    if (lane % LPG == 0) {
+        const long long mrow = app_off / D;
+        reinterpret_cast<uint32_t *>(k_meta)[mrow * NGRP + lane / LPG] = qk.pair;
+        reinterpret_cast<uint32_t *>(v_meta)[mrow * NGRP + lane / LPG] = qv.pair;
+    }
+    fence_proxy_async_global();
+}
+
 // Q8: the cache holds 8-bit codes with a bf16 (scale, bias) pair per 64
 // values of a row (tmap_km / tmap_vm: the pairs); the affine map is applied
 // in fp32 around exact fp16 tensor-core products of the codes:
 //   s = sum_g scale_g (q_g . code_g) + bias_g sum(q_g)            (QK)
 //   O += sum_t (p_t scale_g(t)) code_t + sum_t p_t bias_g(t)      (PV)
-template <int D, int BS, bool TRACE, bool Q8>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
 __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     paged_gqa_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
@@ -247,13 +280,23 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 const uint32_t fb = smem_addr(&full_bar[slot]);
                 // fused append: cache row of token L-1 (its page is the unit's
                 // page (L-1)/BS - pg0), published with the header
+                // (quantised pages: the producer writes the row, quantised,
+                // into the cache while issuing the unit's first stage, ahead
+                // of the last stage's copies that bring it)
                 long long app_off = -1;
-                if (app_unit && st == nst - 1) {
+                if (app_unit && (st == nst - 1 || (Q8 && QAPP && st == 0))) {
                     const int ja = (L - 1) / BS - pg0;
                     const int ida = __shfl_sync(~0u, ja < 32 ? id0 : id1, ja & 31);
                     if ((unsigned)ida < (unsigned)p.NB)
                         app_off = ida * p.kv_page_stride + g * p.kv_head_stride +
                                   ((L - 1) % BS) * p.kv_token_stride;
+                }
+                if constexpr (Q8 && QAPP) {
+                    if (app_off >= 0 && st == 0)
+                        q8_append_to_cache<D>(app_off, p.k_new + ((size_t)s * Hkv + g) * D,
+                                              p.v_new + ((size_t)s * Hkv + g) * D, p.k_cache,
+                                              p.v_cache, p.k_meta, p.v_meta, lane);
+                    __syncwarp();
                 }
                 if constexpr (Q8 && !META_BY_TMA) {
                     // the rows' (scale, bias) pairs, [row][group] per page
@@ -1022,7 +1065,7 @@ __global__ void __launch_bounds__(reduce_threads<D>())
 // ---------------------------------------------------------------- launch
 // Raises the partition kernel's dynamic shared-memory limit, once per
 // device and instantiation.
-template <int D, int BS, bool TRACE, bool Q8>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
 cudaError_t ensure_smem_attribute()
 {
     static std::atomic<unsigned long long> done{0};  // bit per device ordinal < 64
@@ -1033,7 +1076,7 @@ cudaError_t ensure_smem_attribute()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8>,
+    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_smem_bytes<D, Q8>());
     if (e == cudaSuccess)
@@ -1041,11 +1084,11 @@ cudaError_t ensure_smem_attribute()
     return e;
 }
 
-template <int D, int BS, bool TRACE, bool Q8>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
 cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const LaunchConfig &lc)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8>;
-    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8>();
+    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP>;
+    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8, QAPP>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -1087,9 +1130,12 @@ cudaError_t launch_decode_bs(bool trace, bool q8, const KVMaps &m, const DecodeP
                              const LaunchConfig &lc)
 {
     if constexpr (D % 128 == 0) {
-        if (q8)
+        if (q8) {
+            if (p.k_new)  // quantised append (no page trace)
+                return launch_decode_impl<D, BS, false, true, true>(m, p, lc);
             return trace ? launch_decode_impl<D, BS, true, true>(m, p, lc)
                          : launch_decode_impl<D, BS, false, true>(m, p, lc);
+        }
     } else if (q8) {
         return cudaErrorInvalidValue;
     }

@@ -1,0 +1,130 @@
+"""GPU parity of the quantiser (paged_kv_quantize) and of the fused append
+into quantised pages (paged_gqa_decode_q8_append) against the oracle's
+quantise_rows / append_kv_q8 + decode_q8.  Codes and (scale, bias) pairs
+are integers decided in binary32 on both sides: compared bit for bit."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_03_gb300 as pgd
+from paged_gqa_decode_03_gb300.workloads import make_custom, make_q8
+from parity_util import assert_parity
+from test_gpu_q8 import oracle_q8
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    assert pgd.pgd_check_device_error() == 0
+
+
+def _rows(N, Hkv, D, seed):
+    """fp16 rows of mixed kinds: N(0, s) with s from 1e-3 to 300, constant
+    groups, and groups holding exact ties of the rounding rule."""
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((N, Hkv, D)) * g.choice([1e-3, 0.1, 1.0, 7.0, 300.0], (N, Hkv, 1))
+    x[0, 0, :64] = 0.37                                   # constant group
+    j = np.arange(62)
+    x[min(1, N - 1), 0, :64] = np.concatenate([[0.0, 255 / 64], (2 * j + 1) / 128])  # ties
+    return x.astype(np.float16)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_quantize_matches_oracle(D):
+    NB, Hkv, BS, N = 40, 4, 16, 300
+    g = np.random.default_rng(D)
+    codes = torch.from_numpy(g.integers(0, 256, (NB, Hkv, BS, D)).astype(np.uint8)).to(DEV)
+    meta = torch.from_numpy(g.integers(-32768, 32768, (NB, Hkv, BS, D // 64, 2)).astype(np.int16)).to(DEV)
+    src = _rows(N, Hkv, D, seed=D + 1)
+    slots = g.permutation(NB * BS)[:N].astype(np.int32)
+    slots[::7] = -1                                         # skipped rows
+    c0, m0 = codes.cpu().numpy(), meta.cpu().numpy().view(np.uint16)
+    want_c, want_m = oracle.quantise_rows(c0, m0, src, slots)
+    pgd.paged_kv_quantize(codes, meta, torch.from_numpy(src).to(DEV),
+                          torch.from_numpy(slots).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(codes.cpu().numpy(), want_c)
+    assert np.array_equal(meta.cpu().numpy().view(np.uint16), want_m)
+    assert pgd.pgd_check_device_error() == 0
+
+
+def test_quantize_page_out_of_range_is_flagged_and_skipped():
+    NB, Hkv, BS, D = 4, 2, 8, 128
+    codes = torch.zeros((NB, Hkv, BS, D), dtype=torch.uint8, device=DEV)
+    meta = torch.zeros((NB, Hkv, BS, D // 64, 2), dtype=torch.int16, device=DEV)
+    src = torch.from_numpy(_rows(2, Hkv, D, seed=3)).to(DEV)
+    slots = torch.tensor([NB * BS + 3, 5], dtype=torch.int32, device=DEV)
+    pgd.paged_kv_quantize(codes, meta, src, slots)
+    torch.cuda.synchronize()
+    assert pgd.pgd_check_device_error() == pgd.DEVERR_PAGE_RANGE
+    want_c, want_m = oracle.quantise_rows(np.zeros((NB, Hkv, BS, D), np.uint8),
+                                          np.zeros((NB, Hkv, BS, D // 64, 2), np.uint16),
+                                          src[1:].cpu().numpy(), np.array([5], np.int32))
+    assert np.array_equal(codes.cpu().numpy(), want_c)
+    assert np.array_equal(meta.cpu().numpy().view(np.uint16), want_m)
+
+
+def test_quantize_rejects_bad_arguments():
+    codes = torch.zeros((2, 1, 8, 64), dtype=torch.uint8, device=DEV)
+    meta = torch.zeros((2, 1, 8, 1, 2), dtype=torch.int16, device=DEV)
+    src = torch.zeros((1, 1, 64), dtype=torch.float16, device=DEV)
+    slots = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with pytest.raises(pgd.PGDError, match="UNSUPPORTED"):
+        pgd.paged_kv_quantize(codes, meta, src, slots)   # head_dim 64
+
+
+LENS = [0, 1, 2, 7, 8, 9, 15, 16, 17, 33, 255, 256, 257, 511, 512, 513, 1000]
+
+
+def check_q8_append(w, P, seed):
+    c = make_q8(w)
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    kn = (torch.randn((w.S, w.Hkv, w.D), generator=g, device=DEV) * 2).to(torch.float16)
+    vn = (torch.randn((w.S, w.Hkv, w.D), generator=g, device=DEV) * 2).to(torch.float16)
+    host = [t.cpu().numpy() for t in (c.k_codes, c.k_meta, c.v_codes, c.v_meta)]
+    kc, km, vc, vm = oracle.append_kv_q8(host[0], host[1].view(np.uint16), host[2],
+                                         host[3].view(np.uint16), kn.cpu().numpy(),
+                                         vn.cpu().numpy(), w.block_tables.cpu().numpy(),
+                                         w.seq_lens.cpu().numpy())
+    after = dataclasses.replace(
+        c, k_codes=torch.from_numpy(kc).to(DEV), v_codes=torch.from_numpy(vc).to(DEV),
+        k_meta=torch.from_numpy(km.view(np.int16)).to(DEV),
+        v_meta=torch.from_numpy(vm.view(np.int16)).to(DEV))
+    ref = oracle_q8(w, after)
+    out = torch.full((w.S, w.Hq, w.D), float("nan"), dtype=torch.float32, device=DEV)
+    pgd.paged_gqa_decode_q8_append(out, w.q, kn, vn, c.k_codes, c.k_meta, c.v_codes, c.v_meta,
+                                   w.block_tables, w.seq_lens, w.scale, P)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), ref, f"q8 append D{w.D} BS{w.BS} P{P}")
+    # the caches: the new rows quantised as the oracle does, nothing else changed
+    assert np.array_equal(c.k_codes.cpu().numpy(), kc)
+    assert np.array_equal(c.v_codes.cpu().numpy(), vc)
+    assert np.array_equal(c.k_meta.cpu().numpy().view(np.uint16), km)
+    assert np.array_equal(c.v_meta.cpu().numpy().view(np.uint16), vm)
+    assert pgd.pgd_check_device_error() == 0
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("BS", [8, 16, 32])
+def test_q8_append_edge_lengths(D, BS):
+    w = make_custom(S=len(LENS), Hq=16, Hkv=2, D=D, BS=BS, lens=LENS, seed=D + BS + 5,
+                    device=DEV, MB=(1024 + BS - 1) // BS)
+    for P in (256, 512):
+        check_q8_append(w, P, seed=P + BS)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (24, 4)])
+def test_q8_append_groups(Hq, Hkv):
+    w = make_custom(S=len(LENS), Hq=Hq, Hkv=Hkv, D=128, BS=16, lens=LENS, seed=Hq + 9,
+                    device=DEV, MB=64)
+    check_q8_append(w, 512, seed=Hq)
