@@ -96,6 +96,10 @@ def _bind(lib):
     lib.oracle_quantise_rows.restype = I
     lib.oracle_append_kv_q8.argtypes = [P] * 8 + [I] * 6
     lib.oracle_append_kv_q8.restype = I
+    lib.oracle_paged_gqa_decode_q8_strided.argtypes = [P] * 8 + [D] + [I] * 7 + [Lg] * 6 + [I]
+    lib.oracle_paged_gqa_decode_q8_strided.restype = I
+    lib.oracle_append_kv_q8_strided.argtypes = [P] * 8 + [I] * 6 + [Lg] * 6
+    lib.oracle_append_kv_q8_strided.restype = I
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = I
     return lib
@@ -427,6 +431,51 @@ def append_kv_q8(k_codes, k_meta, v_codes, v_meta, k_new, v_new, block_tables, s
     S, MB = bt.shape
     _check(lib.oracle_append_kv_q8(_ptr(kc), _ptr(km), _ptr(vc), _ptr(vm), _ptr(kn), _ptr(vn),
                                    _ptr(bt), _ptr(sl), S, Hkv, D, BS, MB, NB))
+    return kc, km, vc, vm
+
+
+def decode_q8_strided(q, k_codes, k_meta, v_codes, v_meta, block_tables, seq_lens, scale,
+                      num_kv_heads, block_size, num_blocks, code_strides, meta_strides,
+                      threads=None):
+    """``decode_q8`` over quantised caches given as flat arrays: the codes of
+    token r of page b, KV head g at byte b*code_strides[0] + g*code_strides[1]
+    + r*code_strides[2], its (scale, bias) pairs at bf16 element
+    b*meta_strides[0] + g*meta_strides[1] + r*meta_strides[2]."""
+    lib = _load()
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8).ravel()
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8).ravel()
+    km = np.ascontiguousarray(k_meta, dtype=np.uint16).ravel()
+    vm = np.ascontiguousarray(v_meta, dtype=np.uint16).ravel()
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, D = q.shape
+    MB = bt.shape[1]
+    out = np.empty((S, Hq, D), dtype=np.float64)
+    _check(lib.oracle_paged_gqa_decode_q8_strided(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(km), _ptr(vc), _ptr(vm), _ptr(bt), _ptr(sl),
+        float(scale), S, Hq, int(num_kv_heads), D, int(block_size), MB, int(num_blocks),
+        *[int(x) for x in code_strides], *[int(x) for x in meta_strides],
+        int(threads or max_threads())))
+    return out
+
+
+def append_kv_q8_strided(k_codes, k_meta, v_codes, v_meta, k_new, v_new, block_tables, seq_lens,
+                         num_kv_heads, block_size, num_blocks, code_strides, meta_strides):
+    """``append_kv_q8`` over flat quantised arrays at the given strides;
+    returns copies of the four arrays."""
+    lib = _load()
+    kc = np.array(k_codes, dtype=np.uint8, copy=True).ravel()
+    vc = np.array(v_codes, dtype=np.uint8, copy=True).ravel()
+    km = np.array(k_meta, dtype=np.uint16, copy=True).ravel()
+    vm = np.array(v_meta, dtype=np.uint16, copy=True).ravel()
+    kn, vn = _u16(k_new), _u16(v_new)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, MB = bt.shape
+    D = kn.shape[-1]
+    _check(lib.oracle_append_kv_q8_strided(
+        _ptr(kc), _ptr(km), _ptr(vc), _ptr(vm), _ptr(kn), _ptr(vn), _ptr(bt), _ptr(sl), S,
+        int(num_kv_heads), D, int(block_size), MB, int(num_blocks),
+        *[int(x) for x in code_strides], *[int(x) for x in meta_strides]))
     return kc, km, vc, vm
 
 

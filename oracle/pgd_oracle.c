@@ -610,14 +610,22 @@ int oracle_dequant_affine(double *w, const uint8_t *codes, const uint16_t *meta,
     return ORC_OK;
 }
 
+/* The (scale, bias) pairs of the default layout [NB][Hkv][BS][D/64][2]. */
+static kv_strides meta_head_major(int Hkv, int BS, int D)
+{
+    return head_major(Hkv, BS, (D / 64) * 2);
+}
+
 /* The decode definition over quantised caches: every K/V row is first
  * dequantised (oracle_dequant_affine), then attention as in
- * oracle_paged_gqa_decode (natural exp, fp64). */
-int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_codes,
-                               const uint16_t *k_meta, const uint8_t *v_codes,
-                               const uint16_t *v_meta, const int32_t *block_tables,
-                               const int32_t *seq_lens, double scale, int S, int Hq, int Hkv,
-                               int D, int BS, int MB, int NB, int num_threads)
+ * oracle_paged_gqa_decode (natural exp, fp64).  Row t of page b, KV head g:
+ * codes at byte b*cx.page + g*cx.head + t*cx.token, its D/64 pairs at bf16
+ * element b*mx.page + g*mx.head + t*mx.token. */
+static int decode_q8(double *out, const uint16_t *q, const uint8_t *k_codes,
+                     const uint16_t *k_meta, const uint8_t *v_codes, const uint16_t *v_meta,
+                     kv_strides cx, kv_strides mx, const int32_t *block_tables,
+                     const int32_t *seq_lens, double scale, int S, int Hq, int Hkv, int D, int BS,
+                     int MB, int NB, int num_threads)
 {
     int rc = check_inputs(block_tables, seq_lens, S, Hq, Hkv, D, BS, MB, NB);
     if (rc)
@@ -649,8 +657,10 @@ int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_
         }
         const uint16_t *qh = q + sh * D;
         for (long t = 0; t < L; ++t) {
-            long r = ((long)block_tables[(long)s * MB + t / BS] * Hkv + g) * BS + t % BS;
-            oracle_dequant_affine(row, k_codes + r * D, k_meta + r * (D / 64) * 2, D, 64);
+            long pp = block_tables[(long)s * MB + t / BS];
+            oracle_dequant_affine(row, k_codes + pp * cx.page + g * cx.head + (t % BS) * cx.token,
+                                  k_meta + pp * mx.page + g * mx.head + (t % BS) * mx.token, D,
+                                  64);
             double dot = 0.0;
             for (int d = 0; d < D; ++d)
                 dot += g_h2d[qh[d]] * row[d];
@@ -665,8 +675,10 @@ int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_
             den += exp(z[t] - zmax);
         for (long t = 0; t < L; ++t) {
             double w = exp(z[t] - zmax) / den;
-            long r = ((long)block_tables[(long)s * MB + t / BS] * Hkv + g) * BS + t % BS;
-            oracle_dequant_affine(row, v_codes + r * D, v_meta + r * (D / 64) * 2, D, 64);
+            long pp = block_tables[(long)s * MB + t / BS];
+            oracle_dequant_affine(row, v_codes + pp * cx.page + g * cx.head + (t % BS) * cx.token,
+                                  v_meta + pp * mx.page + g * mx.head + (t % BS) * mx.token, D,
+                                  64);
             for (int d = 0; d < D; ++d)
                 o[d] += w * row[d];
         }
@@ -674,6 +686,35 @@ int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_
         free(row);
     }
     return fail ? ORC_NO_MEMORY : ORC_OK;
+}
+
+int oracle_paged_gqa_decode_q8(double *out, const uint16_t *q, const uint8_t *k_codes,
+                               const uint16_t *k_meta, const uint8_t *v_codes,
+                               const uint16_t *v_meta, const int32_t *block_tables,
+                               const int32_t *seq_lens, double scale, int S, int Hq, int Hkv,
+                               int D, int BS, int MB, int NB, int num_threads)
+{
+    return decode_q8(out, q, k_codes, k_meta, v_codes, v_meta, head_major(Hkv, BS, D),
+                     meta_head_major(Hkv, BS, D), block_tables, seq_lens, scale, S, Hq, Hkv, D,
+                     BS, MB, NB, num_threads);
+}
+
+/* The same over quantised caches in any layout: codes strides in bytes, the
+ * pairs' strides in bf16 elements (every stride positive). */
+int oracle_paged_gqa_decode_q8_strided(double *out, const uint16_t *q, const uint8_t *k_codes,
+                                       const uint16_t *k_meta, const uint8_t *v_codes,
+                                       const uint16_t *v_meta, const int32_t *block_tables,
+                                       const int32_t *seq_lens, double scale, int S, int Hq,
+                                       int Hkv, int D, int BS, int MB, int NB, long code_page,
+                                       long code_head, long code_token, long meta_page,
+                                       long meta_head, long meta_token, int num_threads)
+{
+    if (code_page <= 0 || code_head <= 0 || code_token <= 0 || meta_page <= 0 ||
+        meta_head <= 0 || meta_token <= 0)
+        return ORC_BAD_SHAPE;
+    kv_strides cx = {code_page, code_head, code_token}, mx = {meta_page, meta_head, meta_token};
+    return decode_q8(out, q, k_codes, k_meta, v_codes, v_meta, cx, mx, block_tables, seq_lens,
+                     scale, S, Hq, Hkv, D, BS, MB, NB, num_threads);
 }
 
 /* ---------------------------------------------------------------- quantiser
@@ -755,8 +796,9 @@ int oracle_quantise_affine(uint8_t *codes, uint16_t *pairs, const uint16_t *x, l
 /* Rows src[n][h][:] (binary16, [N][Hkv][D]) written into the quantised
  * head-major cache at cache row slots[n] (page * BS + row; negative: row
  * skipped): codes [NB][Hkv][BS][D], pairs [NB][Hkv][BS][D/64][2]. */
-int oracle_quantise_rows(uint8_t *codes, uint16_t *meta, const uint16_t *src,
-                         const int32_t *slots, int N, int Hkv, int D, int BS, int NB)
+static int quantise_rows(uint8_t *codes, uint16_t *meta, kv_strides cx, kv_strides mx,
+                         const uint16_t *src, const int32_t *slots, int N, int Hkv, int D,
+                         int BS, int NB)
 {
     if (N < 0 || Hkv <= 0 || D <= 0 || D % 64 != 0 || BS <= 0 || NB <= 0)
         return ORC_BAD_SHAPE;
@@ -768,13 +810,20 @@ int oracle_quantise_rows(uint8_t *codes, uint16_t *meta, const uint16_t *src,
         if (page >= NB)
             return ORC_BAD_PAGE;
         for (int h = 0; h < Hkv; ++h) {
-            long r = (page * Hkv + h) * BS + row;
+            uint8_t *c = codes + page * cx.page + h * cx.head + row * cx.token;
+            uint16_t *m = meta + page * mx.page + h * mx.head + row * mx.token;
             for (int g = 0; g < D / 64; ++g)
-                quantise_group(codes + r * D + g * 64, meta + (r * (D / 64) + g) * 2,
-                               src + ((long)n * Hkv + h) * D + g * 64, 64);
+                quantise_group(c + g * 64, m + 2 * g, src + ((long)n * Hkv + h) * D + g * 64, 64);
         }
     }
     return ORC_OK;
+}
+
+int oracle_quantise_rows(uint8_t *codes, uint16_t *meta, const uint16_t *src,
+                         const int32_t *slots, int N, int Hkv, int D, int BS, int NB)
+{
+    return quantise_rows(codes, meta, head_major(Hkv, BS, D), meta_head_major(Hkv, BS, D), src,
+                         slots, N, Hkv, D, BS, NB);
 }
 
 /* The decode step's append into quantised pages: sequence s's newest token
@@ -782,8 +831,9 @@ int oracle_quantise_rows(uint8_t *codes, uint16_t *meta, const uint16_t *src,
  * binary16) written, quantised, into its row of page
  * block_tables[s][(L_s - 1) / BS]; the decode then reads them like every
  * other row (oracle_paged_gqa_decode_q8). */
-int oracle_append_kv_q8(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta,
-                        const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_tables,
+static int append_kv_q8(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta,
+                        kv_strides cx, kv_strides mx, const uint16_t *k_new,
+                        const uint16_t *v_new, const int32_t *block_tables,
                         const int32_t *seq_lens, int S, int Hkv, int D, int BS, int MB, int NB)
 {
     if (S < 0 || MB <= 0)
@@ -807,11 +857,37 @@ int oracle_append_kv_q8(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes, ui
         }
     }
     if (!rc)
-        rc = oracle_quantise_rows(k_codes, k_meta, k_new, slots, S, Hkv, D, BS, NB);
+        rc = quantise_rows(k_codes, k_meta, cx, mx, k_new, slots, S, Hkv, D, BS, NB);
     if (!rc)
-        rc = oracle_quantise_rows(v_codes, v_meta, v_new, slots, S, Hkv, D, BS, NB);
+        rc = quantise_rows(v_codes, v_meta, cx, mx, v_new, slots, S, Hkv, D, BS, NB);
     free(slots);
     return rc;
+}
+
+int oracle_append_kv_q8(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta,
+                        const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_tables,
+                        const int32_t *seq_lens, int S, int Hkv, int D, int BS, int MB, int NB)
+{
+    return append_kv_q8(k_codes, k_meta, v_codes, v_meta, head_major(Hkv, BS, D),
+                        meta_head_major(Hkv, BS, D), k_new, v_new, block_tables, seq_lens, S,
+                        Hkv, D, BS, MB, NB);
+}
+
+/* The append into quantised caches in any layout (strides as in
+ * oracle_paged_gqa_decode_q8_strided). */
+int oracle_append_kv_q8_strided(uint8_t *k_codes, uint16_t *k_meta, uint8_t *v_codes,
+                                uint16_t *v_meta, const uint16_t *k_new, const uint16_t *v_new,
+                                const int32_t *block_tables, const int32_t *seq_lens, int S,
+                                int Hkv, int D, int BS, int MB, int NB, long code_page,
+                                long code_head, long code_token, long meta_page, long meta_head,
+                                long meta_token)
+{
+    if (code_page <= 0 || code_head <= 0 || code_token <= 0 || meta_page <= 0 ||
+        meta_head <= 0 || meta_token <= 0)
+        return ORC_BAD_SHAPE;
+    kv_strides cx = {code_page, code_head, code_token}, mx = {meta_page, meta_head, meta_token};
+    return append_kv_q8(k_codes, k_meta, v_codes, v_meta, cx, mx, k_new, v_new, block_tables,
+                        seq_lens, S, Hkv, D, BS, MB, NB);
 }
 
 int oracle_max_threads(void)

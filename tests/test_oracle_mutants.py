@@ -54,8 +54,11 @@ MUTANTS = [
      False),
     ("q8: scale and bias swapped", "meta[2 * gidx]) * codes[i] +\n               oracle_bf16_to_double(meta[2 * gidx + 1]);",
      "meta[2 * gidx + 1]) * codes[i] +\n               oracle_bf16_to_double(meta[2 * gidx]);", False),
-    ("q8: V dequantised with the K metadata", "v_codes + r * D, v_meta + r", "v_codes + r * D, k_meta + r",
+    ("q8: V dequantised with the K metadata",
+     "                                  v_meta + pp * mx.page", "                                  k_meta + pp * mx.page",
      False),
+    ("q8: pairs' head and token strides swapped", "k_meta + pp * mx.page + g * mx.head + (t % BS) * mx.token",
+     "k_meta + pp * mx.page + g * mx.token + (t % BS) * mx.head", False),
     ("q8: bf16 bits shifted by 15", "(uint32_t)h << 16", "(uint32_t)h << 15", False),
     ("quantiser: codes truncated", "float t = rintf(diff / S);", "float t = truncf(diff / S);",
      False),
@@ -67,8 +70,8 @@ MUTANTS = [
     ("quantiser: bf16 truncated", "    u += 0x7FFFu + ((u >> 16) & 1u);\n", "", False),
     ("quantiser: codes from the unrounded bias", "float diff = (float)g_h2d[x[i]] - B;",
      "float diff = (float)g_h2d[x[i]] - mn;", False),
-    ("quantiser: row within the page off by one", "long r = (page * Hkv + h) * BS + row;",
-     "long r = (page * Hkv + h) * BS + (row + 1) % BS;", False),
+    ("quantiser: row within the page off by one", "h * cx.head + row * cx.token;",
+     "h * cx.head + ((row + 1) % BS) * cx.token;", False),
     ("append q8: newest row one late", "(int32_t)(page * (long)BS + (L - 1) % BS)",
      "(int32_t)(page * (long)BS + L % BS)", False),
 ]
@@ -112,6 +115,8 @@ def _pins():
         ("q8 bf16", Q.test_bf16_decoding_matches_torch),
         ("q8 exact fp16", Q.test_equals_fp16_decode_on_exact_values),
         ("q8 sdpa", lambda: Q.test_dense_sdpa_on_dequantised_values(8, 2, 8)),
+        ("q8 strided", lambda: Q.test_strided_q8_equals_head_major(128, 8)),
+        ("q8 strided append", Q.test_strided_q8_append_equals_head_major),
         ("quantise example", Z.test_worked_example_inverted),
         ("quantise grid", Z.test_exact_grid),
         ("quantise ties", Z.test_ties_go_to_even),

@@ -5,6 +5,8 @@ format with bf16 (scale, bias)).
   bf16 decoding                    -> test_bf16_decoding_matches_torch
   code / metadata addressing, K/V  -> test_equals_fp16_decode_on_exact_values,
                                       test_dense_sdpa_on_dequantised_values
+  strided layouts (codes, pairs)   -> test_strided_q8_equals_head_major,
+                                      test_strided_q8_append_equals_head_major
 """
 import json
 import os
@@ -104,3 +106,65 @@ def test_poison_metadata_never_read():
     out = oracle.decode_q8(w.q.numpy(), c.k_codes.numpy(), _np(c.k_meta), c.v_codes.numpy(),
                            _np(c.v_meta), w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
     assert np.all(np.isfinite(out))
+
+
+def _q8_layouts(codes, meta, pad_row=16, pad_page=48):
+    """One quantised array pair in three layouts built by numpy, as (name,
+    codes_flat, meta_flat, code_strides, meta_strides): token-major
+    [NB][BS][Hkv][...], rows padded (codes by pad_row bytes, pairs by one
+    extra pair, both padded with 0xFF / NaN bits), pages padded."""
+    NB, Hkv, BS, D = codes.shape
+    NM = (D // 64) * 2
+    m = meta.reshape(NB, Hkv, BS, NM)
+    tm = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3))
+    pc = np.full((NB, Hkv, BS, D + pad_row), 0xFF, dtype=np.uint8)
+    pc[..., :D] = codes
+    pm = np.full((NB, Hkv, BS, NM + 2), 0x7FC1, dtype=np.uint16)
+    pm[..., :NM] = m
+    gc = np.full((NB, Hkv * BS * D + pad_page), 0xFF, dtype=np.uint8)
+    gc[:, :Hkv * BS * D] = codes.reshape(NB, -1)
+    gm = np.full((NB, Hkv * BS * NM + 8), 0x7FC1, dtype=np.uint16)
+    gm[:, :Hkv * BS * NM] = m.reshape(NB, -1)
+    return [
+        ("token_major", tm(codes), tm(m), (BS * Hkv * D, D, Hkv * D), (BS * Hkv * NM, NM, Hkv * NM)),
+        ("padded_rows", pc, pm, (Hkv * BS * (D + pad_row), BS * (D + pad_row), D + pad_row),
+         (Hkv * BS * (NM + 2), BS * (NM + 2), NM + 2)),
+        ("padded_pages", gc, gm, (Hkv * BS * D + pad_page, BS * D, D),
+         (Hkv * BS * NM + 8, BS * NM, NM)),
+    ]
+
+
+@pytest.mark.parametrize("D,BS", [(128, 8), (256, 16)])
+def test_strided_q8_equals_head_major(D, BS):
+    """The strided quantised decode reads the same numbers whatever the
+    layout: bitwise equal to the head-major one (layouts built by numpy; a
+    swapped head/token stride or a read of the padding fails here)."""
+    w, c = _q8(61 + D, D=D, BS=BS, lens=(0, 1, 9, 23, 40))
+    args = (w.block_tables.numpy(), w.seq_lens.numpy(), w.scale)
+    ref = oracle.decode_q8(w.q.numpy(), c.k_codes.numpy(), _np(c.k_meta), c.v_codes.numpy(),
+                           _np(c.v_meta), *args)
+    NB, Hkv = c.k_codes.shape[:2]
+    lk = _q8_layouts(c.k_codes.numpy(), _np(c.k_meta))
+    lv = _q8_layouts(c.v_codes.numpy(), _np(c.v_meta))
+    for (name, kc, km, cs, ms), (_, vc, vm, _, _) in zip(lk, lv):
+        out = oracle.decode_q8_strided(w.q.numpy(), kc, km, vc, vm, *args, Hkv, BS, NB, cs, ms)
+        assert np.array_equal(out, ref), name
+
+
+def test_strided_q8_append_equals_head_major():
+    w, c = _q8(71, D=128, BS=8, lens=(0, 1, 8, 23))
+    rng = np.random.default_rng(3)
+    kn = rng.standard_normal((w.S, w.Hkv, 128)).astype(np.float16)
+    vn = rng.standard_normal((w.S, w.Hkv, 128)).astype(np.float16)
+    bt, sl = w.block_tables.numpy(), w.seq_lens.numpy()
+    kc, km, vc, vm = c.k_codes.numpy(), _np(c.k_meta), c.v_codes.numpy(), _np(c.v_meta)
+    ref = oracle.append_kv_q8(kc, km, vc, vm, kn, vn, bt, sl)
+    NB, Hkv, BS, D = kc.shape
+    tm = lambda a: np.ascontiguousarray(a.reshape(NB, Hkv, BS, -1).transpose(0, 2, 1, 3))
+    got = oracle.append_kv_q8_strided(tm(kc), tm(km), tm(vc), tm(vm), kn, vn, bt, sl, Hkv, BS,
+                                      NB, (BS * Hkv * D, D, Hkv * D), (BS * Hkv * 4, 4, Hkv * 4))
+    back = lambda a, n: np.ascontiguousarray(a.reshape(NB, BS, Hkv, n).transpose(0, 2, 1, 3))
+    assert np.array_equal(back(got[0], D), ref[0])
+    assert np.array_equal(back(got[1], 4), ref[1].reshape(NB, Hkv, BS, 4))
+    assert np.array_equal(back(got[2], D), ref[2])
+    assert np.array_equal(back(got[3], 4), ref[3].reshape(NB, Hkv, BS, 4))
