@@ -280,6 +280,26 @@ pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_c
                                void *stream);
 
 /*
+ * paged_gqa_decode_q8_strided — paged_gqa_decode_q8 (and, with k_new / v_new
+ * given, paged_gqa_decode_q8_append) over quantised pages in any layout:
+ * the codes of token r of page b, KV head g start at byte
+ * b*code_page_stride + g*code_head_stride + r*code_token_stride (positive
+ * multiples of 16 below 2^39, token stride >= head_dim), their head_dim / 64
+ * (scale, bias) pairs at bf16 element b*meta_page_stride + g*meta_head_stride
+ * + r*meta_token_stride (positive multiples of head_dim / 32 below 2^38).
+ * k_new, v_new: both NULL (no append) or both given.  workspace NULL:
+ * library scratch.  No page trace.
+ */
+pgd_status paged_gqa_decode_q8_strided(
+    float *out, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_codes,
+    uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta, const int32_t *block_tables,
+    const int32_t *seq_lens, float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int partition_size, int max_blocks_per_seq, int num_blocks,
+    int64_t code_page_stride, int64_t code_head_stride, int64_t code_token_stride,
+    int64_t meta_page_stride, int64_t meta_head_stride, int64_t meta_token_stride,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * paged_kv_quantize — writes fp16 rows into quantised pages (the format of
  * paged_gqa_decode_q8).  The pages show the affine format only from the
  * reading side (Kapitsa part 02: value = scale * q + bias); the quantiser

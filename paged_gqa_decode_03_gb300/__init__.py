@@ -29,7 +29,8 @@ import torch
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
            "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
            "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8",
-           "paged_gqa_decode_q8_append", "paged_kv_quantize", "pgd_plan", "pgd_last_partition_size",
+           "paged_gqa_decode_q8_append", "paged_gqa_decode_q8_strided", "q8_strides",
+           "paged_kv_quantize", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
@@ -56,6 +57,7 @@ SIGNATURES = {
     "paged_gqa_decode_q8": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
     "paged_gqa_decode_q8_append": (_I, [_P] * 10 + [_F] + [_I] * 8 + [_P]),
     "paged_kv_quantize": (_I, [_P] * 4 + [_I] * 5 + [_P]),
+    "paged_gqa_decode_q8_strided": (_I, [_P] * 10 + [_F] + [_I] * 8 + [_L] * 6 + [_P, _Z, _P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
@@ -396,6 +398,58 @@ def paged_gqa_decode_q8_append(out, q, k_new, v_new, k_codes, k_meta, v_codes, v
         _ptr(v_codes), _ptr(v_meta), _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq,
         Hkv, D, BS, int(partition_size), block_tables.shape[1], NB,
         _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def q8_strides(layout: str, num_kv_heads: int, block_size: int, head_dim: int):
+    """(code strides in bytes, pair strides in bf16 elements) of contiguous
+    quantised caches in ``layout``: "head_major" (codes [NB, Hkv, BS, D],
+    pairs [NB, Hkv, BS, D/64, 2]) or "token_major" ([NB, BS, Hkv, ...])."""
+    H, B, D, M = num_kv_heads, block_size, head_dim, (head_dim // 64) * 2
+    if layout == "head_major":
+        return (H * B * D, B * D, D), (H * B * M, B * M, M)
+    if layout == "token_major":
+        return (B * H * D, D, H * D), (B * H * M, M, H * M)
+    raise ValueError(f"unknown layout {layout!r}")
+
+
+def paged_gqa_decode_q8_strided(out, q, k_codes, k_meta, v_codes, v_meta, block_tables,
+                                seq_lens, scale, num_kv_heads, block_size, num_blocks,
+                                code_strides, meta_strides, partition_size: int = 0, k_new=None,
+                                v_new=None, workspace=None, stream=None) -> None:
+    """The quantised decode (with the fused append when k_new / v_new are
+    given) over caches at any strides: k_codes / v_codes and k_meta / v_meta
+    are contiguous CUDA tensors (uint8 / int16) holding the rows at
+    ``code_strides`` (bytes) and ``meta_strides`` (bf16 elements)."""
+    lib = load_library()
+    _check(q, "q", torch.float16, 3)
+    _check(out, "out", torch.float32, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    for t, n, dt in ((k_codes, "k_codes", torch.uint8), (v_codes, "v_codes", torch.uint8),
+                     (k_meta, "k_meta", torch.int16), (v_meta, "v_meta", torch.int16)):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or not t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CUDA {dt} tensor")
+    S, Hq, D = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes of q, out, block_tables, seq_lens")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new or neither")
+    if k_new is not None:
+        _check(k_new, "k_new", torch.float16, 3)
+        _check(v_new, "v_new", torch.float16, 3)
+        if tuple(k_new.shape) != (S, num_kv_heads, D) or v_new.shape != k_new.shape:
+            raise ValueError(f"k_new / v_new must be [{S}, {num_kv_heads}, {D}]")
+    ws_bytes = 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.paged_gqa_decode_q8_strided(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(k_meta),
+        _ptr(v_codes), _ptr(v_meta), _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq,
+        int(num_kv_heads), D, int(block_size), int(partition_size), block_tables.shape[1],
+        int(num_blocks), *[int(x) for x in code_strides], *[int(x) for x in meta_strides],
+        _ptr(workspace), ws_bytes, _stream_handle(stream, q.device))
     _raise(st)
 
 

@@ -223,8 +223,8 @@ pgd_status encode_code_map(CUtensorMap *map, const void *base, const CacheGeom &
         return st;
     cuuint64_t dims[5] = {128, (cuuint64_t)g.BS, (cuuint64_t)(g.D / 128), (cuuint64_t)g.Hkv,
                           (cuuint64_t)g.NB};
-    cuuint64_t strides[4] = {(cuuint64_t)g.D, 128, (cuuint64_t)g.BS * g.D,
-                             (cuuint64_t)g.Hkv * g.BS * g.D};
+    cuuint64_t strides[4] = {(cuuint64_t)g.token_stride, 128, (cuuint64_t)g.head_stride,
+                             (cuuint64_t)g.page_stride};  // bytes (the cache's strides)
     cuuint32_t box[5] = {128, (cuuint32_t)box_rows, (cuuint32_t)(g.D / 128), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides,
@@ -613,7 +613,7 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                void *workspace, size_t ws_bytes, bool own_workspace, int32_t *page_trace,
                void *stream_v, unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
                const uint16_t *v_new = nullptr, bool q8 = false, const void *k_meta = nullptr,
-               const void *v_meta = nullptr)
+               const void *v_meta = nullptr, const Strides *meta_strides = nullptr)
 {
     if (q8 && D % 128 != 0)
         return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d", D);
@@ -645,6 +645,31 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
         return st;
     if ((st = check_strides(kv_strides, D)))
         return st;
+    // quantised pages: code strides in bytes (multiples of 16, the tensor
+    // copies' rule), the pairs' strides in bf16 elements (multiples of a
+    // row's pairs, so each row's pairs are one aligned 8- or 16-byte copy)
+    const int NM = (D / kQuantGroup) * 2;
+    const Strides ms = meta_strides ? *meta_strides
+                                    : Strides{(long long)Hkv * BS * NM, (long long)BS * NM, NM};
+    bool q8_rows = false, codes_head_major = true;
+    if (q8) {
+        if (kv_strides.page % 16 || kv_strides.head % 16 || kv_strides.token % 16)
+            return fail(PGD_ERR_INVALID_ARG,
+                        "code strides (%lld, %lld, %lld) must be multiples of 16 bytes",
+                        kv_strides.page, kv_strides.head, kv_strides.token);
+        const long long mv[3] = {ms.page, ms.head, ms.token};
+        for (long long x : mv)
+            if (x <= 0 || x % NM != 0 || x >= (1ll << 38))
+                return fail(PGD_ERR_INVALID_ARG,
+                            "pair strides (%lld, %lld, %lld) must be positive multiples of %d "
+                            "elements below 2^38",
+                            ms.page, ms.head, ms.token, NM);
+        const Strides hm = head_major(Hkv, BS, D);
+        codes_head_major = kv_strides.page == hm.page && kv_strides.head == hm.head &&
+                           kv_strides.token == hm.token;
+        q8_rows = !codes_head_major || ms.page != (long long)Hkv * BS * NM ||
+                  ms.head != (long long)BS * NM || ms.token != NM;
+    }
     if (!own_workspace && workspace && !aligned(workspace, 256))
         return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     Plan plan;
@@ -687,15 +712,18 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                                : v_at >= k_at ? (long long)(v_at - k_at)
                                               : -(long long)(k_at - v_at);
     const long long gap_abs = code_gap < 0 ? -code_gap : code_gap;
-    const bool q8_pair = q8 && box * D <= 4096 && gap_abs > 0 && gap_abs % 16 == 0 &&
-                         gap_abs < (1ll << 40) && (long long)NB * Hkv < (1ll << 31);
+    const bool q8_pair = q8 && codes_head_major && box * D <= 4096 && gap_abs > 0 &&
+                         gap_abs % 16 == 0 && gap_abs < (1ll << 40) &&
+                         (long long)NB * Hkv < (1ll << 31);
+    // (the pairs' tensor map serves head-major pairs only; at other strides
+    // the kernel copies them row by row)
     if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? (q8_pair ? 4 : 2) : 0, &tk, &tv)) ||
-        (q8 && (st = cache_maps(k_meta, v_meta, geom, box, 3, &tkm, &tvm)))) {
+        (q8 && !q8_rows && (st = cache_maps(k_meta, v_meta, geom, box, 3, &tkm, &tvm)))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
     }
-    const KVMaps maps = {tk, tv, q8 ? tkm : tk, q8 ? tvm : tv};
+    const KVMaps maps = {tk, tv, q8 && !q8_rows ? tkm : tk, q8 && !q8_rows ? tvm : tv};
 
     // claim counter: given (static scratch), this stream's, or a per-call one
     int slot = -1;
@@ -739,6 +767,10 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.k_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(k_meta)) : nullptr;
     p.v_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(v_meta)) : nullptr;
     p.q8_pair = q8_pair ? 1 : 0;
+    p.q8_rows = q8_rows ? 1 : 0;
+    p.meta_page_stride = ms.page;
+    p.meta_head_stride = ms.head;
+    p.meta_token_stride = ms.token;
     p.q8_koff = q8_pair && code_gap < 0 ? box * D : 0;  // the lower array lands first
     p.q8_voff = q8_pair && code_gap < 0 ? 0 : box * D;   // (used for pieces of <= 4 KB)
     p.kv_page_stride = kv_strides.page;
@@ -1168,6 +1200,29 @@ pgd_status paged_gqa_decode_q8_append(float *out, const uint16_t *q, const uint1
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
                num_blocks, head_major(num_kv_heads, block_size, head_dim), nullptr, 0, true,
                nullptr, stream, nullptr, k_new, v_new, true, k_meta, v_meta);
+}
+
+pgd_status paged_gqa_decode_q8_strided(
+    float *out, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_codes,
+    uint16_t *k_meta, uint8_t *v_codes, uint16_t *v_meta, const int32_t *block_tables,
+    const int32_t *seq_lens, float scale, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int partition_size, int max_blocks_per_seq, int num_blocks,
+    int64_t code_page_stride, int64_t code_head_stride, int64_t code_token_stride,
+    int64_t meta_page_stride, int64_t meta_head_stride, int64_t meta_token_stride,
+    void *workspace, size_t workspace_bytes, void *stream)
+{
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(PGD_ERR_INVALID_ARG, "give both k_new and v_new or neither");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(PGD_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (num_seqs > 0 && (!k_meta || !v_meta))
+        return fail(PGD_ERR_INVALID_ARG, "null k_meta / v_meta");
+    const Strides ms = {meta_page_stride, meta_head_stride, meta_token_stride};
+    return run(out, q, k_codes, v_codes, block_tables, seq_lens, scale, num_seqs, num_q_heads,
+               num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
+               num_blocks, {code_page_stride, code_head_stride, code_token_stride}, workspace,
+               workspace_bytes, workspace == nullptr, nullptr, stream, nullptr, k_new, v_new,
+               true, k_meta, v_meta, &ms);
 }
 
 pgd_status paged_kv_quantize(uint8_t *codes, uint16_t *meta, const uint16_t *src,

@@ -153,6 +153,15 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                  : "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (through L1); src_bytes 0 writes
+// zeros and reads nothing.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 // Adds one pending arrival to the barrier's current phase now and performs
 // it once this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)

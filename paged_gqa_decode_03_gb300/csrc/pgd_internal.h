@@ -109,6 +109,10 @@ struct DecodeParams {
     int q8_pair;                  // quantised pages: 1 = one tensor copy brings a page's
                                   //   K and V codes (tmap_k spans both arrays)
     int q8_koff, q8_voff;         //   bytes of K / V codes within a page's pair of slots
+    int q8_rows;                  //   1: the pairs' rows at meta strides (any layout)
+    long long meta_page_stride;   // quantised pages: the pairs of token r of page b,
+    long long meta_head_stride;   //   KV head g start at bf16 element b*page + g*head
+    long long meta_token_stride;  //   + r*token (head-major unless q8_rows)
     long long kv_page_stride;     // cache strides in halves (the copies use the
     long long kv_head_stride;     //   same ones through the tensor maps)
     long long kv_token_stride;

@@ -49,12 +49,13 @@ struct StageHeader {
 // Fused append into quantised pages, by the producer warp before it copies
 // the stage that holds the newest token: the warp quantises the token's K and
 // V rows (quantise_row_warp, the library's quantiser) and writes codes and
-// (scale, bias) pairs into the cache at app_off (bytes of the row's codes;
-// head-major pairs at row app_off / D); the stage's copies then bring them
+// (scale, bias) pairs into the cache (the row's codes at byte app_off, its
+// pairs at bf16 element app_meta); the stage's copies then bring them
 // like every other row.  Each lane orders its writes before the warp's later
 // tensor copies (proxy fence) and load-path copies (the caller's __syncwarp).
 template <int D>
-__device__ __forceinline__ void q8_append_to_cache(long long app_off, const __half *k_new,
+__device__ __forceinline__ void q8_append_to_cache(long long app_off, long long app_meta,
+                                                   const __half *k_new,
                                                    const __half *v_new, void *k_cache,
                                                    void *v_cache, uint16_t *k_meta,
                                                    uint16_t *v_meta, int lane)
@@ -72,9 +73,8 @@ __device__ __forceinline__ void q8_append_to_cache(long long app_off, const __ha
         *reinterpret_cast<uint2 *>(vg) = make_uint2(qv.codes[0], qv.codes[1]);
     }
     if (lane % LPG == 0) {
-        const long long mrow = app_off / D;
-        reinterpret_cast<uint32_t *>(k_meta)[mrow * NGRP + lane / LPG] = qk.pair;
-        reinterpret_cast<uint32_t *>(v_meta)[mrow * NGRP + lane / LPG] = qv.pair;
+        reinterpret_cast<uint32_t *>(k_meta + app_meta)[lane / LPG] = qk.pair;
+        reinterpret_cast<uint32_t *>(v_meta + app_meta)[lane / LPG] = qv.pair;
     }
     fence_proxy_async_global();
 }
@@ -84,7 +84,7 @@ __device__ __forceinline__ void q8_append_to_cache(long long app_off, const __ha
 // in fp32 around exact fp16 tensor-core products of the codes:
 //   s = sum_g scale_g (q_g . code_g) + bias_g sum(q_g)            (QK)
 //   O += sum_t (p_t scale_g(t)) code_t + sum_t p_t bias_g(t)      (PV)
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
 __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     paged_gqa_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
@@ -108,7 +108,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
     constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
     // runs of 512 bytes and more go by tensor copy, shorter ones on the load path
-    constexpr bool META_BY_TMA = PAGE_META >= 512;
+    // (QSTR: the pairs' rows at any strides, copied row by row)
+    constexpr bool META_BY_TMA = PAGE_META >= 512 && !QSTR;
     constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
     constexpr int KV_BYTES = stage_kv_bytes<D, Q8>();
     constexpr int META_BYTES = stage_meta_bytes<D, Q8>();
@@ -283,22 +284,58 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 // (quantised pages: the producer writes the row, quantised,
                 // into the cache while issuing the unit's first stage, ahead
                 // of the last stage's copies that bring it)
-                long long app_off = -1;
+                long long app_off = -1, app_meta = -1;
                 if (app_unit && (st == nst - 1 || (Q8 && QAPP && st == 0))) {
                     const int ja = (L - 1) / BS - pg0;
                     const int ida = __shfl_sync(~0u, ja < 32 ? id0 : id1, ja & 31);
-                    if ((unsigned)ida < (unsigned)p.NB)
+                    if ((unsigned)ida < (unsigned)p.NB) {
                         app_off = ida * p.kv_page_stride + g * p.kv_head_stride +
                                   ((L - 1) % BS) * p.kv_token_stride;
+                        if (Q8)
+                            app_meta = ida * p.meta_page_stride + g * p.meta_head_stride +
+                                       ((L - 1) % BS) * p.meta_token_stride;
+                    }
                 }
                 if constexpr (Q8 && QAPP) {
                     if (app_off >= 0 && st == 0)
-                        q8_append_to_cache<D>(app_off, p.k_new + ((size_t)s * Hkv + g) * D,
+                        q8_append_to_cache<D>(app_off, app_meta,
+                                              p.k_new + ((size_t)s * Hkv + g) * D,
                                               p.v_new + ((size_t)s * Hkv + g) * D, p.k_cache,
                                               p.v_cache, p.k_meta, p.v_meta, lane);
                     __syncwarp();
                 }
-                if constexpr (Q8 && !META_BY_TMA) {
+                if constexpr (Q8 && QSTR) {
+                    // the rows' (scale, bias) pairs at the pairs' strides: one
+                    // 8- or 16-byte copy per row on the load path into the
+                    // page's slot ([row][group]); a page outside the pool
+                    // reads as zeros
+                    for (int r0 = 0; r0 < pc * BOX; r0 += 32) {  // warp-uniform trips
+                        const int i = r0 + lane;
+                        const int jj = min(i / BOX, pc - 1), rr = i % BOX;
+                        const int j = pf + jj;
+                        const int ida = __shfl_sync(~0u, id0, j & 31);
+                        const int idb = __shfl_sync(~0u, id1, j & 31);
+                        const int id = j < 32 ? ida : idb;
+                        if (i < pc * BOX) {
+                            const bool in = (unsigned)id < (unsigned)p.NB;
+                            const long long off = in ? id * p.meta_page_stride +
+                                                           g * p.meta_head_stride +
+                                                           (row0 + rr) * p.meta_token_stride
+                                                     : 0;
+                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT + rr * NGRP * 4;
+                            if constexpr (NGRP * 4 == 16) {
+                                cp_async_16(dm, p.k_meta + off, in ? 16u : 0u);
+                                cp_async_16(dm + META_BYTES, p.v_meta + off, in ? 16u : 0u);
+                            } else {
+                                static_assert(NGRP * 4 == 8, "8 or 16 bytes of pairs per row");
+                                cp_async_8(dm, p.k_meta + off, in ? 8u : 0u);
+                                cp_async_8(dm + META_BYTES, p.v_meta + off, in ? 8u : 0u);
+                            }
+                        }
+                    }
+                    cp_async_mbar_arrive(fb);
+                    __syncwarp();
+                } else if constexpr (Q8 && !META_BY_TMA) {
                     // the rows' (scale, bias) pairs, [row][group] per page
                     // piece: one contiguous run per (page, KV head) of under
                     // 512 bytes, copied by the lanes in 16-byte pieces on the
@@ -1065,7 +1102,7 @@ __global__ void __launch_bounds__(reduce_threads<D>())
 // ---------------------------------------------------------------- launch
 // Raises the partition kernel's dynamic shared-memory limit, once per
 // device and instantiation.
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
 cudaError_t ensure_smem_attribute()
 {
     static std::atomic<unsigned long long> done{0};  // bit per device ordinal < 64
@@ -1076,7 +1113,7 @@ cudaError_t ensure_smem_attribute()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP>,
+    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_smem_bytes<D, Q8>());
     if (e == cudaSuccess)
@@ -1084,11 +1121,11 @@ cudaError_t ensure_smem_attribute()
     return e;
 }
 
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
 cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const LaunchConfig &lc)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP>;
-    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8, QAPP>();
+    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR>;
+    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8, QAPP, QSTR>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -1131,6 +1168,9 @@ cudaError_t launch_decode_bs(bool trace, bool q8, const KVMaps &m, const DecodeP
 {
     if constexpr (D % 128 == 0) {
         if (q8) {
+            if (p.q8_rows)  // quantised pages at any strides (no page trace)
+                return p.k_new ? launch_decode_impl<D, BS, false, true, true, true>(m, p, lc)
+                               : launch_decode_impl<D, BS, false, true, false, true>(m, p, lc);
             if (p.k_new)  // quantised append (no page trace)
                 return launch_decode_impl<D, BS, false, true, true>(m, p, lc);
             return trace ? launch_decode_impl<D, BS, true, true>(m, p, lc)

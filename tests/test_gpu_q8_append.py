@@ -128,3 +128,81 @@ def test_q8_append_groups(Hq, Hkv):
     w = make_custom(S=len(LENS), Hq=Hq, Hkv=Hkv, D=128, BS=16, lens=LENS, seed=Hq + 9,
                     device=DEV, MB=64)
     check_q8_append(w, 512, seed=Hq)
+
+
+def _token_major(t):
+    return t.transpose(1, 2).contiguous()
+
+
+def _padded_rows(t, pad):
+    """Rows padded at their end by ``pad`` elements of all-ones bits."""
+    shp = list(t.shape)
+    flat = t.reshape(shp[0], shp[1], shp[2], -1)
+    fill = 255 if t.dtype == torch.uint8 else -1  # 0xFF codes, 0xFFFF (NaN) pairs
+    out = torch.full(flat.shape[:-1] + (flat.shape[-1] + pad,), fill, dtype=t.dtype,
+                     device=t.device)
+    out[..., :flat.shape[-1]] = flat
+    return out
+
+
+@pytest.mark.parametrize("D,BS", [(128, 16), (256, 8), (256, 32)])
+def test_q8_strided_layouts_equal_head_major(D, BS):
+    """The same caches token-major and with padded rows (pads of 0xFF codes
+    and NaN pairs): bitwise the head-major result, with and without the
+    fused append (the caches afterwards hold the same rows)."""
+    w = make_custom(S=len(LENS), Hq=16, Hkv=2, D=D, BS=BS, lens=LENS, seed=D + BS + 11,
+                    device=DEV, MB=(1024 + BS - 1) // BS)
+    c = make_q8(w)
+    base = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    pgd.paged_gqa_decode_q8(base, w.q, c.k_codes, c.k_meta, c.v_codes, c.v_meta,
+                            w.block_tables, w.seq_lens, w.scale, 512)
+    NB, Hkv, NM = c.k_codes.shape[0], w.Hkv, (D // 64) * 2
+    layouts = {
+        "token_major": ([_token_major(t) for t in (c.k_codes, c.k_meta, c.v_codes, c.v_meta)],
+                        pgd.q8_strides("token_major", Hkv, BS, D)),
+        "padded_rows": ([_padded_rows(c.k_codes, 32), _padded_rows(c.k_meta, NM),
+                         _padded_rows(c.v_codes, 32), _padded_rows(c.v_meta, NM)],
+                        ((Hkv * BS * (D + 32), BS * (D + 32), D + 32),
+                         (Hkv * BS * 2 * NM, BS * 2 * NM, 2 * NM))),
+    }
+    for name, (arrs, (cs, ms)) in layouts.items():
+        out = torch.full_like(base, float("nan"))
+        pgd.paged_gqa_decode_q8_strided(out, w.q, *arrs, w.block_tables, w.seq_lens, w.scale,
+                                        Hkv, BS, NB, cs, ms, 512)
+        torch.cuda.synchronize()
+        assert torch.equal(out, base), name
+    # fused append: head-major against token-major, outputs and caches
+    g = torch.Generator(device=DEV).manual_seed(D + BS)
+    kn = torch.randn((w.S, Hkv, D), generator=g, device=DEV).to(torch.float16)
+    vn = torch.randn((w.S, Hkv, D), generator=g, device=DEV).to(torch.float16)
+    arrs, (cs, ms) = layouts["token_major"]
+    out_t = torch.empty_like(base)
+    pgd.paged_gqa_decode_q8_strided(out_t, w.q, *arrs, w.block_tables, w.seq_lens, w.scale, Hkv,
+                                    BS, NB, cs, ms, 512, k_new=kn, v_new=vn)
+    out_h = torch.empty_like(base)
+    pgd.paged_gqa_decode_q8_append(out_h, w.q, kn, vn, c.k_codes, c.k_meta, c.v_codes, c.v_meta,
+                                   w.block_tables, w.seq_lens, w.scale, 512)
+    torch.cuda.synchronize()
+    assert torch.equal(out_t, out_h)
+    for t_tm, t_hm in zip(arrs, (c.k_codes, c.k_meta, c.v_codes, c.v_meta)):
+        assert torch.equal(t_tm.transpose(1, 2), t_hm)
+    assert pgd.pgd_check_device_error() == 0
+
+
+def test_q8_strided_against_oracle():
+    w = make_custom(S=len(LENS), Hq=32, Hkv=8, D=128, BS=16, lens=LENS, seed=5, device=DEV,
+                    MB=64)
+    c = make_q8(w)
+    arrs = [_token_major(t) for t in (c.k_codes, c.k_meta, c.v_codes, c.v_meta)]
+    cs, ms = pgd.q8_strides("token_major", w.Hkv, w.BS, w.D)
+    NB = c.k_codes.shape[0]
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    pgd.paged_gqa_decode_q8_strided(out, w.q, *arrs, w.block_tables, w.seq_lens, w.scale, w.Hkv,
+                                    w.BS, NB, cs, ms, 256)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle_q8(w, c), "q8 token-major")
+    h = [a.cpu().numpy() for a in arrs]
+    ref = oracle.decode_q8_strided(w.q.cpu().numpy(), h[0], h[1].view(np.uint16), h[2],
+                                   h[3].view(np.uint16), w.block_tables.cpu().numpy(),
+                                   w.seq_lens.cpu().numpy(), w.scale, w.Hkv, w.BS, NB, cs, ms)
+    assert_parity(out.cpu().numpy(), ref, "q8 token-major, strided oracle")
