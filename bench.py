@@ -283,8 +283,6 @@ def run_ours(args):
     q8 = None
     if args.kv == "q8":  # the same workload over quantised pages (codes + bf16 pairs)
         from paged_gqa_decode_03_gb300.workloads import make_q8
-        if args.layout != "head_major":
-            raise SystemExit("--kv q8 runs over head-major pages only")
         q8 = make_q8(w)
         kv_bytes = int(w.lens.sum()) * w.Hkv * 2 * (w.D + (w.D // 64) * 4)
         alg_bytes = kv_bytes + w.S * w.Hq * w.D * (2 + 4) + int(w.page_offsets[-1]) * 4
@@ -292,7 +290,16 @@ def run_ours(args):
         gen = torch.Generator(device=dev).manual_seed(7)
         k_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
         v_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
-    if q8 is not None and args.append:
+    if q8 is not None and args.layout != "head_major":
+        # the quantised caches in another layout, through the strided entry point
+        cs, ms = pgd.q8_strides(args.layout, w.Hkv, w.BS, w.D)
+        arrs = [t.transpose(1, 2).contiguous() for t in (q8.k_codes, q8.k_meta, q8.v_codes,
+                                                          q8.v_meta)]
+
+        def call(q, bt, sl):
+            pgd.paged_gqa_decode_q8_strided(out, q, *arrs, bt, sl, w.scale, w.Hkv, w.BS, w.NB,
+                                            cs, ms, P, k_new=k_new, v_new=v_new, stream=stream)
+    elif q8 is not None and args.append:
         def call(q, bt, sl):
             pgd.paged_gqa_decode_q8_append(out, q, k_new, v_new, q8.k_codes, q8.k_meta,
                                            q8.v_codes, q8.v_meta, bt, sl, w.scale, P,
