@@ -46,9 +46,12 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "efd15f02f6df6b52": {("batch_decode_q8", 512): 336_721_920 + 4_054_016},
+    "8ff1b9df9bd74504": {("batch_decode", 512): 633_324_544 + 5_478_656,
+                         ("batch_decode_q8", 512): 336_721_408 + 3_765_760,
+                         ("ragged_tails", 256): 888_202_240 + 6_766_848,
+                         ("long_context", 512): 1_293_075_968 + 7_435_008},
     # the several-query-token kernels (hash of all sources)
-    "b3aa7256cb0eaa62": {("chunked_prefill", 8320): 280_806_144 + 13_987_840},
+    "af0ca759d8a11d4c": {("chunked_prefill", 8320): 286_897_664 + 13_862_400},
 }
 
 
@@ -638,7 +641,11 @@ def run_varlen_bench(args):
                     "peak_source": "measured (MEASURED_PEAKS hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg_bytes}
             e2e_val = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
-        roof.update(kernel="paged_varlen_kernel", kernel_ms=kern_ms)
+        # which kernel the library runs: pairs of query tiles at head_dim 64 /
+        # 128 when a sequence may hold more than one tile (128 / G query tokens)
+        pairs = w.D <= 128 and w.max_q_len > 128 // (w.Hq // w.Hkv)
+        roof.update(kernel="paged_varlen_pair_kernel" if pairs else "paged_varlen_kernel",
+                    kernel_ms=kern_ms)
         line = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
