@@ -96,6 +96,34 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     uint8_t *const kv_ptr = base_ptr + 128 * D * 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // ---- producers' page-table reads, and warp 0's Q and first K copies, go
+    // out before the CTA-wide set-up completes: their latency overlaps the
+    // tensor-memory allocation and the barrier
+    const bool is_v = warp == kVWarp;
+    const int npages = (L + p.BS - 1) >> p.log2BS;
+    const int32_t *bt = p.block_tables + (size_t)s * p.MB;
+    // one copy per page of the stage (a piece of NT rows when pages are
+    // longer): lane c issues copy c, of the 8-row groups of that page
+    const int copies = p.BS <= NT ? NT >> p.log2BS : 1;
+    const int groups = (p.BS <= NT ? p.BS : NT) / 8;
+    auto block_of = [&](int jj) -> int {  // block coordinate of lane's page, -1: none
+        const int pg = (((j0 + jj) * NT) >> p.log2BS) + lane;
+        int b = -1;
+        if (lane < copies && pg < npages) {
+            const int id = __ldg(bt + pg);
+            if ((unsigned)id < (unsigned)p.NB)
+                b = id * p.blk_page + g * p.blk_head;
+            else if (!is_v)
+                atomicOr(p.err, kErrPageRange);  // wholly outside: the copy reads zeros
+        }
+        return b;
+    };
+    auto grp_of = [&](int jj) {  // first 8-row group of stage jj inside its page
+        return p.BS <= NT ? 0 : (((j0 + jj) * NT) & (p.BS - 1)) >> 3;
+    };
+    int blk_next = -1;
+    if (warp == 0 || is_v)
+        blk_next = block_of(0);
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&q_full), 1);
         for (int i = 0; i < NSTG; ++i) {
@@ -111,6 +139,22 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         mbar_init(smem_addr(&mma_done), 1);
         abort_flag = 0;
         fence_mbar_init();
+    }
+    if (warp == 0) {
+        __syncwarp();  // lane 0's barrier set-up before the other lanes' copies
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_q);
+            mbar_arrive_expect_tx(smem_addr(&q_full), SLABS * p.TQ * p.G * 128);
+            for (int sl = 0; sl < SLABS; ++sl)
+                tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
+                            smem_addr(&q_full));
+            mbar_arrive_expect_tx(smem_addr(&k_full[0]), KV_TILE);  // stage 0's K
+        }
+        __syncwarp();
+        if (lane < copies)
+            tma_load_5d(kv_s + lane * groups * GROUP, &tmap_k, 0, 0, 0, grp_of(0), blk_next,
+                        smem_addr(&k_full[0]), l2_evict_first_policy());
     }
     if (warp == 1)
         tc_alloc(smem_addr(&tmem_base_s), kVarlenTmemCols);
@@ -128,50 +172,26 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 
     if (warp == 0 || warp == kVWarp) {
         // ============================================================ producers
-        // warp 0: the Q tile, then K of every stage; warp 10: V of every
-        // stage (the two rings refill independently: K is free again after
-        // S, V only after P V)
-        const bool is_v = warp == kVWarp;
+        // warp 0: the Q tile, then K of every stage (Q and stage 0's K were
+        // issued before the set-up barrier); warp 10: V of every stage (the
+        // two rings refill independently: K is free again after S, V only
+        // after P V)
         const uint64_t pol = l2_evict_first_policy();
-        if (lane == 0) {
-            prefetch_tensormap(is_v ? &tmap_v : &tmap_k);
-            if (!is_v) {
-                prefetch_tensormap(&tmap_q);
-                mbar_arrive_expect_tx(smem_addr(&q_full), SLABS * p.TQ * p.G * 128);
-                for (int sl = 0; sl < SLABS; ++sl)
-                    tma_load_4d(q_s + sl * Q_SLAB, &tmap_q, 0, g * p.G, row0 + i0, sl,
-                                smem_addr(&q_full));
-            }
-        }
+        if (lane == 0 && is_v)
+            prefetch_tensormap(&tmap_v);
         const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
         uint64_t *full = is_v ? v_full : k_full;
         uint64_t *empty = is_v ? v_empty : k_empty;
-        const int npages = (L + p.BS - 1) >> p.log2BS;
-        const int32_t *bt = p.block_tables + (size_t)s * p.MB;
-        // one copy per page of the stage (a piece of NT rows when pages are
-        // longer): lane c issues copy c, of the 8-row groups of that page
-        const int copies = p.BS <= NT ? NT >> p.log2BS : 1;
-        const int groups = (p.BS <= NT ? p.BS : NT) / 8;
-        auto block_of = [&](int jj) -> int {  // block coordinate of lane's page, -1: none
-            const int pg = (((j0 + jj) * NT) >> p.log2BS) + lane;
-            int b = -1;
-            if (lane < copies && pg < npages) {
-                const int id = __ldg(bt + pg);
-                if ((unsigned)id < (unsigned)p.NB)
-                    b = id * p.blk_page + g * p.blk_head;
-                else if (!is_v)
-                    atomicOr(p.err, kErrPageRange);  // wholly outside: the copy reads zeros
-            }
-            return b;
-        };
-        int issued = 0;
-        int blk_next = block_of(0);
-        for (int jj = 0; jj < ntiles; ++jj, ++issued) {
+        const int jstart = is_v ? 0 : 1;
+        int issued = jstart;
+        if (!is_v)
+            blk_next = ntiles > 1 ? block_of(1) : -1;
+        for (int jj = jstart; jj < ntiles; ++jj, ++issued) {
             const int st = jj % NSTG;
             const int blk = blk_next;
             if (jj + 1 < ntiles)
                 blk_next = block_of(jj + 1);  // in flight while this stage waits
-            const int grp0 = p.BS <= NT ? 0 : (((j0 + jj) * NT) & (p.BS - 1)) >> 3;
+            const int grp0 = grp_of(jj);
             const uint32_t dst =
                 kv_s + st * 2 * KV_TILE + (is_v ? KV_TILE : 0) + lane * groups * GROUP;
             bool w = true;
