@@ -280,6 +280,31 @@ pgd_status encode_meta_map(CUtensorMap *map, const void *base, const CacheGeom &
     return PGD_OK;
 }
 
+// Both (scale, bias) pair arrays in one map (head-major): the pairs of a
+// (page, head) block x blocks (page * Hkv + head) x 2 arrays, the array
+// stride being the distance between them (`lo` the lower one); a box of
+// box_rows rows x 1 x 2 lands a piece's pairs of both arrays side by side.
+pgd_status encode_meta_pair_map(CUtensorMap *map, const void *lo, long long pair_stride,
+                                const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    const int ng = g.D / kQuantGroup;
+    cuuint64_t dims[3] = {(cuuint64_t)g.BS * ng, (cuuint64_t)g.NB * g.Hkv, 2};
+    cuuint64_t strides[2] = {(cuuint64_t)g.BS * ng * 4, (cuuint64_t)pair_stride};
+    cuuint32_t box[3] = {(cuuint32_t)(box_rows * ng), 1, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(lo), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (scale pair) failed (CUresult %d)",
+                    (int)r);
+    return PGD_OK;
+}
+
 // The cache viewed for the multi-token kernel, innermost first:
 //   64 halves x 8 token rows (token stride) x D/64 slabs (128 bytes)
 //   x BS/8 row groups (8 token strides) x blocks (u halves),
@@ -426,7 +451,8 @@ thread_local int t_maps_used = 0, t_maps_next = 0;
 // kind 0: the decode view (box = rows per copy); kind 1: the page-group view
 // (box = 8-row groups per copy); kind 2: quantised codes, kind 3: their
 // (scale, bias) pairs (box = rows per copy); kind 4: both code arrays in one
-// map (*tk = *tv, based at the lower array).
+// map, kind 5: both pair arrays in one map (*tk = *tv, based at the lower
+// array).
 pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int box, int kind,
                       const CUtensorMap **tk, const CUtensorMap **tv)
 {
@@ -445,10 +471,11 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
-    if (kind == 4) {
+    if (kind == 4 || kind == 5) {
         const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
         const long long stride = (long long)(ka < va ? va - ka : ka - va);
-        if ((st = encode_code_pair_map(&c.tk, ka < va ? k : v, stride, geom, box))) {
+        if ((st = kind == 4 ? encode_code_pair_map(&c.tk, ka < va ? k : v, stride, geom, box)
+                            : encode_meta_pair_map(&c.tk, ka < va ? k : v, stride, geom, box))) {
             c.k = c.v = nullptr;
             return st;
         }
@@ -466,7 +493,7 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
             return encode_meta_map(m, base, geom, box);
         }
     };
-    if (kind != 4 && ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v)))) {
+    if (kind != 4 && kind != 5 && ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v)))) {
         c.k = c.v = nullptr;
         return st;
     }
@@ -716,9 +743,20 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                          gap_abs % 16 == 0 && gap_abs < (1ll << 40) &&
                          (long long)NB * Hkv < (1ll << 31);
     // (the pairs' tensor map serves head-major pairs only; at other strides
-    // the kernel copies them row by row)
+    // the kernel copies them row by row).  One copy for both pair arrays
+    // under the same conditions, where a piece's pairs fill whole 128-byte
+    // runs (the kernel then keeps a piece's K and V pairs side by side)
+    const uintptr_t km_at = reinterpret_cast<uintptr_t>(k_meta),
+                    vm_at = reinterpret_cast<uintptr_t>(v_meta);
+    const long long meta_gap = km_at < vm_at ? (long long)(vm_at - km_at) : (long long)(km_at - vm_at);
+    const int q8_meta_pair = q8 && !q8_rows && (box * (D / kQuantGroup) * 4) % 128 == 0 &&
+                                     meta_gap > 0 && meta_gap % 16 == 0 && meta_gap < (1ll << 40) &&
+                                     (long long)NB * Hkv < (1ll << 31)
+                                 ? (km_at < vm_at ? 1 : 2)
+                                 : 0;
     if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? (q8_pair ? 4 : 2) : 0, &tk, &tv)) ||
-        (q8 && !q8_rows && (st = cache_maps(k_meta, v_meta, geom, box, 3, &tkm, &tvm)))) {
+        (q8 && !q8_rows &&
+         (st = cache_maps(k_meta, v_meta, geom, box, q8_meta_pair ? 5 : 3, &tkm, &tvm)))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
@@ -767,6 +805,7 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.k_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(k_meta)) : nullptr;
     p.v_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(v_meta)) : nullptr;
     p.q8_pair = q8_pair ? 1 : 0;
+    p.q8_meta_pair = q8_meta_pair;
     p.q8_rows = q8_rows ? 1 : 0;
     p.meta_page_stride = ms.page;
     p.meta_head_stride = ms.head;

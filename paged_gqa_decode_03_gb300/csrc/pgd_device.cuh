@@ -162,6 +162,27 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// Lane-predicated forms of a counter increment and a read-only load whose
+// results are waited for only where they are read (a plain conditional
+// assignment of the result can make the warp wait for it on the spot).
+__device__ __forceinline__ void atomic_add_if(bool pred, unsigned *addr, unsigned v, unsigned &out)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+                 "@p atom.global.add.u32 %0, [%1], %3;\n\t}"
+                 : "+r"(out)
+                 : "l"(addr), "r"((unsigned)pred), "r"(v)
+                 : "memory");
+}
+__device__ __forceinline__ int ldg_if(bool pred, const int32_t *addr)
+{
+    int v;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\tmov.b32 %0, 0;\n\t"
+                 "@p ld.global.nc.b32 %0, [%1];\n\t}"
+                 : "=r"(v)
+                 : "l"(addr), "r"((unsigned)pred));
+    return v;
+}
+
 // Adds one pending arrival to the barrier's current phase now and performs
 // it once this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
@@ -169,8 +190,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) accesses to the same memory.
 // Orders this thread's generic-proxy global-memory writes before later
 // async-proxy (TMA) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_global()
@@ -178,6 +197,8 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

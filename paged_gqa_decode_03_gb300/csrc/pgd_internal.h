@@ -38,7 +38,8 @@ constexpr int kMaxTailStages = 16;
 template <int D> struct Shape;
 // T8 / NC8 / NS8: the same for quantised pages, whose consumers do more work
 // per byte (code conversion, the affine terms): twice the tokens and
-// consumer warps per stage, fewer stages (about the same bytes in flight).
+// consumer warps per stage, fewer stages (one more where the page size
+// leaves room: ring_stages).
 template <> struct Shape<64> {
     static constexpr int T = 64, NC = 4, NS = 6, T8 = 64, NC8 = 4, NS8 = 6;
 };
@@ -62,30 +63,42 @@ template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_kv_byt
     return stage_tokens_of<D, Q8>() * D * (Q8 ? 1 : 2);
 }
 // (scale, bias) pairs of one copied page piece, padded so every piece lands
-// 128-byte aligned (a tensor-copy requirement); the stage reserves room for
-// the worst case, 8-row pages.
+// 128-byte aligned (a tensor-copy requirement).
 __host__ __device__ constexpr int meta_slot_bytes(int rows, int D)
 {
     return (rows * (D / kQuantGroup) * 4 + 127) / 128 * 128;
 }
-template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_meta_bytes()
+// The pairs of one stage: one slot per page piece of min(BS, T) rows.
+template <int D, bool Q8, int BS> __host__ __device__ constexpr int stage_meta_bytes()
 {
-    return Q8 ? (stage_tokens_of<D, Q8>() / 8) * meta_slot_bytes(8, D) : 0;
+    constexpr int T = stage_tokens_of<D, Q8>(), BOX = BS < T ? BS : T;
+    return Q8 ? (T / BOX) * meta_slot_bytes(BOX, D) : 0;
 }
 template <int D> __host__ __device__ constexpr int stage_q_bytes() { return kMaxGroup * D * 2; }
-template <int D, bool Q8 = false> __host__ __device__ constexpr int stage_bytes()
+template <int D, bool Q8, int BS> __host__ __device__ constexpr int stage_bytes()
 {
-    return 2 * stage_kv_bytes<D, Q8>() + 2 * stage_meta_bytes<D, Q8>() + stage_q_bytes<D>();
+    return 2 * stage_kv_bytes<D, Q8>() + 2 * stage_meta_bytes<D, Q8, BS>() + stage_q_bytes<D>();
 }
-template <int D, bool Q8 = false> __host__ __device__ constexpr int ring_stages()
+// Shared memory of one SM, and what a CTA needs beside its ring (the
+// system's 1 KB, the static barriers and stage headers, the alignment slack).
+constexpr int kSmemPerSM = 233472;
+constexpr int kSmemPerCtaExtra = 1024 + 3072 + 1024;
+// Quantised pages take a third stage where two CTAs per SM still fit (the
+// consumers hold a stage longer per byte than with fp16 pages, so more
+// bytes must be in flight per stage held).
+template <int D, bool Q8, int BS> __host__ __device__ constexpr int ring_stages()
 {
-    return Q8 ? Shape<D>::NS8 : Shape<D>::NS;
+    if constexpr (!Q8)
+        return Shape<D>::NS;
+    return 2 * ((Shape<D>::NS8 + 1) * stage_bytes<D, Q8, BS>() + kSmemPerCtaExtra) <= kSmemPerSM
+               ? Shape<D>::NS8 + 1
+               : Shape<D>::NS8;
 }
 // Dynamic shared memory: the ring plus slack to align it to 1024 bytes
 // (required by the 128-byte swizzle of the tensor copies).
-template <int D, bool Q8 = false> __host__ __device__ constexpr size_t dyn_smem_bytes()
+template <int D, bool Q8, int BS> __host__ __device__ constexpr size_t dyn_smem_bytes()
 {
-    return size_t(ring_stages<D, Q8>()) * stage_bytes<D, Q8>() + 1024;
+    return size_t(ring_stages<D, Q8, BS>()) * stage_bytes<D, Q8, BS>() + 1024;
 }
 
 struct DecodeParams {
@@ -108,6 +121,9 @@ struct DecodeParams {
                                   //   append), or null
     int q8_pair;                  // quantised pages: 1 = one tensor copy brings a page's
                                   //   K and V codes (tmap_k spans both arrays)
+    int q8_meta_pair;             // one tensor copy brings a page's K and V (scale,
+                                  //   bias) pairs (tmap_km spans both arrays): 1 with
+                                  //   K's array the lower, 2 with V's; 0: two copies
     int q8_koff, q8_voff;         //   bytes of K / V codes within a page's pair of slots
     int q8_rows;                  //   1: the pairs' rows at meta strides (any layout)
     long long meta_page_stride;   // quantised pages: the pairs of token r of page b,

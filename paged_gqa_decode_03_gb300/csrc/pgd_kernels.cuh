@@ -9,9 +9,11 @@
 //    and claims the next from a counter shortly before it has issued the
 //    current one, so that slower CTAs take fewer units.
 //      * producer warp: loads the unit's page-table entries with one
-//        coalesced warp load, broadcasts each physical page id with a warp
-//        shuffle, and issues one TMA tensor copy of the page's K rows and one
-//        of its V rows (5-D map over 64 halves x page rows x 128-byte slabs x
+//        coalesced warp load, hands page j of a stage to lane j with a warp
+//        shuffle, and the lanes issue together (one warp-wide instruction
+//        per array: issued one by one from a single lane, the copies capped
+//        the producer's rate) one TMA tensor copy of the page's K rows and
+//        one of its V rows (5-D map over 64 halves x page rows x 128-byte slabs x
 //        KV heads x pages, strides from the caller's cache layout; box: the
 //        rows of one page and head, so each slab lands 128-byte swizzled;
 //        evict-first) plus one bulk copy of the group's queries, into a ring
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                              const DecodeParams p)
 {
     constexpr int T = stage_tokens_of<D, Q8>(), NC = consumer_warps<D, Q8>();
-    constexpr int NS = ring_stages<D, Q8>();
+    constexpr int NS = ring_stages<D, Q8, BS>();
     constexpr int ROWB = D * (Q8 ? 1 : 2); // bytes of one cached row
     constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
     constexpr int BOX = BS < T ? BS : T;   // rows per tensor copy
@@ -107,14 +109,21 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     constexpr int NGRP = D / kQuantGroup;  // quantisation groups of a row
     constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
     constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
-    // runs of 512 bytes and more go by tensor copy, shorter ones on the load path
-    // (QSTR: the pairs' rows at any strides, copied row by row)
-    constexpr bool META_BY_TMA = PAGE_META >= 512 && !QSTR;
+    // the pairs of a page piece go by one tensor copy per array (QSTR: the
+    // pairs' rows at any strides, copied row by row on the load path)
+    constexpr bool META_BY_TMA = !QSTR;
     constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
     constexpr int KV_BYTES = stage_kv_bytes<D, Q8>();
-    constexpr int META_BYTES = stage_meta_bytes<D, Q8>();
+    constexpr int META_BYTES = stage_meta_bytes<D, Q8, BS>();
+    // a piece's pairs of K and V side by side where they fill whole 128-byte
+    // runs (one tensor copy over both pair arrays can then bring them:
+    // q8_meta_pair), otherwise K's slots from the stage's pair area and V's
+    // META_BYTES after
+    constexpr bool MPAIRED = Q8 && META_BY_TMA && PAGE_META % 128 == 0;
+    constexpr int MSTR = MPAIRED ? 2 * PAGE_META : META_SLOT;  // piece to piece
+    constexpr int MVOFF = MPAIRED ? PAGE_META : META_BYTES;    // V's pairs after K's
     constexpr int Q_OFF = 2 * KV_BYTES + 2 * META_BYTES;  // the group's queries in a stage
-    constexpr int STAGE = stage_bytes<D, Q8>();
+    constexpr int STAGE = stage_bytes<D, Q8, BS>();
     constexpr int OST = D + 4;             // merge buffer row stride (floats)
     static_assert(NC * 16 == T, "one 16-token tile per consumer warp per stage");
     static_assert(BS <= T ? (T % BS == 0) : (BS % T == 0), "stage/page sizes");
@@ -122,6 +131,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     static_assert(NC * kMaxGroup * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
     static_assert(!Q8 || (D % 128 == 0), "quantised pages: rows of whole 128-byte slabs");
     static_assert(!Q8 || (T / BOX) * META_SLOT <= META_BYTES, "scale slots fit the stage");
+    static_assert(!MPAIRED || (T / BOX) * MSTR <= 2 * META_BYTES, "paired slots fit the stage");
 
     extern __shared__ uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t full_bar[NS];
@@ -239,15 +249,25 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
         // Next unit index: units 0 .. grid-1 are the CTAs' first units; the
         // rest are claimed from the counter, late (two stages before the
         // current unit is fully issued) so that a slow CTA holds little
-        // unstarted work at the end.
+        // unstarted work at the end.  The counter's answer is read one stage
+        // later (its latency overlaps that stage's copies), and before the
+        // unit's last stage the next unit is decoded and its page-table
+        // loads issued (before_last), so that they too overlap copies.
         long long claimed = -1;
-        auto claim = [&]() {
-            unsigned u = 0;
-            if (lane == 0)
-                u = atomicAdd(p.counter, 1u);
-            claimed = (long long)__shfl_sync(~0u, u, 0) + gridDim.x;
+        unsigned claim_raw = 0;
+        bool claim_sent = false;
+        auto claim_send = [&]() {
+            atomic_add_if(lane == 0, p.counter, 1u, claim_raw);
+            claim_sent = true;
         };
-        auto produce = [&](int s, int g, int pi, int L, int id0, int id1) -> bool {
+        auto claim = [&]() {
+            if (!claim_sent)
+                claim_send();
+            claimed = (long long)__shfl_sync(~0u, claim_raw, 0) + gridDim.x;
+            claim_sent = false;
+        };
+        auto produce = [&](int s, int g, int pi, int L, int id0, int id1,
+                           auto &&before_last) -> bool {
             const int tok0 = pi * P;
             const int n = min(P, L - tok0);
             const int pg0 = tok0 / BS;
@@ -257,8 +277,10 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             // last partition) carries it
             const bool app_unit = p.k_new != nullptr && pi == (L - 1) / P;
             for (int st = 0; st < nst; ++st, ++k) {
-                if (claimed < 0 && nst - st <= 2)
-                    claim();
+                if (claimed < 0 && !claim_sent && nst - st <= 2)
+                    claim_send();
+                if (st == nst - 1)
+                    before_last();
                 const int slot = k % NS;
                 bool w = true;
                 if (lane == 0)
@@ -322,48 +344,19 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                                                            g * p.meta_head_stride +
                                                            (row0 + rr) * p.meta_token_stride
                                                      : 0;
-                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT + rr * NGRP * 4;
+                            const uint32_t dm = sb + 2 * KV_BYTES + jj * MSTR + rr * NGRP * 4;
                             if constexpr (NGRP * 4 == 16) {
                                 cp_async_16(dm, p.k_meta + off, in ? 16u : 0u);
-                                cp_async_16(dm + META_BYTES, p.v_meta + off, in ? 16u : 0u);
+                                cp_async_16(dm + MVOFF, p.v_meta + off, in ? 16u : 0u);
                             } else {
                                 static_assert(NGRP * 4 == 8, "8 or 16 bytes of pairs per row");
                                 cp_async_8(dm, p.k_meta + off, in ? 8u : 0u);
-                                cp_async_8(dm + META_BYTES, p.v_meta + off, in ? 8u : 0u);
+                                cp_async_8(dm + MVOFF, p.v_meta + off, in ? 8u : 0u);
                             }
                         }
                     }
                     cp_async_mbar_arrive(fb);
                     __syncwarp();
-                } else if constexpr (Q8 && !META_BY_TMA) {
-                    // the rows' (scale, bias) pairs, [row][group] per page
-                    // piece: one contiguous run per (page, KV head) of under
-                    // 512 bytes, copied by the lanes in 16-byte pieces on the
-                    // load path (the tensor-copy unit takes about as long per
-                    // copy whatever its size, and at 16-row pages these
-                    // copies would double its count); a page outside the
-                    // pool reads as zeros.  Each lane's arrival on the
-                    // stage's barrier waits for its copies.
-                    constexpr int CH = PAGE_META / 16;  // pieces per page
-                    static_assert(PAGE_META % 16 == 0, "16-byte pieces");
-                    for (int r0 = 0; r0 < pc * CH; r0 += 32) {
-                        const int idx = r0 + lane;
-                        const int jj = min(idx / CH, pc - 1), c = idx % CH;
-                        const int j = pf + jj;
-                        const int ida = __shfl_sync(~0u, id0, j & 31);
-                        const int idb = __shfl_sync(~0u, id1, j & 31);
-                        const int id = j < 32 ? ida : idb;
-                        if (idx < pc * CH) {
-                            const bool in = (unsigned)id < (unsigned)p.NB;
-                            const size_t off =
-                                in ? ((((size_t)id * Hkv + g) * BS + row0) * NGRP * 2 + c * 8) : 0;
-                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT + c * 16;
-                            cp_async_16(dm, p.k_meta + off, in ? 16u : 0u);
-                            cp_async_16(dm + META_BYTES, p.v_meta + off, in ? 16u : 0u);
-                        }
-                    }
-                    cp_async_mbar_arrive(fb);
-                    __syncwarp();  // every lane's arrival counted before the producer's own
                 }
                 if (lane == 0) {
                     hdr[slot].s = s;
@@ -377,10 +370,17 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                                            (st == 0 ? G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
-                for (int jj = 0; jj < pc; ++jj) {
+                // lane jj issues the copies of the stage's page jj: one
+                // warp-wide instruction per array for all the stage's pages
+                // (after lane 0's expected-bytes update)
+                __syncwarp();
+                {
+                    const int jj = lane;
                     const int j = pf + jj;
-                    const int id = __shfl_sync(~0u, j < 32 ? id0 : id1, j & 31);
-                    if (lane == 0) {
+                    const int ida = __shfl_sync(~0u, id0, j & 31);
+                    const int idb = __shfl_sync(~0u, id1, j & 31);
+                    const int id = j < 32 ? ida : idb;
+                    if (jj < pc) {
                         int c_page = id;
                         if ((unsigned)id >= (unsigned)p.NB) {
                             atomicOr(p.err, kErrPageRange);
@@ -406,10 +406,15 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                             tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
                         }
                         if (Q8 && META_BY_TMA) {  // the rows' (scale, bias) pairs
-                            const uint32_t dm = sb + 2 * KV_BYTES + jj * META_SLOT;
-                            tma_load_3d(dm, &tmap_km, row0 * NGRP, g, c_page, fb, pol);
-                            tma_load_3d(dm + META_BYTES, &tmap_vm, row0 * NGRP, g, c_page, fb,
-                                        pol);
+                            const uint32_t dm = sb + 2 * KV_BYTES + jj * MSTR;
+                            if (MPAIRED && p.q8_meta_pair) {  // both arrays' pairs in one copy
+                                tma_load_3d(dm, &tmap_km, row0 * NGRP,
+                                            c_page < 0 ? -1 : c_page * Hkv + g, 0, fb, pol);
+                            } else {
+                                tma_load_3d(dm, &tmap_km, row0 * NGRP, g, c_page, fb, pol);
+                                tma_load_3d(dm + MVOFF, &tmap_vm, row0 * NGRP, g, c_page, fb,
+                                            pol);
+                            }
                         }
                     }
                 }
@@ -426,8 +431,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             const int tok0 = pi * P;
             const int npages = (min(P, L - tok0) + BS - 1) / BS;
             const int32_t *bt = p.block_tables + (size_t)s * MB + tok0 / BS;
-            id0 = lane < npages ? __ldg(bt + lane) : 0;
-            id1 = lane + 32 < npages ? __ldg(bt + 32 + lane) : 0;
+            id0 = ldg_if(lane < npages, bt + lane);
+            id1 = ldg_if(lane + 32 < npages, bt + 32 + lane);
         };
 
         // clamped length of sequence s (< S)
@@ -516,16 +521,32 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
         bool has = decode(blockIdx.x, cs, cg, cpi, cL);
         if (has)
             load_ids(cs, cpi, cL, cid0, cid1);
-        while (has && ok) {
-            claimed = -1;
-            ok = produce(cs, cg, cpi, cL, cid0, cid1);
-            if (!ok)
-                break;
+        // the next unit (claimed, decoded, its page ids loading)
+        int ns_ = 0, ng_ = 0, npi_ = 0, nL_ = 0, nid0 = 0, nid1 = 0;
+        bool nhas = false, next_ready = false;
+        auto next_unit = [&]() {
             if (claimed < 0)
                 claim();
-            has = decode(claimed, cs, cg, cpi, cL);
-            if (has)
-                load_ids(cs, cpi, cL, cid0, cid1);
+            nhas = decode(claimed, ns_, ng_, npi_, nL_);
+            if (nhas)
+                load_ids(ns_, npi_, nL_, nid0, nid1);
+            next_ready = true;
+        };
+        while (has && ok) {
+            claimed = -1;
+            next_ready = false;
+            ok = produce(cs, cg, cpi, cL, cid0, cid1, next_unit);
+            if (!ok)
+                break;
+            if (!next_ready)
+                next_unit();
+            has = nhas;
+            cs = ns_;
+            cg = ng_;
+            cpi = npi_;
+            cL = nL_;
+            cid0 = nid0;
+            cid1 = nid1;
         }
         if (ok) {  // end-of-work marker
             const int slot = k % NS;
@@ -734,12 +755,14 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 d2 = c[0][2] + c[1][2];
                 d3 = c[0][3] + c[1][3];
             } else {
-                const uint8_t *kmeta = sp + 2 * KV_BYTES;
+                // (q8_meta_pair 2: the pair arrays' copy landed V's pairs first)
+                const uint8_t *kmeta =
+                    sp + 2 * KV_BYTES + (MPAIRED && p.q8_meta_pair == 2 ? PAGE_META : 0);
                 const int ra = t0 + gb, rb = ra + 8;
                 const uint32_t *kma = reinterpret_cast<const uint32_t *>(
-                    kmeta + (ra / BOX) * META_SLOT + (ra % BOX) * NGRP * 4);
+                    kmeta + (ra / BOX) * MSTR + (ra % BOX) * NGRP * 4);
                 const uint32_t *kmb = reinterpret_cast<const uint32_t *>(
-                    kmeta + (rb / BOX) * META_SLOT + (rb % BOX) * NGRP * 4);
+                    kmeta + (rb / BOX) * MSTR + (rb % BOX) * NGRP * 4);
                 d0 = d1 = d2 = d3 = 0.f;
 #pragma unroll
                 for (int gi = 0; gi < NGRP; ++gi) {
@@ -804,12 +827,13 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 // per group: P scaled by the V rows' scales as the B operand,
                 // the biases into beta; V^T fragments from two codes
                 // (d = 16i + 2gb, +1) of tokens tq, tq+1, tq+8, tq+9
-                const uint8_t *vmeta = sp + 2 * KV_BYTES + META_BYTES;
+                const uint8_t *vmeta =
+                    sp + 2 * KV_BYTES + (MPAIRED && p.q8_meta_pair == 2 ? 0 : MVOFF);
                 const int ra = t0 + gb, rb = ra + 8;
                 const uint32_t *vma = reinterpret_cast<const uint32_t *>(
-                    vmeta + (ra / BOX) * META_SLOT + (ra % BOX) * NGRP * 4);
+                    vmeta + (ra / BOX) * MSTR + (ra % BOX) * NGRP * 4);
                 const uint32_t *vmb = reinterpret_cast<const uint32_t *>(
-                    vmeta + (rb / BOX) * META_SLOT + (rb % BOX) * NGRP * 4);
+                    vmeta + (rb / BOX) * MSTR + (rb % BOX) * NGRP * 4);
                 uint32_t bf[NGRP][2];
 #pragma unroll
                 for (int gi = 0; gi < NGRP; ++gi) {
@@ -1115,7 +1139,7 @@ cudaError_t ensure_smem_attribute()
         return cudaSuccess;
     e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dyn_smem_bytes<D, Q8>());
+                             (int)dyn_smem_bytes<D, Q8, BS>());
     if (e == cudaSuccess)
         done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
@@ -1131,7 +1155,7 @@ cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const Lau
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(lc.grid);
     cfg.blockDim = dim3((consumer_warps<D, Q8>() + 1) * 32);
-    cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8>();
+    cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8, BS>();
     cfg.stream = lc.stream;
     if (lc.ev_before && (e = cudaEventRecord(lc.ev_before, lc.stream)) != cudaSuccess)
         return e;
@@ -1159,7 +1183,7 @@ cudaError_t occupancy_impl(int *ctas)
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas, kern, (consumer_warps<D, Q8>() + 1) * 32, dyn_smem_bytes<D, Q8>());
+        ctas, kern, (consumer_warps<D, Q8>() + 1) * 32, dyn_smem_bytes<D, Q8, BS>());
 }
 
 template <int D, int BS>

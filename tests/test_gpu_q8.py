@@ -95,9 +95,10 @@ def test_repeated_calls_identical():
 
 
 def test_code_arrays_in_either_order_or_shared():
-    """One tensor copy brings a page's K and V codes when both arrays fit one
-    map: with V below K in memory the codes land in the other order; with K
-    and V the same array they cannot share a map and go by two copies."""
+    """One tensor copy brings a page's K and V codes (and one their (scale,
+    bias) pairs) when both arrays fit one map: with V below K in memory they
+    land in the other order; with K and V the same array they cannot share a
+    map and go by two copies."""
     w = make_custom(S=len(LENS), Hq=32, Hkv=8, D=128, BS=16, lens=LENS, seed=77, device=DEV,
                     MB=(1600 + 15) // 16)
     c = make_q8(w)
@@ -110,6 +111,17 @@ def test_code_arrays_in_either_order_or_shared():
                                     v_codes=buf[:n].view(c.v_codes.shape))
     out, _ = run_q8(w, c_swapped)
     assert_parity(out.cpu().numpy(), ref, "q8 V codes below K codes")
+    m = c.k_meta.numel()
+    for v_first in (False, True):
+        mbuf = torch.empty(2 * m, dtype=c.k_meta.dtype, device=DEV)
+        lo, hi = (c.v_meta, c.k_meta) if v_first else (c.k_meta, c.v_meta)
+        mbuf[:m].copy_(lo.reshape(-1))
+        mbuf[m:].copy_(hi.reshape(-1))
+        a, b = mbuf[:m].view(c.k_meta.shape), mbuf[m:].view(c.k_meta.shape)
+        c_meta = dataclasses.replace(c_swapped, k_meta=b if v_first else a,
+                                     v_meta=a if v_first else b)
+        out, _ = run_q8(w, c_meta)
+        assert_parity(out.cpu().numpy(), ref, f"q8 pairs, V's below K's: {v_first}")
     shared = dataclasses.replace(c, v_codes=c.k_codes, v_meta=c.k_meta)
     ref_shared = oracle_q8(w, shared)
     out, _ = run_q8(w, shared)
