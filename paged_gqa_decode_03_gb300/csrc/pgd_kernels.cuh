@@ -973,8 +973,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 }
             }
         }
-        if (!consumers_sync())  // every warp is done with the merge buffer
-            break;
+        // (the stage's barrier counts every warp's arrival: no copy refills
+        // it before all are done with the merge buffer)
         fence_proxy_async_smem();  // generic writes to the stage before its next copies
         __syncwarp();
         if (lane == 0)
