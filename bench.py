@@ -46,12 +46,13 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "8ff1b9df9bd74504": {("batch_decode", 512): 633_324_544 + 5_478_656,
-                         ("batch_decode_q8", 512): 336_721_408 + 3_765_760,
-                         ("ragged_tails", 256): 888_202_240 + 6_766_848,
-                         ("long_context", 512): 1_293_075_968 + 7_435_008},
-    # the several-query-token kernels (hash of all sources)
-    "af0ca759d8a11d4c": {("chunked_prefill", 8320): 286_897_664 + 13_862_400},
+    "8412ac14eef059ac": {("batch_decode", 512): 633_327_360 + 5_634_560,
+                         ("batch_decode_q8", 512): 336_784_128 + 5_757_184,
+                         ("ragged_tails", 256): 888_204_544 + 7_561_216,
+                         ("ragged_tails_q8", 256): 472_735_232 + 7_183_616,
+                         ("long_context", 512): 1_293_085_440 + 7_476_224,
+                         ("long_context_q8", 512): 687_190_784 + 7_269_120},
+    # the several-query-token kernels (hash without the decode kernels' files)
 }
 
 
@@ -72,6 +73,9 @@ def kernel_source_hash(exclude=()):
 
 
 DECODE_HASH_EXCLUDE = ("pgd_varlen.cu",)
+# the several-query-token kernels include neither the decode kernels nor the quantiser
+VARLEN_HASH_EXCLUDE = ("pgd_kernels.cuh", "pgd_kernels_d64.cu", "pgd_kernels_d128.cu",
+                       "pgd_kernels_d256.cu", "pgd_quantize.cu")
 
 
 def measured_peaks():
@@ -627,7 +631,8 @@ def run_varlen_bench(args):
             achieved = flops / (kern_ms * 1e-3) / 1e12
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t, "frac_of_sustained": achieved / peak_t_sus,
-                    "traffic": TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, PK)),
+                    "traffic": TRAFFIC.get(kernel_source_hash(VARLEN_HASH_EXCLUDE), {}).get(
+                        (args.workload, PK)),
                     "peak_source": f"{peak_kind} (MEASURED_PEAKS bf16_tflops; fp16 at the bf16 rate)",
                     "algorithmic_flops_per_launch": flops}
             e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
@@ -637,7 +642,8 @@ def run_varlen_bench(args):
             achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peak_b, "unit": "GB/s",
                     "frac": achieved / peak_b,
-                    "traffic": TRAFFIC.get(kernel_source_hash(), {}).get((args.workload, PK)),
+                    "traffic": TRAFFIC.get(kernel_source_hash(VARLEN_HASH_EXCLUDE), {}).get(
+                        (args.workload, PK)),
                     "peak_source": "measured (MEASURED_PEAKS hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg_bytes}
             e2e_val = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
