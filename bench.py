@@ -53,6 +53,9 @@ TRAFFIC = {
                          ("long_context", 512): 1_293_085_440 + 7_476_224,
                          ("long_context_q8", 512): 687_190_784 + 7_269_120},
     # the several-query-token kernels (hash without the decode kernels' files)
+    "09bea472b14169b9": {("chunked_prefill", 8320): 286_545_152 + 13_403_392,
+                         ("prefill", 2048): 169_858_304 + 80_630_016,
+                         ("spec_verify", 4096): 605_161_472 + 5_032_192},
 }
 
 
