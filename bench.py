@@ -46,7 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "8412ac14eef059ac": {("batch_decode", 512): 633_327_360 + 5_634_560,
+    "8412ac14eef059ac": {("tiny", 512): 4_204_544 + 0,
+                         ("batch_decode", 512): 633_327_360 + 5_634_560,
                          ("batch_decode_q8", 512): 336_784_128 + 5_757_184,
                          ("ragged_tails", 256): 888_204_544 + 7_561_216,
                          ("ragged_tails_q8", 256): 472_735_232 + 7_183_616,
