@@ -46,17 +46,17 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "8412ac14eef059ac": {("tiny", 512): 4_204_544 + 0,
-                         ("batch_decode", 512): 633_327_360 + 5_634_560,
-                         ("batch_decode_q8", 512): 336_784_128 + 5_757_184,
-                         ("ragged_tails", 256): 888_204_544 + 7_561_216,
-                         ("ragged_tails_q8", 256): 472_735_232 + 7_183_616,
-                         ("long_context", 512): 1_293_085_440 + 7_476_224,
-                         ("long_context_q8", 512): 687_190_784 + 7_269_120},
+    "9cce0a5c949d46a2": {("tiny", 512): 4_204_800 + 0,
+                         ("batch_decode", 512): 633_312_512 + 4_884_992,
+                         ("batch_decode_q8", 512): 336_783_616 + 5_120_512,
+                         ("ragged_tails", 256): 888_232_448 + 6_799_360,
+                         ("ragged_tails_q8", 256): 472_704_000 + 6_769_920,
+                         ("long_context", 512): 1_293_067_008 + 7_181_056,
+                         ("long_context_q8", 512): 687_140_864 + 6_992_384},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "09bea472b14169b9": {("chunked_prefill", 8320): 286_545_152 + 13_403_392,
-                         ("prefill", 2048): 169_858_304 + 80_630_016,
-                         ("spec_verify", 4096): 605_161_472 + 5_032_192},
+    "8dcc6648acb385df": {("chunked_prefill", 8320): 286_171_136 + 13_128_704,
+                         ("prefill", 2048): 167_582_208 + 80_290_304,
+                         ("spec_verify", 4096): 605_140_480 + 4_443_392},
 }
 
 

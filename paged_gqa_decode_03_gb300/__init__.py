@@ -32,6 +32,7 @@ __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc"
            "paged_gqa_decode_q8_append", "paged_gqa_decode_q8_strided", "q8_strides",
            "paged_kv_quantize", "pgd_plan", "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
+           "pgd_test_stall_next_decode",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +64,7 @@ SIGNATURES = {
     "pgd_last_error": (ctypes.c_char_p, []),
     "pgd_check_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pgd_set_timing_events": (_I, [_P, _P]),
+    "pgd_test_stall_next_decode": (_I, [_P]),
     "pgd_device_info": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pgd_version": (_I, []),
 }
@@ -539,6 +541,20 @@ def pgd_set_timing_events(before=None, after=None) -> None:
     b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
     a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
     _raise(lib.pgd_set_timing_events(b, a))
+
+
+def pgd_test_stall_next_decode(flag=None) -> None:
+    """Failure-detection test knob: the next decode call on this thread waits
+    (bounded, 2 s) in every CTA for ``flag`` (a 1-element int32/uint32 CUDA
+    tensor) to become non-zero; if it stays zero the call sets the device
+    error word's timeout bit and its output is undefined.  None cancels."""
+    lib = load_library()
+    if flag is not None:
+        if not (flag.is_cuda and flag.element_size() == 4 and flag.numel() >= 1):
+            raise ValueError("flag: a CUDA tensor of 4-byte elements")
+        _raise(lib.pgd_test_stall_next_decode(ctypes.c_void_p(flag.data_ptr())))
+    else:
+        _raise(lib.pgd_test_stall_next_decode(ctypes.c_void_p(0)))
 
 
 def pgd_device_info(head_dim: int, block_size: int):

@@ -31,6 +31,7 @@ thread_local std::string t_last_error;
 thread_local int t_last_partition = 0;
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
+thread_local const unsigned *t_stall_flag = nullptr;  // pgd_test_stall_next_decode
 
 pgd_status fail(pgd_status st, const char *fmt, ...)
 {
@@ -827,6 +828,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.NB = NB;
     p.NPmax = plan.NPmax;
     p.wait_budget_ns = kWaitBudgetNs;
+    p.stall_flag = t_stall_flag;  // one call only
+    t_stall_flag = nullptr;
 
     LaunchConfig lc;
     lc.grid = plan.grid;
@@ -1348,6 +1351,15 @@ pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_di
 int pgd_last_partition_size(void) { return t_last_partition; }
 
 const char *pgd_last_error(void) { return t_last_error.c_str(); }
+
+pgd_status pgd_test_stall_next_decode(const void *device_flag)
+{
+    if (device_flag && !aligned(device_flag, 4))
+        return fail(PGD_ERR_INVALID_ARG, "stall flag not 4-byte aligned");
+    t_stall_flag = static_cast<const unsigned *>(device_flag);
+    t_last_error.clear();
+    return PGD_OK;
+}
 
 pgd_status pgd_check_device_error(void *stream, unsigned *bits)
 {

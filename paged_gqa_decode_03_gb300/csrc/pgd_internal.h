@@ -135,6 +135,8 @@ struct DecodeParams {
     float scale_log2;             // scale * log2(e)
     int S, Hq, Hkv, G, P, logP, MB, NB, NPmax;
     uint64_t wait_budget_ns;
+    const unsigned *stall_flag;   // test knob: every CTA first waits (bounded) for
+                                  //   *stall_flag != 0, or null
 };
 
 struct LaunchConfig {

@@ -225,6 +225,26 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     __syncthreads();
     griddep_launch_dependents();
 
+    // Test knob: wait for a flag (one thread, bounded by the pipeline's wait
+    // budget); if it is never set, flag the timeout and leave before any copy
+    // is issued or any barrier used, so nothing is in flight.
+    if (p.stall_flag) {
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = global_ns();
+            bool set = false;
+            while (!(set = *reinterpret_cast<const volatile unsigned *>(p.stall_flag) != 0u) &&
+                   global_ns() - t0 < p.wait_budget_ns)
+                __nanosleep(1000);
+            if (!set) {
+                atomicOr(p.err, kErrTimeout);
+                abort_flag = 1;
+            }
+        }
+        __syncthreads();
+        if (abort_flag)
+            return;
+    }
+
     if (warp == NC) {
         // ============================================================ producer
         if (lane == 0) {

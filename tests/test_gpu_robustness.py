@@ -86,3 +86,37 @@ def test_decode_step_in_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert pgd.pgd_check_device_error() == 0
+
+
+def test_stalled_wait_runs_out_and_is_reported():
+    """A wait that nothing ends: every CTA of the next decode call first
+    waits for a flag no one sets; the wait gives up after its budget (2 s),
+    the kernel sets the timeout bit and leaves without issuing a copy, and
+    the context stays usable — the same call then runs exactly."""
+    w = make_custom(S=6, Hq=32, Hkv=8, D=128, BS=16, lens=[1, 17, 300, 513, 1000, 64], seed=29,
+                    device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    assert pgd.pgd_check_device_error() == 0
+    pgd.pgd_test_stall_next_decode(flag)
+    pgd.paged_gqa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, 512)
+    torch.cuda.synchronize()
+    assert pgd.pgd_check_device_error() & pgd.DEVERR_TIMEOUT
+    # the knob applies to one call: the next is exact, with a clean error word
+    out2 = run(w, P=512)
+    assert_parity(out2.cpu().numpy(), oracle_out(w), "decode after a timed-out call")
+    assert pgd.pgd_check_device_error() == 0
+
+
+def test_stall_flag_already_set_passes():
+    """The same knob with the flag set: the wait ends at once and the call is
+    exact."""
+    w = make_custom(S=4, Hq=16, Hkv=2, D=256, BS=32, lens=[5, 600, 1100, 33], seed=31,
+                    device=DEV)
+    flag = torch.ones(1, dtype=torch.int32, device=DEV)
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    pgd.pgd_test_stall_next_decode(flag)
+    pgd.paged_gqa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens, w.scale, 0)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle_out(w), "decode with a set stall flag")
+    assert pgd.pgd_check_device_error() == 0
