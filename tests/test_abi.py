@@ -174,3 +174,12 @@ def test_q8_validation(lib):
     assert call_q8(lib, D=64) == UNSUPPORTED             # codes need whole 128-byte rows
     assert call_q8(lib, metas=(ctypes.c_void_p(0), A)) == INVALID
     assert call_q8(lib, metas=(A, ctypes.c_void_p((1 << 20) + 8))) == INVALID
+
+
+def test_stall_knob_arguments(lib):
+    """The failure-detection test knob rejects a misaligned flag, accepts an
+    aligned one and is cancelled by NULL (nothing is launched here)."""
+    assert lib.pgd_test_stall_next_decode(ctypes.c_void_p((1 << 20) + 2)) == INVALID
+    assert "aligned" in lib.pgd_last_error().decode()
+    assert lib.pgd_test_stall_next_decode(A) == OK
+    assert lib.pgd_test_stall_next_decode(ctypes.c_void_p(0)) == OK
