@@ -80,17 +80,22 @@ def library_path() -> str:
     return _LIB_PATH
 
 
-def load_library():
-    """Loads libpgd.so (raises if it has not been built)."""
+def load_library(path: str | None = None):
+    """Loads libpgd.so (raises if it has not been built).  ``path`` loads
+    another build of the same library instead (the timeline tool's stamped
+    copy) for the rest of the process; it must come before any call."""
     global _lib
     with _lock:
-        if _lib is not None:
+        if _lib is not None and path is None:
             return _lib
-        if not os.path.exists(_LIB_PATH):
+        if path is not None and _lib is not None:
+            raise RuntimeError("load_library(path): the library is already loaded")
+        path = path or _LIB_PATH
+        if not os.path.exists(path):
             raise ImportError(
-                f"{_LIB_PATH} is missing: build it with "
+                f"{path} is missing: build it with "
                 "`python -m paged_gqa_decode_03_gb300.build` (there is no fallback path)")
-        lib = ctypes.CDLL(_LIB_PATH)
+        lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)
             fn.restype = res

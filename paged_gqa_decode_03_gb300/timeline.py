@@ -239,11 +239,7 @@ def build_timeline_library(varlen: bool = False) -> str:
 
 def _load(path):
     import paged_gqa_decode_03_gb300 as pgd
-    lib = ctypes.CDLL(path)
-    for name, (res, argtypes) in pgd.SIGNATURES.items():
-        fn = getattr(lib, name)
-        fn.restype, fn.argtypes = res, argtypes
-    pgd._lib = lib  # this process's calls go through the stamped library
+    lib = pgd.load_library(path)  # this process's calls go through the stamped library
     return pgd, lib
 
 
