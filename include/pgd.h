@@ -407,10 +407,12 @@ pgd_status pgd_check_device_error(void *stream, unsigned *bits);
 
 /*
  * pgd_test_stall_next_decode — failure-detection test knob.  The next decode
- * call on this thread (paged_gqa_decode*, any entry point with one query
- * token per sequence) makes every CTA of its partition kernel first wait for
- * the 32-bit word at `device_flag` (device memory, 4-byte aligned, read only)
- * to become non-zero, bounded by the pipeline's wait budget (2 s).  If it
+ * call on this thread that passes argument validation (paged_gqa_decode*, any
+ * entry point with one query token per sequence; a call rejected before
+ * launching leaves the request pending) makes every CTA of its partition
+ * kernel first wait for the 32-bit word at `device_flag` (device memory,
+ * 4-byte aligned, read only) to become non-zero, bounded by the pipeline's
+ * wait budget (2 s).  If it
  * does not, the kernel sets PGD_DEVERR_TIMEOUT in the device error word and
  * its CTAs leave before issuing any copy (the call's output is then
  * undefined); the context stays usable.  NULL cancels a pending request.
