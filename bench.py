@@ -4,11 +4,19 @@
                     [--partition P] [--impl ours|reference] [--no-cpu-baseline]
 
 One step = one decode call (partition kernel + split-KV reduce) over the whole
-seeded synthetic workload (default ``batch_decode``: 64 sequences, GQA
-(32, 8, 128), block size 16, lengths U{512..4096}, partition 512), inputs
-resident in HBM.  K steps are timed with CUDA events after W warm-up steps;
-the K/V bytes per step (~0.6 GB) exceed the 129 MB L2, so there is no flush
+seeded synthetic workload, inputs resident in HBM.  The line's workload is
+``long_context`` at partition 512 (32 sequences, GQA (16, 2, 256), block size
+32, lengths U{8192..32768}, 1.34 GB of K/V per call: the largest of the
+decode workloads); the same run measures the other target workloads the same
+way and reports them under ``per_workload`` (long_context at partition 256,
+ragged_tails at 256, serving_mix with the scheduler's choice, batch_decode at
+512), each with its kernel fraction, clocks, end-to-end figure and CPU
+baseline.  K steps are timed with CUDA events after W warm-up steps; the K/V
+bytes per step (0.6-1.3 GB) exceed the 129 MB L2, so there is no flush
 between steps.  Prints one JSON line.
+
+``--workload NAME`` times that workload alone (``--per-workload`` adds the
+map back).
 
 N > 1 (torchrun): every rank runs the same workload on its own GPU
 (independent replicas, no collective on the data path); rank 0 prints the
@@ -184,28 +192,22 @@ def replica_throughput(kv_bytes_per_rank: int, local_ms_per_step: float, world: 
     return world * kv_bytes_per_rank / (ms * 1e-3) / 1e9, ms
 
 
-def oracle_time(w, seqs, min_seconds=10.0, max_reps=50):
-    """Times the CPU oracle on the listed sequences; returns
-    (seconds per rep, KV bytes per rep, threads, reps)."""
-    import oracle
-
-    c = w.compact(seqs)
-    kv = int(c["seq_lens"].astype("int64").sum()) * w.Hkv * w.D * 4
-    threads = oracle.max_threads()
+def oracle_seconds(fn, min_seconds, max_reps=50):
+    """Wall-clock seconds per call of fn() over >= 1 call and about
+    min_seconds in all; returns (seconds per call, calls)."""
     reps, total = 0, 0.0
     while reps < max_reps and (total < min_seconds or reps < 1):
         t0 = time.perf_counter()
-        oracle.decode(c["q"], c["k_cache"], c["v_cache"], c["block_tables"], c["seq_lens"],
-                      c["scale"], threads=threads)
+        fn()
         total += time.perf_counter() - t0
         reps += 1
-    return total / reps, kv, threads, reps
+    return total / reps, reps
 
 
-def sample_seqs(w, kv_budget_bytes):
+def sample_seqs(w, kv_budget_bytes, per_token_bytes=None):
     """Leading sequences of the workload up to a K/V byte budget (>= 1)."""
     lens = w.lens
-    per = w.Hkv * w.D * 4
+    per = per_token_bytes or w.Hkv * w.D * 4
     acc, seqs = 0, []
     for s in range(w.S):
         if seqs and acc + int(lens[s]) * per > kv_budget_bytes:
@@ -215,15 +217,74 @@ def sample_seqs(w, kv_budget_bytes):
     return seqs
 
 
+def kv_token_bytes(w, q8):
+    """K/V bytes per (token, KV head): fp16 rows, or 8-bit codes plus their
+    bf16 (scale, bias) pairs."""
+    return 2 * (w.D + (w.D // 64) * 4) if q8 else 4 * w.D
+
+
+def cpu_baseline(w, q8c, seconds, seconds_1t, sample_1t_bytes, label):
+    """The fp64 oracle on this host: all host cores on the whole workload,
+    and one thread on its leading sequences (a bounded sample)."""
+    import oracle
+    from paged_gqa_decode_03_gb300.workloads import compact_q8
+
+    per = kv_token_bytes(w, q8c is not None) * w.Hkv
+
+    def runner(seqs, threads):
+        if q8c is None:
+            c = w.compact(seqs)
+            fn = lambda: oracle.decode(c["q"], c["k_cache"], c["v_cache"], c["block_tables"],
+                                       c["seq_lens"], c["scale"], threads=threads)
+        else:
+            c = compact_q8(w, q8c, seqs)
+            fn = lambda: oracle.decode_q8(c["q"], c["k_codes"], c["k_meta"], c["v_codes"],
+                                          c["v_meta"], c["block_tables"], c["seq_lens"],
+                                          c["scale"], threads=threads)
+        return fn, int(c["seq_lens"].astype("int64").sum()) * per
+
+    threads = oracle.max_threads()
+    fn, kv = runner(list(range(w.S)), threads)
+    sec, reps = oracle_seconds(fn, seconds)
+    del fn
+    one = sample_seqs(w, sample_1t_bytes, per)
+    fn1, kv1 = runner(one, 1)
+    sec1, reps1 = oracle_seconds(fn1, seconds_1t)
+    fmt = "8-bit code + pair" if q8c is not None else "fp16"
+    return {"value": kv / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {w.S} sequences of {label} ({kv / 1e9:.3f} GB {fmt} K/V), {reps} "
+                      f"reps, fp64 C oracle on {threads} threads, {sec * 1e3:.1f} ms per call",
+            "single_thread": {"value": kv1 / sec1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"sequences 0..{len(one) - 1} of {label} "
+                                        f"({kv1 / 1e9:.3f} GB K/V), {reps1} reps, "
+                                        f"{sec1 * 1e3:.1f} ms per call"}}
+
+
+def decode_config(w, P, args, world, q8):
+    """The workload of one decode line (shared by both arms, so that they
+    name the same configuration)."""
+    kv = int(w.lens.sum()) * w.Hkv * kv_token_bytes(w, q8)
+    return {"workload": w.name, "num_seqs": w.S, "gqa": [w.Hq, w.Hkv, w.D],
+            "block_size": w.BS, "partition_size": P, "kv_bytes_per_step": kv,
+            "num_blocks": w.NB, "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
+            "parallelism": f"replicas x{world}", "fused_kv_append": bool(args.append),
+            "kv_layout": args.layout,
+            "kv_format": "8-bit codes + bf16 (scale, bias) per 64" if q8 else "fp16"}
+
+
 # --------------------------------------------------------------------- reference arm
 def run_reference(args):
     world, rank, local = dist_setup()
     if rank != 0:
         return 0
-    import torch
     from paged_gqa_decode_03_gb300.workloads import make_workload
 
-    w = make_workload(args.workload, device="cpu")
+    name = args.workload or HEADLINE[0]
+    P = HEADLINE[1] if args.workload is None else (args.partition if args.partition is not None
+                                                     else None)
+    w = make_workload(name, device="cpu")
+    if P is None:
+        P = w.P
     import oracle
 
     oracle.build()
@@ -247,13 +308,13 @@ def run_reference(args):
                       c["scale"], threads=threads)
     dt = (time.perf_counter() - t0) / args.steps
     value = kv / dt / 1e9
-    sample = (f"{len(seqs)} of {w.S} sequences of {args.workload} ({kv / 1e9:.3f} GB K/V per "
-              f"step), fp64 oracle")
+    sample = (f"{len(seqs)} of {w.S} sequences of {name} ({kv / 1e9:.3f} GB K/V per "
+              f"step), fp64 oracle on {threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample": sample},
+            "config": decode_config(w, P, args, world, False), "sample": sample,
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -263,42 +324,25 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------- our arm
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
+# The line's workload: long_context at partition 512, the largest K/V per
+# call of the decode workloads; the other target workloads are measured in
+# the same run (`per_workload`).
+HEADLINE = ("long_context", 512)
+PER_WORKLOAD = [("long_context", 256), ("ragged_tails", 256), ("serving_mix", 0),
+                ("batch_decode", 512)]
 
-    import paged_gqa_decode_03_gb300 as pgd
-    from paged_gqa_decode_03_gb300.workloads import make_workload
 
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    import __graft_entry__
-    if rank == 0:
-        __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
-    pgd.load_library()
-
-    w = make_workload(args.workload, device=dev)
-    P = w.P if args.partition is None else args.partition
-    kv_bytes = w.kv_bytes()
-    alg_bytes = w.total_bytes()
-    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
+def decode_call(pgd, w, P, args, out, stream, dev):
+    """(call(q, block_tables, seq_lens), quantised caches or None) for the
+    entry point the options select."""
     k_new = v_new = None
     q8 = None
     if args.kv == "q8":  # the same workload over quantised pages (codes + bf16 pairs)
         from paged_gqa_decode_03_gb300.workloads import make_q8
         q8 = make_q8(w)
-        kv_bytes = int(w.lens.sum()) * w.Hkv * 2 * (w.D + (w.D // 64) * 4)
-        alg_bytes = kv_bytes + w.S * w.Hq * w.D * (2 + 4) + int(w.page_offsets[-1]) * 4
     if args.append:  # the decode step with its fused KV-cache append
-        gen = torch.Generator(device=dev).manual_seed(7)
+        gen = torch_generator(dev, 7)
+        import torch
         k_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
         v_new = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=dev).to(torch.float16)
     if q8 is not None and args.layout != "head_major":
@@ -321,7 +365,6 @@ def run_ours(args):
                                     w.scale, P, stream=stream)
     elif args.layout != "head_major":
         # the same caches in another layout, through the strided entry point
-        # (the head-major copy stays for the CPU baseline)
         strides = pgd.kv_strides(args.layout, w.Hkv, w.BS, w.D)
         kc = w.k_cache.permute(0, 2, 1, 3).contiguous()
         vc = w.v_cache.permute(0, 2, 1, 3).contiguous()
@@ -337,11 +380,33 @@ def run_ours(args):
         def call(q, bt, sl):
             pgd.paged_gqa_decode(out, q, w.k_cache, w.v_cache, bt, sl, w.scale, P,
                                  stream=stream)
+    return call, q8
+
+
+def torch_generator(dev, seed):
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    return g
+
+
+def measure_decode(pgd, w, P, args, world, local, dev, steps, warmup, e2e_steps, cpu_seconds,
+                   cpu_seconds_1t, with_cpu):
+    """One decode line: the timed passes on the device, the end-to-end pass
+    with host buffers, and the CPU baseline.  Returns a dict of figures."""
+    import torch
+
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call, q8 = decode_call(pgd, w, P, args, out, stream, dev)
+    tok = kv_token_bytes(w, q8 is not None)
+    kv_bytes = int(w.lens.sum()) * w.Hkv * tok
+    alg_bytes = kv_bytes + w.S * w.Hq * w.D * (2 + 4) + int(w.page_offsets[-1]) * 4
 
     def step():
         call(w.q, w.block_tables, w.seq_lens)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
     assert pgd.pgd_check_device_error(stream) == 0
@@ -349,11 +414,9 @@ def run_ours(args):
 
     def barrier():
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize(dev)
-
-
-    peak, peak_kind = measured_peaks()
 
     # ---- timed region, two passes of K steps each, events on the launching
     # stream.  Pass 1 is the production launch sequence (partition kernel,
@@ -362,41 +425,54 @@ def run_ours(args):
     # kernel (the library's timing hook) for the roofline's per-launch
     # duration; those events sit between the two kernels and cost the
     # overlap, so its step time is reported separately.
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev2 = torch.cuda.Event(enable_timing=True)
-    ev3 = torch.cuda.Event(enable_timing=True)
-    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1, ev2, ev3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for e in kb + ka:
         e.record(stream)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        for _ in range(max(args.warmup, 3)):  # clocks back up after the sampler's start
+        for _ in range(max(warmup, 3)):  # clocks back up after the sampler's start
             step()
         barrier()
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         ev1.record(stream)
         barrier()
         ev2.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             pgd.pgd_set_timing_events(kb[i], ka[i])
             step()
         ev3.record(stream)
         barrier()
         pgd.pgd_set_timing_events(None, None)
     clocks = clk.summary()
-    value, ms_per_step = replica_throughput(kv_bytes, ev0.elapsed_time(ev1) / args.steps, world,
-                                            dev)
-    ms_instrumented = max_over_ranks(ev2.elapsed_time(ev3) / args.steps, world, dev)
-    kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(args.steps))
+    value, ms_per_step = replica_throughput(kv_bytes, ev0.elapsed_time(ev1) / steps, world, dev)
+    ms_instrumented = max_over_ranks(ev2.elapsed_time(ev3) / steps, world, dev)
+    kern_ms = statistics.fmean(kb[i].elapsed_time(ka[i]) for i in range(steps))
+    assert pgd.pgd_check_device_error(stream) == 0
 
-    # ---- end to end through the public API with host buffers: per step the
-    # step's inputs (q, block_tables, seq_lens, packed in one pinned buffer)
-    # go host->device in one copy and the output comes back; the K/V cache
-    # stays resident, as it does in a decode loop.
+    e2e = measure_e2e(w, call, out, stream, dev, world, kv_bytes, e2e_steps, barrier)
+
+    cpu = None
+    if with_cpu:
+        cpu = cpu_baseline(w, q8, cpu_seconds, cpu_seconds_1t, args.cpu_sample_1t_bytes,
+                           w.name)
+    return dict(value=value, ms_per_step=ms_per_step, ms_instrumented=ms_instrumented,
+                kern_ms=kern_ms, kv_bytes=kv_bytes, alg_bytes=alg_bytes, P_used=P_used,
+                clocks=clocks, e2e=e2e, cpu=cpu, q8=q8 is not None)
+
+
+def measure_e2e(w, call, out, stream, dev, world, kv_bytes, e2e_steps, barrier):
+    """End to end through the public API with host buffers: per step the
+    step's inputs (q, block_tables, seq_lens, packed in one pinned buffer)
+    go host->device in one copy, the call runs, the output comes back and
+    the host waits for it; the K/V cache stays resident, as it does in a
+    decode loop.  A second pass records events between the parts of a step
+    and times the host's issue of the call, to show where the time goes."""
+    import torch
+
     def _align(n):
         return (n + 255) // 256 * 256
     nq, nbt, nsl = w.q.numel() * 2, w.block_tables.numel() * 4, w.seq_lens.numel() * 4
@@ -413,7 +489,6 @@ def run_ours(args):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = nq + nbt + nsl
     d2h = out_h.numel() * 4
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
@@ -428,53 +503,133 @@ def run_ours(args):
     for _ in range(e2e_steps):
         e2e_step()
     barrier()
-    e2e_value, e2e_ms = replica_throughput(kv_bytes, (time.perf_counter() - t0) / e2e_steps * 1e3,
-                                           world, dev)
-    e2e_s = e2e_ms * 1e-3
+    value, ms = replica_throughput(kv_bytes, (time.perf_counter() - t0) / e2e_steps * 1e3, world,
+                                   dev)
+    # where a step's time goes (a separate pass: the events cost a little)
+    n = max(1, min(e2e_steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    walls, issue = [], []
+    for i in range(n):
+        a, b, c, d = ev[i]
+        t1 = time.perf_counter()
+        a.record(stream)
+        d_in.copy_(h_in, non_blocking=True)
+        b.record(stream)
+        t2 = time.perf_counter()
+        call(q_d, bt_d, sl_d)
+        issue.append(time.perf_counter() - t2)
+        c.record(stream)
+        out_h.copy_(out, non_blocking=True)
+        d.record(stream)
+        stream.synchronize()
+        walls.append(time.perf_counter() - t1)
+    h2d_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    call_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    d2h_ms = statistics.fmean(e[2].elapsed_time(e[3]) for e in ev)
+    span_ms = statistics.fmean(e[0].elapsed_time(e[3]) for e in ev)
+    wall_ms = statistics.fmean(walls) * 1e3
+    return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps, "ms_per_step": ms,
+            "breakdown_us": {"h2d_copy": h2d_ms * 1e3, "call": call_ms * 1e3,
+                             "d2h_copy": d2h_ms * 1e3, "device_span": span_ms * 1e3,
+                             "host_wall": wall_ms * 1e3,
+                             "host_outside_device_span": (wall_ms - span_ms) * 1e3,
+                             "host_issue_of_call": statistics.fmean(issue) * 1e6,
+                             "steps": n}}
 
-    # ---- CPU baseline: the oracle on this host (rank 0, N == 1 only)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and q8 is None:
-        seqs = list(range(w.S))
-        sec, kv_s, threads, reps = oracle_time(w, seqs, min_seconds=args.cpu_seconds)
-        cpu = {"value": kv_s / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"all {len(seqs)} sequences of {args.workload} "
-                         f"({kv_s / 1e9:.3f} GB K/V), {reps} reps, fp64 C oracle, "
-                         f"{sec * 1e3:.1f} ms per call"}
+
+def workload_entry(m, peak, traffic, P_req):
+    """The per_workload figures of one measured line."""
+    achieved = m["alg_bytes"] / (m["kern_ms"] * 1e-3) / 1e9
+    return {"partition_size": m["P_used"], "requested_partition": P_req,
+            "us_per_call": m["ms_per_step"] * 1e3, "kv_gbs": m["value"],
+            "pct_of_hbm_peak": 100.0 * m["value"] / peak,
+            "kernel_us": m["kern_ms"] * 1e3, "kernel_achieved_gbs": achieved,
+            "kernel_frac": achieved / peak, "traffic": traffic,
+            "kv_bytes_per_step": m["kv_bytes"], "algorithmic_bytes_per_launch": m["alg_bytes"],
+            "clocks": m["clocks"], "e2e": m["e2e"], "cpu_baseline": m["cpu"]}
+
+
+def traffic_for(name, P_used, q8):
+    return TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get(
+        (name + ("_q8" if q8 else ""), P_used))
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_gqa_decode_03_gb300 as pgd
+    from paged_gqa_decode_03_gb300.workloads import make_workload
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    pgd.load_library()
+
+    name = args.workload or HEADLINE[0]
+    w = make_workload(name, device=dev)
+    if args.partition is not None:
+        P = args.partition
+    else:
+        P = HEADLINE[1] if args.workload is None else w.P
+    peak, peak_kind = measured_peaks()
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    m = measure_decode(pgd, w, P, args, world, local, dev, args.steps, args.warmup,
+                       max(1, min(args.steps, args.e2e_steps)), args.cpu_seconds,
+                       args.cpu_seconds_1t, with_cpu)
+    config = decode_config(w, P, args, world, m["q8"])
+    del w
+    torch.cuda.empty_cache()
+
+    # the other target workloads, measured the same way in the same run
+    per = None
+    if args.per_workload or (args.workload is None and not args.no_per_workload):
+        per = {}
+        for wname, wP in PER_WORKLOAD:
+            wx = make_workload(wname, device=dev)
+            mx = measure_decode(pgd, wx, wP, args, world, local, dev, args.steps, args.warmup,
+                                max(1, min(args.steps, args.e2e_steps)), args.cpu_seconds_each,
+                                args.cpu_seconds_1t, with_cpu)
+            key = f"{wname}_p{wP}" if wP else f"{wname}_auto"
+            per[key] = workload_entry(mx, peak, traffic_for(wname, mx["P_used"], mx["q8"]), wP)
+            per[key]["workload"] = wname
+            del wx
+            torch.cuda.empty_cache()
 
     if rank == 0:
-        achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-        traffic = TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get(
-            (args.workload + ("_q8" if q8 is not None else ""), P_used))
+        achieved = m["alg_bytes"] / (m["kern_ms"] * 1e-3) / 1e9
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": m["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+            "us_per_call": m["ms_per_step"] * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "pct_of_hbm_peak": 100.0 * value / world / peak,
-            "config": {"workload": args.workload, "num_seqs": w.S,
-                       "gqa": [w.Hq, w.Hkv, w.D], "block_size": w.BS,
-                       "partition_size": P_used, "requested_partition": P,
-                       "kv_bytes_per_step": kv_bytes, "num_blocks": w.NB,
-                       "l2": "no flush: K/V bytes per step exceed the 129 MB L2",
-                       "accumulate": "fp32", "parallelism": f"replicas x{world}",
-                       "fused_kv_append": bool(args.append), "kv_layout": args.layout,
-                       "kv_format": "8-bit codes + bf16 (scale, bias) per 64" if q8 is not None
-                       else "fp16",
-                       "ms_per_step_with_kernel_events": ms_instrumented},
+            "pct_of_hbm_peak": 100.0 * m["value"] / world / peak,
+            "partition_used": m["P_used"], "accumulate": "fp32",
+            "ms_per_step_with_kernel_events": m["ms_instrumented"],
+            "config": config,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
+                         "frac": achieved / peak,
+                         "traffic": traffic_for(name, m["P_used"], m["q8"]),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",
                          "kernel": "paged_gqa_partial_kernel",
-                         "kernel_ms": kern_ms,
-                         "algorithmic_bytes_per_launch": alg_bytes},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": e2e_s * 1e3},
+                         "kernel_ms": m["kern_ms"],
+                         "algorithmic_bytes_per_launch": m["alg_bytes"]},
+            "cpu_baseline": m["cpu"],
+            "e2e": m["e2e"],
             "gpu_launches": 2 * args.steps,
-            "clocks": clocks,
+            "clocks": m["clocks"],
         }
+        if per is not None:
+            line["per_workload"] = per
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -688,7 +843,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="batch_decode")
+    ap.add_argument("--workload", default=None,
+                    help="one workload only (default: long_context at partition 512, with "
+                         "the other target workloads in per_workload)")
     ap.add_argument("--partition", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--append", action="store_true",
@@ -698,13 +855,23 @@ def main():
     ap.add_argument("--kv", choices=["fp16", "q8"], default="fp16",
                     help="cache format: fp16 rows, or quantised pages (paged_gqa_decode_q8)")
     ap.add_argument("--e2e-steps", type=int, default=500)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle seconds (all host cores) on the line's workload")
+    ap.add_argument("--cpu-seconds-each", type=float, default=3.0,
+                    help="oracle seconds (all host cores) on each per_workload entry")
+    ap.add_argument("--cpu-seconds-1t", type=float, default=2.0,
+                    help="oracle seconds on one thread (leading sequences) per line")
+    ap.add_argument("--cpu-sample-1t-bytes", type=float, default=6.4e7,
+                    help="K/V bytes of the one-thread oracle sample")
+    ap.add_argument("--per-workload", action="store_true",
+                    help="measure the per_workload entries even with --workload")
+    ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-sample-bytes", type=float, default=1.6e8)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()
     from paged_gqa_decode_03_gb300.workloads import VARLEN_WORKLOADS
-    if args.workload in VARLEN_WORKLOADS:
+    if args.workload is not None and args.workload in VARLEN_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
                               "the reference arm times the decode workloads only"}))

@@ -109,13 +109,15 @@ typedef enum pgd_status {
  * Scratch for the partition partials is taken from a stream-ordered memory
  * pool owned by the library and returned in stream order, so calls on
  * different streams do not share it.  Use paged_gqa_decode_ex to supply it.
+ * The pool keeps what it has handed out for the next calls until
+ * pgd_release().
  *
  * Work is handed out to the GPU's thread blocks through a 4-byte counter
  * that the library keeps per (device, stream) it has run on; the call
  * leaves it at zero for the next call on that stream.  The counters of a
  * device (1024 of them, 128 bytes apart) are allocated and
- * zeroed by the first call on that device: make that first call outside
- * any stream capture.
+ * zeroed by the first call on that device (and by the first call after a
+ * pgd_release()): make that call outside any stream capture.
  */
 pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cache,
                             const uint16_t *v_cache, const int32_t *block_tables,
@@ -132,6 +134,42 @@ pgd_status paged_gqa_decode(float *out, const uint16_t *q, const uint16_t *k_cac
 pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                     int block_size, int partition_size, int max_blocks_per_seq,
                     int *chosen_partition_size, size_t *workspace_bytes);
+
+/*
+ * pgd_workspace_size — bytes of caller scratch (paged_gqa_decode_ex,
+ * paged_gqa_decode_strided, paged_gqa_decode_q8*) a decode call with these
+ * sizes needs: the partition partials m, l [num_seqs][num_q_heads][NP] and
+ * o [num_seqs][num_q_heads][NP][head_dim] fp32, each region 256-byte
+ * aligned, NP = ceil(max_blocks_per_seq * block_size / partition_size); 0
+ * when NP == 1 ("vllm-metal", "Four speed-up tricks", 4: the partials
+ * contract; "Dispatch layer": the per-call scratch and its 512 MiB cap).
+ * partition_size 0 (the scheduler's choice, made at call time from the SM
+ * count and num_kv_heads, which this call does not take) returns the bytes
+ * for 256, which covers either choice.  Pure arithmetic: needs no GPU and
+ * launches nothing.  A result above PGD_MAX_WORKSPACE_BYTES means the call
+ * itself will be refused with PGD_ERR_WORKSPACE.  Invalid or unsupported
+ * sizes return SIZE_MAX with a message for pgd_last_error().  pgd_plan gives
+ * the exact figure for a resolved partition size on the current device.
+ */
+size_t pgd_workspace_size(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                          int partition_size, int max_blocks_per_seq);
+
+/*
+ * pgd_release — gives back the device memory the library holds on the
+ * current device: the scratch pool of the calls without caller scratch
+ * (which keeps everything it has handed out, so that the next call does
+ * not allocate again) and the claim counters.  It first waits for all work
+ * on the device (cudaDeviceSynchronize), so nothing queued still uses them,
+ * and clears this thread's cache of tensor-map descriptors (host memory).
+ * The next call re-creates what it needs; the library stays usable.
+ * Not freed: the fixed array of paged_gqa_decode_noalloc and the device
+ * error word, which are part of the library's device image.
+ * The caller must make sure no other thread calls the library on this
+ * device meanwhile, must not call it during a stream capture, and must not
+ * replay CUDA graphs captured before it (they hold the old counters'
+ * addresses).  Returns PGD_ERR_CUDA if the wait or a free fails.
+ */
+pgd_status pgd_release(void);
 
 /*
  * paged_gqa_decode_ex — paged_gqa_decode with caller-owned scratch and an
@@ -235,11 +273,16 @@ pgd_status paged_gqa_decode_strided(float *out, const uint16_t *q, const uint16_
  * any launch.
  *
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.
+ * device current; make that first call before any stream capture.  (A
+ * failed lookup is not kept: the next call tries again.)
  * Every call shares the one array: calls whose work overlaps on the GPU
  * (other streams, other threads) race on it, so serialise them.  The array
- * keeps the last call's contents; nothing in it needs to start at zero
- * (every partial is written before it is read within a call).
+ * keeps the last call's contents; the partials need no initial value
+ * (every partial is written before it is read within a call).  The work
+ * counter must read zero at launch: every call leaves it at zero, and a
+ * call that fails after its partition kernel may have started makes the
+ * next call zero it first, in stream order, with cudaMemsetAsync on the
+ * array itself (no allocation).
  */
 #define PGD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -421,6 +464,19 @@ pgd_status pgd_check_device_error(void *stream, unsigned *bits);
 pgd_status pgd_test_stall_next_decode(const void *device_flag);
 
 /*
+ * pgd_test_fail_next_reduce — failure-injection test knob, on the host.  When
+ * enable is non-zero, the next decode call on this thread that passes
+ * argument validation (paged_gqa_decode*, one query token per sequence)
+ * launches its partition kernel and then, instead of launching the reduce
+ * kernel, returns PGD_ERR_CUDA as if that launch had failed: its output is
+ * undefined and its work counter is left as the partition kernel left it.
+ * The library's recovery (the next call on that stream, or the next
+ * paged_gqa_decode_noalloc call, zeroes the counter first) is what a test
+ * then checks.  enable = 0 cancels a pending request.  Tests only.
+ */
+pgd_status pgd_test_fail_next_reduce(int enable);
+
+/*
  * pgd_set_timing_events — measurement hook.  When both are non-NULL, every
  * later call on this thread records `before` (a cudaEvent_t) on its stream
  * just before the partition kernel and `after` just after it, so the kernel's
@@ -434,7 +490,7 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: strided caches,
  * head_dim 64, block sizes 64 and 128; 1.2.0: several query tokens per
- * sequence; 1.3.0: quantised pages). */
+ * sequence; 1.3.0: quantised pages; 1.4.0: pgd_workspace_size, pgd_release). */
 int pgd_version(void);
 
 #ifdef __cplusplus

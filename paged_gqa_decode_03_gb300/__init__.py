@@ -30,9 +30,10 @@ __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc"
            "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
            "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8",
            "paged_gqa_decode_q8_append", "paged_gqa_decode_q8_strided", "q8_strides",
-           "paged_kv_quantize", "pgd_plan", "pgd_last_partition_size",
+           "paged_kv_quantize", "pgd_plan", "pgd_workspace_size", "pgd_release",
+           "pgd_last_partition_size",
            "pgd_last_error", "pgd_check_device_error", "pgd_set_timing_events",
-           "pgd_test_stall_next_decode",
+           "pgd_test_stall_next_decode", "pgd_test_fail_next_reduce",
            "pgd_device_info", "pgd_version", "PGDError", "library_path", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,11 +61,14 @@ SIGNATURES = {
     "paged_kv_quantize": (_I, [_P] * 4 + [_I] * 5 + [_P]),
     "paged_gqa_decode_q8_strided": (_I, [_P] * 10 + [_F] + [_I] * 8 + [_L] * 6 + [_P, _Z, _P]),
     "pgd_plan": (_I, [_I] * 7 + [ctypes.POINTER(_I), ctypes.POINTER(_Z)]),
+    "pgd_workspace_size": (_Z, [_I] * 6),
+    "pgd_release": (_I, []),
     "pgd_last_partition_size": (_I, []),
     "pgd_last_error": (ctypes.c_char_p, []),
     "pgd_check_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "pgd_set_timing_events": (_I, [_P, _P]),
     "pgd_test_stall_next_decode": (_I, [_P]),
+    "pgd_test_fail_next_reduce": (_I, [_I]),
     "pgd_device_info": (_I, [_I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pgd_version": (_I, []),
 }
@@ -82,7 +86,7 @@ def library_path() -> str:
 
 def load_library(path: str | None = None):
     """Loads libpgd.so (raises if it has not been built).  ``path`` loads
-    another build of the same library instead (the timeline tool's stamped
+    another build of the same library instead (for example an instrumented
     copy) for the rest of the process; it must come before any call."""
     global _lib
     with _lock:
@@ -514,6 +518,24 @@ def pgd_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, partitio
     return p.value, b.value
 
 
+def pgd_workspace_size(num_seqs, num_q_heads, head_dim, block_size, partition_size,
+                       max_blocks_per_seq) -> int:
+    """Caller-scratch bytes of a decode call with these sizes (partition_size
+    0: the bytes for 256, enough for either choice).  Needs no GPU."""
+    lib = load_library()
+    n = lib.pgd_workspace_size(num_seqs, num_q_heads, head_dim, block_size, partition_size,
+                               max_blocks_per_seq)
+    if n == ctypes.c_size_t(-1).value:
+        raise PGDError(1, pgd_last_error())
+    return int(n)
+
+
+def pgd_release() -> None:
+    """Waits for the current device and frees the library's scratch pool and
+    claim counters there (the next call re-creates them)."""
+    _raise(load_library().pgd_release())
+
+
 def pgd_last_partition_size() -> int:
     return int(load_library().pgd_last_partition_size())
 
@@ -560,6 +582,13 @@ def pgd_test_stall_next_decode(flag=None) -> None:
         _raise(lib.pgd_test_stall_next_decode(ctypes.c_void_p(flag.data_ptr())))
     else:
         _raise(lib.pgd_test_stall_next_decode(ctypes.c_void_p(0)))
+
+
+def pgd_test_fail_next_reduce(enable: bool = True) -> None:
+    """Failure-injection test knob: the next decode call on this thread
+    launches its partition kernel, withholds the reduce and reports
+    PGD_ERR_CUDA (its output undefined); False cancels."""
+    _raise(load_library().pgd_test_fail_next_reduce(1 if enable else 0))
 
 
 def pgd_device_info(head_dim: int, block_size: int):

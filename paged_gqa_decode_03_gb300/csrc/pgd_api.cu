@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -32,6 +33,7 @@ thread_local int t_last_partition = 0;
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
 thread_local const unsigned *t_stall_flag = nullptr;  // pgd_test_stall_next_decode
+thread_local bool t_skip_reduce = false;               // pgd_test_fail_next_reduce
 
 pgd_status fail(pgd_status st, const char *fmt, ...)
 {
@@ -58,9 +60,8 @@ struct DeviceState {
     int num_sms = 0;
     int ctas[2][3][5] = {};         // [quantised pages][head_dim 64/128/256][block size 8..128]
     unsigned *err_word = nullptr;   // address of g_device_error on this device
-    std::once_flag pool_once;       // the pool is made on first library-owned scratch
-    cudaError_t pool_error = cudaSuccess;
-    cudaMemPool_t pool = nullptr;   // stream-ordered scratch
+    std::mutex pool_mu;             // the pool is made on first library-owned scratch
+    cudaMemPool_t pool = nullptr;   //   (and again after pgd_release): stream-ordered scratch
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -131,16 +132,21 @@ pgd_status device_state(DeviceState **out)
     return PGD_OK;
 }
 
-// The library's scratch pool on the current device (created on first use).
+// The library's scratch pool on the current device, created on first use
+// (a failed creation is retried by the next call that needs it).
 pgd_status device_pool(DeviceState &st, cudaMemPool_t *pool)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    std::call_once(st.pool_once, [&] { st.pool_error = init_pool(dev, st); });
-    if (st.pool_error != cudaSuccess)
-        return cuda_fail(st.pool_error, "scratch pool set-up");
+    std::lock_guard<std::mutex> lock(st.pool_mu);
+    if (!st.pool && (e = init_pool(dev, st)) != cudaSuccess) {
+        if (st.pool)
+            cudaMemPoolDestroy(st.pool);
+        st.pool = nullptr;
+        return cuda_fail(e, "scratch pool set-up");
+    }
     *pool = st.pool;
     return PGD_OK;
 }
@@ -364,32 +370,37 @@ pgd_status encode_cache_map_groups(CUtensorMap *map, const void *base, const Cac
 // The library keeps one counter per (device, stream) it has run on: calls on
 // one stream are serialised and can reuse it, calls on different streams
 // never share one.  A counter whose call failed to launch is zeroed in
-// stream order before its next use.
+// stream order before its next use.  The counters are allocated by the
+// first call on a device that needs one (again after pgd_release).
 constexpr int kCounterSlots = 1024;
 constexpr int kCounterStride = 32;  // unsigned words: 128 bytes apart
 
 struct CounterPool {
-    std::once_flag once;
-    cudaError_t error = cudaSuccess;
+    std::mutex mu;                 // guards everything below
     unsigned *base = nullptr;
-    std::mutex mu;
     std::unordered_map<uintptr_t, int> slot_of;
     std::vector<char> dirty;
 };
 
 CounterPool g_counters[kMaxDevices];
 
+// Allocates and zeroes the counters (cp.mu held); leaves cp.base null on failure.
 cudaError_t init_counters(CounterPool &cp)
 {
-    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&cp.base),
-                               sizeof(unsigned) * kCounterSlots * kCounterStride);
+    unsigned *base = nullptr;
+    const size_t bytes = sizeof(unsigned) * kCounterSlots * kCounterStride;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&base), bytes);
     if (e != cudaSuccess)
         return e;
-    if ((e = cudaMemset(cp.base, 0, sizeof(unsigned) * kCounterSlots * kCounterStride)) !=
-        cudaSuccess)
+    if ((e = cudaMemset(base, 0, bytes)) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cudaFree(base);
         return e;
+    }
+    cp.base = base;
+    cp.slot_of.clear();
     cp.dirty.assign(kCounterSlots, 0);
-    return cudaDeviceSynchronize();
+    return cudaSuccess;
 }
 
 // The counter of `stream` on the current device (null when all slots are
@@ -400,11 +411,12 @@ pgd_status stream_counter(cudaStream_t stream, unsigned **counter, int *slot, bo
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PGD_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
     CounterPool &cp = g_counters[dev];
-    std::call_once(cp.once, [&] { cp.error = init_counters(cp); });
-    if (cp.error != cudaSuccess)
-        return cuda_fail(cp.error, "claim-counter set-up");
     std::lock_guard<std::mutex> lock(cp.mu);
+    if (!cp.base && (e = init_counters(cp)) != cudaSuccess)
+        return cuda_fail(e, "claim-counter set-up");
     const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
     auto it = cp.slot_of.find(key);
     int i;
@@ -432,7 +444,8 @@ void mark_counter_dirty(int slot)
     if (slot < 0 || cudaGetDevice(&dev) != cudaSuccess)
         return;
     std::lock_guard<std::mutex> lock(g_counters[dev].mu);
-    g_counters[dev].dirty[slot] = 1;
+    if (slot < (int)g_counters[dev].dirty.size())
+        g_counters[dev].dirty[slot] = 1;
 }
 
 // Descriptors of the last few (k_cache, v_cache) pairs used by this thread:
@@ -524,6 +537,21 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Scratch of the partition partials: m [S][Hq][NPmax], l [S][Hq][NPmax] and
+// o [S][Hq][NPmax][D] fp32, each region 256-byte aligned; none when no
+// sequence can span two partitions (NPmax == 1).
+size_t partials_bytes(int S, int Hq, int D, int NPmax, size_t *off_l, size_t *off_o)
+{
+    if (NPmax <= 1) {
+        *off_l = *off_o = 0;
+        return 0;
+    }
+    const size_t rows = (size_t)S * Hq * NPmax;
+    *off_l = align256(rows * 4);
+    *off_o = *off_l + align256(rows * 4);
+    return *off_o + align256(rows * D * 4);
+}
+
 pgd_status check_sizes(int S, int Hq, int Hkv, int D, int BS, int P, int MB)
 {
     if (S < 0)
@@ -584,15 +612,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     if (stage_bound >= (1ll << 31))
         return fail(PGD_ERR_UNSUPPORTED, "batch of %d sequences x %d KV heads x %d tokens too large",
                     S, Hkv, maxlen);
-    const size_t rows = (size_t)S * Hq * plan->NPmax;
-    if (plan->NPmax > 1) {
-        plan->off_l = align256(rows * 4);
-        plan->off_o = plan->off_l + align256(rows * 4);
-        plan->ws_bytes = plan->off_o + align256(rows * D * 4);
-    } else {
-        plan->off_l = plan->off_o = 0;
-        plan->ws_bytes = 0;
-    }
+    plan->ws_bytes = partials_bytes(S, Hq, D, plan->NPmax, &plan->off_l, &plan->off_o);
     if (plan->ws_bytes > kMaxWorkspaceBytes)
         return fail(PGD_ERR_WORKSPACE,
                     "partials need %zu bytes, above the %zu-byte cap (lower the length bound "
@@ -633,13 +653,22 @@ pgd_status check_strides(const Strides &x, int D)
     return PGD_OK;
 }
 
+// A claim counter the caller provides (paged_gqa_decode_noalloc's, in its
+// static array) with its flag: set when a call failed after its partition
+// kernel may have moved the counter, so the next call zeroes it first.
+struct GivenCounter {
+    unsigned *word;
+    std::atomic<bool> *dirty;
+};
+
 // q8: the caches hold 8-bit codes (head-major) and k_meta / v_meta their
 // (scale, bias) pairs.
 pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v_cache,
                const int32_t *block_tables, const int32_t *seq_lens, float scale, int S, int Hq,
                int Hkv, int D, int BS, int P, int MB, int NB, const Strides &kv_strides,
                void *workspace, size_t ws_bytes, bool own_workspace, int32_t *page_trace,
-               void *stream_v, unsigned *counter = nullptr, const uint16_t *k_new = nullptr,
+               void *stream_v, const GivenCounter *given = nullptr,
+               const uint16_t *k_new = nullptr,
                const uint16_t *v_new = nullptr, bool q8 = false, const void *k_meta = nullptr,
                const void *v_meta = nullptr, const Strides *meta_strides = nullptr)
 {
@@ -765,27 +794,51 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     const KVMaps maps = {tk, tv, q8 && !q8_rows ? tkm : tk, q8 && !q8_rows ? tvm : tv};
 
     // claim counter: given (static scratch), this stream's, or a per-call one
+    auto release_ws = [&] {
+        if (own_workspace && ws)
+            cudaFreeAsync(ws, stream);
+    };
+    unsigned *counter = given ? given->word : nullptr;
     int slot = -1;
     unsigned *own_counter = nullptr;
-    if (!counter) {
+    if (given) {
+        // an earlier call on it failed after its partition kernel may have
+        // started: zero it in stream order first (allocates nothing)
+        if (given->dirty->load()) {
+            if ((e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream)) != cudaSuccess) {
+                release_ws();
+                return cuda_fail(e, "counter reset");
+            }
+            given->dirty->store(false);
+        }
+    } else {
         bool reset = false;
         if ((st = stream_counter(stream, &counter, &slot, &reset))) {
-            if (own_workspace && ws)
-                cudaFreeAsync(ws, stream);
+            release_ws();
             return st;
         }
         if (!counter) {  // every slot taken: a zeroed counter for this call only
             cudaMemPool_t pool;
-            if ((st = device_pool(*ds, &pool)))
+            if ((st = device_pool(*ds, &pool))) {
+                release_ws();
                 return st;
+            }
             if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&own_counter), 256, pool,
-                                             stream)) != cudaSuccess)
+                                             stream)) != cudaSuccess) {
+                release_ws();
                 return cuda_fail(e, "counter allocation");
+            }
             counter = own_counter;
             reset = true;
         }
-        if (reset && (e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream)) != cudaSuccess)
+        if (reset && (e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream)) != cudaSuccess) {
+            if (slot >= 0)
+                mark_counter_dirty(slot);
+            if (own_counter)
+                cudaFreeAsync(own_counter, stream);
+            release_ws();
             return cuda_fail(e, "counter reset");
+        }
     }
 
     DecodeParams p = {};
@@ -837,6 +890,8 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     lc.stream = stream;
     lc.ev_before = t_ev_before;
     lc.ev_after = t_ev_after;
+    lc.skip_reduce = t_skip_reduce;  // one call only
+    t_skip_reduce = false;
     const bool trace = page_trace != nullptr;
     e = D == 64    ? launch_decode_d64(BS, trace, q8, maps, p, lc)
         : D == 128 ? launch_decode_d128(BS, trace, q8, maps, p, lc)
@@ -851,9 +906,15 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
         if (e == cudaSuccess)
             e = e2;
     }
-    if (e != cudaSuccess) {
-        mark_counter_dirty(slot);  // the reduce may not have zeroed it
-        return cuda_fail(e, "kernel launch");
+    if (e != cudaSuccess || lc.skip_reduce) {
+        // the reduce may not have zeroed the counter
+        mark_counter_dirty(slot);
+        if (given)
+            given->dirty->store(true);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "kernel launch");
+        return fail(PGD_ERR_CUDA, "reduce launch withheld by pgd_test_fail_next_reduce (the "
+                                  "call's output is undefined)");
     }
     t_last_error.clear();
     return PGD_OK;
@@ -1079,17 +1140,20 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
     return PGD_OK;
 }
 
-// Device address of pgd_noalloc_scratch, looked up once per device (with
-// that device current) on the first paged_gqa_decode_noalloc call there.
+// Device address of pgd_noalloc_scratch on each device, looked up (with
+// that device current) by the first paged_gqa_decode_noalloc call there;
+// a failed lookup is not kept, the next call tries again.  `dirty` marks
+// the array's claim counter (its first word) as possibly non-zero after a
+// call that failed once its partition kernel could have started.
 struct NoAllocScratch {
-    std::once_flag once;
-    cudaError_t error = cudaSuccess;
+    std::mutex mu;
     void *ptr = nullptr;
+    std::atomic<bool> dirty{false};
 };
 
 NoAllocScratch g_noalloc[kMaxDevices];
 
-pgd_status noalloc_scratch(void **ptr)
+pgd_status noalloc_scratch(void **ptr, std::atomic<bool> **dirty)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1098,11 +1162,15 @@ pgd_status noalloc_scratch(void **ptr)
     if (dev < 0 || dev >= kMaxDevices)
         return fail(PGD_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
     NoAllocScratch &st = g_noalloc[dev];
-    std::call_once(st.once,
-                   [&] { st.error = cudaGetSymbolAddress(&st.ptr, pgd_noalloc_scratch); });
-    if (st.error != cudaSuccess)
-        return cuda_fail(st.error, "address of the static scratch");
+    std::lock_guard<std::mutex> lock(st.mu);
+    if (!st.ptr) {
+        void *p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, pgd_noalloc_scratch)) != cudaSuccess)
+            return cuda_fail(e, "address of the static scratch");
+        st.ptr = p;
+    }
     *ptr = st.ptr;
+    *dirty = &st.dirty;
     return PGD_OK;
 }
 
@@ -1195,14 +1263,16 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                     "paged_gqa_decode_ex",
                     plan.ws_bytes, (size_t)PGD_NOALLOC_SCRATCH_BYTES - 256);
     void *scratch = nullptr;
-    if ((st = noalloc_scratch(&scratch)))
+    std::atomic<bool> *dirty = nullptr;
+    if ((st = noalloc_scratch(&scratch, &dirty)))
         return st;
     // [256 B: claim counter, zero at load and after every call][partials]
+    const GivenCounter counter = {static_cast<unsigned *>(scratch), dirty};
     return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, num_seqs, num_q_heads,
                num_kv_heads, head_dim, block_size, partition_size, max_blocks_per_seq,
                num_blocks, head_major(num_kv_heads, block_size, head_dim),
                static_cast<char *>(scratch) + 256, PGD_NOALLOC_SCRATCH_BYTES - 256, false,
-               nullptr, stream, static_cast<unsigned *>(scratch));
+               nullptr, stream, &counter);
 }
 
 pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_codes,
@@ -1348,6 +1418,76 @@ pgd_status pgd_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_di
     return PGD_OK;
 }
 
+size_t pgd_workspace_size(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                          int partition_size, int max_blocks_per_seq)
+{
+    const size_t bad = ~(size_t)0;
+    if (num_seqs < 0 || num_q_heads <= 0) {
+        fail(PGD_ERR_INVALID_ARG, "num_seqs %d / num_q_heads %d", num_seqs, num_q_heads);
+        return bad;
+    }
+    if (!supported_head_dim(head_dim) || !supported_block_size(block_size)) {
+        fail(PGD_ERR_UNSUPPORTED, "no kernel for head_dim %d, block_size %d", head_dim,
+             block_size);
+        return bad;
+    }
+    if (partition_size != 0 && partition_size != kPartitionSmall &&
+        partition_size != kPartitionLarge) {
+        fail(PGD_ERR_INVALID_ARG, "partition_size %d not in {0, 256, 512}", partition_size);
+        return bad;
+    }
+    if (max_blocks_per_seq <= 0 || (long long)max_blocks_per_seq * block_size > (1ll << 30)) {
+        fail(PGD_ERR_INVALID_ARG, "max_blocks_per_seq %d (length bound up to 2^30)",
+             max_blocks_per_seq);
+        return bad;
+    }
+    // partition_size 0: the scheduler picks 512 or 256 at call time; 256
+    // needs at least as many partials, so its bytes cover either choice
+    const int P = partition_size ? partition_size : kPartitionSmall;
+    const long long maxlen = (long long)max_blocks_per_seq * block_size;
+    const int NPmax = (int)((maxlen + P - 1) / P);
+    size_t off_l, off_o;
+    t_last_error.clear();
+    return partials_bytes(num_seqs, num_q_heads, head_dim, NPmax, &off_l, &off_o);
+}
+
+pgd_status pgd_release(void)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PGD_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    // calls already queued on this device may still use the scratch and counters
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess)
+        return cuda_fail(e, "device synchronize");
+    DeviceState &ds = g_dev[dev];
+    {
+        std::lock_guard<std::mutex> lock(ds.pool_mu);
+        if (ds.pool) {
+            if ((e = cudaMemPoolTrimTo(ds.pool, 0)) != cudaSuccess ||
+                (e = cudaMemPoolDestroy(ds.pool)) != cudaSuccess)
+                return cuda_fail(e, "scratch pool release");
+            ds.pool = nullptr;
+        }
+    }
+    {
+        CounterPool &cp = g_counters[dev];
+        std::lock_guard<std::mutex> lock(cp.mu);
+        if (cp.base) {
+            if ((e = cudaFree(cp.base)) != cudaSuccess)
+                return cuda_fail(e, "claim-counter release");
+            cp.base = nullptr;
+            cp.slot_of.clear();
+            cp.dirty.clear();
+        }
+    }
+    t_maps_used = t_maps_next = 0;
+    t_last_error.clear();
+    return PGD_OK;
+}
+
 int pgd_last_partition_size(void) { return t_last_partition; }
 
 const char *pgd_last_error(void) { return t_last_error.c_str(); }
@@ -1357,6 +1497,13 @@ pgd_status pgd_test_stall_next_decode(const void *device_flag)
     if (device_flag && !aligned(device_flag, 4))
         return fail(PGD_ERR_INVALID_ARG, "stall flag not 4-byte aligned");
     t_stall_flag = static_cast<const unsigned *>(device_flag);
+    t_last_error.clear();
+    return PGD_OK;
+}
+
+pgd_status pgd_test_fail_next_reduce(int enable)
+{
+    t_skip_reduce = enable != 0;
     t_last_error.clear();
     return PGD_OK;
 }
@@ -1407,6 +1554,6 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
     return PGD_OK;
 }
 
-int pgd_version(void) { return 10300; }
+int pgd_version(void) { return 10400; }
 
 }  // extern "C"

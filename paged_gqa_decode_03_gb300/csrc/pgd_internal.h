@@ -144,6 +144,7 @@ struct LaunchConfig {
     int reduce_blocks;   // reduce-kernel CTAs
     cudaStream_t stream;
     cudaEvent_t ev_before, ev_after;  // optional timing hook (both or neither)
+    bool skip_reduce = false;         // test knob: launch the partition kernel only
 };
 
 // The tensor maps of one decode launch: K and V (fp16 rows, or 8-bit codes),

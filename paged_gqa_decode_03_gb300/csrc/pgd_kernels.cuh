@@ -19,13 +19,15 @@
 //        evict-first) plus one bulk copy of the group's queries, into a ring
 //        of shared-memory stages guarded by mbarriers.  Stage layout:
 //        [page][slab][row][128 B], whatever the layout in HBM.
-//      * consumer warps: per stage of T tokens, S^T = K Q^T on tensor cores
-//        (mma.sync m16n8k16, fp16 in, fp32 accumulate), scores exchanged
-//        through shared memory, one log2-space online-softmax update with
-//        exp2 ("Four speed-up tricks", 1), then O^T += V^T P^T on tensor
-//        cores.  At the unit's end: the final output (single-partition
-//        sequences) or the partition partial (log2-space max, exp-sum,
-//        normalised output) is written.
+//      * consumer warps: warp w owns the 16-token tile w of every stage and
+//        keeps its own running (max, exp-sum, O) per query head: S^T = K Q^T
+//        on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate), one
+//        log2-space online-softmax update with exp2 per tile ("Four speed-up
+//        tricks", 1), then O^T += V^T P^T on tensor cores; no exchange
+//        between warps within a unit.  At the unit's last stage the warps
+//        merge their running states in shared memory and write the final
+//        output (single-partition sequences) or the partition partial
+//        (log2-space max, exp-sum, normalised output).
 // 2. paged_gqa_reduce_kernel — merges the partition partials of every
 //    (sequence, query head) ("Four speed-up tricks", 4) and writes zeros for
 //    empty sequences.  Launched with programmatic dependent launch.
@@ -1183,6 +1185,8 @@ cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const Lau
         return e;
     if (lc.ev_after && (e = cudaEventRecord(lc.ev_after, lc.stream)) != cudaSuccess)
         return e;
+    if (lc.skip_reduce)  // pgd_test_fail_next_reduce: the caller reports the failure
+        return cudaSuccess;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -396,3 +396,25 @@ def make_q8(w: Workload, seed: int | None = None) -> Q8Caches:
         out += [codes, meta.view(torch.int16)]
     return Q8Caches(*out)
 
+
+
+def compact_q8(w: Workload, c: Q8Caches, seqs=None) -> dict:
+    """Numpy quantised caches holding only the pages the listed sequences own,
+    renumbered as in Workload.compact (codes uint8, (scale, bias) pairs as
+    uint16 bf16 bit patterns)."""
+    if seqs is None:
+        seqs = list(range(w.S))
+    seqs = [int(s) for s in seqs]
+    ids, bt, base = [], np.full((len(seqs), w.MB), -1, dtype=np.int32), 0
+    for i, s in enumerate(seqs):
+        a, b = int(w.page_offsets[s]), int(w.page_offsets[s + 1])
+        ids.append(w.page_ids[a:b])
+        bt[i, : b - a] = np.arange(base, base + b - a, dtype=np.int32)
+        base += b - a
+    dev = w.k_cache.device
+    idx = (torch.cat(ids) if base else torch.zeros(1, dtype=torch.int64)).to(dev)
+    take = lambda t: t.index_select(0, idx).cpu().numpy()
+    q = w.q[torch.tensor(seqs, dtype=torch.long, device=w.q.device)].cpu()
+    return dict(q=q.numpy(), k_codes=take(c.k_codes), k_meta=take(c.k_meta).view(np.uint16),
+                v_codes=take(c.v_codes), v_meta=take(c.v_meta).view(np.uint16),
+                block_tables=bt, seq_lens=w.lens[seqs].astype(np.int32), scale=w.scale)

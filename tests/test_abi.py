@@ -183,3 +183,55 @@ def test_stall_knob_arguments(lib):
     assert "aligned" in lib.pgd_last_error().decode()
     assert lib.pgd_test_stall_next_decode(A) == OK
     assert lib.pgd_test_stall_next_decode(ctypes.c_void_p(0)) == OK
+
+
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+
+def test_workspace_size_closed_form(lib):
+    """pgd_workspace_size is arithmetic on the sizes (no GPU): the partials
+    m, l [S][Hq][NP] and o [S][Hq][NP][D] fp32, each region rounded up to
+    256 bytes, NP = ceil(max_blocks_per_seq * block_size / partition_size)."""
+    # batch_decode geometry: 64 seqs, 32 query heads, D 128, BS 16, MB 256
+    # -> NP = 4096 / 512 = 8, rows = 64 * 32 * 8 = 16384
+    assert lib.pgd_workspace_size(64, 32, 128, 16, 512, 256) == 2 * 16384 * 4 + 16384 * 128 * 4
+    # a single partition needs no scratch
+    assert lib.pgd_workspace_size(64, 32, 128, 16, 512, 32) == 0
+    assert lib.pgd_workspace_size(64, 32, 128, 16, 256, 16) == 0
+    # rounding of each region: S 1, Hq 3, D 64, BS 8, P 256, MB 100
+    # -> NP = ceil(800 / 256) = 4, rows = 12: m 48 -> 256, l 48 -> 256, o 3072
+    assert lib.pgd_workspace_size(1, 3, 64, 8, 256, 100) == 256 + 256 + 3072
+    # no sequences, no scratch
+    assert lib.pgd_workspace_size(0, 32, 128, 16, 512, 256) == 0
+    # partition_size 0 reports the bytes of 256 (the larger of the two)
+    assert (lib.pgd_workspace_size(64, 32, 128, 16, 0, 256) ==
+            lib.pgd_workspace_size(64, 32, 128, 16, 256, 256) >
+            lib.pgd_workspace_size(64, 32, 128, 16, 512, 256))
+    assert pgd.pgd_workspace_size(64, 32, 128, 16, 512, 256) == 2 * 16384 * 4 + 16384 * 128 * 4
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 32, 128, 16, 512, 256), (4, 0, 128, 16, 512, 256), (4, 32, 96, 16, 512, 256),
+    (4, 32, 128, 12, 512, 256), (4, 32, 128, 16, 300, 256), (4, 32, 128, 16, 512, 0),
+    (4, 32, 128, 128, 512, 1 << 24),
+])
+def test_workspace_size_rejects_bad_sizes(lib, args):
+    assert lib.pgd_workspace_size(*args) == SIZE_MAX
+    assert lib.pgd_last_error().decode() != ""
+    with pytest.raises(pgd.PGDError):
+        pgd.pgd_workspace_size(*args)
+
+
+def test_release_without_a_device_reports_cuda_error(lib):
+    """pgd_release waits for the current device first; with no GPU that
+    wait cannot happen and the call reports it instead of crashing."""
+    import torch
+    st = lib.pgd_release()
+    assert st == (OK if torch.cuda.is_available() else 4), lib.pgd_last_error()
+
+
+def test_fail_reduce_knob_arguments(lib):
+    """The failure-injection knob is a host flag: set and cancelled without
+    launching anything."""
+    assert lib.pgd_test_fail_next_reduce(1) == OK
+    assert lib.pgd_test_fail_next_reduce(0) == OK

@@ -14,12 +14,13 @@ import torch
 
 import paged_gqa_decode_03_gb300 as pgd
 from paged_gqa_decode_03_gb300.workloads import make_workload
-from parity_util import ATOL, RTOL, errors
+from parity_util import ATOL, RTOL, assert_parity, errors, oracle_out
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 PGD_ERR_WORKSPACE = 3
+PGD_ERR_CUDA = 4
 
 
 @pytest.fixture(scope="module")
@@ -52,6 +53,7 @@ def test_noalloc_matches_default_on_consecutive_calls(lib):
         ref = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
         pgd.paged_gqa_decode(ref, w.q, w.k_cache, w.v_cache, w.block_tables, w.seq_lens,
                              w.scale, P)
+        exact = oracle_out(w)      # the fp64 definition, independent of both GPU calls
         for call in range(2):
             out = torch.full_like(ref, float("nan"))
             assert _noalloc(lib, w, out, P) == 0, lib.pgd_last_error()
@@ -60,6 +62,27 @@ def test_noalloc_matches_default_on_consecutive_calls(lib):
             assert np.all(np.isfinite(got)), f"{w.name} call {call}"
             ab, rel = errors(got, ref.cpu().numpy())
             assert ab <= ATOL and rel <= RTOL, f"{w.name} call {call}: {ab:.2e} {rel:.2e}"
+            assert_parity(got, exact, f"{w.name} call {call} against the oracle")
+    assert pgd.pgd_check_device_error() == 0
+
+
+def test_noalloc_after_a_failed_call_is_exact(lib):
+    """A call that fails after its partition kernel started (injected on the
+    host: the reduce launch withheld) leaves the array's work counter
+    non-zero; the next calls must zero it first (without allocating) and be
+    exact."""
+    w = make_workload("batch_decode", device=DEV, S=24, seed=24)
+    exact = oracle_out(w)
+    out = torch.full((w.S, w.Hq, w.D), float("nan"), dtype=torch.float32, device=DEV)
+    assert lib.pgd_test_fail_next_reduce(1) == 0
+    assert _noalloc(lib, w, out, 512) == PGD_ERR_CUDA
+    assert b"withheld" in lib.pgd_last_error()
+    torch.cuda.synchronize()
+    for call in range(2):
+        out.fill_(float("nan"))
+        assert _noalloc(lib, w, out, 512) == 0, lib.pgd_last_error()
+        torch.cuda.synchronize()
+        assert_parity(out.cpu().numpy(), exact, f"call {call} after the failed one")
     assert pgd.pgd_check_device_error() == 0
 
 
