@@ -294,6 +294,44 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                                     int num_blocks, void *stream);
 
 /*
+ * paged_gqa_decode_host — the decode step for a caller whose per-step inputs
+ * live in host memory: the page tables and lengths that a host-side block
+ * manager and scheduler produce each step ("vllm-metal", introduction: the
+ * serving framework above the attention path owns the scheduler and the
+ * paged block manager), and the step's queries.  The K/V cache stays
+ * resident on the device.
+ *
+ * q_host, block_tables_host, seq_lens_host  host memory, layouts as for
+ *              paged_gqa_decode (read); out_host  host memory (written).
+ *              Page-locked host memory (cudaHostAlloc / cudaHostRegister)
+ *              lets the copies run as direct transfers; pageable memory also
+ *              works, through the driver's bounce buffer.
+ * k_cache, v_cache  device, as for paged_gqa_decode.
+ * staging      device memory of at least pgd_host_staging_bytes() bytes,
+ *              256-byte aligned, caller-owned: the device copies of q,
+ *              block_tables, seq_lens and out.  It must not be used by
+ *              anything else until the call returns.
+ * The call copies the inputs to `staging` on `stream`, runs the decode there
+ * (partition partials from the library's scratch pool, as paged_gqa_decode),
+ * copies the output back and waits for `stream`: when it returns PGD_OK,
+ * out_host holds the result.  Validation and error reporting as for
+ * paged_gqa_decode; a failed copy or wait returns PGD_ERR_CUDA.
+ */
+pgd_status paged_gqa_decode_host(float *out_host, const uint16_t *q_host,
+                                 const int32_t *block_tables_host, const int32_t *seq_lens_host,
+                                 const uint16_t *k_cache, const uint16_t *v_cache, float scale,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int partition_size, int max_blocks_per_seq,
+                                 int num_blocks, void *staging, size_t staging_bytes,
+                                 void *stream);
+
+/* Bytes of device staging paged_gqa_decode_host needs for these sizes (q,
+ * block_tables, seq_lens and out, each region 256-byte aligned); SIZE_MAX
+ * for invalid sizes.  Needs no GPU. */
+size_t pgd_host_staging_bytes(int num_seqs, int num_q_heads, int head_dim,
+                              int max_blocks_per_seq);
+
+/*
  * paged_gqa_decode_q8 — the decode step over quantised pages: the affine
  * group format of the Kapitsa series (blog.hacking.pub, part 02, "how
  * weights are stored": a value is scale * q + bias with an unsigned integer
@@ -490,7 +528,8 @@ pgd_status pgd_device_info(int head_dim, int block_size, int *num_sms, int *ctas
 
 /* Library version, major * 10000 + minor * 100 + patch (1.1.0: strided caches,
  * head_dim 64, block sizes 64 and 128; 1.2.0: several query tokens per
- * sequence; 1.3.0: quantised pages; 1.4.0: pgd_workspace_size, pgd_release). */
+ * sequence; 1.3.0: quantised pages; 1.4.0: pgd_workspace_size, pgd_release,
+ * paged_gqa_decode_host). */
 int pgd_version(void);
 
 #ifdef __cplusplus

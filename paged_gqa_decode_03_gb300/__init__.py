@@ -27,6 +27,7 @@ import threading
 import torch
 
 __all__ = ["paged_gqa_decode", "paged_gqa_decode_ex", "paged_gqa_decode_noalloc",
+           "paged_gqa_decode_host", "pgd_host_staging_bytes",
            "paged_gqa_decode_append", "paged_gqa_decode_strided", "kv_strides",
            "paged_gqa_varlen", "pgd_varlen_plan", "paged_gqa_decode_q8",
            "paged_gqa_decode_q8_append", "paged_gqa_decode_q8_strided", "q8_strides",
@@ -52,6 +53,8 @@ SIGNATURES = {
     "paged_gqa_decode": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_ex": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P, _P]),
     "paged_gqa_decode_noalloc": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P]),
+    "paged_gqa_decode_host": (_I, [_P] * 6 + [_F] + [_I] * 8 + [_P, _Z, _P]),
+    "pgd_host_staging_bytes": (_Z, [_I] * 4),
     "paged_gqa_decode_append": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_P]),
     "paged_gqa_decode_strided": (_I, [_P] * 8 + [_F] + [_I] * 8 + [_L] * 3 + [_P, _Z, _P, _P]),
     "paged_gqa_varlen": (_I, [_P] * 7 + [_F] + [_I] * 9 + [_L] * 3 + [_I, _P, _Z, _P]),
@@ -504,6 +507,49 @@ def paged_gqa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, s
                                       _ptr(block_tables), _ptr(seq_lens), float(scale), S, Hq,
                                       Hkv, D, BS, int(partition_size), MB, NB,
                                       _stream_handle(stream, q.device))
+    _raise(st)
+
+
+def pgd_host_staging_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq) -> int:
+    """Device staging bytes of paged_gqa_decode_host (needs no GPU)."""
+    n = load_library().pgd_host_staging_bytes(num_seqs, num_q_heads, head_dim,
+                                              max_blocks_per_seq)
+    if n == ctypes.c_size_t(-1).value:
+        raise PGDError(1, pgd_last_error())
+    return int(n)
+
+
+def paged_gqa_decode_host(out_host, q_host, block_tables_host, seq_lens_host, k_cache, v_cache,
+                          scale, staging, partition_size: int = 0, stream=None) -> None:
+    """The decode step with the step's inputs and output in host memory
+    (CPU tensors, preferably pinned); k_cache / v_cache and ``staging`` (a
+    uint8 CUDA tensor of at least pgd_host_staging_bytes) on the device.
+    Returns once ``out_host`` holds the result."""
+    lib = load_library()
+    for t, name in ((out_host, "out_host"), (q_host, "q_host"),
+                    (block_tables_host, "block_tables_host"), (seq_lens_host, "seq_lens_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: a contiguous CPU tensor")
+    if (q_host.dtype != torch.float16 or out_host.dtype != torch.float32 or
+            block_tables_host.dtype != torch.int32 or seq_lens_host.dtype != torch.int32):
+        raise TypeError("q_host fp16, out_host fp32, block_tables_host / seq_lens_host int32")
+    _check(k_cache, "k_cache", torch.float16, 4)
+    _check(v_cache, "v_cache", torch.float16, 4)
+    if not (staging.is_cuda and staging.is_contiguous()):
+        raise ValueError("staging: a contiguous CUDA tensor")
+    if q_host.dim() != 3 or block_tables_host.dim() != 2 or seq_lens_host.dim() != 1:
+        raise ValueError("q_host [S, Hq, D], block_tables_host [S, MB], seq_lens_host [S]")
+    S, Hq, D = q_host.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    MB = block_tables_host.shape[1]
+    if (v_cache.shape != k_cache.shape or D2 != D or tuple(out_host.shape) != (S, Hq, D) or
+            block_tables_host.shape[0] != S or seq_lens_host.shape[0] != S):
+        raise ValueError("inconsistent shapes")
+    st = lib.paged_gqa_decode_host(_ptr(out_host), _ptr(q_host), _ptr(block_tables_host),
+                                   _ptr(seq_lens_host), _ptr(k_cache), _ptr(v_cache),
+                                   float(scale), S, Hq, Hkv, D, BS, int(partition_size), MB, NB,
+                                   _ptr(staging), staging.numel() * staging.element_size(),
+                                   _stream_handle(stream, k_cache.device))
     _raise(st)
 
 

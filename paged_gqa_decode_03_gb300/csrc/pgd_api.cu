@@ -1174,6 +1174,24 @@ pgd_status noalloc_scratch(void **ptr, std::atomic<bool> **dirty)
     return PGD_OK;
 }
 
+// Device staging of paged_gqa_decode_host: q [S][Hq][D] fp16, block_tables
+// [S][MB] int32, seq_lens [S] int32, out [S][Hq][D] fp32, each region
+// 256-byte aligned.
+struct HostStaging {
+    size_t q, bt, sl, out, bytes;
+};
+
+HostStaging host_staging(int S, int Hq, int D, int MB)
+{
+    HostStaging h;
+    h.q = 0;
+    h.bt = align256((size_t)S * Hq * D * 2);
+    h.sl = h.bt + align256((size_t)S * MB * 4);
+    h.out = h.sl + align256((size_t)S * 4);
+    h.bytes = h.out + align256((size_t)S * Hq * D * 4);
+    return h;
+}
+
 }  // namespace
 }  // namespace pgd
 
@@ -1273,6 +1291,67 @@ pgd_status paged_gqa_decode_noalloc(float *out, const uint16_t *q, const uint16_
                num_blocks, head_major(num_kv_heads, block_size, head_dim),
                static_cast<char *>(scratch) + 256, PGD_NOALLOC_SCRATCH_BYTES - 256, false,
                nullptr, stream, &counter);
+}
+
+size_t pgd_host_staging_bytes(int num_seqs, int num_q_heads, int head_dim,
+                              int max_blocks_per_seq)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0) {
+        fail(PGD_ERR_INVALID_ARG, "num_seqs %d, num_q_heads %d, head_dim %d, max_blocks_per_seq %d",
+             num_seqs, num_q_heads, head_dim, max_blocks_per_seq);
+        return ~(size_t)0;
+    }
+    t_last_error.clear();
+    return host_staging(num_seqs, num_q_heads, head_dim, max_blocks_per_seq).bytes;
+}
+
+pgd_status paged_gqa_decode_host(float *out_host, const uint16_t *q_host,
+                                 const int32_t *block_tables_host, const int32_t *seq_lens_host,
+                                 const uint16_t *k_cache, const uint16_t *v_cache, float scale,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int partition_size, int max_blocks_per_seq,
+                                 int num_blocks, void *staging, size_t staging_bytes,
+                                 void *stream_v)
+{
+    const int S = num_seqs, Hq = num_q_heads, D = head_dim, MB = max_blocks_per_seq;
+    pgd_status st = check_sizes(S, Hq, num_kv_heads, D, block_size, partition_size, MB);
+    if (st)
+        return st;
+    if (S == 0)
+        return run(nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, scale, S, Hq,
+                   num_kv_heads, D, block_size, partition_size, MB, num_blocks,
+                   head_major(num_kv_heads, block_size, D), nullptr, 0, true, nullptr, stream_v);
+    if (!out_host || !q_host || !block_tables_host || !seq_lens_host || !staging)
+        return fail(PGD_ERR_INVALID_ARG, "null array argument");
+    const HostStaging hs = host_staging(S, Hq, D, MB);
+    if (!aligned(staging, 256) || staging_bytes < hs.bytes)
+        return fail(PGD_ERR_WORKSPACE, "staging of %zu bytes (256-byte aligned) given, %zu needed",
+                    staging_bytes, hs.bytes);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    char *dev = static_cast<char *>(staging);
+    uint16_t *q = reinterpret_cast<uint16_t *>(dev + hs.q);
+    int32_t *bt = reinterpret_cast<int32_t *>(dev + hs.bt);
+    int32_t *sl = reinterpret_cast<int32_t *>(dev + hs.sl);
+    float *out = reinterpret_cast<float *>(dev + hs.out);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(q, q_host, (size_t)S * Hq * D * 2, cudaMemcpyHostToDevice,
+                             stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(bt, block_tables_host, (size_t)S * MB * 4, cudaMemcpyHostToDevice,
+                             stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sl, seq_lens_host, (size_t)S * 4, cudaMemcpyHostToDevice,
+                             stream)) != cudaSuccess)
+        return cuda_fail(e, "copy of the step's inputs to the device");
+    if ((st = run(out, q, k_cache, v_cache, bt, sl, scale, S, Hq, num_kv_heads, D, block_size,
+                  partition_size, MB, num_blocks, head_major(num_kv_heads, block_size, D),
+                  nullptr, 0, true, nullptr, stream_v)))
+        return st;
+    if ((e = cudaMemcpyAsync(out_host, out, (size_t)S * Hq * D * 4, cudaMemcpyDeviceToHost,
+                             stream)) != cudaSuccess)
+        return cuda_fail(e, "copy of the output to the host");
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return cuda_fail(e, "stream synchronize");
+    t_last_error.clear();
+    return PGD_OK;
 }
 
 pgd_status paged_gqa_decode_q8(float *out, const uint16_t *q, const uint8_t *k_codes,

@@ -235,3 +235,32 @@ def test_fail_reduce_knob_arguments(lib):
     launching anything."""
     assert lib.pgd_test_fail_next_reduce(1) == OK
     assert lib.pgd_test_fail_next_reduce(0) == OK
+
+
+def test_host_staging_bytes_closed_form(lib):
+    """q fp16, block_tables and seq_lens int32, out fp32, each region rounded
+    up to 256 bytes (pure arithmetic, no GPU)."""
+    # 64 seqs, 32 heads, D 128, MB 256: 524288 + 65536 + 256 + 1048576
+    assert lib.pgd_host_staging_bytes(64, 32, 128, 256) == 524288 + 65536 + 256 + 1048576
+    # 3 seqs, 4 heads, D 64, MB 5: q 1536, bt 60 -> 256, sl 12 -> 256, out 3072
+    assert lib.pgd_host_staging_bytes(3, 4, 64, 5) == 1536 + 256 + 256 + 3072
+    assert lib.pgd_host_staging_bytes(-1, 4, 64, 5) == SIZE_MAX
+    assert pgd.pgd_host_staging_bytes(3, 4, 64, 5) == 5120
+
+
+def call_host(lib, host=(A, A, A, A), staging=A, staging_bytes=1 << 30, S=4, D=128):
+    return lib.paged_gqa_decode_host(*host, A, A, ctypes.c_float(0.1), S, 32, 8, D, 16, 512, 64,
+                                     1024, staging, staging_bytes, ctypes.c_void_p(0))
+
+
+def test_host_entry_validation(lib):
+    """Rejected before any copy or launch (no GPU needed)."""
+    for i in range(4):
+        host = [A] * 4
+        host[i] = ctypes.c_void_p(0)
+        assert call_host(lib, host=host) == INVALID
+    assert call_host(lib, staging=ctypes.c_void_p(0)) == INVALID
+    need = lib.pgd_host_staging_bytes(4, 32, 128, 64)
+    assert call_host(lib, staging_bytes=need - 1) == WORKSPACE
+    assert call_host(lib, staging=ctypes.c_void_p((1 << 20) + 128)) == WORKSPACE
+    assert call_host(lib, D=96) == UNSUPPORTED
