@@ -761,6 +761,13 @@ def run_varlen_bench(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # which kernel the library runs: the decode kernel's MQ form when every
+    # (sequence, KV head) has at most 8 (query token, head) rows (head_dim
+    # <= 128), else tcgen05 pairs of query tiles at head_dim 64 / 128 when a
+    # sequence may hold more than one tile (128 / G query tokens)
+    G = w.Hq // w.Hkv
+    mq = w.D <= 128 and G <= 8 and w.max_q_len * G <= 8 and kvp in (0, 256, 512)
+    pairs = not mq and w.D <= 128 and w.max_q_len > 128 // G
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -774,10 +781,15 @@ def run_varlen_bench(args):
             step()
         ev1.record(stream)
         barrier()
-        for i in range(args.steps):  # per-call events (kernel time incl. its reduce if any)
-            kb[i].record(stream)
-            step()
-            ka[i].record(stream)
+        for i in range(args.steps):
+            if mq:  # the partition kernel alone (the library's timing hook)
+                pgd.pgd_set_timing_events(kb[i], ka[i])
+                step()
+            else:   # per-call events (kernel time incl. its reduce if any)
+                kb[i].record(stream)
+                step()
+                ka[i].record(stream)
+        pgd.pgd_set_timing_events(None, None)
         barrier()
     clocks = clk.summary()
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
@@ -850,14 +862,14 @@ def run_varlen_bench(args):
                          f"fp64 C oracle, {sec * 1e3:.1f} ms per call"}
 
     if rank == 0:
+        src_hash = kernel_source_hash(DECODE_HASH_EXCLUDE if mq else VARLEN_HASH_EXCLUDE)
         if tensor_bound:
             metric = "paged varlen attention (several query tokens per sequence): TFLOP/s"
             value, unit = tflops, "TFLOP/s"
             achieved = flops / (kern_ms * 1e-3) / 1e12
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t, "frac_of_sustained": achieved / peak_t_sus,
-                    "traffic": TRAFFIC.get(kernel_source_hash(VARLEN_HASH_EXCLUDE), {}).get(
-                        (args.workload, PK)),
+                    "traffic": TRAFFIC.get(src_hash, {}).get((args.workload, PK)),
                     "peak_source": f"{peak_kind} (MEASURED_PEAKS bf16_tflops; fp16 at the bf16 rate)",
                     "algorithmic_flops_per_launch": flops}
             e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
@@ -867,15 +879,12 @@ def run_varlen_bench(args):
             achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peak_b, "unit": "GB/s",
                     "frac": achieved / peak_b,
-                    "traffic": TRAFFIC.get(kernel_source_hash(VARLEN_HASH_EXCLUDE), {}).get(
-                        (args.workload, PK)),
+                    "traffic": TRAFFIC.get(src_hash, {}).get((args.workload, PK)),
                     "peak_source": "measured (MEASURED_PEAKS hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg_bytes}
             e2e_val = kv_bytes * world / (e2e_ms * 1e-3) / 1e9
-        # which kernel the library runs: pairs of query tiles at head_dim 64 /
-        # 128 when a sequence may hold more than one tile (128 / G query tokens)
-        pairs = w.D <= 128 and w.max_q_len > 128 // (w.Hq // w.Hkv)
-        roof.update(kernel="paged_varlen_pair_kernel" if pairs else "paged_varlen_kernel",
+        roof.update(kernel="paged_gqa_partial_kernel (MQ form)" if mq else
+                    "paged_varlen_pair_kernel" if pairs else "paged_varlen_kernel",
                     kernel_ms=kern_ms)
         line = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world,

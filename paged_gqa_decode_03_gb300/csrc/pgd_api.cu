@@ -58,7 +58,7 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_error = cudaSuccess;
     int num_sms = 0;
-    int ctas[2][3][5] = {};         // [quantised pages][head_dim 64/128/256][block size 8..128]
+    int ctas[3][3][5] = {};         // [kind: fp16, quantised, MQ][head_dim 64/128/256][block size]
     unsigned *err_word = nullptr;   // address of g_device_error on this device
     std::mutex pool_mu;             // the pool is made on first library-owned scratch
     cudaMemPool_t pool = nullptr;   //   (and again after pgd_release): stream-ordered scratch
@@ -91,13 +91,13 @@ cudaError_t init_device(int dev, DeviceState &st)
     cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    for (int q8 = 0; q8 < 2; ++q8)
+    for (int kind = 0; kind < 3; ++kind)
         for (int i = 0; i < 5; ++i) {
-            if ((e = occupancy_d64(kBlockSizes[i], q8, &st.ctas[q8][0][i])) != cudaSuccess)
+            if ((e = occupancy_d64(kBlockSizes[i], kind, &st.ctas[kind][0][i])) != cudaSuccess)
                 return e;
-            if ((e = occupancy_d128(kBlockSizes[i], q8, &st.ctas[q8][1][i])) != cudaSuccess)
+            if ((e = occupancy_d128(kBlockSizes[i], kind, &st.ctas[kind][1][i])) != cudaSuccess)
                 return e;
-            if ((e = occupancy_d256(kBlockSizes[i], q8, &st.ctas[q8][2][i])) != cudaSuccess)
+            if ((e = occupancy_d256(kBlockSizes[i], kind, &st.ctas[kind][2][i])) != cudaSuccess)
                 return e;
         }
     return cudaGetSymbolAddress(reinterpret_cast<void **>(&st.err_word), g_device_error);
@@ -589,8 +589,10 @@ int choose_partition(int S, int Hkv, int maxlen, int num_sms, int ctas_per_sm)
     return full512 >= target ? kPartitionLarge : kPartitionSmall;
 }
 
+// kind: 0 fp16 pages, 1 quantised pages, 2 several query tokens per sequence
+// (the MQ form, whose partials are kept per query row: prow rows instead of S)
 pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan *plan,
-                     bool q8 = false)
+                     int kind = 0, int prow = -1)
 {
     pgd_status st = check_sizes(S, Hq, Hkv, D, BS, P, MB);
     if (st)
@@ -598,7 +600,9 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     DeviceState *ds;
     if ((st = device_state(&ds)))
         return st;
-    const int ctas = ds->ctas[q8][d_index(D)][bs_index(BS)];
+    if (prow < 0)
+        prow = S;
+    const int ctas = ds->ctas[kind][d_index(D)][bs_index(BS)];
     if (ctas < 1)
         return fail(PGD_ERR_UNSUPPORTED, "partition kernel does not fit on an SM");
     const int maxlen = MB * BS;
@@ -612,7 +616,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     if (stage_bound >= (1ll << 31))
         return fail(PGD_ERR_UNSUPPORTED, "batch of %d sequences x %d KV heads x %d tokens too large",
                     S, Hkv, maxlen);
-    plan->ws_bytes = partials_bytes(S, Hq, D, plan->NPmax, &plan->off_l, &plan->off_o);
+    plan->ws_bytes = partials_bytes(prow, Hq, D, plan->NPmax, &plan->off_l, &plan->off_o);
     if (plan->ws_bytes > kMaxWorkspaceBytes)
         return fail(PGD_ERR_WORKSPACE,
                     "partials need %zu bytes, above the %zu-byte cap (lower the length bound "
@@ -621,7 +625,7 @@ pgd_status make_plan(int S, int Hq, int Hkv, int D, int BS, int P, int MB, Plan 
     const long long units = (long long)S * Hkv * plan->NPmax;
     const long long slots = (long long)ds->num_sms * ctas;
     plan->grid = (int)(units < slots ? (units > 0 ? units : 1) : slots);
-    plan->reduce_blocks = (int)((long long)S * Hq);
+    plan->reduce_blocks = (int)((long long)prow * Hq);
     if (plan->reduce_blocks < 1)
         plan->reduce_blocks = 1;
     return PGD_OK;
@@ -653,6 +657,13 @@ pgd_status check_strides(const Strides &x, int D)
     return PGD_OK;
 }
 
+// Several query tokens per sequence on the decode kernel (its MQ form):
+// the query rows of each sequence (cu_q), their total and bound.
+struct MultiQuery {
+    const int32_t *cu_q;
+    int total_q, max_q;
+};
+
 // A claim counter the caller provides (paged_gqa_decode_noalloc's, in its
 // static array) with its flag: set when a call failed after its partition
 // kernel may have moved the counter, so the next call zeroes it first.
@@ -670,13 +681,16 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                void *stream_v, const GivenCounter *given = nullptr,
                const uint16_t *k_new = nullptr,
                const uint16_t *v_new = nullptr, bool q8 = false, const void *k_meta = nullptr,
-               const void *v_meta = nullptr, const Strides *meta_strides = nullptr)
+               const void *v_meta = nullptr, const Strides *meta_strides = nullptr,
+               const MultiQuery *mq = nullptr)
 {
     if (q8 && D % 128 != 0)
         return fail(PGD_ERR_UNSUPPORTED, "quantised pages need head_dim 128 or 256, not %d", D);
+    const int kind = mq ? 2 : q8 ? 1 : 0;
+    const int prow = mq ? mq->total_q : S;
     if (S == 0) {  // nothing to read or write: only the sizes are checked
         Plan plan;
-        pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, q8);
+        pgd_status st0 = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, kind, prow);
         if (st0)
             return st0;
         t_last_partition = plan.P;
@@ -729,8 +743,13 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     }
     if (!own_workspace && workspace && !aligned(workspace, 256))
         return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (mq && (!mq->cu_q || D > 128 || mq->total_q < 0 || mq->max_q < 1 ||
+               (long long)mq->max_q * (Hq / Hkv) > kMaxCols || q8 || k_new || page_trace))
+        return fail(PGD_ERR_UNSUPPORTED, "several query tokens on the decode kernel: head_dim "
+                                         "<= 128, max_q_len * group <= %d, fp16 pages only",
+                    kMaxCols);
     Plan plan;
-    if ((st = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, q8)))
+    if ((st = make_plan(S, Hq, Hkv, D, BS, P, MB, &plan, kind, prow)))
         return st;
     DeviceState *ds;
     if ((st = device_state(&ds)))
@@ -883,6 +902,9 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.wait_budget_ns = kWaitBudgetNs;
     p.stall_flag = t_stall_flag;  // one call only
     t_stall_flag = nullptr;
+    p.cu_q = mq ? mq->cu_q : nullptr;
+    p.max_q = mq ? mq->max_q : 0;
+    p.total_q = mq ? mq->total_q : 0;
 
     LaunchConfig lc;
     lc.grid = plan.grid;
@@ -946,6 +968,7 @@ pgd_status encode_q_map(CUtensorMap *map, const void *q, int total_q, int Hq, in
 
 struct VarlenPlan {
     int G, TQ, QT, QP, PK, NP, NT;
+    bool mq;       // few query rows per (sequence, KV head): the decode kernel's MQ form
     bool pairs;    // two query tiles per CTA
     bool ordered;  // units sorted longest first on the device (more than one wave)
     long long grid;
@@ -986,6 +1009,30 @@ pgd_status make_varlen_plan(int S, int total_q, int max_q, int Hq, int Hkv, int 
     if ((st = device_state(&ds)))
         return st;
     vp->G = Hq / Hkv;
+    // Calls with at most kMaxCols (query token, head) rows per (sequence, KV
+    // head) — decode steps, the verification step of speculative decoding —
+    // read each K/V byte for only a few rows: an HBM-bound scan, which the
+    // decode kernel's MQ form does (mma.sync over 16 columns, partitions of
+    // 256 / 512 tokens chosen as for the decode, partials per query row).
+    vp->mq = D <= 128 && vp->G <= kMaxGroup && max_q >= 1 &&
+             (long long)max_q * vp->G <= kMaxCols &&
+             (kv_partition == 0 || kv_partition == kPartitionSmall ||
+              kv_partition == kPartitionLarge);
+    if (vp->mq) {
+        Plan plan;
+        if ((st = make_plan(S, Hq, Hkv, D, BS, kv_partition, MB, &plan, 2, total_q)))
+            return st;
+        vp->TQ = vp->QT = vp->QP = 1;
+        vp->PK = plan.P;
+        vp->NP = plan.NPmax;
+        vp->pairs = vp->ordered = false;
+        vp->grid = plan.grid;
+        vp->ws_bytes = plan.ws_bytes;
+        vp->off_l = plan.off_l;
+        vp->off_o = plan.off_o;
+        vp->off_order = 0;
+        return PGD_OK;
+    }
     vp->TQ = 128 / vp->G;
     vp->QT = (max_q + vp->TQ - 1) / vp->TQ;
     // two query tiles per CTA where they fit in tensor memory and the
@@ -1066,6 +1113,12 @@ pgd_status run_varlen(float *out, const uint16_t *q, const int32_t *cu_q, const 
         return fail(PGD_ERR_INVALID_ARG, "int32 arrays must be 4-byte aligned");
     if ((st = check_strides(kv_strides, D)))
         return st;
+    if (vp.mq) {  // the decode kernel's MQ form (its scratch, tensor maps and launches)
+        const MultiQuery mq = {cu_q, total_q, max_q};
+        return run(out, q, k_cache, v_cache, block_tables, seq_lens, scale, S, Hq, Hkv, D, BS,
+                   vp.PK, MB, NB, kv_strides, workspace, ws_bytes, workspace == nullptr, nullptr,
+                   stream_v, nullptr, nullptr, nullptr, false, nullptr, nullptr, nullptr, &mq);
+    }
     DeviceState *ds;
     if ((st = device_state(&ds)))
         return st;

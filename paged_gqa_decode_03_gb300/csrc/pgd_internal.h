@@ -17,6 +17,11 @@ constexpr int kPartitionLarge = 512;
 constexpr int kPartitionSmall = 256;
 // Most query heads per KV head one CTA handles (one n8 tensor-core tile).
 constexpr int kMaxGroup = 8;
+// Several query tokens per sequence on the decode kernel (its MQ form, for
+// calls with few query rows per (sequence, KV head): decode steps, short
+// verification steps): up to 8 columns (query token x head of the group,
+// one n8 tile, as many as the group's heads in a decode) per unit.
+constexpr int kMaxCols = 8;
 // Cap on the per-call scratch ("Dispatch layer": 512 MiB).
 constexpr size_t kMaxWorkspaceBytes = size_t(512) << 20;
 // Bound on every internal pipeline wait before it reports a timeout.
@@ -50,7 +55,10 @@ template <> struct Shape<256> {
     static constexpr int T = 32, NC = 2, NS = 3, T8 = 64, NC8 = 4, NS8 = 2;
 };
 template <int D, bool Q8> __host__ __device__ constexpr int stage_tokens_of() { return Q8 ? Shape<D>::T8 : Shape<D>::T; }
-template <int D, bool Q8> __host__ __device__ constexpr int consumer_warps() { return Q8 ? Shape<D>::NC8 : Shape<D>::NC; }
+template <int D, bool Q8, bool MQ = false> __host__ __device__ constexpr int consumer_warps()
+{
+    return Q8 ? Shape<D>::NC8 : Shape<D>::NC;
+}
 
 // Quantised pages: 8-bit codes plus one (scale, bias) bf16 pair per 64
 // values of a row.
@@ -74,10 +82,14 @@ template <int D, bool Q8, int BS> __host__ __device__ constexpr int stage_meta_b
     constexpr int T = stage_tokens_of<D, Q8>(), BOX = BS < T ? BS : T;
     return Q8 ? (T / BOX) * meta_slot_bytes(BOX, D) : 0;
 }
-template <int D> __host__ __device__ constexpr int stage_q_bytes() { return kMaxGroup * D * 2; }
-template <int D, bool Q8, int BS> __host__ __device__ constexpr int stage_bytes()
+template <int D, bool MQ = false> __host__ __device__ constexpr int stage_q_bytes()
 {
-    return 2 * stage_kv_bytes<D, Q8>() + 2 * stage_meta_bytes<D, Q8, BS>() + stage_q_bytes<D>();
+    return (MQ ? kMaxCols : kMaxGroup) * D * 2;
+}
+template <int D, bool Q8, int BS, bool MQ = false> __host__ __device__ constexpr int stage_bytes()
+{
+    return 2 * stage_kv_bytes<D, Q8>() + 2 * stage_meta_bytes<D, Q8, BS>() +
+           stage_q_bytes<D, MQ>();
 }
 // Shared memory of one SM, and what a CTA needs beside its ring (the
 // system's 1 KB, the static barriers and stage headers, the alignment slack).
@@ -96,9 +108,9 @@ template <int D, bool Q8, int BS> __host__ __device__ constexpr int ring_stages(
 }
 // Dynamic shared memory: the ring plus slack to align it to 1024 bytes
 // (required by the 128-byte swizzle of the tensor copies).
-template <int D, bool Q8, int BS> __host__ __device__ constexpr size_t dyn_smem_bytes()
+template <int D, bool Q8, int BS, bool MQ = false> __host__ __device__ constexpr size_t dyn_smem_bytes()
 {
-    return size_t(ring_stages<D, Q8, BS>()) * stage_bytes<D, Q8, BS>() + 1024;
+    return size_t(ring_stages<D, Q8, BS>()) * stage_bytes<D, Q8, BS, MQ>() + 1024;
 }
 
 struct DecodeParams {
@@ -137,6 +149,12 @@ struct DecodeParams {
     uint64_t wait_budget_ns;
     const unsigned *stall_flag;   // test knob: every CTA first waits (bounded) for
                                   //   *stall_flag != 0, or null
+    // several query tokens per sequence (the MQ form; cu_q null otherwise):
+    // sequence s owns query rows cu_q[s] .. cu_q[s+1]-1 of q / out [total_q][Hq][D],
+    // the newest n_s of its tokens (query i at position L - n_s + i, causal);
+    // the partials are indexed by (query row, head) instead of (sequence, head)
+    const int32_t *cu_q;
+    int max_q, total_q;
 };
 
 struct LaunchConfig {
@@ -154,18 +172,20 @@ struct KVMaps {
     const CUtensorMap *k, *v, *km, *vm;
 };
 
-// Per-head_dim entry points (pgd_kernels_d64.cu, _d128.cu, _d256.cu).
+// Per-head_dim entry points (pgd_kernels_d64.cu, _d128.cu, _d256.cu); p.cu_q
+// non-null selects the MQ form (head_dim 64 and 128).
 cudaError_t launch_decode_d64(int block_size, bool trace, bool q8, const KVMaps &m,
                               const DecodeParams &p, const LaunchConfig &lc);
 cudaError_t launch_decode_d128(int block_size, bool trace, bool q8, const KVMaps &m,
                                const DecodeParams &p, const LaunchConfig &lc);
 cudaError_t launch_decode_d256(int block_size, bool trace, bool q8, const KVMaps &m,
                                const DecodeParams &p, const LaunchConfig &lc);
-// Resident partition-kernel CTAs per SM for (head_dim, block_size, page kind);
-// 0 where no kernel is built (quantised pages at head_dim 64).
-cudaError_t occupancy_d64(int block_size, bool q8, int *ctas_per_sm);
-cudaError_t occupancy_d128(int block_size, bool q8, int *ctas_per_sm);
-cudaError_t occupancy_d256(int block_size, bool q8, int *ctas_per_sm);
+// Resident partition-kernel CTAs per SM for (head_dim, block_size, kind:
+// 0 fp16 pages, 1 quantised pages, 2 the MQ form); 0 where no kernel is
+// built (quantised pages at head_dim 64, the MQ form at 256).
+cudaError_t occupancy_d64(int block_size, int kind, int *ctas_per_sm);
+cudaError_t occupancy_d128(int block_size, int kind, int *ctas_per_sm);
+cudaError_t occupancy_d256(int block_size, int kind, int *ctas_per_sm);
 
 // Reduce kernel: one CTA per (sequence, query head); two warps suffice for
 // head_dim 64 and 128 (whose workloads have at most 16 partitions per

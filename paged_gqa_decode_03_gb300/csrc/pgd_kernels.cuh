@@ -47,8 +47,25 @@ enum : int { kFirst = 1, kLast = 2, kDirect = 4, kAppend = 16, kTerm = 32 };
 
 struct StageHeader {
     int s, g, p, valid, flags;
+    int tok0;           // position of the stage's first row in its sequence
+    int qn, qrow0;      // MQ: the sequence's query count and first query row,
+    int qpos0;          //   and the position of its first query token (L - qn)
     long long app_off;  // kAppend: element offset of the newest token's cache row, -1: none
 };
+
+// MQ: a sequence takes part with 1 <= n <= min(L, max_q) query tokens (its
+// newest n); a count outside [0, min(L, max_q)] is flagged (by CTA 0) and the
+// sequence is left out, as is one without query tokens.
+__device__ __forceinline__ int mq_len(const DecodeParams &p, int s, int L)
+{
+    const int n = __ldg(p.cu_q + s + 1) - __ldg(p.cu_q + s);
+    if (n < 0 || n > L || n > p.max_q) {
+        if (blockIdx.x == 0)
+            atomicOr(p.err, kErrQueryLen);
+        return 0;
+    }
+    return n == 0 ? 0 : L;
+}
 
 // Fused append into quantised pages, by the producer warp before it copies
 // the stage that holds the newest token: the warp quantises the token's K and
@@ -88,15 +105,23 @@ __device__ __forceinline__ void q8_append_to_cache(long long app_off, long long 
 // in fp32 around exact fp16 tensor-core products of the codes:
 //   s = sum_g scale_g (q_g . code_g) + bias_g sum(q_g)            (QK)
 //   O += sum_t (p_t scale_g(t)) code_t + sum_t p_t bias_g(t)      (PV)
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
-__global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
+//
+// MQ: several query tokens per sequence (the newest n_s of its tokens, query
+// i at position L - n_s + i, causal); the columns of the unit's n8 tile are
+// (query token, head of the group), at most kMaxCols, each with its own
+// causal limit; the partials are kept per (query row, head).  A warp's work
+// per stage is that of the decode.
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false,
+          bool MQ = false>
+__global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     paged_gqa_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ CUtensorMap tmap_km,
                              const __grid_constant__ CUtensorMap tmap_vm,
                              const DecodeParams p)
 {
-    constexpr int T = stage_tokens_of<D, Q8>(), NC = consumer_warps<D, Q8>();
+    constexpr int T = stage_tokens_of<D, Q8>(), NC = consumer_warps<D, Q8, MQ>();
+    constexpr int NTT = T / 16;            // 16-token tiles of a stage (one per consumer warp)
     constexpr int NS = ring_stages<D, Q8, BS>();
     constexpr int ROWB = D * (Q8 ? 1 : 2); // bytes of one cached row
     constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
@@ -125,12 +150,14 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     constexpr int MSTR = MPAIRED ? 2 * PAGE_META : META_SLOT;  // piece to piece
     constexpr int MVOFF = MPAIRED ? PAGE_META : META_BYTES;    // V's pairs after K's
     constexpr int Q_OFF = 2 * KV_BYTES + 2 * META_BYTES;  // the group's queries in a stage
-    constexpr int STAGE = stage_bytes<D, Q8, BS>();
+    constexpr int STAGE = stage_bytes<D, Q8, BS, MQ>();
     constexpr int OST = D + 4;             // merge buffer row stride (floats)
-    static_assert(NC * 16 == T, "one 16-token tile per consumer warp per stage");
+    constexpr int NCOLS = MQ ? kMaxCols : kMaxGroup;  // columns per unit
+    static_assert(!MQ || (!Q8 && !TRACE && !QAPP && !QSTR && D <= 128), "MQ: fp16, head_dim <= 128");
+    static_assert(NTT * 16 == T && NC == NTT, "one 16-token tile per consumer warp per stage");
     static_assert(BS <= T ? (T % BS == 0) : (BS % T == 0), "stage/page sizes");
     static_assert(STAGE % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle alignment");
-    static_assert(NC * kMaxGroup * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
+    static_assert(NTT * NCOLS * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
     static_assert(!Q8 || (D % 128 == 0), "quantised pages: rows of whole 128-byte slabs");
     static_assert(!Q8 || (T / BOX) * META_SLOT <= META_BYTES, "scale slots fit the stage");
     static_assert(!MPAIRED || (T / BOX) * MSTR <= 2 * META_BYTES, "paired slots fit the stage");
@@ -172,7 +199,9 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 const int raw = __ldg(p.seq_lens + i);
                 if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
                     atomicOr(p.err, kErrSeqLen);
-                const int L = raw < 0 ? 0 : (raw > maxlen ? maxlen : raw);
+                int L = raw < 0 ? 0 : (raw > maxlen ? maxlen : raw);
+                if constexpr (MQ)
+                    L = mq_len(p, i, L);
                 lens_s[i] = L;
                 nf += L >> p.logP;
                 const int tail = L & (p.P - 1);
@@ -295,6 +324,9 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             const int pg0 = tok0 / BS;
             const int nst = (n + T - 1) / T;
             const int fixed = L <= P ? kDirect : 0;
+            // MQ: the sequence's query rows (the newest qn of its tokens)
+            const int qrow0 = MQ ? __ldg(p.cu_q + s) : 0;
+            const int qn = MQ ? __ldg(p.cu_q + s + 1) - qrow0 : 1;
             // fused append: the stage holding token L-1 (last stage of the
             // last partition) carries it
             const bool app_unit = p.k_new != nullptr && pi == (L - 1) / P;
@@ -388,8 +420,12 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                     hdr[slot].flags = fixed | (st == 0 ? kFirst : 0) | (st == nst - 1 ? kLast : 0) |
                                       (app_unit && st == nst - 1 ? kAppend : 0);
                     hdr[slot].app_off = app_off;
+                    hdr[slot].tok0 = tok0 + st * T;
+                    hdr[slot].qn = qn;
+                    hdr[slot].qrow0 = qrow0;
+                    hdr[slot].qpos0 = L - qn;
                     const uint32_t bytes = pc * (PAGE_BYTES + (META_BY_TMA ? PAGE_META : 0)) * 2 +
-                                           (st == 0 ? G * D * 2 : 0);
+                                           (st == 0 ? qn * G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
                 // lane jj issues the copies of the stage's page jj: one
@@ -440,9 +476,17 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                         }
                     }
                 }
-                if (st == 0 && lane == 0)
+                if constexpr (MQ) {
+                    // the G heads of query token `lane` (contiguous in q): columns
+                    // lane * G .. lane * G + G - 1
+                    if (st == 0 && lane < qn)
+                        bulk_load(sb + Q_OFF + lane * G * D * 2,
+                                  p.q + ((size_t)(qrow0 + lane) * p.Hq + (size_t)g * G) * D,
+                                  G * D * 2, fb);
+                } else if (st == 0 && lane == 0) {
                     bulk_load(sb + Q_OFF, p.q + ((size_t)s * p.Hq + (size_t)g * G) * D,
                               G * D * 2, fb);
+                }
             }
             return true;
         };
@@ -464,6 +508,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             const int raw = __ldg(p.seq_lens + s);
             if ((raw < 0 || raw > maxlen) && blockIdx.x == 0)
                 atomicOr(p.err, kErrSeqLen);
+            if constexpr (MQ)
+                return mq_len(p, s, clamp_len(raw));
             return clamp_len(raw);
         };
 
@@ -598,13 +644,15 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
     // ================================================================ consumers
     // Consumer warp w owns token tile w (tokens [16w, 16w+16)) of every
     // stage and runs its own log2-space online softmax over the whole of
-    // head_dim for the group's query heads; the NC warps merge their states
-    // once per unit, in the shared memory of the unit's last stage.
+    // head_dim for the unit's columns (the group's query heads; MQ: query
+    // token x head); the NC warps merge their states once per unit, in the
+    // shared memory of the unit's last stage.
     const int w = warp;
+    const int tt = w;                    // token tile
     const int gb = lane >> 2;            // C-fragment row: token within the tile
     const int tq = (lane & 3) * 2;       // C-fragment columns: query heads tq, tq+1
     const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix index, row in it
-    const int t0 = 16 * w;               // this warp's tile within a stage
+    const int t0 = 16 * tt;              // this warp's tile within a stage
     float o[KT][4];                      // O^T[D x 8]: 16-row tile i, columns tq, tq+1
     uint32_t qf[KT][2];                  // Q^T B-fragments
     // Q8: rows of O^T are interleaved: tile i, fragment rows gb / gb+8 hold
@@ -623,8 +671,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
 #pragma unroll
     for (int gi = 0; gi < (NGRP > 0 ? NGRP : 1); ++gi)
         qsum[gi][0] = qsum[gi][1] = beta[gi][0] = beta[gi][1] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads tq, tq+1 (log2 units)
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max of columns tq, tq+1 (log2 units)
     float l0 = 0.f, l1 = 0.f;              // this lane's share of the running exp2-sums
+    // MQ: the last position column tq (+1) sees (its query token's
+    // position), -1 for a column past the unit's rows
+    int lim0 = -1, lim1 = -1;
     uint32_t msync = 0;                    // merge-barrier phases passed
 
     // Bounded rendezvous of the NC consumer warps (false: give up).
@@ -658,7 +709,10 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
             const uint8_t *qs = sp + Q_OFF;
-            const bool live = gb < p.G;
+            // columns of the unit: the group's heads, or (MQ) query token x head
+            const int ncols = MQ ? hdr[slot].qn * p.G : p.G;
+            const int col = gb;  // B-fragment column of this lane
+            const bool live = col < ncols;
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
                 o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -667,8 +721,15 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 // ldmatrix row piece gives a lane)
                 const int d0 = Q8 ? i * 16 + 2 * tq : i * 16 + tq;
                 const int d1 = Q8 ? d0 + 2 : d0 + 8;
-                qf[i][0] = live ? *reinterpret_cast<const uint32_t *>(qs + (gb * D + d0) * 2) : 0u;
-                qf[i][1] = live ? *reinterpret_cast<const uint32_t *>(qs + (gb * D + d1) * 2) : 0u;
+                qf[i][0] = live ? *reinterpret_cast<const uint32_t *>(qs + (col * D + d0) * 2) : 0u;
+                qf[i][1] = live ? *reinterpret_cast<const uint32_t *>(qs + (col * D + d1) * 2) : 0u;
+            }
+            if constexpr (MQ) {
+                // column c is query token c / G, at position L - qn + c / G
+                const int qpos0 = hdr[slot].qpos0;
+                const int c0 = tq, c1 = c0 + 1;
+                lim0 = c0 < ncols ? qpos0 + c0 / p.G : -1;
+                lim1 = c1 < ncols ? qpos0 + c1 / p.G : -1;
             }
             if constexpr (Q8) {
                 // sum of q over each group for head gb (four lanes hold its
@@ -797,12 +858,23 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                     d3 += fmaf(eb.x, c[gi][3], bb * qsum[gi][1]);
                 }
             }
-            const float x0 = va ? d0 * sc : -INFINITY;  // token gb,   head tq
-            const float x1 = va ? d1 * sc : -INFINITY;  // token gb,   head tq+1
-            const float x2 = vb ? d2 * sc : -INFINITY;  // token gb+8, head tq
-            const float x3 = vb ? d3 * sc : -INFINITY;  // token gb+8, head tq+1
-            // ---- one online-softmax step over the tile (token 0 of the tile is valid,
-            // so every column max is finite)
+            // scores, -inf where masked (MQ: also past the column's query position)
+            bool ka0 = va, ka1 = va, kb0 = vb, kb1 = vb;
+            if constexpr (MQ) {
+                const int pa_ = hdr[slot].tok0 + t0 + gb, pb_ = pa_ + 8;
+                ka0 = va && pa_ <= lim0;
+                ka1 = va && pa_ <= lim1;
+                kb0 = vb && pb_ <= lim0;
+                kb1 = vb && pb_ <= lim1;
+            }
+            const float x0 = ka0 ? d0 * sc : -INFINITY;  // token gb,   head tq
+            const float x1 = ka1 ? d1 * sc : -INFINITY;  // token gb,   head tq+1
+            const float x2 = kb0 ? d2 * sc : -INFINITY;  // token gb+8, head tq
+            const float x3 = kb1 ? d3 * sc : -INFINITY;  // token gb+8, head tq+1
+            // ---- one online-softmax step over the tile.  Outside MQ token 0
+            // of the tile is valid for every column, so every column max is
+            // finite; in MQ a column may have seen nothing yet (its max stays
+            // -inf: offset 0, every p and alpha is then 0)
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -810,11 +882,13 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
                 mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, off));
             }
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            const float sn0 = MQ && mn0 == -INFINITY ? 0.f : mn0;
+            const float sn1 = MQ && mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2(m0 - sn0), al1 = ex2(m1 - sn1);
             m0 = mn0;
             m1 = mn1;
-            const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);  // P[gb][tq..tq+1]
-            const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);  // P[gb+8][..]
+            const float p0 = ex2(x0 - sn0), p1 = ex2(x1 - sn1);  // P[gb][tq..tq+1]
+            const float p2 = ex2(x2 - sn0), p3 = ex2(x3 - sn1);  // P[gb+8][..]
             const uint32_t pa = pack_half2(p0, p1), pb = pack_half2(p2, p3);
             const float2 fa = unpack_half2(pa), fb = unpack_half2(pb);
             l0 = l0 * al0 + (fa.x + fb.x);
@@ -910,9 +984,10 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
         // ---- end of the unit: merge the NC warps' states through this
         // stage's shared memory (still held), then write the output row or
         // the partition partial, then release the stage.
-        float *mg_m = reinterpret_cast<float *>(sp);            // [NC][8]
-        float *mg_l = mg_m + NC * kMaxGroup;                     // [NC][8]
-        float *mg_o = mg_l + NC * kMaxGroup;                     // [NC][8][OST]
+        // [warp][column]
+        float *mg_m = reinterpret_cast<float *>(sp);            // [NTT][NCOLS]
+        float *mg_l = mg_m + NTT * NCOLS;                        // [NTT][NCOLS]
+        float *mg_o = mg_l + NTT * NCOLS;                        // [NTT][NCOLS][OST]
         float lt0 = l0, lt1 = l1;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -941,22 +1016,23 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
         }
         if (!consumers_sync())  // every warp is done reading the stage
             break;
+        const int c0 = tq;  // this lane's columns c0, c0 + 1
         if (gb == 0) {
-            mg_m[w * kMaxGroup + tq] = m0;
-            mg_m[w * kMaxGroup + tq + 1] = m1;
-            mg_l[w * kMaxGroup + tq] = lt0;
-            mg_l[w * kMaxGroup + tq + 1] = lt1;
+            mg_m[tt * NCOLS + c0] = m0;
+            mg_m[tt * NCOLS + c0 + 1] = m1;
+            mg_l[tt * NCOLS + c0] = lt0;
+            mg_l[tt * NCOLS + c0 + 1] = lt1;
         }
         {
-            float *ow = mg_o + w * kMaxGroup * OST;
+            float *ow = mg_o + tt * NCOLS * OST;
 #pragma unroll
             for (int i = 0; i < KT; ++i) {
                 const int d = Q8 ? i * 16 + 2 * gb : i * 16 + gb;   // fragment row gb
                 const int d8 = Q8 ? d + 1 : d + 8;                  // fragment row gb+8
-                ow[tq * OST + d] = o[i][0];
-                ow[(tq + 1) * OST + d] = o[i][1];
-                ow[tq * OST + d8] = o[i][2];
-                ow[(tq + 1) * OST + d8] = o[i][3];
+                ow[c0 * OST + d] = o[i][0];
+                ow[(c0 + 1) * OST + d] = o[i][1];
+                ow[c0 * OST + d8] = o[i][2];
+                ow[(c0 + 1) * OST + d8] = o[i][3];
             }
         }
         if (!consumers_sync())  // all states written
@@ -964,27 +1040,34 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8>() + 1) * 32, 2)
         {
             const int G = p.G;
             const bool direct = flags & kDirect;
-            for (int idx = threadIdx.x; idx < G * (D / 4); idx += NC * 32) {
+            // columns: the group's heads, or (MQ) query token x head
+            const int ncols = MQ ? hdr[slot].qn * G : G;
+            for (int idx = threadIdx.x; idx < ncols * (D / 4); idx += NC * 32) {
                 const int g = idx / (D / 4), d4 = idx % (D / 4);
                 float M = -INFINITY;
 #pragma unroll
-                for (int wi = 0; wi < NC; ++wi)
-                    M = fmaxf(M, mg_m[wi * kMaxGroup + g]);
+                for (int wi = 0; wi < NTT; ++wi)
+                    M = fmaxf(M, mg_m[wi * NCOLS + g]);
+                // MQ: a column that saw no token in this unit (M = -inf) gets
+                // a zero exp-sum, which the reduce skips
+                const float Ms = MQ && M == -INFINITY ? 0.f : M;
                 float den = 0.f;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int wi = 0; wi < NC; ++wi) {
-                    const float scw = ex2(mg_m[wi * kMaxGroup + g] - M);
-                    den += scw * mg_l[wi * kMaxGroup + g];
+                for (int wi = 0; wi < NTT; ++wi) {
+                    const float scw = ex2(mg_m[wi * NCOLS + g] - Ms);
+                    den += scw * mg_l[wi * NCOLS + g];
                     const float4 v =
-                        *reinterpret_cast<const float4 *>(mg_o + (wi * kMaxGroup + g) * OST + 4 * d4);
+                        *reinterpret_cast<const float4 *>(mg_o + (wi * NCOLS + g) * OST + 4 * d4);
                     acc.x += scw * v.x;
                     acc.y += scw * v.y;
                     acc.z += scw * v.z;
                     acc.w += scw * v.w;
                 }
-                const float inv = 1.f / den;
-                const size_t h = (size_t)hs * p.Hq + hg * G + g;
+                const float inv = MQ ? (den > 0.f ? 1.f / den : 0.f) : 1.f / den;
+                // output row: (sequence, head), or (MQ) (query row, head)
+                const size_t h = MQ ? (size_t)(hdr[slot].qrow0 + g / G) * p.Hq + hg * G + g % G
+                                    : (size_t)hs * p.Hq + hg * G + g;
                 float4 *dst = direct
                                   ? reinterpret_cast<float4 *>(p.out + h * D)
                                   : reinterpret_cast<float4 *>(p.ws_o + (h * p.NPmax + hp) * D);
@@ -1145,10 +1228,98 @@ __global__ void __launch_bounds__(reduce_threads<D>())
     }
 }
 
+// MQ: one warp per (query row, head), four per CTA: merges the row's
+// partition partials, out = sum_i w_i o_i / sum_i w_i with w_i = l_i *
+// exp2(m_i - max m) over the non-empty ones (a row whose query position lies
+// before a partition has an empty partial there).  Rows of single-partition
+// sequences were written by the partition kernel; rows of a sequence whose
+// query count is invalid are left unwritten.  Launched with programmatic
+// dependent launch; the row's sequence and length are read before the wait.
+template <int D>
+__global__ void __launch_bounds__(128) paged_gqa_reduce_rows_kernel(const DecodeParams p,
+                                                                    int max_len)
+{
+    constexpr int V4 = D / 4;             // float4 per row
+    constexpr int PL = (V4 + 31) / 32;    // float4 per lane
+    const int lane = threadIdx.x & 31;
+    const int rh = blockIdx.x * 4 + (threadIdx.x >> 5);  // (query row, head)
+    const int rows = p.total_q * p.Hq;
+    int np = 1;
+    if (rh < rows) {
+        const int r = rh / p.Hq;
+        int lo = 0, hi = p.S - 1;  // the sequence owning query row r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.cu_q + mid) <= r)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        int L = __ldg(p.seq_lens + lo);
+        L = L < 0 ? 0 : (L > max_len ? max_len : L);
+        const int n = __ldg(p.cu_q + lo + 1) - __ldg(p.cu_q + lo);
+        np = (n < 0 || n > L || n > p.max_q) ? 1 : (L + p.P - 1) / p.P;
+    }
+    griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.counter)
+        *p.counter = 0;  // the partition kernel is done with it: ready for the next call
+    if (rh >= rows || np <= 1)
+        return;
+    const float *mp = p.ws_m + (size_t)rh * p.NPmax;
+    const float *lp = p.ws_l + (size_t)rh * p.NPmax;
+    const float4 *op = reinterpret_cast<const float4 *>(p.ws_o + (size_t)rh * p.NPmax * D);
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32)
+        if (lp[i] > 0.f)
+            M = fmaxf(M, mp[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(~0u, M, off));
+    float4 acc[PL];
+#pragma unroll
+    for (int v = 0; v < PL; ++v)
+        acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    constexpr int U = 4;  // partitions in flight
+    for (int i0 = 0; i0 < np; i0 += U) {
+        float wu[U];
+        float4 x[U][PL];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u;
+            const float li = i < np ? lp[i] : 0.f;
+            wu[u] = li > 0.f ? li * ex2(mp[i] - M) : 0.f;
+#pragma unroll
+            for (int v = 0; v < PL; ++v)
+                x[u][v] = wu[u] > 0.f && lane + 32 * v < V4 ? op[(size_t)i * V4 + lane + 32 * v]
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            den += wu[u];
+#pragma unroll
+            for (int v = 0; v < PL; ++v) {
+                acc[v].x += wu[u] * x[u][v].x;
+                acc[v].y += wu[u] * x[u][v].y;
+                acc[v].z += wu[u] * x[u][v].z;
+                acc[v].w += wu[u] * x[u][v].w;
+            }
+        }
+    }
+    const float inv = 1.f / den;
+    float4 *o4 = reinterpret_cast<float4 *>(p.out + (size_t)rh * D);
+#pragma unroll
+    for (int v = 0; v < PL; ++v)
+        if (lane + 32 * v < V4)
+            o4[lane + 32 * v] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv,
+                                            acc[v].w * inv);
+}
+
 // ---------------------------------------------------------------- launch
 // Raises the partition kernel's dynamic shared-memory limit, once per
 // device and instantiation.
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false,
+          bool MQ = false>
 cudaError_t ensure_smem_attribute()
 {
     static std::atomic<unsigned long long> done{0};  // bit per device ordinal < 64
@@ -1159,25 +1330,26 @@ cudaError_t ensure_smem_attribute()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR>,
+    e = cudaFuncSetAttribute(paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR, MQ>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dyn_smem_bytes<D, Q8, BS>());
+                             (int)dyn_smem_bytes<D, Q8, BS, MQ>());
     if (e == cudaSuccess)
         done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 
-template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false>
+template <int D, int BS, bool TRACE, bool Q8, bool QAPP = false, bool QSTR = false,
+          bool MQ = false>
 cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const LaunchConfig &lc)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR>;
-    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8, QAPP, QSTR>();
+    auto kern = paged_gqa_partial_kernel<D, BS, TRACE, Q8, QAPP, QSTR, MQ>;
+    cudaError_t e = ensure_smem_attribute<D, BS, TRACE, Q8, QAPP, QSTR, MQ>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(lc.grid);
-    cfg.blockDim = dim3((consumer_warps<D, Q8>() + 1) * 32);
-    cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8, BS>();
+    cfg.blockDim = dim3((consumer_warps<D, Q8, MQ>() + 1) * 32);
+    cfg.dynamicSmemBytes = dyn_smem_bytes<D, Q8, BS, MQ>();
     cfg.stream = lc.stream;
     if (lc.ev_before && (e = cudaEventRecord(lc.ev_before, lc.stream)) != cudaSuccess)
         return e;
@@ -1191,29 +1363,40 @@ cudaError_t launch_decode_impl(const KVMaps &m, const DecodeParams &p, const Lau
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = {};
-    rcfg.gridDim = dim3(lc.reduce_blocks);
-    rcfg.blockDim = dim3(reduce_threads<D>());
     rcfg.stream = lc.stream;
     rcfg.attrs = attr;
     rcfg.numAttrs = 1;
+    if constexpr (MQ) {  // one warp per (query row, head)
+        rcfg.gridDim = dim3((lc.reduce_blocks + 3) / 4);
+        rcfg.blockDim = dim3(128);
+        return cudaLaunchKernelEx(&rcfg, paged_gqa_reduce_rows_kernel<D>, p, p.MB * BS);
+    }
+    rcfg.gridDim = dim3(lc.reduce_blocks);
+    rcfg.blockDim = dim3(reduce_threads<D>());
     return cudaLaunchKernelEx(&rcfg, paged_gqa_reduce_kernel<D>, p, p.MB * BS);
 }
 
-template <int D, int BS, bool Q8>
+template <int D, int BS, bool Q8, bool MQ = false>
 cudaError_t occupancy_impl(int *ctas)
 {
-    auto kern = paged_gqa_partial_kernel<D, BS, false, Q8>;
-    cudaError_t e = ensure_smem_attribute<D, BS, false, Q8>();
+    auto kern = paged_gqa_partial_kernel<D, BS, false, Q8, false, false, MQ>;
+    cudaError_t e = ensure_smem_attribute<D, BS, false, Q8, false, false, MQ>();
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas, kern, (consumer_warps<D, Q8>() + 1) * 32, dyn_smem_bytes<D, Q8, BS>());
+        ctas, kern, (consumer_warps<D, Q8, MQ>() + 1) * 32, dyn_smem_bytes<D, Q8, BS, MQ>());
 }
 
 template <int D, int BS>
 cudaError_t launch_decode_bs(bool trace, bool q8, const KVMaps &m, const DecodeParams &p,
                              const LaunchConfig &lc)
 {
+    if (p.cu_q) {  // several query tokens per sequence (fp16 pages, no trace)
+        if constexpr (D <= 128)
+            return launch_decode_impl<D, BS, false, false, false, false, true>(m, p, lc);
+        else
+            return cudaErrorInvalidValue;
+    }
     if constexpr (D % 128 == 0) {
         if (q8) {
             if (p.q8_rows)  // quantised pages at any strides (no page trace)
@@ -1251,32 +1434,39 @@ cudaError_t launch_decode_dispatch(int block_size, bool trace, bool q8, const KV
     }
 }
 
-template <int D, bool Q8>
+template <int D, bool Q8, bool MQ = false>
 cudaError_t occupancy_bs(int block_size, int *ctas)
 {
     switch (block_size) {
     case 8:
-        return occupancy_impl<D, 8, Q8>(ctas);
+        return occupancy_impl<D, 8, Q8, MQ>(ctas);
     case 16:
-        return occupancy_impl<D, 16, Q8>(ctas);
+        return occupancy_impl<D, 16, Q8, MQ>(ctas);
     case 32:
-        return occupancy_impl<D, 32, Q8>(ctas);
+        return occupancy_impl<D, 32, Q8, MQ>(ctas);
     case 64:
-        return occupancy_impl<D, 64, Q8>(ctas);
+        return occupancy_impl<D, 64, Q8, MQ>(ctas);
     case 128:
-        return occupancy_impl<D, 128, Q8>(ctas);
+        return occupancy_impl<D, 128, Q8, MQ>(ctas);
     default:
         return cudaErrorInvalidValue;
     }
 }
 
+// kind: 0 fp16 pages, 1 quantised pages, 2 the MQ form
 template <int D>
-cudaError_t occupancy_dispatch(int block_size, bool q8, int *ctas)
+cudaError_t occupancy_dispatch(int block_size, int kind, int *ctas)
 {
+    if (kind == 2) {
+        if constexpr (D <= 128)
+            return occupancy_bs<D, false, true>(block_size, ctas);
+        *ctas = 0;
+        return cudaSuccess;
+    }
     if constexpr (D % 128 == 0) {
-        if (q8)
+        if (kind == 1)
             return occupancy_bs<D, true>(block_size, ctas);
-    } else if (q8) {
+    } else if (kind == 1) {
         *ctas = 0;
         return cudaSuccess;
     }

@@ -9,9 +9,9 @@ cudaError_t launch_decode_d256(int block_size, bool trace, bool q8, const KVMaps
     return launch_decode_dispatch<256>(block_size, trace, q8, m, p, lc);
 }
 
-cudaError_t occupancy_d256(int block_size, bool q8, int *ctas_per_sm)
+cudaError_t occupancy_d256(int block_size, int kind, int *ctas_per_sm)
 {
-    return occupancy_dispatch<256>(block_size, q8, ctas_per_sm);
+    return occupancy_dispatch<256>(block_size, kind, ctas_per_sm);
 }
 
 }  // namespace pgd

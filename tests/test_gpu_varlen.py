@@ -77,7 +77,7 @@ def test_split_kv_partitions(D, PK):
 
 
 def test_single_token_rows_match_decode():
-    """n_s = 1 everywhere: the decode step, through the other kernel."""
+    """n_s = 1 everywhere: the decode step through the varlen entry point."""
     w = make_varlen(S=12, Hq=32, Hkv=8, D=128, BS=16, ctx=[0, 1, 15, 16, 100, 511, 512, 1000,
                                                           2047, 3000, 33, 64],
                     n=[1] * 12, seed=3, device=DEV)
