@@ -829,39 +829,32 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 break;
             }
             tc_fence_after();
-            // pass 1: the row's extreme over the scores it sees (the max for
-            // a scale >= 0, the min for a negative one; masked scores count as
-            // the value that scales to -inf), 64 scores per tensor-memory wait;
-            // the second half stays in registers for pass 2
-            static_assert(NT == 128, "two 64-token halves per stage");
-            const bool masked_tile = t0 + NT - 1 > lim;
+            // the stage's 128 scores of this row in one tensor-memory round
+            // trip; then the row's extreme over the scores it sees (the max
+            // for a scale >= 0, the min for a negative one; masked scores
+            // count as the value that scales to -inf)
+            static_assert(NT == 128, "four 32-token chunks per stage");
+            float v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tc_ld32(t_lane + s_col + 32 * c, v[c]);
+            tc_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tc_ld_ready(v[c]);
+            if (t0 + NT - 1 > lim) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[c][i] = t0 + 32 * c + i > lim ? masked : v[c][i];
+            }
             float e = masked;
-            float v[2][32];
-            auto load_half = [&](int h) {
-                tc_ld32(t_lane + s_col + 64 * h, v[0]);
-                tc_ld32(t_lane + s_col + 64 * h + 32, v[1]);
-                tc_wait_ld();
-                tc_ld_ready(v[0]);
-                tc_ld_ready(v[1]);
-                if (masked_tile) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[c][i] = t0 + 64 * h + 32 * c + i > lim ? masked : v[c][i];
-                }
-            };
-            auto extreme = [&]() {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        e = neg ? fmin3(e, v[c][i], v[c][i + 1]) : fmax3(e, v[c][i], v[c][i + 1]);
-            };
-            load_half(0);
-            extreme();
-            load_half(1);
-            extreme();
+                for (int i = 0; i < 32; i += 2)
+                    e = neg ? fmin3(e, v[c][i], v[c][i + 1]) : fmax3(e, v[c][i], v[c][i + 1]);
             const float mt = e == masked ? -INFINITY : e * sc;
             // lazy reference max: moves only by more than 8 (log2 units), so
             // every p <= 256 stays exact enough in fp16
@@ -872,34 +865,30 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                 alpha = rescale ? ex2(m_ref - mt) : 1.f;
                 m_ref = mt;
             }
-            // pass 2: p = exp2(s * scale_log2 - m_ref) (offset 0 while the row
-            // has seen nothing: its scores are all masked, every p is 0; masked
-            // scores are infinite with the sign that scales to -inf), as fp16 pairs;
-            // half h goes to columns 32h .. 32h+31, the A operand of P V.  The
-            // second half is still in registers; the first is read again
-            // before P of the second overwrites its last 32 scores.
+            // p = exp2(s * scale_log2 - m_ref) (offset 0 while the row has
+            // seen nothing: its scores are all masked, every p is 0; masked
+            // scores are infinite with the sign that scales to -inf), as fp16
+            // pairs: tokens 64h .. 64h+63 go to columns 32h .. 32h+31, the A
+            // operand of P V.  Every score is in registers before the first
+            // P store.
             const float off = m_ref == -INFINITY ? 0.f : -m_ref;
             const float2 off2 = make_float2(off, off);
             float2 sum2 = make_float2(0.f, 0.f);
-            uint32_t pk[32];
-            auto exp_half = [&](int h) {
+#pragma unroll
+            for (int h = 1; h >= 0; --h) {
+                uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        float2 a = ffma2(make_float2(v[c][i], v[c][i + 1]), sc2, off2);
+                        float2 a = ffma2(make_float2(v[2 * h + c][i], v[2 * h + c][i + 1]), sc2, off2);
                         a.x = ex2(a.x);
                         a.y = ex2(a.y);
                         pk[16 * c + i / 2] = pack_half2(a.x, a.y);
                         sum2 = fadd2(sum2, a);
                     }
-            };
-            exp_half(1);
-            tc_ld_ready(pk);  // half 1 done before half 0's scores come back
-            load_half(0);
-            tc_st32u(t_lane + s_col + 32, pk);
-            exp_half(0);
-            tc_st32u(t_lane + s_col, pk);
+                tc_st32u(t_lane + s_col + 32 * h, pk);
+            }
             l = l * alpha + (sum2.x + sum2.y);
             // this tile's previous P V has completed (S_jj was issued after
             // it): its O may be rescaled
