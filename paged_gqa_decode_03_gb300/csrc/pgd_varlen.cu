@@ -727,28 +727,33 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                     ok = false;
                 return ok;
             };
+            // shared-memory descriptors: every address here is below 2^18,
+            // where the start-address field is the address / 16, so the
+            // descriptor of base + off is the base's plus off / 16: one add
+            // per operand on the issuing thread, which shares its issue slots
+            // with two softmax warps
+            const uint64_t q_desc = tc_sdesc(q_s, 16, 1024);
+            const uint64_t k_desc = tc_sdesc(kv_s, 16, GROUP);
+            const uint64_t v_desc = tc_sdesc(kv_s + KV_TILE, 1024, GROUP);
             // S_x(j) = Q_x K_j^T into tile x's score columns
             auto issue_s = [&](int x, int j) {
-                const uint32_t ks = kv_s + (j % NSTG) * 2 * KV_TILE;
-                const uint32_t qx = q_s + x * Q_TILE;
+                const uint64_t ks = k_desc + (((j % NSTG) * 2 * KV_TILE) >> 4);
+                const uint64_t qx = q_desc + ((x * Q_TILE) >> 4);
+                const uint32_t d = tmem + x * NT;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc_sdesc(qx + (kk / 4) * Q_SLAB + (kk % 4) * 32, 16, 1024);
-                    const uint64_t b = tc_sdesc(ks + (kk / 4) * 1024 + (kk % 4) * 32, 16, GROUP);
-                    tc_mma(tmem + x * NT, a, b, IDESC_S, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma(d, qx + (((kk / 4) * Q_SLAB + (kk % 4) * 32) >> 4),
+                           ks + (((kk / 4) * 1024 + (kk % 4) * 32) >> 4), IDESC_S, kk > 0);
                 tc_commit(smem_addr(&s_full[x]));
             };
             // O_x += P_x(j) V_j, P in the score columns (16 tokens = 8 columns
             // per instruction)
             auto issue_pv = [&](int x, int j) {
-                const uint32_t vs = kv_s + (j % NSTG) * 2 * KV_TILE + KV_TILE;
+                const uint64_t vs = v_desc + (((j % NSTG) * 2 * KV_TILE) >> 4);
+                const uint32_t d = tmem + O_COL + x * D, a = tmem + x * NT;
 #pragma unroll
-                for (int kk = 0; kk < NT / 16; ++kk) {
-                    const uint64_t b = tc_sdesc(vs + kk * 2 * GROUP, 1024, GROUP);
-                    tc_mma_ta(tmem + O_COL + x * D, tmem + x * NT + kk * 8, b, IDESC_O,
-                              j > 0 || kk > 0);
-                }
+                for (int kk = 0; kk < NT / 16; ++kk)
+                    tc_mma_ta(d, a + kk * 8, vs + ((kk * 2 * GROUP) >> 4), IDESC_O, j > 0 || kk > 0);
             };
             if (wait(&k_full[0], 0)) {
                 tc_fence_after();
@@ -849,12 +854,18 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         v[c][i] = t0 + 32 * c + i > lim ? masked : v[c][i];
             }
-            float e = masked;
+            // one running extreme per 32-token chunk (four independent
+            // chains of dependent three-input min / max instead of one)
+            float ec[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                ec[c] = masked;
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
-                    e = neg ? fmin3(e, v[c][i], v[c][i + 1]) : fmax3(e, v[c][i], v[c][i + 1]);
+                    ec[c] = neg ? fmin3(ec[c], v[c][i], v[c][i + 1]) : fmax3(ec[c], v[c][i], v[c][i + 1]);
+            }
+            const float e = neg ? fmin3(ec[0], ec[1], fminf(ec[2], ec[3]))
+                                : fmax3(ec[0], ec[1], fmaxf(ec[2], ec[3]));
             const float mt = e == masked ? -INFINITY : e * sc;
             // lazy reference max: moves only by more than 8 (log2 units), so
             // every p <= 256 stays exact enough in fp16
@@ -889,7 +900,6 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
                     }
                 tc_st32u(t_lane + s_col + 32 * h, pk);
             }
-            l = l * alpha + (sum2.x + sum2.y);
             // this tile's previous P V has completed (S_jj was issued after
             // it): its O may be rescaled
             if (jj > 0 && __any_sync(~0u, rescale)) {
@@ -929,6 +939,8 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&p_full[x]));
+            // the exp-sum is not needed for P V: after the hand-off
+            l = l * alpha + (sum2.x + sum2.y);
         }
         // ---- epilogue: out = O / l, or the partition's partial
         if (ok && ntx > 0)
