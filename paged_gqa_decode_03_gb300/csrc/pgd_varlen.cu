@@ -523,11 +523,12 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
 //     tiles, PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), so that one tile's matrix
 //     products run while the other tile's softmax works.
 //   * warps 2-5 softmax of tile A, warps 6-9 of tile B: thread = row of the
-//     tile, every column of the stage.  Per stage: the row's extreme from
-//     tensor memory (pass 1), then p = exp2(s * scale_log2 - m) written back
-//     as fp16 over the scores (pass 2), the same lazy reference max as
-//     paged_varlen_kernel; S_j completing implies P_{j-1} V_{j-1} completed,
-//     so O may be rescaled then without another wait.
+//     tile, every column of the stage.  Per stage: the row's 128 scores in
+//     one tensor-memory round trip, its extreme, then p = exp2(s *
+//     scale_log2 - m) written back from registers as fp16 over the scores,
+//     the same lazy reference max as paged_varlen_kernel; S_j completing
+//     implies P_{j-1} V_{j-1} completed, so O may be rescaled then without
+//     another wait.
 template <int D>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
     paged_varlen_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
