@@ -446,7 +446,11 @@ pgd_status paged_gqa_decode_q8_append(float *out, const uint16_t *q, const uint1
  *               256-byte aligned.
  *
  * Supported: head_dim 64/128/256, block sizes 8..128, groups of up to 128
- * query heads per KV head.  Runs on the tcgen05 tensor cores.  Device-side
+ * query heads per KV head.  Calls with head_dim <= 128, kv_partition 0, 256
+ * or 512 and at most 8 (query token, head) rows per (sequence, KV head)
+ * (max_q_len x group <= 8: decode steps, short verification steps) run on
+ * the decode's persistent partition kernel, an HBM-bound scan; the rest on
+ * the tcgen05 tensor cores.  Device-side
  * checks as for the decode: a sequence whose n_s is negative, above its
  * length or above max_q_len sets PGD_DEVERR_QUERY_LEN and is skipped (its
  * output rows are not written).
