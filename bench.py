@@ -54,15 +54,19 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "8699ef01d40e5f9f": {("long_context", 512): 1_293_085_952 + 7_318_528,
-                         ("long_context", 256): 1_293_055_488 + 7_843_840,
-                         ("ragged_tails", 256): 888_245_504 + 6_966_528,
-                         ("serving_mix", 512): 1_212_308_480 + 7_031_808,
-                         ("batch_decode", 512): 633_329_664 + 5_183_232},
+    "1bcc8d873bddb934": {("long_context", 512): 1_293_166_848 + 7_584_768,
+                         ("long_context", 256): 1_293_076_736 + 7_466_496,
+                         ("ragged_tails", 256): 888_261_632 + 7_029_760,
+                         ("serving_mix", 512): 1_212_324_096 + 6_937_856,
+                         ("batch_decode", 512): 633_308_416 + 5_217_024,
+                         ("batch_decode_q8", 512): 336_779_776 + 5_091_328,
+                         ("long_context_q8", 512): 687_151_104 + 7_019_776,
+                         ("ragged_tails_q8", 256): 472_751_360 + 6_460_672,
+                         ("serving_mix_q8", 512): 644_779_776 + 6_981_376},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "8dcc6648acb385df": {("chunked_prefill", 8320): 286_171_136 + 13_128_704,
-                         ("prefill", 2048): 167_582_208 + 80_290_304,
-                         ("spec_verify", 4096): 605_140_480 + 4_443_392},
+    "a024cccf6ba443d5": {("chunked_prefill", 8320): 289_198_080 + 12_453_376,
+                         ("prefill", 2048): 167_980_032 + 79_201_024,
+                         ("spec_verify", 4096): 605_141_248 + 4_790_016},
 }
 
 
