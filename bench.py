@@ -54,7 +54,7 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "1bcc8d873bddb934": {("long_context", 512): 1_293_166_848 + 7_584_768,
+    "8569eb3729f9a84e": {("long_context", 512): 1_293_166_848 + 7_584_768,
                          ("long_context", 256): 1_293_076_736 + 7_466_496,
                          ("ragged_tails", 256): 888_261_632 + 7_029_760,
                          ("serving_mix", 512): 1_212_324_096 + 6_937_856,
@@ -64,16 +64,42 @@ TRAFFIC = {
                          ("ragged_tails_q8", 256): 472_751_360 + 6_460_672,
                          ("serving_mix_q8", 512): 644_779_776 + 6_981_376},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "a024cccf6ba443d5": {("chunked_prefill", 8320): 289_198_080 + 12_453_376,
+    "236e3c48de63c699": {("chunked_prefill", 8320): 289_198_080 + 12_453_376,
                          ("prefill", 2048): 167_980_032 + 79_201_024,
                          ("spec_verify", 4096): 605_141_248 + 4_790_016},
 }
 
 
+def _code_only(text):
+    """C / C++ / CUDA source without its comments, whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(exclude=()):
-    """Hash of the CUDA sources (csrc/), less the files in `exclude`: the
-    decode kernels do not include pgd_varlen.cu, so their traffic figure
-    stays valid while only that file changes."""
+    """Hash of the code of the CUDA sources (csrc/; comments and layout
+    left out), less the files in `exclude`: the decode kernels do not
+    include pgd_varlen.cu, so their traffic figure stays valid while only
+    that file changes."""
     import glob
     import hashlib
     h = hashlib.sha256()
@@ -81,8 +107,8 @@ def kernel_source_hash(exclude=()):
         if os.path.basename(f) in exclude:
             continue
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8", errors="surrogateescape") as fh:
+            h.update(_code_only(fh.read()).encode("utf-8", errors="surrogateescape"))
     return h.hexdigest()[:16]
 
 

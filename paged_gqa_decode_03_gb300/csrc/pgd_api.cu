@@ -1012,7 +1012,7 @@ pgd_status make_varlen_plan(int S, int total_q, int max_q, int Hq, int Hkv, int 
     // Calls with at most kMaxCols (query token, head) rows per (sequence, KV
     // head) — decode steps, the verification step of speculative decoding —
     // read each K/V byte for only a few rows: an HBM-bound scan, which the
-    // decode kernel's MQ form does (mma.sync over 16 columns, partitions of
+    // decode kernel's MQ form does (one n8 column tile of mma.sync, partitions of
     // 256 / 512 tokens chosen as for the decode, partials per query row).
     vp->mq = D <= 128 && vp->G <= kMaxGroup && max_q >= 1 &&
              (long long)max_q * vp->G <= kMaxCols &&

@@ -28,9 +28,15 @@
 //        merge their running states in shared memory and write the final
 //        output (single-partition sequences) or the partition partial
 //        (log2-space max, exp-sum, normalised output).
+//    The MQ instantiation (several query tokens per sequence, at most 8
+//    (query token, head) rows per (sequence, KV head)) takes the n8 column
+//    tile as (query token, head) columns, each with its own causal limit,
+//    and keeps its partials per query row.
 // 2. paged_gqa_reduce_kernel — merges the partition partials of every
 //    (sequence, query head) ("Four speed-up tricks", 4) and writes zeros for
 //    empty sequences.  Launched with programmatic dependent launch.
+// 3. paged_gqa_reduce_rows_kernel — the same merge per (query row, head)
+//    for the MQ instantiation.
 #pragma once
 
 #include <atomic>
