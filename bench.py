@@ -64,9 +64,9 @@ TRAFFIC = {
                          ("ragged_tails_q8", 256): 472_751_360 + 6_460_672,
                          ("serving_mix_q8", 512): 644_779_776 + 6_981_376},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "236e3c48de63c699": {("chunked_prefill", 8320): 289_198_080 + 12_453_376,
-                         ("prefill", 2048): 167_980_032 + 79_201_024,
-                         ("spec_verify", 4096): 605_141_248 + 4_790_016},
+    "0acedd27c2b2c2e9": {("chunked_prefill", 8320): 269_372_928 + 40_933_376,
+                         ("prefill", 2048): 103_586_560 + 82_871_552,
+                         ("spec_verify", 4096): 605_143_296 + 4_416_512},
 }
 
 

@@ -35,6 +35,15 @@
 
 namespace pgd {
 
+// L2 policy for data that other CTAs read again soon: kept ahead of the
+// other lines (the tile pairs of one sequence and KV head read the same pages)
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kVarlenThreads, 1)
     paged_varlen_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -658,7 +667,7 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
         __syncwarp();
         if (lane < copies)
             tma_load_5d(kv_s + lane * groups * GROUP, &tmap_k, 0, 0, 0, grp_of(0), blk_next,
-                        smem_addr(&k_full[0]), l2_evict_first_policy());
+                        smem_addr(&k_full[0]), l2_evict_last_policy());
     }
     if (warp == 1)
         tc_alloc(smem_addr(&tmem_base_s), kVarlenTmemCols);
@@ -677,7 +686,9 @@ __global__ void __launch_bounds__(kVarlenThreads, 1)
     if (warp == 0 || warp == kVWarp) {
         // ============================================================ producers
         // (warp 0 issued Q and stage 0's K before the set-up barrier)
-        const uint64_t pol = l2_evict_first_policy();
+        // the tile pairs of a sequence and KV head read the same pages: keep
+        // them in L2 for the next pairs
+        const uint64_t pol = l2_evict_last_policy();
         if (lane == 0 && is_v)
             prefetch_tensormap(&tmap_v);
         const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
