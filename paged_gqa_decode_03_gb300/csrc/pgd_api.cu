@@ -287,6 +287,65 @@ pgd_status encode_meta_map(CUtensorMap *map, const void *base, const CacheGeom &
     return PGD_OK;
 }
 
+// (scale, bias) pairs at any strides where a row's pairs are 16 bytes
+// (head_dim 256; strides are multiples of a row's pairs, so of 16 bytes):
+// 32-bit elements viewed as D/64 pairs x BS rows (token stride) x Hkv heads
+// (head stride) x NB pages (page stride), strides in bf16 elements, and
+// with pair_stride > 0 both arrays (`lo` the lower one) as a fifth
+// dimension; a box of D/64 x box_rows x 1 x 1 (x 2) lands box_rows rows of
+// one (page, head) as [array][row][pair], the layout of the head-major
+// copies.
+pgd_status encode_meta_rows_map(CUtensorMap *map, const void *lo, long long pair_stride,
+                                const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    const int ng = g.D / kQuantGroup;
+    const cuuint32_t rank = pair_stride > 0 ? 5 : 4;
+    cuuint64_t dims[5] = {(cuuint64_t)ng, (cuuint64_t)g.BS, (cuuint64_t)g.Hkv, (cuuint64_t)g.NB, 2};
+    cuuint64_t strides[4] = {(cuuint64_t)g.token_stride * 2, (cuuint64_t)g.head_stride * 2,
+                             (cuuint64_t)g.page_stride * 2, (cuuint64_t)pair_stride};
+    cuuint32_t box[5] = {(cuuint32_t)ng, (cuuint32_t)box_rows, 1, 1, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<void *>(lo), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (strided scales) failed (CUresult %d)",
+                    (int)r);
+    return PGD_OK;
+}
+
+// Both quantised code arrays in one map where a row's D codes and the KV
+// heads of a token are adjacent (head stride D bytes, e.g. token-major
+// caches): 128 bytes x rows (token stride) x (head, slab) pairs (head * D/128
+// + slab, 128 bytes apart) x NB pages (page stride) x 2 arrays; a box of 128
+// x rows x D/128 x 1 x 2 lands a page's codes of both arrays as
+// [array][slab][row][128 B] (128-byte swizzle), like the head-major pair map.
+pgd_status encode_code_pair_rows_map(CUtensorMap *map, const void *lo, long long pair_stride,
+                                     const CacheGeom &g, int box_rows)
+{
+    EncodeTiledFn fn;
+    pgd_status st = encode_fn(&fn);
+    if (st)
+        return st;
+    cuuint64_t dims[5] = {128, (cuuint64_t)g.BS, (cuuint64_t)g.Hkv * (g.D / 128),
+                          (cuuint64_t)g.NB, 2};
+    cuuint64_t strides[4] = {(cuuint64_t)g.token_stride, 128, (cuuint64_t)g.page_stride,
+                             (cuuint64_t)pair_stride};  // bytes
+    cuuint32_t box[5] = {128, (cuuint32_t)box_rows, (cuuint32_t)(g.D / 128), 1, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(lo), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PGD_ERR_CUDA, "cuTensorMapEncodeTiled (code rows pair) failed (CUresult %d)",
+                    (int)r);
+    return PGD_OK;
+}
+
 // Both (scale, bias) pair arrays in one map (head-major): the pairs of a
 // (page, head) block x blocks (page * Hkv + head) x 2 arrays, the array
 // stride being the distance between them (`lo` the lower one); a box of
@@ -485,11 +544,18 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
     }
     MapCacheEntry &c = t_maps[t_maps_next];
     pgd_status st;
-    if (kind == 4 || kind == 5) {
+    // kinds: 0 fp16 rows, 1 fp16 8-row groups, 2 codes, 3 head-major pairs,
+    // 6 pairs of 16-byte rows at any strides; both arrays in one map: 4
+    // codes (head-major), 5 head-major pairs, 7 pairs of 16-byte rows, 8
+    // codes with adjacent heads
+    if (kind == 4 || kind == 5 || kind == 7 || kind == 8) {
         const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
         const long long stride = (long long)(ka < va ? va - ka : ka - va);
-        if ((st = kind == 4 ? encode_code_pair_map(&c.tk, ka < va ? k : v, stride, geom, box)
-                            : encode_meta_pair_map(&c.tk, ka < va ? k : v, stride, geom, box))) {
+        const void *lo = ka < va ? k : v;
+        if ((st = kind == 4   ? encode_code_pair_map(&c.tk, lo, stride, geom, box)
+                  : kind == 5 ? encode_meta_pair_map(&c.tk, lo, stride, geom, box)
+                  : kind == 7 ? encode_meta_rows_map(&c.tk, lo, stride, geom, box)
+                              : encode_code_pair_rows_map(&c.tk, lo, stride, geom, box))) {
             c.k = c.v = nullptr;
             return st;
         }
@@ -503,11 +569,14 @@ pgd_status cache_maps(const void *k, const void *v, const CacheGeom &geom, int b
             return encode_cache_map_groups(m, base, geom, box);
         case 2:
             return encode_code_map(m, base, geom, box);
+        case 6:
+            return encode_meta_rows_map(m, base, 0, geom, box);
         default:
             return encode_meta_map(m, base, geom, box);
         }
     };
-    if (kind != 4 && kind != 5 && ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v)))) {
+    if (kind != 4 && kind != 5 && kind != 7 && kind != 8 &&
+        ((st = enc(&c.tk, k)) || (st = enc(&c.tv, v)))) {
         c.k = c.v = nullptr;
         return st;
     }
@@ -722,7 +791,11 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     const int NM = (D / kQuantGroup) * 2;
     const Strides ms = meta_strides ? *meta_strides
                                     : Strides{(long long)Hkv * BS * NM, (long long)BS * NM, NM};
-    bool q8_rows = false, codes_head_major = true;
+    // q8_rows: the pairs are not head-major; 1: the kernel copies them row by
+    // row, 2: by a tensor copy of 16-byte rows (head_dim 256: the strides,
+    // multiples of a row's pairs, are multiples of 16 bytes)
+    int q8_rows = 0;
+    bool codes_head_major = true;
     if (q8) {
         if (kv_strides.page % 16 || kv_strides.head % 16 || kv_strides.token % 16)
             return fail(PGD_ERR_INVALID_ARG,
@@ -738,8 +811,9 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
         const Strides hm = head_major(Hkv, BS, D);
         codes_head_major = kv_strides.page == hm.page && kv_strides.head == hm.head &&
                            kv_strides.token == hm.token;
-        q8_rows = !codes_head_major || ms.page != (long long)Hkv * BS * NM ||
-                  ms.head != (long long)BS * NM || ms.token != NM;
+        const bool rows = !codes_head_major || ms.page != (long long)Hkv * BS * NM ||
+                          ms.head != (long long)BS * NM || ms.token != NM;
+        q8_rows = !rows ? 0 : (NM * 2 == 16 ? 2 : 1);
     }
     if (!own_workspace && workspace && !aligned(workspace, 256))
         return fail(PGD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -788,29 +862,37 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
                                : v_at >= k_at ? (long long)(v_at - k_at)
                                               : -(long long)(k_at - v_at);
     const long long gap_abs = code_gap < 0 ? -code_gap : code_gap;
-    const bool q8_pair = q8 && codes_head_major && box * D <= 4096 && gap_abs > 0 &&
-                         gap_abs % 16 == 0 && gap_abs < (1ll << 40) &&
-                         (long long)NB * Hkv < (1ll << 31);
-    // (the pairs' tensor map serves head-major pairs only; at other strides
-    // the kernel copies them row by row).  One copy for both pair arrays
-    // under the same conditions, where a piece's pairs fill whole 128-byte
-    // runs (the kernel then keeps a piece's K and V pairs side by side)
+    // (1: head-major codes; 2: a token's heads adjacent, head stride D bytes,
+    // as token-major caches have them)
+    const bool gap_ok = gap_abs > 0 && gap_abs % 16 == 0 && gap_abs < (1ll << 40);
+    const int q8_pair = !q8 || box * D > 4096 || !gap_ok ? 0
+                        : codes_head_major                ? ((long long)NB * Hkv < (1ll << 31) ? 1 : 0)
+                        : kv_strides.head == D            ? 2
+                                                          : 0;
+    // One copy for both pair arrays under the same conditions, where a
+    // piece's pairs fill whole 128-byte runs (the kernel then keeps a piece's
+    // K and V pairs side by side): head-major pairs, or 16-byte rows at any
+    // strides (q8_rows 2); the kernel copies other pairs row by row
     const uintptr_t km_at = reinterpret_cast<uintptr_t>(k_meta),
                     vm_at = reinterpret_cast<uintptr_t>(v_meta);
     const long long meta_gap = km_at < vm_at ? (long long)(vm_at - km_at) : (long long)(km_at - vm_at);
-    const int q8_meta_pair = q8 && !q8_rows && (box * (D / kQuantGroup) * 4) % 128 == 0 &&
+    const int q8_meta_pair = q8 && q8_rows != 1 && (box * (D / kQuantGroup) * 4) % 128 == 0 &&
                                      meta_gap > 0 && meta_gap % 16 == 0 && meta_gap < (1ll << 40) &&
-                                     (long long)NB * Hkv < (1ll << 31)
+                                     (q8_rows || (long long)NB * Hkv < (1ll << 31))
                                  ? (km_at < vm_at ? 1 : 2)
                                  : 0;
-    if ((st = cache_maps(k_cache, v_cache, geom, box, q8 ? (q8_pair ? 4 : 2) : 0, &tk, &tv)) ||
+    const CacheGeom meta_geom = {NB, Hkv, BS, D, ms.page, ms.head, ms.token};
+    const int code_kind = !q8 ? 0 : q8_pair == 1 ? 4 : q8_pair == 2 ? 8 : 2;
+    if ((st = cache_maps(k_cache, v_cache, geom, box, code_kind, &tk, &tv)) ||
         (q8 && !q8_rows &&
-         (st = cache_maps(k_meta, v_meta, geom, box, q8_meta_pair ? 5 : 3, &tkm, &tvm)))) {
+         (st = cache_maps(k_meta, v_meta, geom, box, q8_meta_pair ? 5 : 3, &tkm, &tvm))) ||
+        (q8 && q8_rows == 2 &&
+         (st = cache_maps(k_meta, v_meta, meta_geom, box, q8_meta_pair ? 7 : 6, &tkm, &tvm)))) {
         if (own_workspace && ws)
             cudaFreeAsync(ws, stream);
         return st;
     }
-    const KVMaps maps = {tk, tv, q8 && !q8_rows ? tkm : tk, q8 && !q8_rows ? tvm : tv};
+    const KVMaps maps = {tk, tv, q8 && q8_rows != 1 ? tkm : tk, q8 && q8_rows != 1 ? tvm : tv};
 
     // claim counter: given (static scratch), this stream's, or a per-call one
     auto release_ws = [&] {
@@ -877,9 +959,9 @@ pgd_status run(float *out, const uint16_t *q, const void *k_cache, const void *v
     p.v_cache = reinterpret_cast<__half *>(const_cast<void *>(v_cache));
     p.k_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(k_meta)) : nullptr;
     p.v_meta = q8 ? static_cast<uint16_t *>(const_cast<void *>(v_meta)) : nullptr;
-    p.q8_pair = q8_pair ? 1 : 0;
+    p.q8_pair = q8_pair;
     p.q8_meta_pair = q8_meta_pair;
-    p.q8_rows = q8_rows ? 1 : 0;
+    p.q8_rows = q8_rows;
     p.meta_page_stride = ms.page;
     p.meta_head_stride = ms.head;
     p.meta_token_stride = ms.token;

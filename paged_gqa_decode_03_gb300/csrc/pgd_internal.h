@@ -131,13 +131,15 @@ struct DecodeParams {
     uint16_t *k_meta;             // quantised pages: [NB][Hkv][BS][D/64][2] bf16
     uint16_t *v_meta;             //   (scale, bias) pairs (written by the fused
                                   //   append), or null
-    int q8_pair;                  // quantised pages: 1 = one tensor copy brings a page's
-                                  //   K and V codes (tmap_k spans both arrays)
+    int q8_pair;                  // quantised pages: one tensor copy brings a page's
+                                  //   K and V codes (tmap_k spans both arrays), 1: over
+                                  //   (page, head) blocks, 2: over (head, slab) pairs
     int q8_meta_pair;             // one tensor copy brings a page's K and V (scale,
                                   //   bias) pairs (tmap_km spans both arrays): 1 with
                                   //   K's array the lower, 2 with V's; 0: two copies
     int q8_koff, q8_voff;         //   bytes of K / V codes within a page's pair of slots
-    int q8_rows;                  //   1: the pairs' rows at meta strides (any layout)
+    int q8_rows;                  //   the pairs at meta strides (any layout), copied
+                                  //   1: row by row, 2: by a tensor copy of 16-byte rows
     long long meta_page_stride;   // quantised pages: the pairs of token r of page b,
     long long meta_head_stride;   //   KV head g start at bf16 element b*page + g*head
     long long meta_token_stride;  //   + r*token (head-major unless q8_rows)

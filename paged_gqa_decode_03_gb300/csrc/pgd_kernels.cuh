@@ -143,8 +143,10 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     constexpr int PAGE_META = Q8 ? BOX * NGRP * 4 : 0;        // bytes copied per page piece
     constexpr int META_SLOT = Q8 ? meta_slot_bytes(BOX, D) : 0;  // their 128-aligned slot
     // the pairs of a page piece go by one tensor copy per array (QSTR: the
-    // pairs' rows at any strides, copied row by row on the load path)
+    // pairs' rows at any strides, by a tensor copy of 16-byte rows where a
+    // row's pairs are 16 bytes (q8_rows 2), else row by row on the load path)
     constexpr bool META_BY_TMA = !QSTR;
+    constexpr bool META_ROWS_TMA = QSTR && NGRP * 4 == 16;
     constexpr int KT = D / 16;             // k-steps of QK; 16-row tiles of O^T
     constexpr int KV_BYTES = stage_kv_bytes<D, Q8>();
     constexpr int META_BYTES = stage_meta_bytes<D, Q8, BS>();
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     // runs (one tensor copy over both pair arrays can then bring them:
     // q8_meta_pair), otherwise K's slots from the stage's pair area and V's
     // META_BYTES after
-    constexpr bool MPAIRED = Q8 && META_BY_TMA && PAGE_META % 128 == 0;
+    constexpr bool MPAIRED = Q8 && (META_BY_TMA || META_ROWS_TMA) && PAGE_META % 128 == 0;
     constexpr int MSTR = MPAIRED ? 2 * PAGE_META : META_SLOT;  // piece to piece
     constexpr int MVOFF = MPAIRED ? PAGE_META : META_BYTES;    // V's pairs after K's
     constexpr int Q_OFF = 2 * KV_BYTES + 2 * META_BYTES;  // the group's queries in a stage
@@ -165,6 +167,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     static_assert(STAGE % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle alignment");
     static_assert(NTT * NCOLS * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
     static_assert(!Q8 || (D % 128 == 0), "quantised pages: rows of whole 128-byte slabs");
+    static_assert(!Q8 || NGRP * 4 == 8 || NGRP * 4 == 16, "8 or 16 bytes of pairs per row");
     static_assert(!Q8 || (T / BOX) * META_SLOT <= META_BYTES, "scale slots fit the stage");
     static_assert(!MPAIRED || (T / BOX) * MSTR <= 2 * META_BYTES, "paired slots fit the stage");
 
@@ -386,7 +389,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                                               p.v_cache, p.k_meta, p.v_meta, lane);
                     __syncwarp();
                 }
-                if constexpr (Q8 && QSTR) {
+                const bool meta_tma = META_BY_TMA || (META_ROWS_TMA && p.q8_rows == 2);
+                if (Q8 && QSTR && !meta_tma) {
                     // the rows' (scale, bias) pairs at the pairs' strides: one
                     // 8- or 16-byte copy per row on the load path into the
                     // page's slot ([row][group]); a page outside the pool
@@ -409,7 +413,6 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                                 cp_async_16(dm, p.k_meta + off, in ? 16u : 0u);
                                 cp_async_16(dm + MVOFF, p.v_meta + off, in ? 16u : 0u);
                             } else {
-                                static_assert(NGRP * 4 == 8, "8 or 16 bytes of pairs per row");
                                 cp_async_8(dm, p.k_meta + off, in ? 8u : 0u);
                                 cp_async_8(dm + MVOFF, p.v_meta + off, in ? 8u : 0u);
                             }
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                     hdr[slot].qn = qn;
                     hdr[slot].qrow0 = qrow0;
                     hdr[slot].qpos0 = L - qn;
-                    const uint32_t bytes = pc * (PAGE_BYTES + (META_BY_TMA ? PAGE_META : 0)) * 2 +
+                    const uint32_t bytes = pc * (PAGE_BYTES + (meta_tma ? PAGE_META : 0)) * 2 +
                                            (st == 0 ? qn * G * D * 2 : 0);
                     mbar_arrive_expect_tx(fb, bytes);
                 }
@@ -459,9 +462,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                         // with both code arrays in one map: one copy of
                         // [array][slab][row][128 B] for the pair of slots
                         const uint32_t dk = sb + jj * PSTR;
-                        if (PAIRED && p.q8_pair) {
+                        if (PAIRED && p.q8_pair == 1) {
                             tma_load_5d(dk, &tmap_k, 0, row0, 0, c_page < 0 ? -1 : c_page * Hkv + g,
                                         0, fb, pol);
+                        } else if (QSTR && PAIRED && p.q8_pair == 2) {  // a token's heads adjacent
+                            tma_load_5d(dk, &tmap_k, 0, row0, g * SLABS, c_page, 0, fb, pol);
                         } else if (PAIRED) {
                             tma_load_5d(dk + p.q8_koff, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
                             tma_load_5d(dk + p.q8_voff, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
@@ -469,9 +474,15 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                             tma_load_5d(dk, &tmap_k, 0, row0, 0, g, c_page, fb, pol);
                             tma_load_5d(dk + KV_BYTES, &tmap_v, 0, row0, 0, g, c_page, fb, pol);
                         }
-                        if (Q8 && META_BY_TMA) {  // the rows' (scale, bias) pairs
+                        if (Q8 && meta_tma) {  // the rows' (scale, bias) pairs
                             const uint32_t dm = sb + 2 * KV_BYTES + jj * MSTR;
-                            if (MPAIRED && p.q8_meta_pair) {  // both arrays' pairs in one copy
+                            if (QSTR && MPAIRED && p.q8_meta_pair) {
+                                // BOX rows of (page, head g) at the pairs' strides, both arrays
+                                tma_load_5d(dm, &tmap_km, 0, row0, g, c_page, 0, fb, pol);
+                            } else if (QSTR) {
+                                tma_load_4d(dm, &tmap_km, 0, row0, g, c_page, fb, pol);
+                                tma_load_4d(dm + MVOFF, &tmap_vm, 0, row0, g, c_page, fb, pol);
+                            } else if (MPAIRED && p.q8_meta_pair) {  // both arrays' pairs in one copy
                                 tma_load_3d(dm, &tmap_km, row0 * NGRP,
                                             c_page < 0 ? -1 : c_page * Hkv + g, 0, fb, pol);
                             } else {

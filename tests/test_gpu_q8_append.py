@@ -189,9 +189,57 @@ def test_q8_strided_layouts_equal_head_major(D, BS):
     assert pgd.pgd_check_device_error() == 0
 
 
-def test_q8_strided_against_oracle():
-    w = make_custom(S=len(LENS), Hq=32, Hkv=8, D=128, BS=16, lens=LENS, seed=5, device=DEV,
-                    MB=64)
+@pytest.mark.parametrize("D,BS", [(128, 16), (256, 8), (256, 32)])
+def test_q8_token_major_arrays_in_either_order_or_shared(D, BS):
+    """Token-major caches where one tensor copy brings a page's K and V codes
+    (a token's heads adjacent) and, at head_dim 256, one their pairs: with V
+    below K in memory, either order of the pair arrays, and K and V one
+    array (two copies) - bitwise the head-major result of the same rows."""
+    w = make_custom(S=len(LENS), Hq=16, Hkv=2, D=D, BS=BS, lens=LENS, seed=D + BS + 23,
+                    device=DEV, MB=(1024 + BS - 1) // BS)
+    c = make_q8(w)
+    NB = c.k_codes.shape[0]
+    cs, ms = pgd.q8_strides("token_major", w.Hkv, BS, D)
+
+    def both(lo, hi):  # one buffer: `lo` below `hi`, as token-major views
+        lo_t, hi_t = _token_major(lo), _token_major(hi)
+        buf = torch.empty((2,) + lo_t.shape, dtype=lo.dtype, device=DEV)
+        buf[0].copy_(lo_t)
+        buf[1].copy_(hi_t)
+        return buf[0], buf[1]
+
+    def run(kc, km, vc, vm, strided):
+        out = torch.full((w.S, w.Hq, w.D), float("nan"), dtype=torch.float32, device=DEV)
+        if strided:
+            pgd.paged_gqa_decode_q8_strided(out, w.q, kc, km, vc, vm, w.block_tables,
+                                            w.seq_lens, w.scale, w.Hkv, BS, NB, cs, ms, 512)
+        else:
+            pgd.paged_gqa_decode_q8(out, w.q, kc, km, vc, vm, w.block_tables, w.seq_lens,
+                                    w.scale, 512)
+        torch.cuda.synchronize()
+        return out
+
+    base = run(c.k_codes, c.k_meta, c.v_codes, c.v_meta, False)
+    vc_t, kc_t = both(c.v_codes, c.k_codes)  # V's codes below K's
+    for v_first in (False, True):
+        if v_first:
+            vm_t, km_t = both(c.v_meta, c.k_meta)
+        else:
+            km_t, vm_t = both(c.k_meta, c.v_meta)
+        out = run(kc_t, km_t, vc_t, vm_t, True)
+        assert torch.equal(out, base), f"V's pairs below K's: {v_first}"
+    shared = run(c.k_codes, c.k_meta, c.k_codes, c.k_meta, False)
+    kc1, km1 = _token_major(c.k_codes), _token_major(c.k_meta)
+    assert torch.equal(run(kc1, km1, kc1, km1, True), shared), "K and V one array"
+    assert pgd.pgd_check_device_error() == 0
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv", [(128, 16, 32, 8), (256, 8, 24, 4), (256, 32, 16, 2)])
+def test_q8_strided_against_oracle(D, BS, Hq, Hkv):
+    """Token-major quantised caches against the oracle (head_dim 128: the
+    pairs copied row by row; 256: by the tensor copy of 16-byte rows)."""
+    w = make_custom(S=len(LENS), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=LENS, seed=5 + D + BS,
+                    device=DEV, MB=(1024 + BS - 1) // BS)
     c = make_q8(w)
     arrs = [_token_major(t) for t in (c.k_codes, c.k_meta, c.v_codes, c.v_meta)]
     cs, ms = pgd.q8_strides("token_major", w.Hkv, w.BS, w.D)
