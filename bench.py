@@ -54,19 +54,19 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "8569eb3729f9a84e": {("long_context", 512): 1_293_166_848 + 7_584_768,
-                         ("long_context", 256): 1_293_076_736 + 7_466_496,
-                         ("ragged_tails", 256): 888_261_632 + 7_029_760,
-                         ("serving_mix", 512): 1_212_324_096 + 6_937_856,
-                         ("batch_decode", 512): 633_308_416 + 5_217_024,
-                         ("batch_decode_q8", 512): 336_779_776 + 5_091_328,
-                         ("long_context_q8", 512): 687_151_104 + 7_019_776,
-                         ("ragged_tails_q8", 256): 472_751_360 + 6_460_672,
-                         ("serving_mix_q8", 512): 644_779_776 + 6_981_376},
+    "ce6fd6553eb01471": {("long_context", 512): 1_293_057_536 + 7_561_216,
+                         ("long_context", 256): 1_293_076_480 + 7_345_664,
+                         ("ragged_tails", 256): 888_201_216 + 6_739_968,
+                         ("serving_mix", 512): 1_212_346_112 + 6_936_320,
+                         ("batch_decode", 512): 633_320_960 + 5_342_464,
+                         ("batch_decode_q8", 512): 336_778_240 + 5_188_608,
+                         ("long_context_q8", 512): 687_138_304 + 6_933_248,
+                         ("ragged_tails_q8", 256): 472_704_768 + 6_682_112,
+                         ("serving_mix_q8", 512): 644_729_088 + 6_886_144},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "0acedd27c2b2c2e9": {("chunked_prefill", 8320): 269_372_928 + 40_933_376,
-                         ("prefill", 2048): 103_586_560 + 82_871_552,
-                         ("spec_verify", 4096): 605_143_296 + 4_416_512},
+    "920a60cd8900d2ce": {("chunked_prefill", 8320): 269_665_536 + 42_012_672,
+                         ("prefill", 2048): 103_034_368 + 82_572_800,
+                         ("spec_verify", 4096): 605_140_480 + 4_452_608},
 }
 
 
@@ -646,7 +646,12 @@ def workload_entry(m, peak, traffic, P_req):
             "clocks": m["clocks"], "e2e": m["e2e"], "cpu_baseline": m["cpu"]}
 
 
-def traffic_for(name, P_used, q8):
+def traffic_for(name, P_used, q8, args):
+    """DRAM bytes of one launch of the dominant kernel, captured for the
+    head-major caches without the fused append only (other layouts and the
+    append run other instantiations: null)."""
+    if args.layout != "head_major" or args.append:
+        return None
     return TRAFFIC.get(kernel_source_hash(DECODE_HASH_EXCLUDE), {}).get(
         (name + ("_q8" if q8 else ""), P_used))
 
@@ -696,7 +701,8 @@ def run_ours(args):
                                 max(1, min(args.steps, args.e2e_steps)), args.cpu_seconds_each,
                                 args.cpu_seconds_1t, with_cpu)
             key = f"{wname}_p{wP}" if wP else f"{wname}_auto"
-            per[key] = workload_entry(mx, peak, traffic_for(wname, mx["P_used"], mx["q8"]), wP)
+            per[key] = workload_entry(mx, peak, traffic_for(wname, mx["P_used"], mx["q8"], args),
+                                      wP)
             per[key]["workload"] = wname
             del wx
             torch.cuda.empty_cache()
@@ -714,7 +720,7 @@ def run_ours(args):
             "config": config,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
-                         "traffic": traffic_for(name, m["P_used"], m["q8"]),
+                         "traffic": traffic_for(name, m["P_used"], m["q8"], args),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",
                          "kernel": "paged_gqa_partial_kernel",
                          "kernel_ms": m["kern_ms"],

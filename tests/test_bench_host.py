@@ -1,6 +1,7 @@
 """Host logic of bench.py that needs no GPU: the code-only source hash that
 keys the recorded DRAM traffic (comments and layout do not change it, code
 does, string literals are kept) and the traffic lookup."""
+import argparse
 import os
 import shutil
 
@@ -60,6 +61,12 @@ def test_traffic_recorded_for_the_current_sources():
                 ("serving_mix", 512), ("batch_decode", 512), ("batch_decode_q8", 512),
                 ("long_context_q8", 512), ("ragged_tails_q8", 256), ("serving_mix_q8", 512)]:
         assert d[key] > 0
-        assert bench.traffic_for(key[0].replace("_q8", ""), key[1], key[0].endswith("_q8")) == d[key]
+        plain = argparse.Namespace(layout="head_major", append=False)
+        assert bench.traffic_for(key[0].replace("_q8", ""), key[1], key[0].endswith("_q8"),
+                                 plain) == d[key]
+    # other layouts and the fused append run other instantiations: no figure
+    for other in (argparse.Namespace(layout="token_major", append=False),
+                  argparse.Namespace(layout="head_major", append=True)):
+        assert bench.traffic_for("batch_decode", 512, False, other) is None
     v = bench.TRAFFIC[hv]
     assert set(v) == {("chunked_prefill", 8320), ("prefill", 2048), ("spec_verify", 4096)}
