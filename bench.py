@@ -54,19 +54,19 @@ FALLBACK_HBM_GBS = 6800.0
 # partition size).
 TRAFFIC = {
     # decode kernels (hash without pgd_varlen.cu)
-    "ce6fd6553eb01471": {("long_context", 512): 1_293_057_536 + 7_561_216,
-                         ("long_context", 256): 1_293_076_480 + 7_345_664,
-                         ("ragged_tails", 256): 888_201_216 + 6_739_968,
-                         ("serving_mix", 512): 1_212_346_112 + 6_936_320,
-                         ("batch_decode", 512): 633_320_960 + 5_342_464,
-                         ("batch_decode_q8", 512): 336_778_240 + 5_188_608,
-                         ("long_context_q8", 512): 687_138_304 + 6_933_248,
-                         ("ragged_tails_q8", 256): 472_704_768 + 6_682_112,
-                         ("serving_mix_q8", 512): 644_729_088 + 6_886_144},
+    "22686a0c259250ef": {("long_context", 512): 1_293_085_440 + 7_323_904,
+                         ("long_context", 256): 1_293_064_192 + 7_469_312,
+                         ("ragged_tails", 256): 888_242_432 + 6_854_144,
+                         ("serving_mix", 512): 1_212_329_984 + 6_878_464,
+                         ("batch_decode", 512): 633_321_472 + 5_394_432,
+                         ("batch_decode_q8", 512): 336_775_168 + 4_792_576,
+                         ("long_context_q8", 512): 687_138_560 + 6_665_216,
+                         ("ragged_tails_q8", 256): 472_754_688 + 6_605_056,
+                         ("serving_mix_q8", 512): 644_722_176 + 6_985_472},
     # the several-query-token kernels (hash without the decode kernels' files)
-    "920a60cd8900d2ce": {("chunked_prefill", 8320): 269_665_536 + 42_012_672,
-                         ("prefill", 2048): 103_034_368 + 82_572_800,
-                         ("spec_verify", 4096): 605_140_480 + 4_452_608},
+    "dca98565443fa7ab": {("chunked_prefill", 8320): 267_655_168 + 41_203_200,
+                         ("prefill", 2048): 102_982_400 + 83_275_008,
+                         ("spec_verify", 4096): 605_178_624 + 4_264_704},
 }
 
 

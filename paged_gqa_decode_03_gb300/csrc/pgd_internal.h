@@ -42,14 +42,16 @@ constexpr int kMaxTailStages = 16;
 // ring holds about 100 KB for every head_dim (two CTAs per SM).
 template <int D> struct Shape;
 // T8 / NC8 / NS8: the same for quantised pages, whose consumers do more work
-// per byte (code conversion, the affine terms): twice the tokens and
-// consumer warps per stage, fewer stages (one more where the page size
-// leaves room: ring_stages).
+// per byte (code conversion, the affine terms): twice the tokens per stage,
+// fewer stages (one more where the page size leaves room: ring_stages); at
+// head_dim 128 four consumer warps of two 16-token tiles each (the tiles
+// share a warp's softmax reductions and the unit merge has half the states;
+// eight warps of one tile measured 7-10 % slower), at 256 one tile each.
 template <> struct Shape<64> {
     static constexpr int T = 64, NC = 4, NS = 6, T8 = 64, NC8 = 4, NS8 = 6;
 };
 template <> struct Shape<128> {
-    static constexpr int T = 64, NC = 4, NS = 3, T8 = 128, NC8 = 8, NS8 = 2;
+    static constexpr int T = 64, NC = 4, NS = 3, T8 = 128, NC8 = 4, NS8 = 2;
 };
 template <> struct Shape<256> {
     static constexpr int T = 32, NC = 2, NS = 3, T8 = 64, NC8 = 4, NS8 = 2;

@@ -127,7 +127,8 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                              const DecodeParams p)
 {
     constexpr int T = stage_tokens_of<D, Q8>(), NC = consumer_warps<D, Q8, MQ>();
-    constexpr int NTT = T / 16;            // 16-token tiles of a stage (one per consumer warp)
+    constexpr int NTT = T / 16;            // 16-token tiles of a stage
+    constexpr int TPW = NTT / NC;          // of them per consumer warp
     constexpr int NS = ring_stages<D, Q8, BS>();
     constexpr int ROWB = D * (Q8 ? 1 : 2); // bytes of one cached row
     constexpr int SLABS = ROWB / 128;      // 128-byte column slabs of a row
@@ -162,10 +163,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     constexpr int OST = D + 4;             // merge buffer row stride (floats)
     constexpr int NCOLS = MQ ? kMaxCols : kMaxGroup;  // columns per unit
     static_assert(!MQ || (!Q8 && !TRACE && !QAPP && !QSTR && D <= 128), "MQ: fp16, head_dim <= 128");
-    static_assert(NTT * 16 == T && NC == NTT, "one 16-token tile per consumer warp per stage");
+    static_assert(NTT * 16 == T && NC * TPW == NTT && (TPW == 1 || (Q8 && !MQ)),
+                  "16-token tiles per consumer warp and stage (several: quantised pages)");
     static_assert(BS <= T ? (T % BS == 0) : (BS % T == 0), "stage/page sizes");
     static_assert(STAGE % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle alignment");
-    static_assert(NTT * NCOLS * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
+    static_assert(NC * NCOLS * (2 + OST) * 4 <= STAGE, "merge buffer fits a stage");
     static_assert(!Q8 || (D % 128 == 0), "quantised pages: rows of whole 128-byte slabs");
     static_assert(!Q8 || NGRP * 4 == 8 || NGRP * 4 == 16, "8 or 16 bytes of pairs per row");
     static_assert(!Q8 || (T / BOX) * META_SLOT <= META_BYTES, "scale slots fit the stage");
@@ -665,11 +667,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
     // token x head); the NC warps merge their states once per unit, in the
     // shared memory of the unit's last stage.
     const int w = warp;
-    const int tt = w;                    // token tile
+    const int tt = w;                    // merge-state index of the warp
     const int gb = lane >> 2;            // C-fragment row: token within the tile
     const int tq = (lane & 3) * 2;       // C-fragment columns: query heads tq, tq+1
     const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix index, row in it
-    const int t0 = 16 * tt;              // this warp's tile within a stage
+    const int t0 = 16 * TPW * w;         // this warp's (first) tile within a stage
     float o[KT][4];                      // O^T[D x 8]: 16-row tile i, columns tq, tq+1
     uint32_t qf[KT][2];                  // Q^T B-fragments
     // Q8: rows of O^T are interleaved: tile i, fragment rows gb / gb+8 hold
@@ -767,7 +769,170 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                 }
             }
         }
-        if (t0 < valid) {
+        if constexpr (TPW > 1) {
+            // quantised pages, TPW tiles per warp (tokens t0 .. t0 + 16 TPW -
+            // 1): each tile's scores as below, one online-softmax step over
+            // all of them, then each tile's P V products
+            if (t0 < valid) {
+                const uint8_t *kmeta =
+                    sp + 2 * KV_BYTES + (MPAIRED && p.q8_meta_pair == 2 ? PAGE_META : 0);
+                const uint8_t *vmeta =
+                    sp + 2 * KV_BYTES + (MPAIRED && p.q8_meta_pair == 2 ? 0 : MVOFF);
+                const float sc = p.scale_log2;
+                float x[TPW][4];  // tile j: token gb / gb+8, head tq / tq+1
+#pragma unroll
+                for (int j = 0; j < TPW; ++j) {
+                    const int tj = t0 + 16 * j;
+                    x[j][0] = x[j][1] = x[j][2] = x[j][3] = -INFINITY;
+                    if (tj < valid) {
+                        float c[NGRP][4];
+#pragma unroll
+                        for (int a = 0; a < NGRP; ++a)
+                            c[a][0] = c[a][1] = c[a][2] = c[a][3] = 0.f;
+                        const int tok = tj + r8 + (mi & 1) * 8;
+                        const uint32_t rowaddr = sb + (PAIRED ? p.q8_koff : 0) + (tok / BOX) * PSTR +
+                                                 (tok % BOX) * 128;
+                        const int sw = tok & 7;
+#pragma unroll
+                        for (int kk = 0; kk < KT; kk += 2) {
+                            const int chunk = kk + (mi >> 1);
+                            const uint32_t addr =
+                                rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
+                            uint32_t r0, r1, r2, r3;
+                            ldsm_x4(addr, r0, r1, r2, r3);
+                            mma_16816(c[kk / 4], codes_to_half2_offset(r0, false),
+                                      codes_to_half2_offset(r1, false),
+                                      codes_to_half2_offset(r0, true),
+                                      codes_to_half2_offset(r1, true), qf[kk][0], qf[kk][1]);
+                            mma_16816(c[(kk + 1) / 4], codes_to_half2_offset(r2, false),
+                                      codes_to_half2_offset(r3, false),
+                                      codes_to_half2_offset(r2, true),
+                                      codes_to_half2_offset(r3, true), qf[kk + 1][0],
+                                      qf[kk + 1][1]);
+                        }
+                        const int ra = tj + gb, rb = ra + 8;
+                        const uint32_t *kma = reinterpret_cast<const uint32_t *>(
+                            kmeta + (ra / BOX) * MSTR + (ra % BOX) * NGRP * 4);
+                        const uint32_t *kmb = reinterpret_cast<const uint32_t *>(
+                            kmeta + (rb / BOX) * MSTR + (rb % BOX) * NGRP * 4);
+                        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+                        for (int gi = 0; gi < NGRP; ++gi) {
+                            const float2 ea = bf16_pair(kma[gi]), eb = bf16_pair(kmb[gi]);
+                            const float ba = fmaf(-1024.f, ea.x, ea.y),
+                                        bb = fmaf(-1024.f, eb.x, eb.y);
+                            d0 += fmaf(ea.x, c[gi][0], ba * qsum[gi][0]);
+                            d1 += fmaf(ea.x, c[gi][1], ba * qsum[gi][1]);
+                            d2 += fmaf(eb.x, c[gi][2], bb * qsum[gi][0]);
+                            d3 += fmaf(eb.x, c[gi][3], bb * qsum[gi][1]);
+                        }
+                        const bool va = ra < valid, vb = rb < valid;
+                        x[j][0] = va ? d0 * sc : -INFINITY;
+                        x[j][1] = va ? d1 * sc : -INFINITY;
+                        x[j][2] = vb ? d2 * sc : -INFINITY;
+                        x[j][3] = vb ? d3 * sc : -INFINITY;
+                    }
+                }
+                // token 0 of tile 0 is valid: every column max is finite
+                float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+                for (int j = 1; j < TPW; ++j) {
+                    mx0 = fmax3(mx0, x[j][0], x[j][2]);
+                    mx1 = fmax3(mx1, x[j][1], x[j][3]);
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                float pp[TPW][4];
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < TPW; ++j) {
+                    pp[j][0] = ex2(x[j][0] - mn0);
+                    pp[j][1] = ex2(x[j][1] - mn1);
+                    pp[j][2] = ex2(x[j][2] - mn0);
+                    pp[j][3] = ex2(x[j][3] - mn1);
+                    const float2 fa = unpack_half2(pack_half2(pp[j][0], pp[j][1]));
+                    const float2 fb = unpack_half2(pack_half2(pp[j][2], pp[j][3]));
+                    ls0 += fa.x + fb.x;
+                    ls1 += fa.y + fb.y;
+                }
+                l0 = l0 * al0 + ls0;
+                l1 = l1 * al1 + ls1;
+                // (skipped when neither head's max moved, al = 1 exactly)
+                if (__any_sync(~0u, (al0 != 1.f) | (al1 != 1.f))) {
+#pragma unroll
+                    for (int i = 0; i < KT; ++i) {
+                        o[i][0] *= al0;
+                        o[i][1] *= al1;
+                        o[i][2] *= al0;
+                        o[i][3] *= al1;
+                    }
+#pragma unroll
+                    for (int gi = 0; gi < NGRP; ++gi) {
+                        beta[gi][0] *= al0;
+                        beta[gi][1] *= al1;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < TPW; ++j) {
+                    const int tj = t0 + 16 * j;
+                    if (tj >= valid)
+                        continue;
+                    // as the one-tile form below: P scaled by the V rows'
+                    // scales per group, the biases and the offset into beta
+                    const int ra = tj + gb, rb = ra + 8;
+                    const bool va = ra < valid, vb = rb < valid;
+                    const uint32_t *vma = reinterpret_cast<const uint32_t *>(
+                        vmeta + (ra / BOX) * MSTR + (ra % BOX) * NGRP * 4);
+                    const uint32_t *vmb = reinterpret_cast<const uint32_t *>(
+                        vmeta + (rb / BOX) * MSTR + (rb % BOX) * NGRP * 4);
+                    uint32_t bf[NGRP][2];
+#pragma unroll
+                    for (int gi = 0; gi < NGRP; ++gi) {
+                        float2 ea = bf16_pair(vma[gi]), eb = bf16_pair(vmb[gi]);
+                        if (!va)
+                            ea = make_float2(0.f, 0.f);
+                        if (!vb)
+                            eb = make_float2(0.f, 0.f);
+                        const uint32_t ha = pack_half2(pp[j][0] * ea.x, pp[j][1] * ea.x);
+                        const uint32_t hb = pack_half2(pp[j][2] * eb.x, pp[j][3] * eb.x);
+                        bf[gi][0] = movmatrix_trans(ha);
+                        bf[gi][1] = movmatrix_trans(hb);
+                        const float2 fa = unpack_half2(ha), fb = unpack_half2(hb);
+                        beta[gi][0] += fmaf(-1024.f, fa.x + fb.x, pp[j][0] * ea.y) + pp[j][2] * eb.y;
+                        beta[gi][1] += fmaf(-1024.f, fa.y + fb.y, pp[j][1] * ea.y) + pp[j][3] * eb.y;
+                    }
+                    const int tok = tj + r8 + (mi & 1) * 8;
+                    const uint32_t rowaddr = sb + (PAIRED ? p.q8_voff : KV_BYTES) +
+                                             (tok / BOX) * PSTR + (tok % BOX) * 128;
+                    const int sw = tok & 7;
+#pragma unroll
+                    for (int i = 0; i < KT; i += 2) {
+                        const int chunk = i + (mi >> 1);
+                        const uint32_t addr =
+                            rowaddr + (chunk >> 3) * (BOX * 128) + (((chunk & 7) ^ sw) << 4);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4_t(addr, r0, r1, r2, r3);
+                        mma_16816(o[i], codes_to_half2_strided_offset(r0, false),
+                                  codes_to_half2_strided_offset(r0, true),
+                                  codes_to_half2_strided_offset(r1, false),
+                                  codes_to_half2_strided_offset(r1, true), bf[i / 4][0],
+                                  bf[i / 4][1]);
+                        mma_16816(o[i + 1], codes_to_half2_strided_offset(r2, false),
+                                  codes_to_half2_strided_offset(r2, true),
+                                  codes_to_half2_strided_offset(r3, false),
+                                  codes_to_half2_strided_offset(r3, true), bf[(i + 1) / 4][0],
+                                  bf[(i + 1) / 4][1]);
+                    }
+                }
+            }
+        } else if (t0 < valid) {
             if constexpr (!Q8) {
                 if (t0 + 16 > valid) {
                     // rows of this tile past the unit's end: zero V so that
@@ -1002,9 +1167,9 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
         // stage's shared memory (still held), then write the output row or
         // the partition partial, then release the stage.
         // [warp][column]
-        float *mg_m = reinterpret_cast<float *>(sp);            // [NTT][NCOLS]
-        float *mg_l = mg_m + NTT * NCOLS;                        // [NTT][NCOLS]
-        float *mg_o = mg_l + NTT * NCOLS;                        // [NTT][NCOLS][OST]
+        float *mg_m = reinterpret_cast<float *>(sp);            // [NC][NCOLS]
+        float *mg_l = mg_m + NC * NCOLS;                         // [NC][NCOLS]
+        float *mg_o = mg_l + NC * NCOLS;                         // [NC][NCOLS][OST]
         float lt0 = l0, lt1 = l1;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -1063,7 +1228,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                 const int g = idx / (D / 4), d4 = idx % (D / 4);
                 float M = -INFINITY;
 #pragma unroll
-                for (int wi = 0; wi < NTT; ++wi)
+                for (int wi = 0; wi < NC; ++wi)
                     M = fmaxf(M, mg_m[wi * NCOLS + g]);
                 // MQ: a column that saw no token in this unit (M = -inf) gets
                 // a zero exp-sum, which the reduce skips
@@ -1071,7 +1236,7 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
                 float den = 0.f;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int wi = 0; wi < NTT; ++wi) {
+                for (int wi = 0; wi < NC; ++wi) {
                     const float scw = ex2(mg_m[wi * NCOLS + g] - Ms);
                     den += scw * mg_l[wi * NCOLS + g];
                     const float4 v =
