@@ -19,10 +19,11 @@
 //        evict-first) plus one bulk copy of the group's queries, into a ring
 //        of shared-memory stages guarded by mbarriers.  Stage layout:
 //        [page][slab][row][128 B], whatever the layout in HBM.
-//      * consumer warps: warp w owns the 16-token tile w of every stage and
+//      * consumer warps: warp w owns the 16-token tile w of every stage (two
+//        tiles, 2w and 2w+1, with quantised pages at head_dim 128) and
 //        keeps its own running (max, exp-sum, O) per query head: S^T = K Q^T
 //        on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate), one
-//        log2-space online-softmax update with exp2 per tile ("Four speed-up
+//        log2-space online-softmax update with exp2 per stage ("Four speed-up
 //        tricks", 1), then O^T += V^T P^T on tensor cores; no exchange
 //        between warps within a unit.  At the unit's last stage the warps
 //        merge their running states in shared memory and write the final
@@ -662,10 +663,11 @@ __global__ void __launch_bounds__((consumer_warps<D, Q8, MQ>() + 1) * 32, 2)
 
     // ================================================================ consumers
     // Consumer warp w owns token tile w (tokens [16w, 16w+16)) of every
-    // stage and runs its own log2-space online softmax over the whole of
-    // head_dim for the unit's columns (the group's query heads; MQ: query
-    // token x head); the NC warps merge their states once per unit, in the
-    // shared memory of the unit's last stage.
+    // stage (TPW > 1: tiles TPW w .. TPW w + TPW - 1) and runs its own
+    // log2-space online softmax over the whole of head_dim for the unit's
+    // columns (the group's query heads; MQ: query token x head); the NC
+    // warps merge their states once per unit, in the shared memory of the
+    // unit's last stage.
     const int w = warp;
     const int tt = w;                    // merge-state index of the warp
     const int gb = lane >> 2;            // C-fragment row: token within the tile
